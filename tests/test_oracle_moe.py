@@ -1,0 +1,232 @@
+"""Pins of the oracle's routing, slot sort, GEMM and MoE forward against brute
+force, closed forms and special cases (no GPU)."""
+import numpy as np
+import pytest
+
+from oracle import nvfp4_oracle as O
+from nvfp4_mixture_experts_expert_gb300 import workloads as W
+
+
+# ----------------------------------------------------------------- routing
+
+def brute_route(logits, k):
+    T, E = logits.shape
+    ids = np.zeros((T, k), np.int64)
+    w = np.zeros((T, k))
+    for t in range(T):
+        # pick k times the largest remaining logit; ties -> lower expert index
+        left = list(range(E))
+        for j in range(k):
+            best = left[0]
+            for e in left[1:]:
+                if logits[t, e] > logits[t, best]:
+                    best = e
+            ids[t, j] = best
+            left.remove(best)
+        p = np.exp(logits[t].astype(np.float64) - logits[t].max())
+        p /= p.sum()                       # softmax over all experts ...
+        w[t] = p[ids[t]] / p[ids[t]].sum()  # ... renormalised over the k chosen
+    return ids, w
+
+
+@pytest.mark.parametrize("T,E,k", [(17, 8, 2), (40, 48, 6), (9, 5, 5), (12, 3, 1)])
+def test_route_matches_brute_force(T, E, k):
+    rng = np.random.default_rng(T * 100 + E)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    logits[0, :] = 0.5  # all tied: lowest indices win
+    logits[1, 0] = logits[1, E - 1] = 9.0  # a tie between two experts
+    ids, w = O.route(logits, k)
+    bids, bw = brute_route(logits, k)
+    np.testing.assert_array_equal(ids, bids)
+    np.testing.assert_allclose(w, bw, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(w.sum(1), 1.0, rtol=1e-12)
+    assert ids[0].tolist() == list(range(k))
+
+
+def brute_sort(ids, w, E):
+    T, k = ids.shape
+    rows = []
+    off = [0]
+    for e in range(E):
+        mine = [(t, j) for t in range(T) for j in range(k) if ids[t, j] == e]
+        pad = (len(mine) + 127) // 128 * 128
+        rows += [(t, w[t, j], t * k + j) for (t, j) in mine] + [(-1, 0.0, -1)] * (pad - len(mine))
+        off.append(off[-1] + pad)
+    return off, rows
+
+
+@pytest.mark.parametrize("T,E,k", [(64, 8, 2), (200, 3, 2), (150, 4, 1), (30, 6, 3)])
+def test_sort_slots_matches_brute_force(T, E, k):
+    rng = np.random.default_rng(T + E)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    if E == 3:
+        logits[:, 0] += 4  # expert 0 takes >128 rows: several 128-row chunks
+    if E == 6:
+        logits[:, 5] = -np.inf  # an empty expert
+    ids, w = O.route(logits, k)
+    m = O.sort_slots(ids, w, E)
+    off, rows = brute_sort(ids, w, E)
+    assert m["offsets"].tolist() == off
+    assert m["P"] == len(rows) == off[-1]
+    assert m["sorted_token_ids"].tolist() == [r[0] for r in rows]
+    np.testing.assert_array_equal(m["row_weight"], [r[1] for r in rows])
+    for row, (t, _, f) in enumerate(rows):
+        if f >= 0:
+            assert m["inverse"][f] == row
+    assert np.all(np.asarray(off) % 128 == 0)
+    assert m["P"] <= O.slot_capacity(T, k, E)
+
+
+# ----------------------------------------------------------------- GEMM closed forms
+
+def test_gemm_identity_weight_returns_dequantized_activation():
+    rng = np.random.default_rng(7)
+    M, K = 40, 64
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    gs_a = O.global_scale(np.max(np.abs(x)))
+    a_nib, a_s = O.quantize_blocks(x, gs_a)
+    eye = np.eye(K, dtype=np.float32)  # one 1.0 per row: exactly representable
+    b_nib, b_s, b_gs = O.weight_quantize(eye)
+    np.testing.assert_array_equal(O.dequant_blocks(b_nib, b_s) / b_gs, eye)
+    C = O.nvfp4_gemm(a_nib, a_s, gs_a, b_nib, b_s, b_gs)
+    np.testing.assert_array_equal(C, O.dequant_blocks(a_nib, a_s) / np.float64(gs_a))
+
+
+def test_gemm_permutation_weight_is_a_column_permutation():
+    rng = np.random.default_rng(8)
+    M, K = 8, 32
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    gs_a = O.global_scale(np.max(np.abs(x)))
+    a_nib, a_s = O.quantize_blocks(x, gs_a)
+    perm = rng.permutation(K)
+    P = np.zeros((K, K), np.float32)
+    P[np.arange(K), perm] = 1.0  # output column n reads input column perm[n]
+    b_nib, b_s, b_gs = O.weight_quantize(P)
+    C = O.nvfp4_gemm(a_nib, a_s, gs_a, b_nib, b_s, b_gs)
+    A = O.dequant_blocks(a_nib, a_s) / np.float64(gs_a)
+    np.testing.assert_array_equal(C, A[:, perm])
+
+
+def test_gemm_equals_plain_matmul_of_dequantized_operands():
+    rng = np.random.default_rng(9)
+    a = rng.standard_normal((16, 48)).astype(np.float32)
+    b = rng.standard_normal((24, 48)).astype(np.float32)
+    an, as_ = O.quantize_blocks(a, np.float32(2))
+    bn, bs = O.quantize_blocks(b, np.float32(4))
+    A = O.dequant_blocks(an, as_) / 2
+    B = O.dequant_blocks(bn, bs) / 4
+    ref = np.array([[sum(A[i, kk] * B[j, kk] for kk in range(48)) for j in range(24)] for i in range(16)])
+    np.testing.assert_allclose(O.nvfp4_gemm(an, as_, 2, bn, bs, 4), ref, rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------- MoE
+
+def small_layer(T=48, H=64, I=32, E=5, k=2, seed=11):
+    wl = W.moe_workload(T, H, I, E, k, seed, zero_block_frac=0.05, tiny_block_frac=0.05)
+    hidden = W.bf16_bits_to_f32(wl.hidden)
+    w13 = W.bf16_bits_to_f32(wl.w13)
+    w2 = W.bf16_bits_to_f32(wl.w2)
+    w13q = O.quantize_expert_weights(w13)
+    w2q = O.quantize_expert_weights(w2)
+    a1, a2 = O.calibrate_activation_scales(hidden, wl.logits, k, w13q)
+    return wl, hidden, w13, w2, w13q, w2q, a1, a2
+
+
+def dense_brute_moe(hidden, logits, k, w13q, w2q, a1, a2, gl, ul):
+    """Every expert on every token, then masked by the routing: no slots, no sort."""
+    T, H = hidden.shape
+    E = w13q[0].shape[0]
+    I = w13q[0].shape[1] // 2
+    ids, w = brute_route(logits, k)
+    out = np.zeros((T, H))
+    for e in range(E):
+        A = O.dequant_blocks(*O.quantize_blocks(hidden, a1[e])) / np.float64(a1[e])
+        B = O.dequant_blocks(w13q[0][e], w13q[1][e]) / np.float64(w13q[2][e])
+        G = A @ B.T
+        g = np.minimum(G[:, :I], gl)
+        u = np.clip(G[:, I:], -ul, ul)
+        h = O.bf16_round((g / (1 + np.exp(-g)) * u).astype(np.float32))
+        A2 = O.dequant_blocks(*O.quantize_blocks(h, a2[e])) / np.float64(a2[e])
+        B2 = O.dequant_blocks(w2q[0][e], w2q[1][e]) / np.float64(w2q[2][e])
+        Y = A2 @ B2.T
+        mask = np.zeros(T)
+        for t in range(T):
+            for j in range(k):
+                if ids[t, j] == e:
+                    mask[t] += w[t, j]
+        out += mask[:, None] * Y
+    return O.bf16_round(out.astype(np.float32))
+
+
+def test_sparse_moe_equals_dense_brute_force():
+    wl, hidden, w13, w2, w13q, w2q, a1, a2 = small_layer()
+    out = O.moe_forward(hidden, wl.logits, wl.top_k, w13q, w2q, a1, a2, 10.0, 10.0)
+    ref = dense_brute_moe(hidden, wl.logits, wl.top_k, w13q, w2q, a1, a2, 10.0, 10.0)
+    np.testing.assert_allclose(out, ref, rtol=1e-2, atol=1e-6)
+    # identical up to the last bf16 rounding of sums formed in a different order
+    assert np.mean(out != ref) < 0.01
+
+
+def test_single_expert_top1_is_a_dense_swiglu_ffn():
+    wl = W.moe_workload(20, 64, 32, 1, 1, 3)
+    hidden = W.bf16_bits_to_f32(wl.hidden)
+    w13q = O.quantize_expert_weights(W.bf16_bits_to_f32(wl.w13))
+    w2q = O.quantize_expert_weights(W.bf16_bits_to_f32(wl.w2))
+    a1 = np.float32([O.global_scale(np.abs(hidden).max())])
+    a2 = np.float32([7.0])
+    out = O.moe_forward(hidden, wl.logits, 1, w13q, w2q, a1, a2, 10.0, 10.0)
+    # textbook FFN on the dequantized operands: y = W2 (silu(W1 x) * W3 x)
+    xq = O.dequant_blocks(*O.quantize_blocks(hidden, a1[0])) / np.float64(a1[0])
+    Wg = O.dequant_blocks(w13q[0][0][:32], w13q[1][0][:32]) / np.float64(w13q[2][0])
+    Wu = O.dequant_blocks(w13q[0][0][32:], w13q[1][0][32:]) / np.float64(w13q[2][0])
+    gate = np.minimum(xq @ Wg.T, 10.0)
+    up = np.clip(xq @ Wu.T, -10.0, 10.0)
+    h = O.bf16_round((gate * (1 / (1 + np.exp(-gate))) * up).astype(np.float32))
+    hq = O.dequant_blocks(*O.quantize_blocks(h, a2[0])) / np.float64(a2[0])
+    W2 = O.dequant_blocks(w2q[0][0], w2q[1][0]) / np.float64(w2q[2][0])
+    ref = O.bf16_round((hq @ W2.T).astype(np.float32))
+    # same arithmetic up to where 1/gs enters an FP64 product: agree to bf16 rounding
+    np.testing.assert_allclose(out, ref, rtol=8e-3, atol=1e-6 * np.abs(ref).max())
+    assert np.mean(out == ref) > 0.99
+
+
+def test_quantized_moe_tracks_unquantized_moe():
+    """Sanity against an unquantized FP64 MoE: cosine in the range the pages
+    report for NVFP4 layers vs BF16 (about 0.99)."""
+    wl, hidden, w13, w2, w13q, w2q, a1, a2 = small_layer(T=64, H=128, I=64, E=4, k=2, seed=12)
+    out = O.moe_forward(hidden, wl.logits, 2, w13q, w2q, a1, a2)
+    ids, w = O.route(wl.logits, 2)
+    ref = np.zeros(out.shape)
+    for t in range(wl.T):
+        for j in range(2):
+            e = ids[t, j]
+            G = w13[e].astype(np.float64) @ hidden[t].astype(np.float64)
+            g, u = np.minimum(G[:64], 10), np.clip(G[64:], -10, 10)
+            ref[t] += w[t, j] * (w2[e].astype(np.float64) @ (g / (1 + np.exp(-g)) * u))
+    cos = np.sum(out * ref) / np.linalg.norm(out) / np.linalg.norm(ref)
+    assert 0.97 < cos < 0.9999
+
+
+def test_moe_is_linear_in_w2_scale_and_zero_for_zero_input():
+    wl, hidden, w13, w2, w13q, w2q, a1, a2 = small_layer(T=16, H=64, I=32, E=3, k=2, seed=13)
+    zero = np.zeros_like(hidden)
+    out0 = O.moe_forward(zero, wl.logits, 2, w13q, w2q, np.ones(3, np.float32), a2)
+    assert np.all(out0 == 0)
+    # halving the W2 global scale (same nibbles and block scales) doubles the output
+    w2q_half = (w2q[0], w2q[1], (w2q[2] / 2).astype(np.float32))
+    o1 = O.moe_forward(hidden, wl.logits, 2, w13q, w2q, a1, a2)
+    o2 = O.moe_forward(hidden, wl.logits, 2, w13q, w2q_half, a1, a2)
+    np.testing.assert_allclose(o2, 2 * o1, rtol=8e-3, atol=1e-30)
+
+
+def test_tiny_workload_exercises_forced_blocks():
+    wl = W.tiny_moe()
+    hidden = W.bf16_bits_to_f32(wl.hidden)
+    gs = O.global_scale(np.abs(hidden).max())
+    _, s = O.quantize_blocks(hidden, gs)
+    xs = (hidden * gs).reshape(-1, 16)
+    b = np.abs(xs).max(1)
+    zero_blocks = b == 0
+    under = (b > 0) & (b < 6 * 2.0 ** -9)
+    assert zero_blocks.sum() >= 40 and under.sum() >= 10
+    assert np.all(s.reshape(-1)[zero_blocks | under] == 0)
