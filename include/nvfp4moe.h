@@ -1,0 +1,198 @@
+/*
+ * nvfp4moe.h -- C ABI of the GB300 (sm_103a) NVFP4 mixture-of-experts FFN forward.
+ *
+ * The method: the nvfp4-megamoe-kernel commit pages (cutedsl/bridge.py page,
+ * commit 50e9b5da; vllm page, commit bde81b95; cutedsl page, commit dfd9c10a).
+ * Those pages have no numbered sections; each entry point below names the
+ * commit paragraph that defines its operation.
+ *
+ * Conventions for every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    allocates no device memory and keeps no pointer after the call returns.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *    asynchronous on that stream: no host synchronisation, no host<->device
+ *    copy, and sizes that depend on the data stay on the device.
+ *  - Return value: an nvfp4_status.  Argument errors are detected on the host
+ *    before anything is launched; nothing is launched when a call fails.
+ *    nvfp4_last_error() gives a one-line reason for the last failure on the
+ *    calling thread.  Errors found on the device (a bounded wait that timed
+ *    out) are recorded in a device status word, read by nvfp4_device_status().
+ *  - NVFP4 tensors: E2M1 values packed two per byte along K (element 2j in the
+ *    low nibble of byte j), one FP8-E4M3 scale per 16 consecutive K elements,
+ *    and an FP32 global scale gs per tensor or group, multiplied into the
+ *    data before encoding (decoded value = e2m1 * scale / gs).
+ *  - Scale ("SF") buffers use the 128x4 tile layout of the block-scaled MMA:
+ *    for a tensor with R rows (R a multiple of 128) and C = K/16 scale columns
+ *    (C a multiple of 4), scale (r, c) is at byte
+ *        ((r/128)*(C/4) + c/4)*512 + (r%32)*16 + ((r%128)/32)*4 + c%4,
+ *    i.e. R*C bytes in 512-byte tiles.
+ *  - Alignment: every pointer 16-byte aligned; K a multiple of 64.
+ */
+#ifndef NVFP4MOE_H
+#define NVFP4MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID_ARG = 1,    /* bad pointer, size, stride or alignment        */
+  NVFP4_ERR_UNSUPPORTED = 2,    /* valid request outside what is implemented     */
+  NVFP4_ERR_WORKSPACE = 3,      /* workspace missing or too small                */
+  NVFP4_ERR_CUDA = 4,           /* a CUDA runtime / driver call failed           */
+  NVFP4_ERR_DEVICE = 5,         /* no usable sm_103a device                      */
+  NVFP4_ERR_DEVICE_TIMEOUT = 6  /* a device-side bounded wait ran out            */
+} nvfp4_status;
+
+/* Library version as 10000*major + 100*minor + patch. */
+int nvfp4_version(void);
+/* Static description of a status code. */
+const char* nvfp4_status_string(int status);
+/* One-line reason of the last failing call on this thread ("" if none). */
+const char* nvfp4_last_error(void);
+
+/*
+ * nvfp4_quantize -- NVFP4 activation / weight quantization
+ * (bridge.py page: "Bug #3 fix", "Bug #4 fix", the 13-byte lookup-table
+ * paragraph, and quantize_activation_nvfp4 with a precomputed global scale;
+ * cutedsl page: the (T,G,D) -> (G,T,D) permute paragraph for strided groups).
+ *
+ * Quantizes `groups` groups of `rows` rows of K bf16 values each.  Row r of
+ * group g is read at x + g*group_stride_x + r*ld_x (elements, K contiguous).
+ * Output row g*rows_padded + r of `fp4` ([groups*rows_padded][K/2] bytes) and
+ * of the swizzled scale buffer `sf` (groups*rows_padded*K/16 bytes) receives
+ * it; rows rows..rows_padded-1 of every group are written as zeros.
+ *   gs       device f32[groups] encode scales, or NULL: then gs = 2688/amax of
+ *            the group (1 if the group is all zero) is computed on the device
+ *            and written to gs_out (required in that case).
+ *   gs_out   device f32[groups] or NULL (when gs != NULL it receives a copy).
+ *   workspace, workspace_bytes: device scratch of at least
+ *            nvfp4_quantize_workspace_size(groups) bytes when gs == NULL
+ *            (ignored otherwise).
+ * Requirements: K % 64 == 0, rows_padded % 128 == 0, rows <= rows_padded,
+ * ld_x % 8 == 0, group_stride_x % 8 == 0, groups >= 1.
+ */
+size_t nvfp4_quantize_workspace_size(int groups);
+int nvfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, int64_t group_stride_x, int groups,
+                   const float* gs, float* gs_out, void* workspace, size_t workspace_bytes, void* fp4, void* sf,
+                   int64_t rows_padded, void* stream);
+
+/*
+ * nvfp4_assemble_scales -- place per-group linear scales into 128-row padded
+ * slots in the tile layout (vllm page: "Root cause of garbage output",
+ * "Bug 9" multi-chunk slots, and the wish for an assembly call that takes a
+ * flat scale tensor plus offsets; cutedsl page: assemble_scales_2d_side).
+ *   sf_linear       device u8 [offsets[G]][sf_cols] (row-major E4M3 codes)
+ *   offsets         device i32[G+1], rows of group g are offsets[g]..offsets[g+1]-1
+ *   padded_offsets  device i32[G+1], multiples of 128, with
+ *                   padded_offsets[g+1]-padded_offsets[g] >= offsets[g+1]-offsets[g]
+ *   rows_capacity   rows of the output buffer (multiple of 128, >= padded_offsets[G])
+ *   sf_swizzled     device u8 [rows_capacity * roundup(sf_cols,4)] (tile layout);
+ *                   every byte is written, pad rows and pad columns as 0.
+ */
+int nvfp4_assemble_scales(const void* sf_linear, int64_t sf_cols, const int32_t* offsets,
+                          const int32_t* padded_offsets, int groups, int64_t rows_capacity, void* sf_swizzled,
+                          void* stream);
+
+/*
+ * nvfp4_grouped_gemm -- block-scaled NVFP4 grouped GEMM with BF16 output
+ * (vllm page: the GEMM reads scale_a by 128-aligned expert offsets; cutedsl
+ * page: group g's rows at their own offset range, single-group linear and
+ * shared-expert runners with num_groups = 1).
+ *
+ *   D[g][i][n] = bf16( alpha_g * sum_k A[padded_offsets[g] + i][k] * B[g][n][k] ),
+ *   alpha_g = 1 / (a_gs[g] * b_gs[g]), FP32 accumulation.
+ *   A    device u8 [rows_capacity][K/2], SFA tile layout over rows_capacity rows
+ *   B    device u8 [G][N][K/2] (K-major),  SFB [G][N*K/16] tile layout per group
+ *   a_gs, b_gs      device f32[G]
+ *   padded_offsets  device i32[G+1], multiples of 128, padded_offsets[G] <= rows_capacity
+ *   counts          device i32[G] rows actually stored per group (<= its padded
+ *                   range), or NULL to store every padded row
+ *   D    device bf16; row i of group g starts at D + g*group_stride_d + i*ldd (elements)
+ * Requirements: K % 64 == 0, N % 256 == 0, ldd % 8 == 0, group_stride_d % 8 == 0,
+ * rows_capacity % 128 == 0, 1 <= G <= 1024.
+ */
+int nvfp4_grouped_gemm(const void* A, const void* SFA, const float* a_gs, const void* B, const void* SFB,
+                       const float* b_gs, const int32_t* padded_offsets, const int32_t* counts, int groups,
+                       int64_t rows_capacity, int64_t N, int64_t K, void* D, int64_t ldd, int64_t group_stride_d,
+                       void* stream);
+
+/*
+ * nvfp4_moe_forward -- the NVFP4 mixture-of-experts FFN forward
+ * (vllm page: the MoE runner -- 128-row slots, multi-chunk slots "Bug 9",
+ * sorted_token_ids gather, quantize_activation_nvfp4 with calibrated global
+ * scales, scatter_add combine with zero-weight padding; bridge.py page: fused
+ * SwiGLU L1 epilogue and run_nvfp4_moe_fused; cutedsl page: gate clamped
+ * before SiLU).
+ *
+ * For each token t: experts = top_k router logits (ties -> lower expert),
+ * weights = softmax renormalised over the chosen experts; for each chosen
+ * expert e with weight w:
+ *   G  = dq(quant(x_t, a1_gs[e])) . dq(W13[e])^T           (2I outputs)
+ *   h  = bf16( silu(min(G[:I], gate_limit)) * clamp(G[I:], -up_limit, up_limit) )
+ *   Y  = dq(quant(h, a2_gs[e])) . dq(W2[e])^T              (H outputs)
+ *   out[t] += w * Y,   out is written as bf16.
+ *   hidden         device bf16 [T][H]
+ *   router_logits  device f32 [T][E]
+ *   w13            device u8 [E][2I][H/2]  (rows 0..I-1 gate, I..2I-1 up)
+ *   w13_sf         device u8 [E][2I*H/16]  (tile layout per expert)
+ *   w2             device u8 [E][H][I/2],  w2_sf device u8 [E][H*I/16]
+ *   w13_gs, w2_gs, a1_gs, a2_gs   device f32[E] global (encode) scales
+ *   workspace      device scratch of nvfp4_moe_workspace_size(...) bytes, 256-aligned;
+ *                  it also holds every intermediate (see nvfp4_moe_workspace_layout).
+ *   out            device bf16 [T][H]
+ * Requirements: H % 256 == 0, I % 128 == 0, 1 <= E <= 256, 1 <= top_k <= min(8, E),
+ * T >= 0 (T == 0 launches nothing).
+ */
+size_t nvfp4_moe_workspace_size(int64_t T, int64_t H, int64_t I, int E, int top_k);
+int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T, int64_t H, int64_t I, int E,
+                      int top_k, const void* w13, const void* w13_sf, const float* w13_gs, const void* w2,
+                      const void* w2_sf, const float* w2_gs, const float* a1_gs, const float* a2_gs,
+                      float gate_limit, float up_limit, void* workspace, size_t workspace_bytes, void* out,
+                      void* stream);
+
+/*
+ * Byte offsets of the forward's intermediates inside the workspace, for
+ * inspection by tests.  Sizes: cap = padded-row capacity
+ * (roundup(T*top_k + 127*min(E, T*top_k), 128)); A = T*top_k assignments.
+ *   topk_ids i32[A], topk_w f32[A]   (token-major: index t*top_k + j)
+ *   counts i32[E], offsets i32[E+1]  (padded slot starts, multiples of 128)
+ *   meta i32[4] = {P (padded rows), P/128, 0, 0}
+ *   tile_expert i32[cap/128], sorted_token_ids i32[cap] (-1 pad),
+ *   row_weight f32[cap] (0 pad), inverse i32[A] (assignment -> row)
+ *   a1 u8[cap][H/2], sfa1 u8[cap*H/16], a2 u8[cap][I/2], sfa2 u8[cap*I/16]
+ *   acc f32[T][H] (combine accumulator)
+ * Only rows < P of the row-indexed buffers are defined after a call.
+ */
+typedef struct {
+  size_t topk_ids, topk_w, block_counts, counts, offsets, meta, tile_expert, sorted_token_ids, row_weight,
+      inverse, a1, sfa1, a2, sfa2, acc, total;
+  int64_t capacity;
+  int64_t route_blocks;
+} nvfp4_moe_layout;
+int nvfp4_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int E, int top_k, nvfp4_moe_layout* out);
+
+/*
+ * Device status word shared by all kernels of the library on the current
+ * device: NVFP4_OK or NVFP4_ERR_DEVICE_TIMEOUT.  Synchronises the device.
+ * reset != 0 clears it afterwards.
+ */
+int nvfp4_device_status(int* status_out, int reset);
+
+/*
+ * Optional per-stage timing of nvfp4_moe_forward: when set, the forward
+ * records events[i] (cudaEvent_t) on its stream before stage i, i = 0..6, and
+ * events[7] after the last stage (stages: route, slot scan, slot scatter,
+ * gather+quantize, L1 GEMM, L2 GEMM, finalize).  n_events must be 8, or 0
+ * with events NULL to switch it off.  Process-wide; not thread-safe.
+ */
+int nvfp4_moe_set_stage_events(void* const* events, int n_events);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4MOE_H */

@@ -1,0 +1,124 @@
+"""Torch-side convenience layer over the C ABI: allocates outputs and
+workspaces with torch on the current CUDA device and calls the binding.
+No arithmetic of the method happens here."""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import binding as B
+
+
+def _round_up(x, m):
+    return (x + m - 1) // m * m
+
+
+def _u8(n, device):
+    return torch.empty(max(int(n), 1), dtype=torch.uint8, device=device)
+
+
+def quantize(x: torch.Tensor, gs: torch.Tensor | None = None, rows_padded: int | None = None, stream=None):
+    """NVFP4-quantize the rows of a 2-D bf16 tensor.  Returns (fp4 [Rp, K/2] u8,
+    sf (tile layout, Rp*K/16 bytes) u8, gs f32[1])."""
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    R, K = x.shape
+    Rp = rows_padded if rows_padded is not None else _round_up(max(R, 1), 128)
+    dev = x.device
+    fp4 = torch.empty((Rp, K // 2), dtype=torch.uint8, device=dev)
+    sf = _u8(Rp * K // 16, dev)
+    gs_out = torch.empty(1, dtype=torch.float32, device=dev)
+    ws = None
+    wsb = 0
+    if gs is None:
+        wsb = B.nvfp4_quantize_workspace_size(1)
+        ws = _u8(wsb, dev)
+    B.nvfp4_quantize(x, R, K, x.stride(0), 0, 1, gs, gs_out, ws, wsb, fp4, sf, Rp, stream)
+    return fp4, sf, gs_out
+
+
+def quantize_groups(x: torch.Tensor, rows: int, K: int, ld_x: int, group_stride_x: int, groups: int,
+                    gs: torch.Tensor | None = None, rows_padded: int | None = None, stream=None):
+    """Quantize `groups` strided groups of rows of a bf16 buffer (see nvfp4_quantize)."""
+    Rp = rows_padded if rows_padded is not None else _round_up(max(rows, 1), 128)
+    dev = x.device
+    fp4 = torch.empty((groups * Rp, K // 2), dtype=torch.uint8, device=dev)
+    sf = _u8(groups * Rp * K // 16, dev)
+    gs_out = torch.empty(groups, dtype=torch.float32, device=dev)
+    ws = None
+    wsb = 0
+    if gs is None:
+        wsb = B.nvfp4_quantize_workspace_size(groups)
+        ws = _u8(wsb, dev)
+    B.nvfp4_quantize(x, rows, K, ld_x, group_stride_x, groups, gs, gs_out, ws, wsb, fp4, sf, Rp, stream)
+    return fp4, sf, gs_out
+
+
+def quantize_expert_weights(w: torch.Tensor, gs: torch.Tensor | None = None, stream=None):
+    """w: bf16 [E, N, K] (K contiguous, N % 128 == 0).  One global scale per expert
+    (2688/amax of the expert unless gs is given).  Returns (fp4 [E, N, K/2],
+    sf [E, N*K/16], gs [E])."""
+    E, N, K = w.shape
+    assert N % 128 == 0 and w.is_contiguous()
+    fp4, sf, gs_out = quantize_groups(w, N, K, K, N * K, E, gs=gs, rows_padded=N, stream=stream)
+    return fp4.view(E, N, K // 2), sf.view(E, N * K // 16), gs_out
+
+
+def grouped_gemm(A, SFA, a_gs, Bw, SFB, b_gs, padded_offsets, counts, N, K, D, ldd, group_stride_d, stream=None):
+    G = a_gs.numel()
+    B.nvfp4_grouped_gemm(A, SFA, a_gs, Bw, SFB, b_gs, padded_offsets, counts, G, A.shape[0], N, K, D, ldd,
+                         group_stride_d, stream)
+    return D
+
+
+@dataclass
+class MoEWeights:
+    w13: torch.Tensor      # u8 [E, 2I, H/2]
+    w13_sf: torch.Tensor   # u8 [E, 2I*H/16]
+    w13_gs: torch.Tensor   # f32 [E]
+    w2: torch.Tensor       # u8 [E, H, I/2]
+    w2_sf: torch.Tensor    # u8 [E, H*I/16]
+    w2_gs: torch.Tensor    # f32 [E]
+
+    @property
+    def E(self):
+        return self.w13.shape[0]
+
+    @property
+    def I(self):
+        return self.w13.shape[1] // 2
+
+    @property
+    def H(self):
+        return self.w2.shape[1]
+
+
+def quantize_moe_weights(w13_bf16, w2_bf16, stream=None) -> MoEWeights:
+    a = quantize_expert_weights(w13_bf16, stream=stream)
+    b = quantize_expert_weights(w2_bf16, stream=stream)
+    return MoEWeights(a[0], a[1], a[2], b[0], b[1], b[2])
+
+
+class MoEForward:
+    """Holds a workspace sized for (T, H, I, E, top_k) and runs nvfp4_moe_forward."""
+
+    def __init__(self, T, H, I, E, top_k, device="cuda"):
+        self.T, self.H, self.I, self.E, self.top_k = T, H, I, E, top_k
+        self.ws_bytes = B.nvfp4_moe_workspace_size(T, H, I, E, top_k)
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.layout = B.nvfp4_moe_workspace_layout(T, H, I, E, top_k)
+
+    def __call__(self, hidden, logits, w: MoEWeights, a1_gs, a2_gs, gate_limit=10.0, up_limit=10.0, out=None,
+                 stream=None):
+        if out is None:
+            out = torch.empty((self.T, self.H), dtype=torch.bfloat16, device=hidden.device)
+        B.nvfp4_moe_forward(hidden, logits, self.T, self.H, self.I, self.E, self.top_k, w.w13, w.w13_sf,
+                            w.w13_gs, w.w2, w.w2_sf, w.w2_gs, a1_gs, a2_gs, gate_limit, up_limit,
+                            self.workspace, self.ws_bytes, out, stream)
+        return out
+
+    def view(self, name, dtype, count):
+        """A view of one intermediate of the last call (see nvfp4_moe_workspace_layout)."""
+        off = self.layout[name]
+        nbytes = count * torch.empty((), dtype=dtype).element_size()
+        return self.workspace[off:off + nbytes].view(dtype)

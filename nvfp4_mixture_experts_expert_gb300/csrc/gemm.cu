@@ -1,0 +1,401 @@
+// Block-scaled NVFP4 grouped GEMM for sm_103a on the 5th-generation tensor
+// cores (tcgen05.mma kind::mxf4nvf4, 16-element UE4M3 block scales), with
+// three fused epilogues:
+//   kEpiBf16         D = alpha_g * acc as bf16 (grouped / dense linear)
+//   kEpiSwigluQuant  MoE L1: h = bf16(silu(min(alpha*gate, gl)) * clamp(alpha*up, +-ul)),
+//                    requantized to NVFP4 with the expert's L2 activation scale,
+//                    nibbles and tile-layout scales written for the L2 GEMM
+//                    (bridge.py page: fused SwiGLU epilogue; cutedsl page: gate
+//                    clamped before SiLU)
+//   kEpiCombine      MoE L2: out[token] += w_row * alpha * acc (FP32 red.add),
+//                    pad rows skipped (vllm page: scatter_add with zero-weight pads)
+//
+// Design (one CTA per SM, persistent over output tiles, warp-specialised):
+//   warp 0   TMA producer: per K-stage of 256 elements, one 128x128-byte A box,
+//            two 128x128-byte B boxes (SWIZZLE_128B) and the matching 512-byte
+//            scale tiles (plain bulk copies), into a 4-deep shared-memory ring.
+//   warp 1   TMEM allocator and MMA issuer: copies the scale tiles to TMEM
+//            (tcgen05.cp 32x128b.warpx4) and issues 4 MMAs of 128x256x64 per
+//            stage into a 128-lane x 256-column FP32 accumulator in TMEM.
+//   warps 2-5 epilogue: each warp owns the 32 TMEM lanes of its quarter
+//            (warp % 4), i.e. 32 output rows, and reads the accumulator with
+//            tcgen05.ld.
+// A tile is 128 rows x 256 MMA columns.  For the SwiGLU epilogue the two B
+// boxes are the gate rows [n0, n0+128) and the up rows [I+n0, I+n0+128) of the
+// expert's W13, so gate and up of one output feature sit in the same TMEM lane
+// 128 columns apart, and the 16-wide requantization blocks are in-register.
+// Tiles are ordered m-tile major, n-tile minor; m-tiles map to groups through
+// the 128-aligned group offsets read from device memory (no host sync).
+// Every mbarrier wait is bounded (timeout -> device status word, abort, drain
+// of copies/MMAs in flight, TMEM freed, return).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "nvfp4_format.cuh"
+#include "ptx.cuh"
+
+namespace nvfp4 {
+
+__device__ int g_device_status;
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK_BYTES = 128;  // 256 FP4 elements per stage
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK_BYTES;
+constexpr int B_BYTES = BN * BK_BYTES;
+constexpr int SFA_BYTES = 4 * 512;
+constexpr int SFB_BYTES = 8 * 512;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+constexpr int TMEM_COLS = 512;
+constexpr int SF_COL0 = 256;         // scale columns start after the accumulator
+constexpr int SF_COLS_PER_STAGE = 48;  // 4 x (4 SFA + 8 SFB)
+constexpr int NUM_THREADS = 192;
+constexpr int MAX_GROUPS = 1024;
+static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
+static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+
+// Instruction descriptor: E2M1 x E2M1, UE4M3 scales, K-major A and B, dense K=64.
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 7) << 27);
+}
+
+struct SmemLayout {
+  uint8_t* stages;
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* acc_full;
+  uint64_t* acc_empty;
+  uint64_t* drain;
+  uint32_t* tmem_slot;
+  int* abort_flag;
+  int* offsets;
+};
+
+__device__ __forceinline__ SmemLayout carve(uint8_t* raw) {
+  SmemLayout L;
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  L.stages = base;
+  uint8_t* p = base + STAGES * STAGE_BYTES;
+  L.full = reinterpret_cast<uint64_t*>(p);
+  L.empty = L.full + STAGES;
+  L.acc_full = L.empty + STAGES;
+  L.acc_empty = L.acc_full + 1;
+  L.drain = L.acc_empty + 1;
+  L.tmem_slot = reinterpret_cast<uint32_t*>(L.drain + 1);
+  L.abort_flag = reinterpret_cast<int*>(L.tmem_slot + 1);
+  L.offsets = reinterpret_cast<int*>(L.abort_flag + 3);
+  return L;
+}
+
+__device__ __forceinline__ int find_group(const int* off, int G, int row) {
+  int lo = 0, hi = G;  // largest g in [0, G) with off[g] <= row
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (off[mid] <= row) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// ------------------------------------------------------------------ producer
+__device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total) {
+  volatile int* abort = L.abort_flag;
+  int issued_parity[STAGES];
+#pragma unroll
+  for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+  uint32_t stage = 0, phase = 0;
+  const int kt = p.K / 64;  // scale tiles per 128-row band
+  if (!p.debug_no_loads) {
+    for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+      const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
+      const int g = find_group(L.offsets, p.G, mt * BM);
+      const int b_r0 = nt * p.b_tile_stride;
+      const int b_r1 = b_r0 + p.b_second_offset;
+      const int64_t b_row0 = (int64_t)g * p.b_rows_per_group + b_r0;
+      const int64_t b_row1 = (int64_t)g * p.b_rows_per_group + b_r1;
+      const uint8_t* sfa = p.sfa + (int64_t)mt * kt * 512;
+      const uint8_t* sfb0 = p.sfb + g * p.sfb_group_bytes + (int64_t)(b_r0 >> 7) * kt * 512;
+      const uint8_t* sfb1 = p.sfb + g * p.sfb_group_bytes + (int64_t)(b_r1 >> 7) * kt * 512;
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        const int nmma = min(4, (p.K - kb * 256) / 64);
+        if (!wait_bounded(smem_u32(&L.empty[stage]), phase ^ 1u, abort, p.status, p.timeout_ns)) break;
+        uint8_t* st = L.stages + stage * STAGE_BYTES;
+        const uint32_t bar = smem_u32(&L.full[stage]);
+        mbar_arrive_expect_tx(bar, A_BYTES + B_BYTES + 3 * nmma * 512);
+        tma_load_2d(smem_u32(st), &p.tmap_a, kb * BK_BYTES, mt * BM, bar);
+        tma_load_2d(smem_u32(st + A_BYTES), &p.tmap_b, kb * BK_BYTES, (int32_t)b_row0, bar);
+        tma_load_2d(smem_u32(st + A_BYTES + B_BYTES / 2), &p.tmap_b, kb * BK_BYTES, (int32_t)b_row1, bar);
+        bulk_load(smem_u32(st + A_BYTES + B_BYTES), sfa + kb * 2048, nmma * 512, bar);
+        bulk_load(smem_u32(st + A_BYTES + B_BYTES + SFA_BYTES), sfb0 + kb * 2048, nmma * 512, bar);
+        bulk_load(smem_u32(st + A_BYTES + B_BYTES + SFA_BYTES + 2048), sfb1 + kb * 2048, nmma * 512, bar);
+        issued_parity[stage] = (int)phase;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  }
+  if (*abort) {  // let copies already issued land before the CTA exits
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s)
+      if (issued_parity[s] >= 0) {
+        volatile int no_abort = 0;
+        wait_bounded(smem_u32(&L.full[s]), (uint32_t)issued_parity[s], &no_abort, nullptr, p.timeout_ns);
+      }
+  }
+}
+
+// ------------------------------------------------------------------ MMA issuer
+__device__ void mma_loop(const GemmArgs& p, const SmemLayout& L, int total, uint32_t tmem) {
+  volatile int* abort = L.abort_flag;
+  const uint32_t idesc = idesc_nvf4(BM, BN);
+  uint32_t stage = 0, phase = 0, acc_phase = 0;
+  bool issued_any = false;
+  for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+    if (!wait_bounded(smem_u32(L.acc_empty), acc_phase ^ 1u, abort, p.status, p.timeout_ns)) break;
+    tc_fence_after();
+    bool ok = true;
+    for (int kb = 0; kb < p.num_kb; ++kb) {
+      const int nmma = min(4, (p.K - kb * 256) / 64);
+      if (!wait_bounded(smem_u32(&L.full[stage]), phase, abort, p.status, p.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a_s = smem_u32(L.stages + stage * STAGE_BYTES);
+      const uint32_t b_s = a_s + A_BYTES;
+      const uint32_t sfa_s = b_s + B_BYTES;
+      const uint32_t sfb_s = sfa_s + SFA_BYTES;
+      const uint32_t sf_col = tmem + SF_COL0 + stage * SF_COLS_PER_STAGE;
+      for (int i = 0; i < nmma; ++i) {
+        tc_cp_sf(sf_col + 4 * i, smem_desc(sfa_s + 512 * i, 0, 128, 0));
+        tc_cp_sf(sf_col + 16 + 8 * i, smem_desc(sfb_s + 512 * i, 0, 128, 0));
+        tc_cp_sf(sf_col + 16 + 8 * i + 4, smem_desc(sfb_s + 2048 + 512 * i, 0, 128, 0));
+      }
+      for (int i = 0; i < nmma; ++i) {
+        const uint64_t ad = smem_desc(a_s + 32 * i, 16, 1024, 2);
+        const uint64_t bd = smem_desc(b_s + 32 * i, 16, 1024, 2);
+        tc_mma_nvf4(tmem, ad, bd, idesc, sf_col + 4 * i, sf_col + 16 + 8 * i, (kb | i) != 0);
+      }
+      issued_any = true;
+      tc_commit(smem_u32(&L.empty[stage]));
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) break;
+    tc_commit(smem_u32(L.acc_full));
+    acc_phase ^= 1u;
+  }
+  if (*abort && issued_any) {  // every MMA / copy issued must finish before TMEM is freed
+    tc_commit(smem_u32(L.drain));
+    volatile int no_abort = 0;
+    wait_bounded(smem_u32(L.drain), 0, &no_abort, nullptr, p.timeout_ns);
+  }
+}
+
+// ------------------------------------------------------------------ epilogues
+__device__ __forceinline__ float silu_clamped_product(float g, float u, float gl, float ul) {
+  g = fminf(g, gl);
+  u = fminf(fmaxf(u, -ul), ul);
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+template <int EPI>
+__device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total, uint32_t tmem) {
+  volatile int* abort = L.abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3;
+  const int row_in_tile = quarter * 32 + lane;
+  const uint32_t t_base = tmem + ((uint32_t)(quarter * 32) << 16);
+  uint32_t acc_phase = 0;
+  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    int ok = 1;
+    if (lane == 0) ok = wait_bounded(smem_u32(L.acc_full), acc_phase, abort, p.status, p.timeout_ns);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) break;
+    __syncwarp();
+    tc_fence_after();
+    const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
+    const int g = find_group(L.offsets, p.G, mt * BM);
+    const int64_t row = (int64_t)mt * BM + row_in_tile;
+    const float alpha = 1.0f / (p.a_gs[g] * p.b_gs[g]);
+
+    if constexpr (EPI == kEpiBf16) {
+      const int64_t i_local = row - L.offsets[g];
+      const bool valid = p.counts ? i_local < p.counts[g] : true;
+      uint16_t* drow = p.D + g * p.gstride_d + i_local * p.ldd + (int64_t)nt * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_load_32(t_base + c * 32, r);
+        tmem_load_wait();
+        if (valid) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]) * alpha, __uint_as_float(r[2 * j + 1]) * alpha);
+          uint4* dst = reinterpret_cast<uint4*>(drow + c * 32);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+      }
+    } else if constexpr (EPI == kEpiSwigluQuant) {
+      const float qgs = p.q_gs[g];
+      const int64_t q_cols = p.I / 16;
+#pragma unroll 1
+      for (int h2 = 0; h2 < 2; ++h2) {
+        uint32_t scales = 0;
+#pragma unroll 1
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int col = h2 * 64 + c2 * 32;
+          uint32_t gr[32], ur[32];
+          tmem_load_32(t_base + col, gr);
+          tmem_load_32(t_base + 128 + col, ur);
+          tmem_load_wait();
+          uint32_t words[4];
+#pragma unroll
+          for (int blk = 0; blk < 2; ++blk) {
+            float xs[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float h = silu_clamped_product(__uint_as_float(gr[blk * 16 + i]) * alpha,
+                                                   __uint_as_float(ur[blk * 16 + i]) * alpha, p.gate_limit,
+                                                   p.up_limit);
+              xs[i] = __fmul_rn(__uint_as_float(f32_to_bf16_rn(h) << 16), qgs);
+            }
+            uint32_t lo, hi;
+            const uint32_t s = quant_block16(xs, lo, hi);
+            words[blk * 2] = lo;
+            words[blk * 2 + 1] = hi;
+            scales |= s << (8 * (c2 * 2 + blk));
+          }
+          const int64_t ocol = (int64_t)nt * 128 + col;  // first output feature of this chunk
+          *reinterpret_cast<uint4*>(p.q_out + row * (p.I / 2) + ocol / 2) =
+              make_uint4(words[0], words[1], words[2], words[3]);
+        }
+        *reinterpret_cast<uint32_t*>(p.q_sf + sf_offset(row, ((int64_t)nt * 128 + h2 * 64) / 16, q_cols)) = scales;
+      }
+    } else {  // kEpiCombine
+      const int tok = p.sorted_ids[row];
+      const float wgt = tok >= 0 ? p.row_w[row] * alpha : 0.f;
+      float* dst = p.acc + (int64_t)(tok >= 0 ? tok : 0) * p.H + (int64_t)nt * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_load_32(t_base + c * 32, r);
+        tmem_load_wait();
+        if (tok >= 0) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + 4 * j),
+                      make_float4(__uint_as_float(r[4 * j]) * wgt, __uint_as_float(r[4 * j + 1]) * wgt,
+                                  __uint_as_float(r[4 * j + 2]) * wgt, __uint_as_float(r[4 * j + 3]) * wgt));
+        }
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(L.acc_empty));
+    acc_phase ^= 1u;
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid_constant__ GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  const SmemLayout L = carve(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&L.full[s]), 1);
+      mbar_init(smem_u32(&L.empty[s]), 1);
+    }
+    mbar_init(smem_u32(L.acc_full), 1);
+    mbar_init(smem_u32(L.acc_empty), 4);
+    mbar_init(smem_u32(L.drain), 1);
+    *L.abort_flag = 0;
+    fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i <= p.G; i += blockDim.x) L.offsets[i] = p.padded_offsets[i];
+  if (warp == 1) {
+    tmem_alloc(smem_u32(L.tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&p.tmap_a);
+    prefetch_tmap(&p.tmap_b);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *L.tmem_slot;
+  const int total = (L.offsets[p.G] / BM) * p.n_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) producer_loop(p, L, total);
+  } else if (warp == 1) {
+    if (lane == 0) mma_loop(p, L, total, tmem);
+  } else {
+    epilogue_loop<EPI>(p, L, total, tmem);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+template <int EPI>
+cudaError_t launch_one(const GemmArgs& a, int grid, cudaStream_t s) {
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const size_t smem = gemm_smem_bytes(MAX_GROUPS);
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(nvfp4_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  nvfp4_gemm_kernel<EPI><<<grid, NUM_THREADS, gemm_smem_bytes(a.G), s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes(int G) {
+  return 1024 + (size_t)STAGES * STAGE_BYTES + 8 * (2 * STAGES + 3) + 16 + 4 * (size_t)(G + 1) + 16;
+}
+
+cudaError_t launch_gemm(int kind, const GemmArgs& args, int grid, cudaStream_t s) {
+  if (args.G < 1 || args.G > MAX_GROUPS) return cudaErrorInvalidValue;
+  switch (kind) {
+    case kEpiBf16: return launch_one<kEpiBf16>(args, grid, s);
+    case kEpiSwigluQuant: return launch_one<kEpiSwigluQuant>(args, grid, s);
+    case kEpiCombine: return launch_one<kEpiCombine>(args, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t gemm_status_ptr(int** ptr) { return cudaGetSymbolAddress(reinterpret_cast<void**>(ptr), g_device_status); }
+
+cudaError_t gemm_read_status(int* out, int reset) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(out, g_device_status, sizeof(int));
+  if (e != cudaSuccess) return e;
+  if (reset) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
+  }
+  return e;
+}
+
+}  // namespace nvfp4

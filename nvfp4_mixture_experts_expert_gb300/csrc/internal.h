@@ -1,0 +1,86 @@
+// Internal launch interface between the C ABI (abi.cu) and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace nvfp4 {
+
+// ---------------------------------------------------------------- quant.cu
+// Per-group amax of bf16 rows into partial maxima, then gs = 2688/amax.
+constexpr int kAmaxBlocksPerGroup = 128;
+cudaError_t launch_group_amax(const uint16_t* x, int64_t rows, int64_t K, int64_t ld_x, int64_t gstride_x,
+                              int groups, float* partial, float* gs_out, cudaStream_t s);
+cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, int64_t ld_x, int64_t gstride_x,
+                            int groups, const float* gs, float* gs_copy, uint8_t* fp4, uint8_t* sf,
+                            int64_t rows_padded, int num_sms, cudaStream_t s);
+cudaError_t launch_assemble_scales(const uint8_t* sf_linear, int64_t sf_cols, const int32_t* offsets,
+                                   const int32_t* padded_offsets, int groups, int64_t rows_capacity,
+                                   uint8_t* sf_swz, int num_sms, cudaStream_t s);
+// MoE: gather hidden rows into expert slots and quantize them (one slot row per thread group).
+cudaError_t launch_gather_quantize(const uint16_t* hidden, int64_t H, const int32_t* sorted_ids,
+                                   const int32_t* tile_expert, const int32_t* meta, const float* a1_gs,
+                                   int64_t capacity, uint8_t* a1, uint8_t* sfa1, int num_sms, cudaStream_t s);
+
+// ---------------------------------------------------------------- route.cu
+constexpr int kRouteTokensPerBlock = 64;
+cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
+                              int32_t* block_counts, float* acc, int64_t H, cudaStream_t s);
+cudaError_t launch_slot_scan(int32_t* block_counts, int nblocks, int E, int32_t* counts, int32_t* offsets,
+                             int32_t* meta, int32_t* tile_expert, int32_t* sorted_ids, float* row_w,
+                             cudaStream_t s);
+cudaError_t launch_slot_scatter(const int32_t* ids, const float* w, int64_t T, int E, int k,
+                                const int32_t* block_base, const int32_t* offsets, int32_t* sorted_ids,
+                                float* row_w, int32_t* inverse, cudaStream_t s);
+cudaError_t launch_finalize(const float* acc, int64_t n, uint16_t* out, int num_sms, cudaStream_t s);
+
+// ---------------------------------------------------------------- gemm.cu
+enum EpilogueKind { kEpiBf16 = 0, kEpiSwigluQuant = 1, kEpiCombine = 2 };
+
+struct GemmArgs {
+  CUtensorMap tmap_a;  // A: [rows][K/2] bytes, box 128 B x 128 rows, 128-byte swizzle
+  CUtensorMap tmap_b;  // B: [G * b_rows_per_group][K/2] bytes, same box
+  const uint8_t* sfa;  // tile-layout scales of A (rows x K/16)
+  const uint8_t* sfb;  // tile-layout scales of B, sfb_group_bytes per group
+  const int32_t* padded_offsets;  // [G+1]
+  const int32_t* counts;          // [G] or null (plain epilogue)
+  const float* a_gs;              // [G]
+  const float* b_gs;              // [G]
+  int G;
+  int K;
+  int num_kb;            // ceil(K / 256)
+  int b_rows_per_group;  // N (plain / combine) or 2I (SwiGLU)
+  int n_tiles;           // output tiles per 128-row m-tile
+  int b_second_offset;   // rows from the first to the second 128-row B box
+  int b_tile_stride;     // B rows between consecutive n-tiles
+  int64_t sfb_group_bytes;
+  // kEpiBf16
+  uint16_t* D;
+  int64_t ldd;
+  int64_t gstride_d;
+  // kEpiSwigluQuant
+  uint8_t* q_out;
+  uint8_t* q_sf;
+  const float* q_gs;
+  int I;
+  float gate_limit;
+  float up_limit;
+  // kEpiCombine
+  float* acc;
+  const int32_t* sorted_ids;
+  const float* row_w;
+  int H;
+  // bounded waits
+  int* status;
+  unsigned long long timeout_ns;
+  int debug_no_loads;  // test hook: the producer issues nothing, so consumers time out
+};
+
+size_t gemm_smem_bytes(int G);
+cudaError_t launch_gemm(int kind, const GemmArgs& args, int grid, cudaStream_t s);
+cudaError_t gemm_status_ptr(int** ptr);
+cudaError_t gemm_read_status(int* out, int reset);
+
+}  // namespace nvfp4

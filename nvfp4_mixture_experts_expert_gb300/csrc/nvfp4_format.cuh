@@ -1,0 +1,91 @@
+// NVFP4 encoding on the device: 16-element blocks along K, E2M1 nibbles
+// (low nibble = even K index), one FP8-E4M3 block scale per block, under an
+// FP32 global scale gs that is multiplied into x.
+//
+// Rules (nvfp4-megamoe-kernel commit pages, cutedsl/bridge.py page,
+// "Bug #3 fix" and "Bug #4 fix" paragraphs):
+//   x' = x * gs (FP32), b = max |x'| over the block,
+//   b < 6 * 2^-9  -> scale 0 and all 16 nibbles 0 (zero and underflow blocks),
+//   else scale = E4M3(b / 6) (IEEE division, round to nearest even, saturating),
+//        q = x' / dec(scale) (IEEE division), nibble = E2M1(q) (nearest, ties to even,
+//        saturating at 6); a magnitude that rounds to 0 carries no sign.
+// Scales are stored in the 128-row x 4-column tile layout read by the
+// block-scaled MMA: see sf_offset().
+#pragma once
+#include <cstdint>
+
+namespace nvfp4 {
+
+constexpr float kUnderflowAmax = 0.01171875f;  // 6 * 2^-9, exact in FP32
+constexpr float kGsNumerator = 2688.0f;        // 448 * 6
+
+// Byte offset of scale (row r, scale column c) in a buffer with `cols4`
+// scale columns (a multiple of 4): 512-byte tiles of 128 rows x 4 columns,
+// tiles ordered along the columns first; inside a tile the 16-byte line
+// r%32 holds rows r%32, +32, +64, +96 (4 bytes each, one per column).
+__host__ __device__ __forceinline__ int64_t sf_offset(int64_t r, int64_t c, int64_t cols4) {
+  return (((r >> 7) * (cols4 >> 2) + (c >> 2)) << 9) + ((r & 31) << 4) + (((r & 127) >> 5) << 2) + (c & 3);
+}
+
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  const uint32_t e = (code >> 3) & 0xFu, m = code & 7u;
+  return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;
+}
+
+// Round-to-nearest-even, saturating FP32 -> E4M3 (PTX cvt, both halves from one value).
+__device__ __forceinline__ uint32_t e4m3_code(float v) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(d) : "f"(v));
+  return d & 0xFFu;
+}
+
+// E2M1 code of one value (PTX cvt; both nibbles of the result hold the same code).
+__device__ __forceinline__ uint32_t e2m1_code(float v) {
+  uint16_t d;
+  asm("{\n.reg .b8 t;\ncvt.rn.satfinite.e2m1x2.f32 t, %1, %1;\ncvt.u16.u8 %0, t;\n}" : "=h"(d) : "f"(v));
+  return d & 0xFu;
+}
+
+// Clear the sign bit of every nibble whose magnitude bits are zero (-0 -> 0).
+__device__ __forceinline__ uint32_t drop_negative_zero(uint32_t w) {
+  const uint32_t mag = w & 0x77777777u;
+  const uint32_t nonzero = (mag + 0x77777777u) & 0x88888888u;
+  return mag | (w & nonzero);
+}
+
+// Quantize one block of 16 already globally-scaled values.  Returns the
+// scale code; writes 8 packed bytes (element 2j in the low nibble of byte j).
+__device__ __forceinline__ uint32_t quant_block16(const float (&xs)[16], uint32_t& lo, uint32_t& hi) {
+  float b = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) b = fmaxf(b, fabsf(xs[i]));
+  if (!(b >= kUnderflowAmax)) {
+    lo = hi = 0u;
+    return 0u;
+  }
+  const uint32_t s = e4m3_code(__fdiv_rn(b, 6.0f));
+  const float d = e4m3_value(s);
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i >> 3] |= e2m1_code(__fdiv_rn(xs[i], d)) << ((i & 7) * 4);
+  lo = drop_negative_zero(w[0]);
+  hi = drop_negative_zero(w[1]);
+  return s;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// FP32 -> bf16 bits, round to nearest even (finite inputs).
+__device__ __forceinline__ uint32_t f32_to_bf16_rn(float f) {
+  uint16_t h;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(f));
+  return h;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+}  // namespace nvfp4

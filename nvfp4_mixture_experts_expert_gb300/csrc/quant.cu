@@ -1,0 +1,238 @@
+// NVFP4 quantization kernels: per-group amax -> global scale, strided
+// quantization with scales written straight into the 128x4 tile layout,
+// scale assembly into 128-row padded slots, and the MoE gather+quantize.
+//
+// All kernels are HBM-bound streaming kernels: one thread owns 64
+// consecutive K elements of one row (4 blocks of 16 = one MMA K-step), so a
+// warp reads 4 KB of contiguous bf16 with 16-byte loads, writes 1 KB of
+// contiguous nibbles, and each thread writes its 4 scale codes as one
+// aligned 32-bit word of the tile layout.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "nvfp4_format.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+__device__ __forceinline__ uint4 ldg_nc(const uint16_t* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// Quantize 64 bf16 values (8 x uint4 of raw bits) with global scale gs.
+// Writes 32 packed bytes and returns 4 scale codes (column c in byte c).
+__device__ __forceinline__ uint32_t quant_chunk64(const uint4 (&raw)[8], float gs, uint4& o0, uint4& o1) {
+  uint32_t sc = 0, w[8];
+#pragma unroll
+  for (int blk = 0; blk < 4; ++blk) {
+    float xs[16];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint4 v = raw[blk * 2 + j];
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        xs[j * 8 + q * 2 + 0] = __fmul_rn(bf16_lo(u[q]), gs);
+        xs[j * 8 + q * 2 + 1] = __fmul_rn(bf16_hi(u[q]), gs);
+      }
+    }
+    uint32_t lo, hi;
+    const uint32_t s = quant_block16(xs, lo, hi);
+    w[blk * 2] = lo;
+    w[blk * 2 + 1] = hi;
+    sc |= s << (8 * blk);
+  }
+  o0 = make_uint4(w[0], w[1], w[2], w[3]);
+  o1 = make_uint4(w[4], w[5], w[6], w[7]);
+  return sc;
+}
+
+// ---------------------------------------------------------------- amax
+__global__ void group_amax_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ld_x,
+                                  int64_t gstride_x, float* __restrict__ partial) {
+  const int g = blockIdx.y;
+  const int nb = gridDim.x;
+  const int64_t vec_per_row = K / 8;
+  const int64_t total = rows * vec_per_row;
+  const int64_t per_block = (total + nb - 1) / nb;
+  const int64_t begin = per_block * blockIdx.x;
+  const int64_t end = min(total, begin + per_block);
+  const uint16_t* xg = x + (int64_t)g * gstride_x;
+  uint32_t m = 0;  // max of |bf16| bit patterns (monotone for non-negative floats)
+  for (int64_t i = begin + threadIdx.x; i < end; i += blockDim.x) {
+    const int64_t r = i / vec_per_row, c = i - r * vec_per_row;
+    const uint4 v = ldg_nc(xg + r * ld_x + c * 8);
+    const uint32_t u[4] = {v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu, v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) m = max(m, max(u[q] & 0xFFFFu, u[q] >> 16));
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ uint32_t red[32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0u;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (threadIdx.x == 0) partial[(int64_t)g * nb + blockIdx.x] = __uint_as_float(m << 16);
+  }
+}
+
+// gs = 2688 / amax (IEEE division), 1 when the group is all zero.
+__global__ void group_gs_kernel(const float* __restrict__ partial, int nb, int groups, float* __restrict__ gs) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= groups) return;
+  float a = 0.f;
+  for (int i = 0; i < nb; ++i) a = fmaxf(a, partial[(int64_t)g * nb + i]);
+  gs[g] = a > 0.f ? __fdiv_rn(kGsNumerator, a) : 1.0f;
+}
+
+// ---------------------------------------------------------------- quantize
+__global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
+                                                       int64_t ld_x, int64_t gstride_x, int groups,
+                                                       const float* __restrict__ gs, float* __restrict__ gs_copy,
+                                                       uint8_t* __restrict__ fp4, uint8_t* __restrict__ sf,
+                                                       int64_t rows_padded) {
+  const int64_t chunks = K / 64;
+  const int64_t per_group = rows_padded * chunks;
+  const int64_t total = per_group * groups;
+  if (gs_copy && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < groups; i += blockDim.x) gs_copy[i] = gs[i];
+  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += (int64_t)gridDim.x * blockDim.x) {
+    const int g = (int)(it / per_group);
+    const int64_t rem = it - (int64_t)g * per_group;
+    const int64_t r = rem / chunks, c = rem - r * chunks;
+    const int64_t orow = (int64_t)g * rows_padded + r;
+    uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
+    uint32_t sc = 0;
+    if (r < rows) {
+      const uint16_t* src = x + (int64_t)g * gstride_x + r * ld_x + c * 64;
+      uint4 raw[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) raw[j] = ldg_nc(src + j * 8);
+      sc = quant_chunk64(raw, gs[g], o0, o1);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(fp4 + orow * (K / 2) + c * 32);
+    dst[0] = o0;
+    dst[1] = o1;
+    *reinterpret_cast<uint32_t*>(sf + sf_offset(orow, c * 4, K / 16)) = sc;
+  }
+}
+
+// ---------------------------------------------------------------- scale assembly
+__global__ void assemble_scales_kernel(const uint8_t* __restrict__ lin, int64_t sf_cols,
+                                       const int32_t* __restrict__ offsets,
+                                       const int32_t* __restrict__ padded_offsets, int groups,
+                                       int64_t rows_capacity, uint8_t* __restrict__ out) {
+  extern __shared__ int32_t s_off[];  // [groups+1] padded, then [groups+1] real
+  for (int i = threadIdx.x; i <= groups; i += blockDim.x) {
+    s_off[i] = padded_offsets[i];
+    s_off[groups + 1 + i] = offsets[i];
+  }
+  __syncthreads();
+  const int64_t cols4 = (sf_cols + 3) / 4 * 4;
+  const int64_t words = rows_capacity * (cols4 / 4);
+  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < words;
+       it += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = it / (cols4 / 4), c4 = (it - r * (cols4 / 4)) * 4;
+    uint32_t v = 0;
+    if (r < s_off[groups]) {
+      int lo = 0, hi = groups;  // largest g with padded_offsets[g] <= r
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_off[mid] <= r) lo = mid; else hi = mid;
+      }
+      const int64_t local = r - s_off[lo];
+      const int64_t n = (int64_t)s_off[groups + 1 + lo + 1] - s_off[groups + 1 + lo];
+      if (local < n) {
+        const uint8_t* src = lin + ((int64_t)s_off[groups + 1 + lo] + local) * sf_cols;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (c4 + j < sf_cols) v |= (uint32_t)src[c4 + j] << (8 * j);
+      }
+    }
+    *reinterpret_cast<uint32_t*>(out + sf_offset(r, c4, cols4)) = v;
+  }
+}
+
+// ---------------------------------------------------------------- MoE gather + quantize
+__global__ void __launch_bounds__(256) gather_quantize_kernel(const uint16_t* __restrict__ hidden, int64_t H,
+                                                              const int32_t* __restrict__ sorted_ids,
+                                                              const int32_t* __restrict__ tile_expert,
+                                                              const int32_t* __restrict__ meta,
+                                                              const float* __restrict__ a1_gs, int64_t capacity,
+                                                              uint8_t* __restrict__ a1, uint8_t* __restrict__ sfa1) {
+  const int64_t chunks = H / 64;
+  const int64_t P = meta[0];
+  const int64_t total = min(P, capacity) * chunks;
+  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+       it += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = it / chunks, c = it - r * chunks;
+    const int t = sorted_ids[r];
+    uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
+    uint32_t sc = 0;
+    if (t >= 0) {
+      const float gs = a1_gs[tile_expert[r >> 7]];
+      const uint16_t* src = hidden + (int64_t)t * H + c * 64;
+      uint4 raw[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) raw[j] = ldg_nc(src + j * 8);
+      sc = quant_chunk64(raw, gs, o0, o1);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(a1 + r * (H / 2) + c * 32);
+    dst[0] = o0;
+    dst[1] = o1;
+    *reinterpret_cast<uint32_t*>(sfa1 + sf_offset(r, c * 4, H / 16)) = sc;
+  }
+}
+
+int grid_for(int64_t items, int threads, int num_sms, int per_sm) {
+  const int64_t need = (items + threads - 1) / threads;
+  const int64_t cap = (int64_t)num_sms * per_sm;
+  return (int)(need < 1 ? 1 : (need < cap ? need : cap));
+}
+
+}  // namespace
+
+cudaError_t launch_group_amax(const uint16_t* x, int64_t rows, int64_t K, int64_t ld_x, int64_t gstride_x,
+                              int groups, float* partial, float* gs_out, cudaStream_t s) {
+  dim3 grid(kAmaxBlocksPerGroup, groups);
+  group_amax_kernel<<<grid, 256, 0, s>>>(x, rows, K, ld_x, gstride_x, partial);
+  group_gs_kernel<<<(groups + 127) / 128, 128, 0, s>>>(partial, kAmaxBlocksPerGroup, groups, gs_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, int64_t ld_x, int64_t gstride_x,
+                            int groups, const float* gs, float* gs_copy, uint8_t* fp4, uint8_t* sf,
+                            int64_t rows_padded, int num_sms, cudaStream_t s) {
+  const int64_t items = rows_padded * (K / 64) * groups;
+  const int grid = grid_for(items, 256, num_sms, 8);
+  quantize_kernel<<<grid, 256, 0, s>>>(x, rows, K, ld_x, gstride_x, groups, gs, gs_copy, fp4, sf, rows_padded);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_assemble_scales(const uint8_t* sf_linear, int64_t sf_cols, const int32_t* offsets,
+                                   const int32_t* padded_offsets, int groups, int64_t rows_capacity,
+                                   uint8_t* sf_swz, int num_sms, cudaStream_t s) {
+  const int64_t words = rows_capacity * ((sf_cols + 3) / 4);
+  const int grid = grid_for(words, 256, num_sms, 8);
+  const size_t smem = sizeof(int32_t) * 2 * (groups + 1);
+  assemble_scales_kernel<<<grid, 256, smem, s>>>(sf_linear, sf_cols, offsets, padded_offsets, groups,
+                                                 rows_capacity, sf_swz);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_quantize(const uint16_t* hidden, int64_t H, const int32_t* sorted_ids,
+                                   const int32_t* tile_expert, const int32_t* meta, const float* a1_gs,
+                                   int64_t capacity, uint8_t* a1, uint8_t* sfa1, int num_sms, cudaStream_t s) {
+  const int64_t items = capacity * (H / 64);
+  const int grid = grid_for(items, 256, num_sms, 8);
+  gather_quantize_kernel<<<grid, 256, 0, s>>>(hidden, H, sorted_ids, tile_expert, meta, a1_gs, capacity, a1,
+                                              sfa1);
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

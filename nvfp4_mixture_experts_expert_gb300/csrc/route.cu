@@ -1,0 +1,230 @@
+// Routing and slot construction for the MoE forward, all on the device with
+// no host synchronisation (vllm page, cudagraph paragraph: GPU-only expert
+// offsets, no .item(), padding slots with zero weight).
+//
+//  route_topk     one warp per token: top-k of the FP32 logits (ties -> lower
+//                 expert), weights = exp(l_j - l_max) / sum over the chosen
+//                 (softmax renormalised over the top-k); per-block expert
+//                 histogram in shared memory; zeroes the token's combine rows.
+//  slot_scan      one block: per-expert exclusive scan of the block histograms,
+//                 padded offsets (multiples of 128, multi-chunk experts --
+//                 vllm page "Bug 9"), the m-tile -> expert table, pad rows.
+//  slot_scatter   per block, the stable rank of each assignment inside its
+//                 expert (ascending flat index t*k+j) via warp match/ballot,
+//                 giving the slot row; writes sorted_token_ids, row weights and
+//                 the inverse map.  Deterministic: no atomics decide a row.
+//  finalize       FP32 combine accumulator -> bf16 output.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "nvfp4_format.cuh"
+
+namespace nvfp4 {
+
+namespace {
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 8;
+constexpr int kRouteWarps = 8;
+
+__global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
+    const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ ids, float* __restrict__ w,
+    int32_t* __restrict__ block_counts, float* __restrict__ acc, int64_t H) {
+  __shared__ int32_t hist[kMaxExperts];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int64_t t0 = (int64_t)blockIdx.x * kRouteTokensPerBlock;
+  const int64_t t1 = min(T, t0 + kRouteTokensPerBlock);
+  for (int64_t t = t0 + warp; t < t1; t += kRouteWarps) {
+    float v[kMaxExperts / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int e = i * 32 + lane;
+      v[i] = e < E ? logits[t * E + e] : -INFINITY;
+    }
+    uint32_t taken = 0;  // bit i: expert i*32+lane already chosen
+    float sel_l[kMaxTopK];
+    int sel_e[kMaxTopK];
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int be = 0x7FFFFFFF;
+#pragma unroll
+      for (int i = 0; i < kMaxExperts / 32; ++i) {
+        const int e = i * 32 + lane;
+        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || be == 0x7FFFFFFF)) {
+          bv = v[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (ov > bv || (ov == bv && oe < be) || be == 0x7FFFFFFF) {
+          if (oe != 0x7FFFFFFF) {
+            bv = ov;
+            be = oe;
+          }
+        }
+      }
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      sel_l[j] = bv;
+      sel_e[j] = be;
+    }
+    if (lane == 0) {
+      float z[kMaxTopK], sum = 0.f;
+      for (int j = 0; j < k; ++j) {
+        z[j] = expf(sel_l[j] - sel_l[0]);
+        sum += z[j];
+      }
+      for (int j = 0; j < k; ++j) {
+        ids[t * k + j] = sel_e[j];
+        w[t * k + j] = z[j] / sum;
+        atomicAdd(&hist[sel_e[j]], 1);
+      }
+    }
+    // zero this token's combine accumulator row (H floats)
+    float4* row = reinterpret_cast<float4*>(acc + t * H);
+    for (int64_t i = lane; i < H / 4; i += 32) row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) block_counts[(int64_t)blockIdx.x * E + e] = hist[e];
+}
+
+__global__ void __launch_bounds__(1024) slot_scan_kernel(int32_t* __restrict__ block_counts, int nblocks, int E,
+                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ meta,
+                                                         int32_t* __restrict__ tile_expert,
+                                                         int32_t* __restrict__ sorted_ids,
+                                                         float* __restrict__ row_w) {
+  __shared__ int32_t s_cnt[kMaxExperts];
+  __shared__ int32_t s_off[kMaxExperts + 1];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int b = 0; b < nblocks; ++b) {  // exclusive scan over blocks, in place
+      const int c = block_counts[(int64_t)b * E + e];
+      block_counts[(int64_t)b * E + e] = run;
+      run += c;
+    }
+    s_cnt[e] = run;
+    counts[e] = run;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int off = 0;
+    for (int e = 0; e < E; ++e) {
+      s_off[e] = off;
+      off += (s_cnt[e] + 127) / 128 * 128;
+    }
+    s_off[E] = off;
+    meta[0] = off;
+    meta[1] = off / 128;
+    meta[2] = 0;
+    meta[3] = 0;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = s_off[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    for (int mt = s_off[e] / 128; mt < s_off[e + 1] / 128; ++mt) tile_expert[mt] = e;
+  // pad rows of every slot: token -1, weight 0
+  for (int i = threadIdx.x; i < E * 128; i += blockDim.x) {
+    const int e = i >> 7, j = i & 127;
+    const int r = s_off[e] + s_cnt[e] + j;
+    if (r < s_off[e + 1]) {
+      sorted_ids[r] = -1;
+      row_w[r] = 0.f;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) slot_scatter_kernel(const int32_t* __restrict__ ids,
+                                                           const float* __restrict__ w, int64_t T, int E, int k,
+                                                           const int32_t* __restrict__ block_base,
+                                                           const int32_t* __restrict__ offsets,
+                                                           int32_t* __restrict__ sorted_ids,
+                                                           float* __restrict__ row_w, int32_t* __restrict__ inverse) {
+  __shared__ int32_t running[kMaxExperts];
+  __shared__ int32_t warp_cnt[8][kMaxExperts];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    running[e] = block_base[(int64_t)blockIdx.x * E + e] + offsets[e];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) warp_cnt[q][e] = 0;
+  }
+  __syncthreads();
+  const int64_t f0 = (int64_t)blockIdx.x * kRouteTokensPerBlock * k;
+  const int64_t f1 = min(T, (int64_t)(blockIdx.x + 1) * kRouteTokensPerBlock) * k;
+  for (int64_t base = f0; base < f1; base += blockDim.x) {
+    const int64_t f = base + threadIdx.x;
+    const bool valid = f < f1;
+    const int e = valid ? ids[f] : -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (valid && rank == 0) warp_cnt[warp][e] = __popc(peers);
+    __syncthreads();
+    if (valid) {
+      int pre = running[e] + rank;
+      for (int q = 0; q < warp; ++q) pre += warp_cnt[q][e];
+      sorted_ids[pre] = (int32_t)(f / k);
+      row_w[pre] = w[f];
+      inverse[f] = pre;
+    }
+    __syncthreads();
+    for (int x = threadIdx.x; x < E; x += blockDim.x) {
+      int add = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        add += warp_cnt[q][x];
+        warp_cnt[q][x] = 0;
+      }
+      running[x] += add;
+    }
+    __syncthreads();
+  }
+}
+
+__global__ void finalize_kernel(const float4* __restrict__ acc, int64_t n4, uint2* __restrict__ out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+    const float4 v = acc[i];
+    out[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
+                              int32_t* block_counts, float* acc, int64_t H, cudaStream_t s) {
+  const int64_t nb = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
+  route_topk_kernel<<<(unsigned)nb, kRouteWarps * 32, 0, s>>>(logits, T, E, k, ids, w, block_counts, acc, H);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_slot_scan(int32_t* block_counts, int nblocks, int E, int32_t* counts, int32_t* offsets,
+                             int32_t* meta, int32_t* tile_expert, int32_t* sorted_ids, float* row_w,
+                             cudaStream_t s) {
+  slot_scan_kernel<<<1, 1024, 0, s>>>(block_counts, nblocks, E, counts, offsets, meta, tile_expert, sorted_ids,
+                                      row_w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_slot_scatter(const int32_t* ids, const float* w, int64_t T, int E, int k,
+                                const int32_t* block_base, const int32_t* offsets, int32_t* sorted_ids,
+                                float* row_w, int32_t* inverse, cudaStream_t s) {
+  const int64_t nb = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
+  slot_scatter_kernel<<<(unsigned)nb, 256, 0, s>>>(ids, w, T, E, k, block_base, offsets, sorted_ids, row_w,
+                                                   inverse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const float* acc, int64_t n, uint16_t* out, int num_sms, cudaStream_t s) {
+  const int64_t n4 = n / 4;
+  int64_t grid = (n4 + 255) / 256;
+  if (grid > (int64_t)num_sms * 8) grid = (int64_t)num_sms * 8;
+  if (grid < 1) grid = 1;
+  finalize_kernel<<<(unsigned)grid, 256, 0, s>>>(reinterpret_cast<const float4*>(acc), n4,
+                                                 reinterpret_cast<uint2*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace nvfp4

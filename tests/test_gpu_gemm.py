@@ -1,0 +1,113 @@
+"""GPU parity of the tcgen05 block-scaled grouped GEMM against the oracle's FP64
+GEMM on identical quantized operands (both quantized by the oracle).
+
+Tolerance: the kernel accumulates in FP32 and stores bf16, so both sides are
+compared after rounding to bf16: relative Frobenius error <= 1e-3 (the bound
+for the GEMM); elementwise the kernel may differ from the FP64 result by at
+most one bf16 rounding plus FP32 accumulation error."""
+import numpy as np
+import pytest
+
+from oracle import nvfp4_oracle as O
+from nvfp4_mixture_experts_expert_gb300 import workloads as W
+from helpers import bf16_host, dev, rel_frob
+
+pytestmark = pytest.mark.gpu
+
+
+def make_problem(counts, N, K, seed, b_gs=None):
+    rng = np.random.default_rng(seed)
+    G = len(counts)
+    padded = np.concatenate([[0], np.cumsum([(c + 127) // 128 * 128 for c in counts])]).astype(np.int32)
+    cap = int(padded[-1]) + 128  # a spare tile of capacity beyond the last group
+    A = np.zeros((cap, K // 2), np.uint8)
+    s_lin = np.zeros((cap, K // 16), np.uint8)
+    a_gs = np.ones(G, np.float32)
+    a_deq = []
+    for g, c in enumerate(counts):
+        x = W.bf16_bits_to_f32(W.f32_to_bf16_bits(
+            rng.standard_normal((c, K)).astype(np.float32) * np.exp(rng.standard_normal((c, 1))).astype(np.float32)))
+        a_gs[g] = O.global_scale(np.abs(x).max()) if c else np.float32(1)
+        nib, s = O.quantize_blocks(x, a_gs[g])
+        A[padded[g]:padded[g] + c] = O.pack_nibbles(nib)
+        s_lin[padded[g]:padded[g] + c] = s
+        a_deq.append((nib, s))
+    SFA = O.assemble_scales(s_lin, np.array([0, cap]), np.array([0, cap]))
+    w = W.bf16_bits_to_f32(W.f32_to_bf16_bits(rng.standard_normal((G, N, K)).astype(np.float32) * np.float32(0.02)))
+    bn, bs, bg = O.quantize_expert_weights(w, gs=b_gs)
+    Bp = np.stack([O.pack_nibbles(bn[g]) for g in range(G)])
+    SFB = np.stack([O.assemble_scales(bs[g], np.array([0, N]), np.array([0, N])) for g in range(G)])
+    ref = [O.nvfp4_gemm(a_deq[g][0], a_deq[g][1], a_gs[g], bn[g], bs[g], bg[g]) for g in range(G)]
+    return dict(A=A, SFA=SFA, a_gs=a_gs, B=Bp, SFB=SFB, b_gs=bg, padded=padded, counts=np.int32(counts),
+                cap=cap, ref=ref, G=G, N=N, K=K)
+
+
+def run_gpu(pb, use_counts=True):
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import binding as B
+    G, N, K = pb["G"], pb["N"], pb["K"]
+    maxrows = int(np.diff(pb["padded"]).max())
+    D = torch.full((G, max(maxrows, 1), N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    B.nvfp4_grouped_gemm(dev(pb["A"]), dev(pb["SFA"]), dev(pb["a_gs"]), dev(pb["B"]), dev(pb["SFB"]),
+                         dev(pb["b_gs"]), dev(pb["padded"]), dev(pb["counts"]) if use_counts else None, G,
+                         pb["cap"], N, K, D, N, max(maxrows, 1) * N)
+    torch.cuda.synchronize()
+    return bf16_host(D)
+
+
+def check(pb, D):
+    for g, c in enumerate(pb["counts"]):
+        if c == 0:
+            continue
+        ref = pb["ref"][g]
+        got = D[g, :c]
+        assert np.all(np.isfinite(got))
+        ref_b = O.bf16_round(ref.astype(np.float32))
+        assert rel_frob(got, ref_b) <= 1e-3, (g, rel_frob(got, ref_b))
+        # elementwise: within one bf16 rounding of the FP64 result (+ accumulation slack)
+        tol = np.abs(ref) * 2.0 ** -8 + 1e-5 * np.abs(ref).max()
+        assert np.all(np.abs(got - ref) <= tol), (g, np.max(np.abs(got - ref) - tol))
+
+
+@pytest.mark.parametrize("counts,N,K", [
+    ([128], 256, 256),               # one tile, one K stage
+    ([100, 0, 260], 512, 320),       # ragged groups, an empty group, partial last K stage
+    ([37, 129], 256, 128),           # K = 128: a single half stage
+    ([300], 768, 1024),              # several tiles and K stages
+])
+def test_grouped_gemm_matches_oracle(counts, N, K):
+    pb = make_problem(counts, N, K, seed=sum(counts) + N + K)
+    check(pb, run_gpu(pb))
+
+
+def test_gemm_rows_beyond_counts_are_not_written():
+    pb = make_problem([10, 50], 256, 256, seed=1)
+    D = run_gpu(pb)
+    assert np.all(np.isnan(D[0, 10:128])) and np.all(np.isnan(D[1, 50:128]))
+
+
+def test_gemm_identity_weight_returns_dequantized_activation():
+    """Closed form: B = identity (exactly representable) -> D = dequant(A)."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import binding as B
+    K = N = 256
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((128, K)).astype(np.float32)
+    gs_a = O.global_scale(np.abs(x).max())
+    nib, s = O.quantize_blocks(x, gs_a)
+    eye_n, eye_s, eye_gs = O.weight_quantize(np.eye(K, dtype=np.float32))
+    D = torch.empty((128, N), dtype=torch.bfloat16, device="cuda")
+    B.nvfp4_grouped_gemm(dev(O.pack_nibbles(nib)), dev(O.assemble_scales(s, np.array([0, 128]), np.array([0, 128]))),
+                         dev(np.float32([gs_a])), dev(O.pack_nibbles(eye_n)),
+                         dev(O.assemble_scales(eye_s, np.array([0, K]), np.array([0, K]))),
+                         dev(np.float32([eye_gs])), dev(np.int32([0, 128])), None, 1, 128, N, K, D, N, 0)
+    torch.cuda.synchronize()
+    expect = O.bf16_round((O.dequant_blocks(nib, s) / np.float64(gs_a)).astype(np.float32))
+    np.testing.assert_allclose(bf16_host(D), expect, rtol=2.0 ** -7, atol=0)  # at most one bf16 ulp
+
+
+def test_gemm_device_status_is_clean():
+    from nvfp4_mixture_experts_expert_gb300 import binding as B
+    pb = make_problem([64], 256, 256, seed=2)
+    run_gpu(pb)
+    assert B.nvfp4_device_status(reset=False) == 0

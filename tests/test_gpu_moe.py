@@ -1,0 +1,120 @@
+"""GPU parity of the full NVFP4 MoE forward against the oracle.
+
+Bit-exact: routing ids, slot counts / offsets / sorted token ids / inverse
+map, quantized expert weights and the gathered L1 activations (nibbles and
+tile-layout scales).  Routing weights: 1e-6 relative.  L1 output
+requantization: FP32 (kernel) vs FP64 (oracle) accumulation may flip a
+rounding boundary, so the L2 input is compared on its dequantized values.
+End-to-end output: relative Frobenius <= 2e-2 and cosine >= 0.999."""
+import numpy as np
+import pytest
+
+from oracle import nvfp4_oracle as O
+from nvfp4_mixture_experts_expert_gb300 import workloads as W
+from helpers import OracleMoE, bf16_dev, bf16_host, cosine, dev, host, rel_frob
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(wl, orc):
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    fwd = api.MoEForward(wl.T, wl.H, wl.I, wl.E, wl.top_k)
+    out = fwd(bf16_dev(wl.hidden), dev(wl.logits), w, dev(orc.a1_gs), dev(orc.a2_gs), wl.gate_limit, wl.up_limit)
+    torch.cuda.synchronize()
+    return w, fwd, out
+
+
+def check_all(wl, orc, w, fwd, out, check_a2=True):
+    import torch
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.top_k
+    # quantized weights (GPU quantizer) == oracle quantizer
+    np.testing.assert_array_equal(host(w.w13_gs), orc.w13q[2])
+    np.testing.assert_array_equal(host(w.w2_gs), orc.w2q[2])
+    for e in range(E):
+        np.testing.assert_array_equal(host(w.w13[e]), O.pack_nibbles(orc.w13q[0][e]))
+        np.testing.assert_array_equal(host(w.w2[e]), O.pack_nibbles(orc.w2q[0][e]))
+        np.testing.assert_array_equal(
+            host(w.w13_sf[e]), O.assemble_scales(orc.w13q[1][e], np.array([0, 2 * I]), np.array([0, 2 * I])))
+    # routing and slots
+    A = T * k
+    np.testing.assert_array_equal(host(fwd.view("topk_ids", torch.int32, A)).reshape(T, k), orc.ids)
+    wts = host(fwd.view("topk_w", torch.float32, A)).reshape(T, k)
+    np.testing.assert_allclose(wts, orc.w, rtol=1e-6, atol=1e-7)
+    m = orc.meta
+    P = m["P"]
+    np.testing.assert_array_equal(host(fwd.view("counts", torch.int32, E)), m["counts"])
+    np.testing.assert_array_equal(host(fwd.view("offsets", torch.int32, E + 1)), m["offsets"])
+    assert host(fwd.view("meta", torch.int32, 2)).tolist() == [P, P // 128]
+    np.testing.assert_array_equal(host(fwd.view("sorted_token_ids", torch.int32, P)), m["sorted_token_ids"])
+    np.testing.assert_array_equal(host(fwd.view("inverse", torch.int32, A)), m["inverse"])
+    np.testing.assert_allclose(host(fwd.view("row_weight", torch.float32, P)), m["row_weight"], rtol=1e-6, atol=1e-7)
+    # gathered + quantized L1 activations
+    a1_ref, sfa1_ref = orc.slot_activations()
+    np.testing.assert_array_equal(host(fwd.view("a1", torch.uint8, P * H // 2)).reshape(P, H // 2), a1_ref)
+    np.testing.assert_array_equal(host(fwd.view("sfa1", torch.uint8, P * H // 16)), sfa1_ref)
+    # end to end
+    ref, inter = orc.forward()
+    got = bf16_host(out)
+    assert np.all(np.isfinite(got))
+    rf, cs = rel_frob(got, ref), cosine(got, ref)
+    assert rf <= 2e-2 and cs >= 0.999, (rf, cs)
+    if check_a2:
+        # L2 input: compare dequantized requantized activations on real rows
+        a2 = host(fwd.view("a2", torch.uint8, P * I // 2)).reshape(P, I // 2)
+        sfa2 = host(fwd.view("sfa2", torch.uint8, P * I // 16))
+        s_lin = O.unswizzle_scales(sfa2, P, I // 16)
+        deq = O.dequant_blocks(O.unpack_nibbles(a2), s_lin)
+        for e, d in inter["experts"].items():
+            lo, n = int(m["offsets"][e]), int(m["counts"][e])
+            nib, s = O.quantize_blocks(d["h"], orc.a2_gs[e])
+            ref_deq = O.dequant_blocks(nib, s)
+            assert rel_frob(deq[lo:lo + n], ref_deq) <= 2e-2
+            assert np.mean(O.unpack_nibbles(a2[lo:lo + n]) != nib) <= 0.02
+        # pad rows of the L2 input stay zero
+        for e in range(E):
+            lo, n, hi = int(m["offsets"][e]), int(m["counts"][e]), int(m["offsets"][e + 1])
+            assert not a2[lo + n:hi].any()
+    return rf, cs
+
+
+def test_tiny_moe_matches_oracle():
+    wl = W.tiny_moe()
+    orc = OracleMoE(wl)
+    check_all(wl, orc, *run_gpu(wl, orc))
+
+
+@pytest.mark.parametrize("case", ["empty_expert", "heavy_expert", "top1", "single_expert", "ragged_T", "K128"])
+def test_moe_edge_cases(case):
+    kw = dict(T=96, H=256, I=128, E=6, top_k=2, seed=21)
+    extra = {}
+    if case == "empty_expert":
+        extra["dead_experts"] = (1, 4)
+    elif case == "heavy_expert":
+        kw.update(T=300)
+        extra["logit_bias_std"] = 3.0  # one or two experts take well over 128 rows
+    elif case == "top1":
+        kw.update(top_k=1)
+    elif case == "single_expert":
+        kw.update(E=1, top_k=1)
+    elif case == "ragged_T":
+        kw.update(T=133, H=512, I=256, E=5, top_k=3)
+    elif case == "K128":
+        kw.update(H=256, I=128, E=3)
+    wl = W.moe_workload(kw["T"], kw["H"], kw["I"], kw["E"], kw["top_k"], kw["seed"], **extra)
+    orc = OracleMoE(wl)
+    if case == "heavy_expert":
+        assert orc.meta["counts"].max() > 128
+    if case == "empty_expert":
+        assert orc.meta["counts"][1] == 0 and orc.meta["counts"][4] == 0
+    check_all(wl, orc, *run_gpu(wl, orc))
+
+
+def test_moe_zero_tokens_is_a_no_op():
+    from nvfp4_mixture_experts_expert_gb300 import binding as B
+    import torch
+    assert B.nvfp4_moe_workspace_size(0, 256, 128, 4, 2) > 0
+    B.nvfp4_moe_forward(None, None, 0, 256, 128, 4, 2, None, None, None, None, None, None, None, None, 10.0, 10.0,
+                        None, 0, None)
+    torch.cuda.synchronize()

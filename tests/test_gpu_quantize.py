@@ -1,0 +1,103 @@
+"""GPU parity of NVFP4 quantization and scale assembly: nibbles, FP8 scales in
+the tile layout and global scales must equal the oracle's bit for bit."""
+import numpy as np
+import pytest
+
+from oracle import nvfp4_oracle as O
+from nvfp4_mixture_experts_expert_gb300 import workloads as W
+from helpers import bf16_dev, dev, host, oracle_packed_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def api():
+    from nvfp4_mixture_experts_expert_gb300 import api as A
+    return A
+
+
+def special_rows(R, K, seed):
+    """Rows N(0,1) with a per-row lognormal gain, 5% zero blocks, 5% blocks below the
+    underflow threshold after scaling, 2% channels x20."""
+    wl = W.moe_workload(R, K, 128, 2, 1, seed, zero_block_frac=0.05, tiny_block_frac=0.05,
+                        outlier_frac=0.02)
+    x = W.bf16_bits_to_f32(wl.hidden) * np.exp(np.random.default_rng(seed).standard_normal((R, 1))).astype(np.float32)
+    return W.f32_to_bf16_bits(x)
+
+
+@pytest.mark.parametrize("R,K", [(1, 64), (130, 256), (300, 512), (257, 3584)])
+def test_quantize_with_computed_global_scale(R, K):
+    bits = special_rows(R, K, R + K)
+    x = W.bf16_bits_to_f32(bits)
+    gs = O.global_scale(np.abs(x).max())
+    Rp = (R + 127) // 128 * 128
+    packed, swz, _, _ = oracle_packed_rows(x, gs, Rp)
+    fp4, sf, gs_dev = api().quantize(bf16_dev(bits))
+    assert host(gs_dev)[0] == gs
+    np.testing.assert_array_equal(host(fp4), packed)
+    np.testing.assert_array_equal(host(sf), swz)
+
+
+@pytest.mark.parametrize("gs", [1.0, 1234.5, 3e-3])
+def test_quantize_with_given_global_scale(gs):
+    R, K = 200, 320
+    bits = special_rows(R, K, 7)
+    x = W.bf16_bits_to_f32(bits)
+    packed, swz, _, _ = oracle_packed_rows(x, np.float32(gs), 256)
+    fp4, sf, gs_out = api().quantize(bf16_dev(bits), gs=dev(np.float32([gs])))
+    np.testing.assert_array_equal(host(fp4), packed)
+    np.testing.assert_array_equal(host(sf), swz)
+    assert host(gs_out)[0] == np.float32(gs)
+
+
+def test_quantize_all_zero_tensor_gives_unit_scale():
+    bits = np.zeros((128, 64), np.uint16)
+    fp4, sf, gs = api().quantize(bf16_dev(bits))
+    assert host(gs)[0] == 1.0
+    assert not host(fp4).any() and not host(sf).any()
+
+
+def test_quantize_strided_groups_like_grouped_linear():
+    """(T, G, D) input read as G groups of T rows (group stride D, row stride G*D)."""
+    wl = W.grouped_linear(seed=3, T=200, G=3, D=256, R=256)
+    x = W.bf16_bits_to_f32(wl.x)
+    Rp = 256
+    fp4, sf, gs = api().quantize_groups(bf16_dev(wl.x), wl.T, wl.D, wl.G * wl.D, wl.D, wl.G, rows_padded=Rp)
+    fp4, sf, gs = host(fp4), host(sf), host(gs)
+    for g in range(wl.G):
+        xg = x[:, g, :]
+        gsg = O.global_scale(np.abs(xg).max())
+        assert gs[g] == gsg
+        packed, swz, _, _ = oracle_packed_rows(xg, gsg, Rp)
+        np.testing.assert_array_equal(fp4[g * Rp:(g + 1) * Rp], packed)
+        n = Rp * wl.D // 16
+        np.testing.assert_array_equal(sf[g * n:(g + 1) * n], swz)
+
+
+def test_expert_weight_quantization():
+    rng = np.random.default_rng(5)
+    w = W.f32_to_bf16_bits(rng.standard_normal((3, 256, 192)).astype(np.float32) * np.float32(0.02))
+    fp4, sf, gs = api().quantize_expert_weights(bf16_dev(w))
+    nibs, scs, gss = O.quantize_expert_weights(W.bf16_bits_to_f32(w))
+    np.testing.assert_array_equal(host(gs), gss)
+    for e in range(3):
+        np.testing.assert_array_equal(host(fp4)[e], O.pack_nibbles(nibs[e]))
+        np.testing.assert_array_equal(host(sf)[e], O.assemble_scales(scs[e], np.array([0, 256]), np.array([0, 256])))
+
+
+def test_assemble_scales_matches_oracle():
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import binding as B
+    rng = np.random.default_rng(9)
+    counts = [5, 0, 130, 128, 1]
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    padded = np.concatenate([[0], np.cumsum([(c + 127) // 128 * 128 for c in counts])]).astype(np.int32)
+    cap = int(padded[-1]) + 128
+    for C in (6, 8, 256):
+        lin = rng.integers(1, 0x7E, (offsets[-1], C), dtype=np.uint8)
+        ref = O.assemble_scales(lin, offsets, padded)
+        C4 = (C + 3) // 4 * 4
+        out = torch.full((cap * C4,), 0xAB, dtype=torch.uint8, device="cuda")
+        B.nvfp4_assemble_scales(dev(lin), C, dev(offsets), dev(padded), len(counts), cap, out)
+        got = host(out)
+        np.testing.assert_array_equal(got[:ref.size], ref)
+        assert not got[ref.size:].any()  # capacity rows beyond the last slot are zero
