@@ -1,0 +1,457 @@
+#!/usr/bin/env python
+"""Benchmark of the NVFP4 mixture-of-experts FFN forward on GB300.
+
+One step = one full forward of the MoE layer (routing, slot sort, gather +
+NVFP4 quantization, L1 grouped GEMM with fused SwiGLU + requantization, L2
+grouped GEMM with fused weighted combine, bf16 finalize) over one batch of
+the prefill workload: T=8192 tokens, H=4096, I=2048, E=48 local experts,
+top_k=6, Zipf(1.1) expert popularity, 2% outlier channels x20 (synthetic,
+seeded).  Weights are random N(0, 0.02), quantized to NVFP4 by the library;
+activation global scales are calibrated on the device before timing.
+
+Prints ONE JSON line (rank 0).  `value` is whole-job tokens/s with inputs
+resident in HBM; `e2e` times the same call with pinned host inputs copied in
+and the output copied back inside the timed region.  `roofline` is the L1
+grouped GEMM (the dominant kernel) against the dense FP4 tensor peak.
+`--impl reference` times the CPU oracle on a bounded sample of the same
+workload (there is no other implementation of this method to run).
+
+Multi-GPU (torchrun): every rank runs its own batch of T tokens with the full
+local expert set (data parallel over tokens, no collective on the data path);
+scaling is weak and the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "moe_layer_tokens_per_s"
+UNIT = "tokens/s"
+SHAPES = {
+    "prefill": dict(T=8192, H=4096, I=2048, E=48, top_k=6),
+    "decode": dict(T=128, H=4096, I=2048, E=32, top_k=6),
+}
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 / BF16 tensor throughput ratio
+GATE_LIMIT = UP_LIMIT = 10.0
+
+
+def workload_name(shape_key):
+    s = SHAPES[shape_key]
+    extra = "Zipf(1.1) expert prior, 2% outlier channels x20" if shape_key == "prefill" else \
+        "per-expert logit bias N(0,0.5)"
+    return (f"{shape_key} NVFP4 MoE layer forward T={s['T']} H={s['H']} I={s['I']} E={s['E']} "
+            f"top_k={s['top_k']}, {extra}")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(SHAPES), default="prefill")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-extras", action="store_true", help="skip the decode-size side measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def stored_traffic(kernel):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, or None when
+    the kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    ent = d.get(kernel)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "nvfp4_mixture_experts_expert_gb300", "csrc", "gemm.cu")
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest()[:16] != ent.get("gemm_cu_sha256_16"):
+            return None
+    return ent.get("bytes_per_launch")
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 8:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- distributed
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- our implementation
+
+def build_layer(shape_key, seed, rank):
+    import numpy as np
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    from nvfp4_mixture_experts_expert_gb300 import workloads as W
+    s = SHAPES[shape_key]
+    T, H, I, E, k = s["T"], s["H"], s["I"], s["E"], s["top_k"]
+    wl = (W.prefill_moe if shape_key == "prefill" else W.decode_moe)(seed=seed + rank, with_weights=False)
+    hidden = torch.from_numpy(wl.hidden.view(np.int16)).view(torch.bfloat16).cuda()
+    logits = torch.from_numpy(wl.logits).cuda()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1000 + seed)
+    w13 = (torch.randn((E, 2 * I, H), generator=g, device="cuda", dtype=torch.float32) * 0.02).to(torch.bfloat16)
+    w2 = (torch.randn((E, H, I), generator=g, device="cuda", dtype=torch.float32) * 0.02).to(torch.bfloat16)
+    weights = api.quantize_moe_weights(w13, w2)
+    del w13, w2
+    fwd = api.MoEForward(T, H, I, E, k)
+    a1, a2 = fwd.calibrate(hidden, logits, weights, GATE_LIMIT, UP_LIMIT)
+    torch.cuda.synchronize()
+    return dict(T=T, H=H, I=I, E=E, k=k, hidden=hidden, logits=logits, w=weights, fwd=fwd, a1=a1, a2=a2,
+                wl=wl)
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import binding as B
+    L = build_layer(args.workload, args.seed, rank)
+    T, H, I, E, k = L["T"], L["H"], L["I"], L["E"], L["k"]
+    fwd, w = L["fwd"], L["w"]
+    out = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fwd(L["hidden"], L["logits"], w, L["a1"], L["a2"], GATE_LIMIT, UP_LIMIT, out=out)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+
+    # ---- device-resident timed region, per-stage events on the launching stream
+    stage_events = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        B.nvfp4_moe_set_stage_events(stage_events[i])
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    B.nvfp4_moe_set_stage_events(None)
+    clk = clocks.stop()
+    barrier(world)
+    ms = t_start.elapsed_time(t_end) / args.steps
+    ms = max_over_ranks(ms, world)
+    names = ["route", "slot_scan", "slot_scatter", "gather_quantize", "l1_gemm_swiglu_quant", "l2_gemm_combine",
+             "finalize"]
+    stages = {n: statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in stage_events) for i, n in enumerate(names)}
+
+    # ---- end to end through the C ABI with pinned host buffers
+    h_hidden = torch.empty((T, H), dtype=torch.bfloat16, pin_memory=True)
+    h_hidden.copy_(L["hidden"].cpu())
+    h_logits = torch.empty((T, E), dtype=torch.float32, pin_memory=True)
+    h_logits.copy_(L["logits"].cpu())
+    h_out = torch.empty((T, H), dtype=torch.bfloat16, pin_memory=True)
+    d_hidden = torch.empty_like(L["hidden"])
+    d_logits = torch.empty_like(L["logits"])
+
+    def e2e_step():
+        d_hidden.copy_(h_hidden, non_blocking=True)
+        d_logits.copy_(h_logits, non_blocking=True)
+        fwd(d_hidden, d_logits, w, L["a1"], L["a2"], GATE_LIMIT, UP_LIMIT, out=out)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+
+    status = B.nvfp4_device_status()
+    P = int(fwd.view("meta", torch.int32, 1).cpu()[0])
+
+    # ---- roofline of the dominant kernel (L1 grouped GEMM)
+    peaks = measured_peaks()
+    fp4_peak = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
+    A = T * k
+    l1_flops = 2.0 * A * H * (2 * I)
+    l2_flops = 2.0 * A * I * H
+    l1_tflops = l1_flops / (stages["l1_gemm_swiglu_quant"] * 1e-3) / 1e12
+    l2_tflops = l2_flops / (stages["l2_gemm_combine"] * 1e-3) / 1e12
+    traffic = stored_traffic("l1_gemm_swiglu_quant_" + args.workload)
+    roofline = {"kernel": "l1_gemm_swiglu_quant", "bound": "tensor", "achieved": round(l1_tflops, 1),
+                "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(l1_tflops / fp4_peak, 4),
+                "traffic": traffic,
+                "peak_source": f"{peaks['source']} bf16 sustained {peaks['bf16_tflops_sustained']} TFLOP/s x "
+                               f"{FP4_OVER_BF16:g} (nominal dense FP4/BF16 ratio)",
+                "flops_per_launch": l1_flops, "flops_rule": "2*T*top_k*H*2I (real rows only)"}
+    res = {
+        "metric": METRIC, "value": round(T * world / (ms * 1e-3), 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4 (e2m1 x e2m1 block-scaled, fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": workload_name(args.workload), "tokens_per_gpu": T, "hidden": H,
+                   "intermediate": I, "experts": E, "top_k": k, "padded_rows": P,
+                   "parallelism": f"dp{world} over tokens (replicated local experts)",
+                   "l2_flush": "not needed: weights (0.76 GB NVFP4) and activations exceed the 129 MB L2"},
+        "roofline": roofline,
+        "stages_ms": {n: round(v, 4) for n, v in stages.items()},
+        "l2_gemm": {"achieved": round(l2_tflops, 1), "unit": "TFLOP/s", "frac": round(l2_tflops / fp4_peak, 4)},
+        "e2e": {"value": round(T * world / (e2e_ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": T * H * 2 + T * E * 4, "d2h_bytes_per_step": T * H * 2},
+        "clocks": clk,
+        "gpu_launches": 7 * args.steps,
+        "device_status": status,
+    }
+    return res, L
+
+
+def decode_side_measurement(seed):
+    """Decode-size forward (T=128, E=32): HBM-bound weight streaming."""
+    import torch
+    L = build_layer("decode", seed, 0)
+    fwd, w = L["fwd"], L["w"]
+    out = torch.empty((L["T"], L["H"]), dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+
+    def step():
+        fwd(L["hidden"], L["logits"], w, L["a1"], L["a2"], GATE_LIMIT, UP_LIMIT, out=out)
+
+    for _ in range(5):
+        step()
+    times = []
+    for _ in range(20):
+        flush.fill_(1)  # evict the weights from L2 between iterations
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    counts = fwd.view("counts", torch.int32, L["E"]).cpu()
+    active = [e for e in range(L["E"]) if int(counts[e]) > 0]
+    H, I = L["H"], L["I"]
+    wbytes = len(active) * (2 * I * H // 2 + 2 * I * H // 16 + H * I // 2 + H * I // 16)
+    peaks = measured_peaks()
+    gbs = wbytes / (ms * 1e-3) / 1e9
+    return {"workload": workload_name("decode"), "ms_per_step": round(ms, 4),
+            "tokens_per_s": round(L["T"] / (ms * 1e-3), 1), "active_experts": len(active),
+            "weight_bytes": wbytes, "weight_stream_gbs": round(gbs, 1),
+            "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "l2": "flushed (512 MB write) before each step"}
+
+
+# --------------------------------------------------------------------------- CPU oracle (baseline / reference arm)
+
+_WEIGHT_CACHE = {}
+
+
+def oracle_sample_seconds(shape_key, seed, target_rows):
+    """Time the CPU oracle on a bounded sample of the workload: routing and slot
+    sort of all T tokens, plus the full per-expert pipeline (quantize, L1,
+    SwiGLU, requantize, L2, weighted combine) for the rows of the first experts
+    until `target_rows` assignment rows are covered.  Returns (seconds for the
+    whole batch, extrapolated by assignment rows; sample description)."""
+    import numpy as np
+    from oracle import nvfp4_oracle as O
+    from nvfp4_mixture_experts_expert_gb300 import workloads as W
+    s = SHAPES[shape_key]
+    T, H, I, E, k = s["T"], s["H"], s["I"], s["E"], s["top_k"]
+    wl = (W.prefill_moe if shape_key == "prefill" else W.decode_moe)(seed=seed, with_weights=False)
+    hidden = W.bf16_bits_to_f32(wl.hidden)
+    t0 = time.perf_counter()
+    ids, wts = O.route(wl.logits, k)
+    meta = O.sort_slots(ids, wts, E)
+    t_route = time.perf_counter() - t0
+    order = np.argsort(-meta["counts"], kind="stable")
+    chosen, rows = [], 0
+    for e in order:  # largest experts first: fewest weight sets to prepare
+        if rows >= target_rows:
+            break
+        chosen.append(int(e))
+        rows += int(meta["counts"][e])
+    rng = np.random.default_rng(seed + 7)
+    acc = np.zeros((T, H))
+    t_exp = 0.0
+    done = 0
+    for e in chosen:
+        key = (shape_key, seed, e)
+        if key not in _WEIGHT_CACHE:  # weight quantization is offline prepacking: not timed
+            w13 = W.bf16_bits_to_f32(W.f32_to_bf16_bits(rng.standard_normal((2 * I, H), dtype=np.float32) * 0.02))
+            w2 = W.bf16_bits_to_f32(W.f32_to_bf16_bits(rng.standard_normal((H, I), dtype=np.float32) * 0.02))
+            _WEIGHT_CACHE[key] = (O.quantize_expert_weights(w13[None]), O.quantize_expert_weights(w2[None]))
+        q13, q2 = _WEIGHT_CACHE[key]
+        lo, n = int(meta["offsets"][e]), min(int(meta["counts"][e]), target_rows - done)
+        toks = meta["sorted_token_ids"][lo:lo + n]
+        t1 = time.perf_counter()
+        x = hidden[toks]
+        a1 = O.global_scale(np.abs(x).max())
+        h = O.expert_l1(x, a1, q13[0][0], q13[1][0], q13[2][0], GATE_LIMIT, UP_LIMIT)
+        a2 = O.global_scale(np.abs(h).max())
+        Y = O.expert_l2(h, a2, q2[0][0], q2[1][0], q2[2][0])
+        np.add.at(acc, toks, meta["row_weight"][lo:lo + n, None] * Y)
+        t_exp += time.perf_counter() - t1
+        done += n
+    A = T * k
+    total = t_route + t_exp * (A / done)
+    desc = (f"routing+slot sort of all {T} tokens ({t_route:.2f} s) + full per-expert pipeline on {done} of {A} "
+            f"assignment rows ({len(chosen)} experts, {t_exp:.2f} s), scaled to the whole batch by rows")
+    return total, desc, t_route + t_exp
+
+
+def cpu_cores():
+    n = os.environ.get("OMP_NUM_THREADS") or os.environ.get("OPENBLAS_NUM_THREADS")
+    return int(n) if n else (os.cpu_count() or 1)
+
+
+def cpu_baseline(shape_key, seed):
+    total, desc, spent = oracle_sample_seconds(shape_key, seed, target_rows=12288)
+    T = SHAPES[shape_key]["T"]
+    return {"value": round(T / total, 2), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": desc, "cpu_seconds_spent": round(spent, 2)}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    vals, descs = [], []
+    for i in range(args.warmup + args.steps):
+        total, desc, _ = oracle_sample_seconds(args.workload, args.seed, target_rows=256)
+        if i >= args.warmup:
+            vals.append(SHAPES[args.workload]["T"] / total)
+            descs.append(desc)
+    value = statistics.mean(vals)
+    T = SHAPES[args.workload]["T"]
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(T / value * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle; fp32 quantizer)",
+            "data": "synthetic", "config": {"workload": workload_name(args.workload)},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": descs[-1]},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        res = run_reference(args)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    world, rank, local = dist_setup()
+    res, _ = run_ours(args, world, rank, local)
+    if rank == 0:
+        if not args.no_extras and world == 1:
+            res["extra"] = {"decode": decode_side_measurement(args.seed)}
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(args.workload, args.seed)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

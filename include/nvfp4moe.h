@@ -156,6 +156,23 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
                       void* stream);
 
 /*
+ * nvfp4_moe_calibrate -- per-expert activation global scales from sample data
+ * (vllm page: compute_activation_global_scales -- L1 scale from the gathered
+ * hidden rows, L2 scale from the actual L1 output, local expert ids, run
+ * before graph capture so the forward can use fixed scales).
+ *   a1_gs_out[e] = 2688 / amax(hidden rows routed to e)
+ *   a2_gs_out[e] = 2688 / amax(bf16 SwiGLU output of those rows, with the L1
+ *                  input quantized by a1_gs_out[e])
+ * and 1 for an expert with no rows (or an all-zero amax).  Same arguments,
+ * workspace and requirements as nvfp4_moe_forward (W2 is not needed).
+ *   a1_gs_out, a2_gs_out   device f32[E]
+ */
+int nvfp4_moe_calibrate(const void* hidden, const float* router_logits, int64_t T, int64_t H, int64_t I, int E,
+                        int top_k, const void* w13, const void* w13_sf, const float* w13_gs, float gate_limit,
+                        float up_limit, void* workspace, size_t workspace_bytes, float* a1_gs_out, float* a2_gs_out,
+                        void* stream);
+
+/*
  * Byte offsets of the forward's intermediates inside the workspace, for
  * inspection by tests.  Sizes: cap = padded-row capacity
  * (roundup(T*top_k + 127*min(E, T*top_k), 128)); A = T*top_k assignments.
@@ -165,12 +182,12 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
  *   tile_expert i32[cap/128], sorted_token_ids i32[cap] (-1 pad),
  *   row_weight f32[cap] (0 pad), inverse i32[A] (assignment -> row)
  *   a1 u8[cap][H/2], sfa1 u8[cap*H/16], a2 u8[cap][I/2], sfa2 u8[cap*I/16]
- *   acc f32[T][H] (combine accumulator)
+ *   acc f32[T][H] (combine accumulator), calib u32[2E] (calibration amax bits)
  * Only rows < P of the row-indexed buffers are defined after a call.
  */
 typedef struct {
   size_t topk_ids, topk_w, block_counts, counts, offsets, meta, tile_expert, sorted_token_ids, row_weight,
-      inverse, a1, sfa1, a2, sfa2, acc, total;
+      inverse, a1, sfa1, a2, sfa2, acc, calib, total;
   int64_t capacity;
   int64_t route_blocks;
 } nvfp4_moe_layout;

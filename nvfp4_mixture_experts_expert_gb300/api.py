@@ -117,6 +117,14 @@ class MoEForward:
                             self.workspace, self.ws_bytes, out, stream)
         return out
 
+    def calibrate(self, hidden, logits, w: MoEWeights, gate_limit=10.0, up_limit=10.0, stream=None):
+        """Per-expert activation global scales (a1_gs, a2_gs) from this batch."""
+        a1 = torch.empty(self.E, dtype=torch.float32, device=hidden.device)
+        a2 = torch.empty(self.E, dtype=torch.float32, device=hidden.device)
+        B.nvfp4_moe_calibrate(hidden, logits, self.T, self.H, self.I, self.E, self.top_k, w.w13, w.w13_sf,
+                              w.w13_gs, gate_limit, up_limit, self.workspace, self.ws_bytes, a1, a2, stream)
+        return a1, a2
+
     def view(self, name, dtype, count):
         """A view of one intermediate of the last call (see nvfp4_moe_workspace_layout)."""
         off = self.layout[name]

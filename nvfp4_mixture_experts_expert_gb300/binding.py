@@ -47,7 +47,7 @@ class Nvfp4Error(RuntimeError):
 class MoeLayout(ctypes.Structure):
     _fields_ = [(n, c_size) for n in (
         "topk_ids", "topk_w", "block_counts", "counts", "offsets", "meta", "tile_expert",
-        "sorted_token_ids", "row_weight", "inverse", "a1", "sfa1", "a2", "sfa2", "acc", "total")] + [
+        "sorted_token_ids", "row_weight", "inverse", "a1", "sfa1", "a2", "sfa2", "acc", "calib", "total")] + [
         ("capacity", c_i64), ("route_blocks", c_i64)]
 
 
@@ -73,6 +73,9 @@ _moe_layout = _sig("nvfp4_moe_workspace_layout", c_int, [c_i64, c_i64, c_i64, c_
 _moe_forward = _sig("nvfp4_moe_forward", c_int, [c_ptr, c_ptr, c_i64, c_i64, c_i64, c_int, c_int, c_ptr, c_ptr,
                                                  c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_float, c_float, c_ptr,
                                                  c_size, c_ptr, c_ptr])
+_moe_calibrate = _sig("nvfp4_moe_calibrate", c_int, [c_ptr, c_ptr, c_i64, c_i64, c_i64, c_int, c_int, c_ptr,
+                                                     c_ptr, c_ptr, c_float, c_float, c_ptr, c_size, c_ptr, c_ptr,
+                                                     c_ptr])
 _device_status = _sig("nvfp4_device_status", c_int, [ctypes.POINTER(c_int), c_int])
 _stage_events = _sig("nvfp4_moe_set_stage_events", c_int, [ctypes.POINTER(c_ptr), c_int])
 
@@ -157,6 +160,13 @@ def nvfp4_moe_forward(hidden, router_logits, T, H, I, E, top_k, w13, w13_sf, w13
     _check(_moe_forward(_p(hidden), _p(router_logits), T, H, I, E, top_k, _p(w13), _p(w13_sf), _p(w13_gs),
                         _p(w2), _p(w2_sf), _p(w2_gs), _p(a1_gs), _p(a2_gs), gate_limit, up_limit,
                         _p(workspace), workspace_bytes, _p(out), _stream(stream)))
+
+
+def nvfp4_moe_calibrate(hidden, router_logits, T, H, I, E, top_k, w13, w13_sf, w13_gs, gate_limit, up_limit,
+                        workspace, workspace_bytes, a1_gs_out, a2_gs_out, stream=None):
+    _check(_moe_calibrate(_p(hidden), _p(router_logits), T, H, I, E, top_k, _p(w13), _p(w13_sf), _p(w13_gs),
+                          gate_limit, up_limit, _p(workspace), workspace_bytes, _p(a1_gs_out), _p(a2_gs_out),
+                          _stream(stream)))
 
 
 def nvfp4_device_status(reset=False):

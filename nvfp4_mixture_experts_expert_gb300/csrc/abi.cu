@@ -272,6 +272,7 @@ int nvfp4_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int E, int top_k
   out->a2 = take(cap * I / 2);
   out->sfa2 = take(cap * I / 16);
   out->acc = take(T * H * 4);
+  out->calib = take((int64_t)2 * E * 4);
   out->total = off;
   out->capacity = cap;
   out->route_blocks = nb;
@@ -387,7 +388,8 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
   if ((e = launch_route_topk(router_logits, T, E, top_k, ids, wts, bcnt, acc, H, s)) != cudaSuccess)
     return cuda_fail(e, "route launch");
   stage_mark(1, s);
-  if ((e = launch_slot_scan(bcnt, nb, E, counts, offsets, meta, tile_expert, sorted_ids, row_w, s)) != cudaSuccess)
+  if ((e = launch_slot_scan(bcnt, nb, E, counts, offsets, meta, tile_expert, sorted_ids, row_w, nullptr, 0, s)) !=
+      cudaSuccess)
     return cuda_fail(e, "slot scan launch");
   stage_mark(2, s);
   if ((e = launch_slot_scatter(ids, wts, T, E, top_k, bcnt, offsets, sorted_ids, row_w, inverse, s)) !=
@@ -408,6 +410,100 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
   if ((e = launch_finalize(acc, T * H, (uint16_t*)out, dev->sms, s)) != cudaSuccess)
     return cuda_fail(e, "finalize launch");
   stage_mark(7, s);
+  return NVFP4_OK;
+}
+
+int nvfp4_moe_calibrate(const void* hidden, const float* router_logits, int64_t T, int64_t H, int64_t I, int E,
+                        int top_k, const void* w13, const void* w13_sf, const float* w13_gs, float gate_limit,
+                        float up_limit, void* workspace, size_t workspace_bytes, float* a1_gs_out, float* a2_gs_out,
+                        void* stream) {
+  g_err[0] = 0;
+  if (T < 0) return fail(NVFP4_ERR_INVALID_ARG, "T must be >= 0");
+  if (H <= 0 || H % 256) return fail(NVFP4_ERR_UNSUPPORTED, "H must be a positive multiple of 256");
+  if (I <= 0 || I % 128) return fail(NVFP4_ERR_UNSUPPORTED, "I must be a positive multiple of 128");
+  if (E < 1 || E > 256) return fail(NVFP4_ERR_UNSUPPORTED, "E must be in [1, 256]");
+  if (top_k < 1 || top_k > 8 || top_k > E) return fail(NVFP4_ERR_INVALID_ARG, "top_k must be in [1, min(8, E)]");
+  if (!(gate_limit > 0.f) || !(up_limit > 0.f)) return fail(NVFP4_ERR_INVALID_ARG, "limits must be positive");
+  nvfp4_moe_layout L;
+  if (int rc = nvfp4_moe_workspace_layout(T, H, I, E, top_k, &L)) return rc;
+  if (!a1_gs_out || !a2_gs_out) return fail(NVFP4_ERR_INVALID_ARG, "null output pointer");
+  if (T > 0 && (!hidden || !router_logits || !w13 || !w13_sf || !w13_gs))
+    return fail(NVFP4_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(hidden) || !aligned16(w13) || !aligned16(w13_sf) || !aligned16(router_logits))
+    return fail(NVFP4_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (!workspace || workspace_bytes < L.total)
+    return fail(NVFP4_ERR_WORKSPACE, "workspace of %zu bytes needed, got %zu", L.total, workspace_bytes);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(NVFP4_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if ((int64_t)E * 2 * I > INT32_MAX || L.capacity > INT32_MAX)
+    return fail(NVFP4_ERR_UNSUPPORTED, "row counts beyond 2^31");
+  DeviceInfo* dev = nullptr;
+  if (int rc = device_info(&dev)) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* ws = (uint8_t*)workspace;
+  int32_t* ids = (int32_t*)(ws + L.topk_ids);
+  float* wts = (float*)(ws + L.topk_w);
+  int32_t* bcnt = (int32_t*)(ws + L.block_counts);
+  int32_t* counts = (int32_t*)(ws + L.counts);
+  int32_t* offsets = (int32_t*)(ws + L.offsets);
+  int32_t* meta = (int32_t*)(ws + L.meta);
+  int32_t* tile_expert = (int32_t*)(ws + L.tile_expert);
+  int32_t* sorted_ids = (int32_t*)(ws + L.sorted_token_ids);
+  float* row_w = (float*)(ws + L.row_weight);
+  int32_t* inverse = (int32_t*)(ws + L.inverse);
+  uint8_t* a1 = ws + L.a1;
+  uint8_t* sfa1 = ws + L.sfa1;
+  float* acc = (float*)(ws + L.acc);
+  uint32_t* amax = (uint32_t*)(ws + L.calib);
+  const int64_t cap = L.capacity;
+  cudaError_t e;
+  if (T == 0) {  // no rows: every expert gets gs 1
+    if ((e = launch_slot_scan(bcnt, 0, E, counts, offsets, meta, tile_expert, sorted_ids, row_w, amax, 2 * E, s)) !=
+            cudaSuccess ||
+        (e = launch_gs_from_amax(amax, E, a1_gs_out, s)) != cudaSuccess ||
+        (e = launch_gs_from_amax(amax + E, E, a2_gs_out, s)) != cudaSuccess)
+      return cuda_fail(e, "calibration launch");
+    return NVFP4_OK;
+  }
+  GemmArgs g1;
+  memset(&g1, 0, sizeof(g1));
+  if (int rc = make_fp4_map(&g1.tmap_a, a1, cap, H)) return rc;
+  if (int rc = make_fp4_map(&g1.tmap_b, w13, (int64_t)E * 2 * I, H)) return rc;
+  g1.sfa = sfa1;
+  g1.sfb = (const uint8_t*)w13_sf;
+  g1.padded_offsets = offsets;
+  g1.a_gs = a1_gs_out;
+  g1.b_gs = w13_gs;
+  g1.G = E;
+  g1.K = (int)H;
+  g1.num_kb = (int)((H + 255) / 256);
+  g1.b_rows_per_group = (int)(2 * I);
+  g1.n_tiles = (int)(I / 128);
+  g1.b_second_offset = (int)I;
+  g1.b_tile_stride = 128;
+  g1.sfb_group_bytes = 2 * I * (H / 16);
+  g1.I = (int)I;
+  g1.gate_limit = gate_limit;
+  g1.up_limit = up_limit;
+  g1.amax_bits = amax + E;
+  g1.status = dev->status;
+  g1.timeout_ns = 2000000000ull;
+  const int nb = (int)L.route_blocks;
+  if ((e = launch_route_topk(router_logits, T, E, top_k, ids, wts, bcnt, acc, H, s)) != cudaSuccess ||
+      (e = launch_slot_scan(bcnt, nb, E, counts, offsets, meta, tile_expert, sorted_ids, row_w, amax, 2 * E, s)) !=
+          cudaSuccess ||
+      (e = launch_slot_scatter(ids, wts, T, E, top_k, bcnt, offsets, sorted_ids, row_w, inverse, s)) !=
+          cudaSuccess ||
+      (e = launch_gather_amax((const uint16_t*)hidden, H, sorted_ids, tile_expert, meta, cap, amax, dev->sms, s)) !=
+          cudaSuccess ||
+      (e = launch_gs_from_amax(amax, E, a1_gs_out, s)) != cudaSuccess ||
+      (e = launch_gather_quantize((const uint16_t*)hidden, H, sorted_ids, tile_expert, meta, a1_gs_out, cap, a1,
+                                  sfa1, dev->sms, s)) != cudaSuccess)
+    return cuda_fail(e, "calibration launch");
+  const int64_t t1 = cap / 128 * g1.n_tiles;
+  if ((e = launch_gemm(kEpiSwigluAmax, g1, (int)(t1 < dev->sms ? t1 : dev->sms), s)) != cudaSuccess ||
+      (e = launch_gs_from_amax(amax + E, E, a2_gs_out, s)) != cudaSuccess)
+    return cuda_fail(e, "calibration launch");
   return NVFP4_OK;
 }
 

@@ -9,6 +9,8 @@
 //                    clamped before SiLU)
 //   kEpiCombine      MoE L2: out[token] += w_row * alpha * acc (FP32 red.add),
 //                    pad rows skipped (vllm page: scatter_add with zero-weight pads)
+//   kEpiSwigluAmax   MoE calibration: per-expert amax of the bf16 SwiGLU output
+//                    (vllm page: L2 global scale from the actual L1 output)
 //
 // Design (one CTA per SM, persistent over output tiles, warp-specialised):
 //   warp 0   TMA producer: per K-stage of 256 elements, one 128x128-byte A box,
@@ -281,6 +283,25 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
         }
         *reinterpret_cast<uint32_t*>(p.q_sf + sf_offset(row, ((int64_t)nt * 128 + h2 * 64) / 16, q_cols)) = scales;
       }
+    } else if constexpr (EPI == kEpiSwigluAmax) {
+      // calibration: amax of the bf16 SwiGLU output of this row's 128 features
+      uint32_t m = 0;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t gr[32], ur[32];
+        tmem_load_32(t_base + c * 32, gr);
+        tmem_load_32(t_base + 128 + c * 32, ur);
+        tmem_load_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float h = silu_clamped_product(__uint_as_float(gr[i]) * alpha, __uint_as_float(ur[i]) * alpha,
+                                               p.gate_limit, p.up_limit);
+          m = max(m, f32_to_bf16_rn(h) & 0x7FFFu);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0 && m) atomicMax(&p.amax_bits[g], m << 16);
     } else {  // kEpiCombine
       const int tok = p.sorted_ids[row];
       const float wgt = tok >= 0 ? p.row_w[row] * alpha : 0.f;
@@ -380,6 +401,7 @@ cudaError_t launch_gemm(int kind, const GemmArgs& args, int grid, cudaStream_t s
     case kEpiBf16: return launch_one<kEpiBf16>(args, grid, s);
     case kEpiSwigluQuant: return launch_one<kEpiSwigluQuant>(args, grid, s);
     case kEpiCombine: return launch_one<kEpiCombine>(args, grid, s);
+    case kEpiSwigluAmax: return launch_one<kEpiSwigluAmax>(args, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

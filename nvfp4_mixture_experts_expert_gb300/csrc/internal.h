@@ -23,6 +23,12 @@ cudaError_t launch_assemble_scales(const uint8_t* sf_linear, int64_t sf_cols, co
 cudaError_t launch_gather_quantize(const uint16_t* hidden, int64_t H, const int32_t* sorted_ids,
                                    const int32_t* tile_expert, const int32_t* meta, const float* a1_gs,
                                    int64_t capacity, uint8_t* a1, uint8_t* sfa1, int num_sms, cudaStream_t s);
+// Calibration: per-expert amax of the gathered hidden rows (as float bits, atomicMax
+// into a zeroed array), and gs = 2688/amax (1 for an empty / all-zero expert).
+cudaError_t launch_gather_amax(const uint16_t* hidden, int64_t H, const int32_t* sorted_ids,
+                               const int32_t* tile_expert, const int32_t* meta, int64_t capacity,
+                               uint32_t* amax_bits, int num_sms, cudaStream_t s);
+cudaError_t launch_gs_from_amax(const uint32_t* amax_bits, int n, float* gs, cudaStream_t s);
 
 // ---------------------------------------------------------------- route.cu
 constexpr int kRouteTokensPerBlock = 64;
@@ -30,14 +36,14 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int3
                               int32_t* block_counts, float* acc, int64_t H, cudaStream_t s);
 cudaError_t launch_slot_scan(int32_t* block_counts, int nblocks, int E, int32_t* counts, int32_t* offsets,
                              int32_t* meta, int32_t* tile_expert, int32_t* sorted_ids, float* row_w,
-                             cudaStream_t s);
+                             uint32_t* zero_words, int n_zero_words, cudaStream_t s);
 cudaError_t launch_slot_scatter(const int32_t* ids, const float* w, int64_t T, int E, int k,
                                 const int32_t* block_base, const int32_t* offsets, int32_t* sorted_ids,
                                 float* row_w, int32_t* inverse, cudaStream_t s);
 cudaError_t launch_finalize(const float* acc, int64_t n, uint16_t* out, int num_sms, cudaStream_t s);
 
 // ---------------------------------------------------------------- gemm.cu
-enum EpilogueKind { kEpiBf16 = 0, kEpiSwigluQuant = 1, kEpiCombine = 2 };
+enum EpilogueKind { kEpiBf16 = 0, kEpiSwigluQuant = 1, kEpiCombine = 2, kEpiSwigluAmax = 3 };
 
 struct GemmArgs {
   CUtensorMap tmap_a;  // A: [rows][K/2] bytes, box 128 B x 128 rows, 128-byte swizzle
@@ -67,6 +73,8 @@ struct GemmArgs {
   int I;
   float gate_limit;
   float up_limit;
+  // kEpiSwigluAmax: per-group amax of h (float bits, atomicMax)
+  uint32_t* amax_bits;
   // kEpiCombine
   float* acc;
   const int32_t* sorted_ids;

@@ -189,6 +189,39 @@ __global__ void __launch_bounds__(256) gather_quantize_kernel(const uint16_t* __
   }
 }
 
+// One warp per slot row: max |x| of the token's hidden row, folded into its
+// expert's amax with an order-independent atomicMax on the float bits.
+__global__ void __launch_bounds__(256) gather_amax_kernel(const uint16_t* __restrict__ hidden, int64_t H,
+                                                          const int32_t* __restrict__ sorted_ids,
+                                                          const int32_t* __restrict__ tile_expert,
+                                                          const int32_t* __restrict__ meta, int64_t capacity,
+                                                          uint32_t* __restrict__ amax_bits) {
+  const int lane = threadIdx.x & 31;
+  const int64_t P = min((int64_t)meta[0], capacity);
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < P; r += warps) {
+    const int t = sorted_ids[r];
+    if (t < 0) continue;
+    uint32_t m = 0;
+    for (int64_t c = lane; c < H / 8; c += 32) {
+      const uint4 v = ldg_nc(hidden + (int64_t)t * H + c * 8);
+      const uint32_t u[4] = {v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu, v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) m = max(m, max(u[q] & 0xFFFFu, u[q] >> 16));
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0 && m) atomicMax(&amax_bits[tile_expert[r >> 7]], m << 16);
+  }
+}
+
+__global__ void gs_from_amax_kernel(const uint32_t* __restrict__ amax_bits, int n, float* __restrict__ gs) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float a = __uint_as_float(amax_bits[i]);
+  gs[i] = a > 0.f ? __fdiv_rn(kGsNumerator, a) : 1.0f;
+}
+
 int grid_for(int64_t items, int threads, int num_sms, int per_sm) {
   const int64_t need = (items + threads - 1) / threads;
   const int64_t cap = (int64_t)num_sms * per_sm;
@@ -232,6 +265,19 @@ cudaError_t launch_gather_quantize(const uint16_t* hidden, int64_t H, const int3
   const int grid = grid_for(items, 256, num_sms, 8);
   gather_quantize_kernel<<<grid, 256, 0, s>>>(hidden, H, sorted_ids, tile_expert, meta, a1_gs, capacity, a1,
                                               sfa1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_amax(const uint16_t* hidden, int64_t H, const int32_t* sorted_ids,
+                               const int32_t* tile_expert, const int32_t* meta, int64_t capacity,
+                               uint32_t* amax_bits, int num_sms, cudaStream_t s) {
+  const int grid = grid_for(capacity * 32, 256, num_sms, 8);
+  gather_amax_kernel<<<grid, 256, 0, s>>>(hidden, H, sorted_ids, tile_expert, meta, capacity, amax_bits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gs_from_amax(const uint32_t* amax_bits, int n, float* gs, cudaStream_t s) {
+  gs_from_amax_kernel<<<(n + 127) / 128, 128, 0, s>>>(amax_bits, n, gs);
   return cudaGetLastError();
 }
 

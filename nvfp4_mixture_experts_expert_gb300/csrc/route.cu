@@ -97,8 +97,10 @@ __global__ void __launch_bounds__(1024) slot_scan_kernel(int32_t* __restrict__ b
                                                          int32_t* __restrict__ meta,
                                                          int32_t* __restrict__ tile_expert,
                                                          int32_t* __restrict__ sorted_ids,
-                                                         float* __restrict__ row_w) {
+                                                         float* __restrict__ row_w,
+                                                         uint32_t* __restrict__ zero_words, int n_zero_words) {
   __shared__ int32_t s_cnt[kMaxExperts];
+  for (int i = threadIdx.x; i < n_zero_words; i += blockDim.x) zero_words[i] = 0u;
   __shared__ int32_t s_off[kMaxExperts + 1];
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = 0;
@@ -202,9 +204,9 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int3
 
 cudaError_t launch_slot_scan(int32_t* block_counts, int nblocks, int E, int32_t* counts, int32_t* offsets,
                              int32_t* meta, int32_t* tile_expert, int32_t* sorted_ids, float* row_w,
-                             cudaStream_t s) {
+                             uint32_t* zero_words, int n_zero_words, cudaStream_t s) {
   slot_scan_kernel<<<1, 1024, 0, s>>>(block_counts, nblocks, E, counts, offsets, meta, tile_expert, sorted_ids,
-                                      row_w);
+                                      row_w, zero_words, n_zero_words);
   return cudaGetLastError();
 }
 

@@ -8,8 +8,8 @@ CUDA tests / benchmark take their inputs from here, so both sides see
 identical bytes.
 
 Draw order per workload (fixed, so that a seed names one input set):
-hidden/activations, router logits, logit bias or prior, W13 (expert by
-expert), W2 (expert by expert), then the special blocks.
+hidden/activations, router logits, logit bias or prior, outlier channels,
+zero / tiny blocks, then W13 (expert by expert) and W2 (expert by expert).
 
 Workload shapes follow the five configurations the method is measured on:
   tiny      T=64   H=256  I=128  E=8  top_k=2  (zero / underflow blocks)
@@ -85,7 +85,7 @@ def _expert_weights(rng, E, rows, cols, std=0.02):
 def moe_workload(T, H, I, E, top_k, seed=0, *, name="moe", logit_bias_std=0.0,
                  zipf_s=None, outlier_frac=0.0, outlier_gain=20.0,
                  zero_block_frac=0.0, tiny_block_frac=0.0, tiny_amax_range=(1e-9, 0.0117),
-                 dead_experts=()):
+                 dead_experts=(), with_weights=True):
     """Generic seeded MoE layer input.
 
     logit_bias_std: per-expert bias N(0, std) added to N(0,1) logits.
@@ -95,6 +95,8 @@ def moe_workload(T, H, I, E, top_k, seed=0, *, name="moe", logit_bias_std=0.0,
     zero_block_frac / tiny_block_frac: fraction of 16-element hidden blocks set to
             exact zero / rescaled so their raw amax is log-uniform in tiny_amax_range.
     dead_experts: experts whose logits are set to -inf (they receive no token).
+    with_weights: False leaves w13 / w2 as None (activations and logits are
+            drawn first, so they do not depend on this flag).
     """
     rng = np.random.default_rng(seed)
     hid = rng.standard_normal((T, H), dtype=np.float32)
@@ -113,8 +115,6 @@ def moe_workload(T, H, I, E, top_k, seed=0, *, name="moe", logit_bias_std=0.0,
         prior[perm] = np.log(p)
         logits = (logits.astype(np.float64) + prior[None, :]).astype(np.float32)
         meta["zipf_prior"] = prior.astype(np.float32)
-    w13 = _expert_weights(rng, E, 2 * I, H)
-    w2 = _expert_weights(rng, E, H, I)
     if outlier_frac:
         n_out = int(round(outlier_frac * H))
         ch = np.sort(rng.choice(H, size=n_out, replace=False))
@@ -137,6 +137,8 @@ def moe_workload(T, H, I, E, top_k, seed=0, *, name="moe", logit_bias_std=0.0,
         meta["tiny_blocks"] = np.sort(pick[n_zero:])
     for e in dead_experts:
         logits[:, e] = -np.inf
+    w13 = _expert_weights(rng, E, 2 * I, H) if with_weights else None
+    w2 = _expert_weights(rng, E, H, I) if with_weights else None
     return MoEWorkload(name=name, T=T, H=H, I=I, E=E, top_k=top_k,
                        hidden=f32_to_bf16_bits(hid), logits=np.ascontiguousarray(logits, np.float32),
                        w13=w13, w2=w2, meta=meta)
@@ -148,15 +150,16 @@ def tiny_moe(seed=0):
                         zero_block_frac=0.05, tiny_block_frac=0.05)
 
 
-def decode_moe(seed=0):
+def decode_moe(seed=0, with_weights=True):
     """T=128, H=4096, I=2048, E=32, top_k=6; logits N(0,1) + per-expert bias N(0,0.5)."""
-    return moe_workload(128, 4096, 2048, 32, 6, seed, name="decode_moe", logit_bias_std=0.5)
+    return moe_workload(128, 4096, 2048, 32, 6, seed, name="decode_moe", logit_bias_std=0.5,
+                        with_weights=with_weights)
 
 
-def prefill_moe(seed=0, T=8192):
+def prefill_moe(seed=0, T=8192, with_weights=True):
     """T=8192, H=4096, I=2048, E=48, top_k=6; Zipf(1.1) prior, 2% outlier channels x20."""
     return moe_workload(T, 4096, 2048, 48, 6, seed, name="prefill_moe", zipf_s=1.1,
-                        outlier_frac=0.02, outlier_gain=20.0)
+                        outlier_frac=0.02, outlier_gain=20.0, with_weights=with_weights)
 
 
 @dataclass

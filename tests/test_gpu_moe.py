@@ -118,3 +118,19 @@ def test_moe_zero_tokens_is_a_no_op():
     B.nvfp4_moe_forward(None, None, 0, 256, 128, 4, 2, None, None, None, None, None, None, None, None, 10.0, 10.0,
                         None, 0, None)
     torch.cuda.synchronize()
+
+
+def test_device_calibration_matches_oracle_scales():
+    """nvfp4_moe_calibrate: L1 scales bit-exact (same amax, same FP32 division);
+    L2 scales from the kernel's own FP32 L1 output within 1% of the oracle's."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    wl = W.moe_workload(150, 256, 128, 6, 2, 33, dead_experts=(3,), outlier_frac=0.02)
+    orc = OracleMoE(wl)
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    fwd = api.MoEForward(wl.T, wl.H, wl.I, wl.E, wl.top_k)
+    a1, a2 = fwd.calibrate(bf16_dev(wl.hidden), dev(wl.logits), w, wl.gate_limit, wl.up_limit)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host(a1), orc.a1_gs)
+    np.testing.assert_allclose(host(a2), orc.a2_gs, rtol=1e-2)
+    assert host(a1)[3] == 1.0 and host(a2)[3] == 1.0  # the expert with no rows
