@@ -218,6 +218,10 @@ def run_ours(args, world, rank, local):
 
     # ---- device-resident timed region, per-stage events on the launching stream
     stage_events = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    for evs in stage_events:  # torch creates the CUDA event on its first record
+        for ev in evs:
+            ev.record(stream)
+    torch.cuda.synchronize()
     clocks = ClockSampler(local)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)

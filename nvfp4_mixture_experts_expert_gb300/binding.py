@@ -180,5 +180,8 @@ def nvfp4_moe_set_stage_events(events):
     if not events:
         _check(_stage_events(None, 0))
         return
-    arr = (c_ptr * len(events))(*[e.cuda_event for e in events])
+    handles = [e.cuda_event for e in events]
+    if not all(handles):
+        raise ValueError("stage events must have been recorded once (torch creates CUDA events lazily)")
+    arr = (c_ptr * len(events))(*handles)
     _check(_stage_events(arr, len(events)))

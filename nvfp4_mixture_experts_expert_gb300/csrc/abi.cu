@@ -375,6 +375,7 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
   g2.b_second_offset = 128;
   g2.b_tile_stride = 256;
   g2.sfb_group_bytes = H * (I / 16);
+  g2.n_major = 1;  // all CTAs on one 256-column slice of the combine accumulator at a time
   g2.acc = acc;
   g2.sorted_ids = sorted_ids;
   g2.row_w = row_w;

@@ -19,9 +19,9 @@
 //   warp 1   TMEM allocator and MMA issuer: copies the scale tiles to TMEM
 //            (tcgen05.cp 32x128b.warpx4) and issues 4 MMAs of 128x256x64 per
 //            stage into a 128-lane x 256-column FP32 accumulator in TMEM.
-//   warps 2-5 epilogue: each warp owns the 32 TMEM lanes of its quarter
-//            (warp % 4), i.e. 32 output rows, and reads the accumulator with
-//            tcgen05.ld.
+//   warps 2-9 epilogue: each warp owns the 32 TMEM lanes of its quarter
+//            (warp % 4), i.e. 32 output rows, and one half of the tile's
+//            columns; it reads the accumulator with tcgen05.ld.
 // A tile is 128 rows x 256 MMA columns.  For the SwiGLU epilogue the two B
 // boxes are the gate rows [n0, n0+128) and the up rows [I+n0, I+n0+128) of the
 // expert's W13, so gate and up of one output feature sit in the same TMEM lane
@@ -55,7 +55,8 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
 constexpr int TMEM_COLS = 512;
 constexpr int SF_COL0 = 256;         // scale columns start after the accumulator
 constexpr int SF_COLS_PER_STAGE = 48;  // 4 x (4 SFA + 8 SFB)
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_EPI_WARPS = 8;  // two per TMEM lane quarter, each owning half of the columns
+constexpr int NUM_THREADS = 64 + NUM_EPI_WARPS * 32;
 constexpr int MAX_GROUPS = 1024;
 static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
 static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
@@ -102,6 +103,19 @@ __device__ __forceinline__ int find_group(const int* off, int G, int row) {
   return lo;
 }
 
+// Tile index -> (m-tile, n-tile).  m-major keeps consecutive CTAs on one
+// activation tile (and one expert's weights); n-major keeps every CTA on one
+// output column slice, which bounds the live part of a scattered output.
+__device__ __forceinline__ void decode_tile(int tile, int num_mtiles, int n_tiles, int n_major, int& mt, int& nt) {
+  if (n_major) {
+    nt = tile / num_mtiles;
+    mt = tile - nt * num_mtiles;
+  } else {
+    mt = tile / n_tiles;
+    nt = tile - mt * n_tiles;
+  }
+}
+
 // ------------------------------------------------------------------ producer
 __device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total) {
   volatile int* abort = L.abort_flag;
@@ -111,8 +125,10 @@ __device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total)
   uint32_t stage = 0, phase = 0;
   const int kt = p.K / 64;  // scale tiles per 128-row band
   if (!p.debug_no_loads) {
+    const int num_mtiles = L.offsets[p.G] / BM;
     for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
-      const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
+      int mt, nt;
+      decode_tile(tile, num_mtiles, p.n_tiles, p.n_major, mt, nt);
       const int g = find_group(L.offsets, p.G, mt * BM);
       const int b_r0 = nt * p.b_tile_stride;
       const int b_r1 = b_r0 + p.b_second_offset;
@@ -212,9 +228,11 @@ template <int EPI>
 __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total, uint32_t tmem) {
   volatile int* abort = L.abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int quarter = warp & 3;
+  const int quarter = warp & 3;        // TMEM lanes this warp may access
+  const int half = (warp - 2) >> 2;    // which half of the tile's columns it owns
   const int row_in_tile = quarter * 32 + lane;
   const uint32_t t_base = tmem + ((uint32_t)(quarter * 32) << 16);
+  const int num_mtiles = L.offsets[p.G] / BM;
   uint32_t acc_phase = 0;
   for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
     int ok = 1;
@@ -223,7 +241,8 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
     if (!ok) break;
     __syncwarp();
     tc_fence_after();
-    const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
+    int mt, nt;
+    decode_tile(tile, num_mtiles, p.n_tiles, p.n_major, mt, nt);
     const int g = find_group(L.offsets, p.G, mt * BM);
     const int64_t row = (int64_t)mt * BM + row_in_tile;
     const float alpha = 1.0f / (p.a_gs[g] * p.b_gs[g]);
@@ -231,11 +250,11 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
     if constexpr (EPI == kEpiBf16) {
       const int64_t i_local = row - L.offsets[g];
       const bool valid = p.counts ? i_local < p.counts[g] : true;
-      uint16_t* drow = p.D + g * p.gstride_d + i_local * p.ldd + (int64_t)nt * BN;
+      uint16_t* drow = p.D + g * p.gstride_d + i_local * p.ldd + (int64_t)nt * BN + half * (BN / 2);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < BN / 64; ++c) {
         uint32_t r[32];
-        tmem_load_32(t_base + c * 32, r);
+        tmem_load_32(t_base + half * (BN / 2) + c * 32, r);
         tmem_load_wait();
         if (valid) {
           uint32_t pk[16];
@@ -248,49 +267,50 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
         }
       }
     } else if constexpr (EPI == kEpiSwigluQuant) {
+      // this thread: output features [nt*128 + half*64, +64) of one row = 4 quantization blocks
       const float qgs = p.q_gs[g];
-      const int64_t q_cols = p.I / 16;
-#pragma unroll 1
-      for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t scales = 0;
-#pragma unroll 1
-        for (int c2 = 0; c2 < 2; ++c2) {
-          const int col = h2 * 64 + c2 * 32;
-          uint32_t gr[32], ur[32];
-          tmem_load_32(t_base + col, gr);
-          tmem_load_32(t_base + 128 + col, ur);
-          tmem_load_wait();
-          uint32_t words[4];
+      uint32_t scales = 0;
+      uint4 packed[2];
 #pragma unroll
-          for (int blk = 0; blk < 2; ++blk) {
-            float xs[16];
+      for (int c = 0; c < 2; ++c) {
+        const int col = half * 64 + c * 32;
+        uint32_t gr[32], ur[32];
+        tmem_load_32(t_base + col, gr);
+        tmem_load_32(t_base + 128 + col, ur);
+        tmem_load_wait();
+        uint32_t words[4];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float h = silu_clamped_product(__uint_as_float(gr[blk * 16 + i]) * alpha,
-                                                   __uint_as_float(ur[blk * 16 + i]) * alpha, p.gate_limit,
-                                                   p.up_limit);
-              xs[i] = __fmul_rn(__uint_as_float(f32_to_bf16_rn(h) << 16), qgs);
-            }
-            uint32_t lo, hi;
-            const uint32_t s = quant_block16(xs, lo, hi);
-            words[blk * 2] = lo;
-            words[blk * 2 + 1] = hi;
-            scales |= s << (8 * (c2 * 2 + blk));
+        for (int blk = 0; blk < 2; ++blk) {
+          float xs[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float h = silu_clamped_product(__uint_as_float(gr[blk * 16 + i]) * alpha,
+                                                 __uint_as_float(ur[blk * 16 + i]) * alpha, p.gate_limit,
+                                                 p.up_limit);
+            xs[i] = __fmul_rn(__uint_as_float(f32_to_bf16_rn(h) << 16), qgs);
           }
-          const int64_t ocol = (int64_t)nt * 128 + col;  // first output feature of this chunk
-          *reinterpret_cast<uint4*>(p.q_out + row * (p.I / 2) + ocol / 2) =
-              make_uint4(words[0], words[1], words[2], words[3]);
+          uint32_t lo, hi;
+          const uint32_t sc = quant_block16(xs, lo, hi);
+          words[blk * 2] = lo;
+          words[blk * 2 + 1] = hi;
+          scales |= sc << (8 * (c * 2 + blk));
         }
-        *reinterpret_cast<uint32_t*>(p.q_sf + sf_offset(row, ((int64_t)nt * 128 + h2 * 64) / 16, q_cols)) = scales;
+        packed[c] = make_uint4(words[0], words[1], words[2], words[3]);
       }
+      const int64_t f0 = (int64_t)nt * 128 + half * 64;  // first output feature of this thread
+      uint4* dst = reinterpret_cast<uint4*>(p.q_out + row * (p.I / 2) + f0 / 2);
+      dst[0] = packed[0];
+      dst[1] = packed[1];
+      *reinterpret_cast<uint32_t*>(p.q_sf + sf_offset(row, f0 / 16, p.I / 16)) = scales;
     } else if constexpr (EPI == kEpiSwigluAmax) {
-      // calibration: amax of the bf16 SwiGLU output of this row's 128 features
+      // calibration: amax of the bf16 SwiGLU output of this row's features
       uint32_t m = 0;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
+        const int col = half * 64 + c * 32;
         uint32_t gr[32], ur[32];
-        tmem_load_32(t_base + c * 32, gr);
-        tmem_load_32(t_base + 128 + c * 32, ur);
+        tmem_load_32(t_base + col, gr);
+        tmem_load_32(t_base + 128 + col, ur);
         tmem_load_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -305,11 +325,11 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
     } else {  // kEpiCombine
       const int tok = p.sorted_ids[row];
       const float wgt = tok >= 0 ? p.row_w[row] * alpha : 0.f;
-      float* dst = p.acc + (int64_t)(tok >= 0 ? tok : 0) * p.H + (int64_t)nt * BN;
+      float* dst = p.acc + (int64_t)(tok >= 0 ? tok : 0) * p.H + (int64_t)nt * BN + half * (BN / 2);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < BN / 64; ++c) {
         uint32_t r[32];
-        tmem_load_32(t_base + c * 32, r);
+        tmem_load_32(t_base + half * (BN / 2) + c * 32, r);
         tmem_load_wait();
         if (tok >= 0) {
 #pragma unroll
@@ -338,7 +358,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid
       mbar_init(smem_u32(&L.empty[s]), 1);
     }
     mbar_init(smem_u32(L.acc_full), 1);
-    mbar_init(smem_u32(L.acc_empty), 4);
+    mbar_init(smem_u32(L.acc_empty), NUM_EPI_WARPS);
     mbar_init(smem_u32(L.drain), 1);
     *L.abort_flag = 0;
     fence_mbar_init();

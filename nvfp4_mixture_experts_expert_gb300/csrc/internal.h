@@ -61,6 +61,7 @@ struct GemmArgs {
   int n_tiles;           // output tiles per 128-row m-tile
   int b_second_offset;   // rows from the first to the second 128-row B box
   int b_tile_stride;     // B rows between consecutive n-tiles
+  int n_major;           // tile order: 0 = m-tile major, 1 = n-tile major
   int64_t sfb_group_bytes;
   // kEpiBf16
   uint16_t* D;

@@ -39,11 +39,13 @@ __device__ __forceinline__ uint32_t e4m3_code(float v) {
   return d & 0xFFu;
 }
 
-// E2M1 code of one value (PTX cvt; both nibbles of the result hold the same code).
-__device__ __forceinline__ uint32_t e2m1_code(float v) {
-  uint16_t d;
-  asm("{\n.reg .b8 t;\ncvt.rn.satfinite.e2m1x2.f32 t, %1, %1;\ncvt.u16.u8 %0, t;\n}" : "=h"(d) : "f"(v));
-  return d & 0xFu;
+// Two E2M1 codes in one byte: `lo` -> bits 0-3, `hi` -> bits 4-7 (round to
+// nearest even, saturating at 6).  The PTX cvt puts its first source operand
+// in the upper half of the result.
+__device__ __forceinline__ uint32_t e2m1x2_code(float lo, float hi) {
+  uint32_t r;
+  asm("{\n.reg .b8 t;\ncvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\ncvt.u32.u8 %0, t;\n}" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // Clear the sign bit of every nibble whose magnitude bits are zero (-0 -> 0).
@@ -51,6 +53,18 @@ __device__ __forceinline__ uint32_t drop_negative_zero(uint32_t w) {
   const uint32_t mag = w & 0x77777777u;
   const uint32_t nonzero = (mag + 0x77777777u) & 0x88888888u;
   return mag | (w & nonzero);
+}
+
+// x / d rounded to nearest even, for a block scale d and y = RN(1/d):
+// q0 = RN(x*y) is within one ulp of x/d, the remainder x - q0*d is exact
+// with a fused multiply-add, and one correction step q0 + r*y rounds to the
+// correctly rounded quotient (Markstein's theorem for a correctly rounded
+// reciprocal).  Equality with the IEEE division is checked exhaustively on
+// the device by the test-suite for every E4M3 scale value.
+__device__ __forceinline__ float div_by_scale(float x, float d, float y) {
+  const float q0 = __fmul_rn(x, y);
+  const float r = __fmaf_rn(-q0, d, x);
+  return __fmaf_rn(r, y, q0);
 }
 
 // Quantize one block of 16 already globally-scaled values.  Returns the
@@ -65,9 +79,11 @@ __device__ __forceinline__ uint32_t quant_block16(const float (&xs)[16], uint32_
   }
   const uint32_t s = e4m3_code(__fdiv_rn(b, 6.0f));
   const float d = e4m3_value(s);
+  const float y = __frcp_rn(d);
   uint32_t w[2] = {0u, 0u};
 #pragma unroll
-  for (int i = 0; i < 16; ++i) w[i >> 3] |= e2m1_code(__fdiv_rn(xs[i], d)) << ((i & 7) * 4);
+  for (int j = 0; j < 8; ++j)
+    w[j >> 2] |= e2m1x2_code(div_by_scale(xs[2 * j], d, y), div_by_scale(xs[2 * j + 1], d, y)) << ((j & 3) * 8);
   lo = drop_negative_zero(w[0]);
   hi = drop_negative_zero(w[1]);
   return s;

@@ -102,15 +102,30 @@ __global__ void __launch_bounds__(1024) slot_scan_kernel(int32_t* __restrict__ b
   __shared__ int32_t s_cnt[kMaxExperts];
   for (int i = threadIdx.x; i < n_zero_words; i += blockDim.x) zero_words[i] = 0u;
   __shared__ int32_t s_off[kMaxExperts + 1];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int b = 0; b < nblocks; ++b) {  // exclusive scan over blocks, in place
+  // one warp per expert: exclusive scan over the route blocks, in place
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int chunk = (nblocks + 31) / 32;  // consecutive blocks per lane
+  for (int e = warp; e < E; e += nwarps) {
+    const int b0 = min(nblocks, lane * chunk), b1 = min(nblocks, b0 + chunk);
+    int local = 0;
+    for (int b = b0; b < b1; ++b) local += block_counts[(int64_t)b * E + e];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int b = b0; b < b1; ++b) {
       const int c = block_counts[(int64_t)b * E + e];
       block_counts[(int64_t)b * E + e] = run;
       run += c;
     }
-    s_cnt[e] = run;
-    counts[e] = run;
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (lane == 0) {
+      s_cnt[e] = total;
+      counts[e] = total;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {

@@ -101,3 +101,23 @@ def test_assemble_scales_matches_oracle():
         got = host(out)
         np.testing.assert_array_equal(got[:ref.size], ref)
         assert not got[ref.size:].any()  # capacity rows beyond the last slot are zero
+
+
+def test_quantize_ties_saturation_and_thresholds():
+    """Hand-picked blocks: exact E2M1 midpoints (ties to even), saturation, the
+    underflow threshold on both sides, negative values rounding to zero."""
+    rows = [
+        [6, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5, -0.25, -0.75, -1.25, -1.75, -2.5, -3.5, -5, -6],
+        [7, 6.5, -7, 0.1, -0.1, 3, 4, 2, 1, 0.5, 0, -0.0, 5.5, 4.5, 2.25, 0.125],
+        [0.01171875, 0.001953125] + [0] * 14,
+        [0.0117187, 0.005] + [0] * 14,
+        [448 * 6 * 1.5] + [1] * 15,
+    ]
+    x = np.zeros((len(rows), 64), np.float32)  # K must be a multiple of 64: one hand block per row
+    x[:, :16] = np.float32(rows)
+    bits = W.f32_to_bf16_bits(x)
+    xb = W.bf16_bits_to_f32(bits)
+    packed, swz, _, _ = oracle_packed_rows(xb, np.float32(1.0), 128)
+    fp4, sf, _ = api().quantize(bf16_dev(bits), gs=dev(np.float32([1.0])))
+    np.testing.assert_array_equal(host(fp4), packed)
+    np.testing.assert_array_equal(host(sf), swz)
