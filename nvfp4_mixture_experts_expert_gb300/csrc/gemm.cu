@@ -224,6 +224,9 @@ __device__ __forceinline__ float silu_clamped_product(float g, float u, float gl
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
+// Each epilogue thread first copies its 128 accumulator columns (one row)
+// from TMEM into registers and releases the accumulator, so the MMAs of the
+// next tile overlap all of the epilogue arithmetic and stores below.
 template <int EPI>
 __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total, uint32_t tmem) {
   volatile int* abort = L.abort_flag;
@@ -241,6 +244,24 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
     if (!ok) break;
     __syncwarp();
     tc_fence_after();
+    // SwiGLU kinds: gate columns [half*64, +64) and up columns 128 + [half*64, +64);
+    // other kinds: columns [half*128, +128).
+    uint32_t v[4][32];
+    if constexpr (EPI == kEpiSwigluQuant || EPI == kEpiSwigluAmax) {
+      tmem_load_32(t_base + half * 64, v[0]);
+      tmem_load_32(t_base + half * 64 + 32, v[1]);
+      tmem_load_32(t_base + 128 + half * 64, v[2]);
+      tmem_load_32(t_base + 128 + half * 64 + 32, v[3]);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_load_32(t_base + half * 128 + c * 32, v[c]);
+    }
+    tmem_load_wait();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(L.acc_empty));
+    acc_phase ^= 1u;
+
     int mt, nt;
     decode_tile(tile, num_mtiles, p.n_tiles, p.n_major, mt, nt);
     const int g = find_group(L.offsets, p.G, mt * BM);
@@ -250,100 +271,72 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
     if constexpr (EPI == kEpiBf16) {
       const int64_t i_local = row - L.offsets[g];
       const bool valid = p.counts ? i_local < p.counts[g] : true;
-      uint16_t* drow = p.D + g * p.gstride_d + i_local * p.ldd + (int64_t)nt * BN + half * (BN / 2);
-#pragma unroll 1
-      for (int c = 0; c < BN / 64; ++c) {
-        uint32_t r[32];
-        tmem_load_32(t_base + half * (BN / 2) + c * 32, r);
-        tmem_load_wait();
-        if (valid) {
+      if (valid) {
+        uint16_t* drow = p.D + g * p.gstride_d + i_local * p.ldd + (int64_t)nt * BN + half * (BN / 2);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]) * alpha, __uint_as_float(r[2 * j + 1]) * alpha);
+            pk[j] = pack_bf16x2(__uint_as_float(v[c][2 * j]) * alpha, __uint_as_float(v[c][2 * j + 1]) * alpha);
           uint4* dst = reinterpret_cast<uint4*>(drow + c * 32);
 #pragma unroll
           for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
         }
       }
     } else if constexpr (EPI == kEpiSwigluQuant) {
-      // this thread: output features [nt*128 + half*64, +64) of one row = 4 quantization blocks
+      // output features [nt*128 + half*64, +64) of one row = 4 quantization blocks
       const float qgs = p.q_gs[g];
       uint32_t scales = 0;
-      uint4 packed[2];
+      uint32_t words[8];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int col = half * 64 + c * 32;
-        uint32_t gr[32], ur[32];
-        tmem_load_32(t_base + col, gr);
-        tmem_load_32(t_base + 128 + col, ur);
-        tmem_load_wait();
-        uint32_t words[4];
+      for (int blk = 0; blk < 4; ++blk) {
+        float xs[16];
 #pragma unroll
-        for (int blk = 0; blk < 2; ++blk) {
-          float xs[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float h = silu_clamped_product(__uint_as_float(gr[blk * 16 + i]) * alpha,
-                                                 __uint_as_float(ur[blk * 16 + i]) * alpha, p.gate_limit,
-                                                 p.up_limit);
-            xs[i] = __fmul_rn(__uint_as_float(f32_to_bf16_rn(h) << 16), qgs);
-          }
-          uint32_t lo, hi;
-          const uint32_t sc = quant_block16(xs, lo, hi);
-          words[blk * 2] = lo;
-          words[blk * 2 + 1] = hi;
-          scales |= sc << (8 * (c * 2 + blk));
+        for (int i = 0; i < 16; ++i) {
+          const int f = blk * 16 + i;
+          const float h = silu_clamped_product(__uint_as_float(v[f >> 5][f & 31]) * alpha,
+                                               __uint_as_float(v[2 + (f >> 5)][f & 31]) * alpha, p.gate_limit,
+                                               p.up_limit);
+          xs[i] = __fmul_rn(__uint_as_float(f32_to_bf16_rn(h) << 16), qgs);
         }
-        packed[c] = make_uint4(words[0], words[1], words[2], words[3]);
+        uint32_t lo, hi;
+        scales |= quant_block16(xs, lo, hi) << (8 * blk);
+        words[blk * 2] = lo;
+        words[blk * 2 + 1] = hi;
       }
       const int64_t f0 = (int64_t)nt * 128 + half * 64;  // first output feature of this thread
       uint4* dst = reinterpret_cast<uint4*>(p.q_out + row * (p.I / 2) + f0 / 2);
-      dst[0] = packed[0];
-      dst[1] = packed[1];
+      dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
+      dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
       *reinterpret_cast<uint32_t*>(p.q_sf + sf_offset(row, f0 / 16, p.I / 16)) = scales;
     } else if constexpr (EPI == kEpiSwigluAmax) {
       // calibration: amax of the bf16 SwiGLU output of this row's features
       uint32_t m = 0;
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        const int col = half * 64 + c * 32;
-        uint32_t gr[32], ur[32];
-        tmem_load_32(t_base + col, gr);
-        tmem_load_32(t_base + 128 + col, ur);
-        tmem_load_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float h = silu_clamped_product(__uint_as_float(gr[i]) * alpha, __uint_as_float(ur[i]) * alpha,
-                                               p.gate_limit, p.up_limit);
-          m = max(m, f32_to_bf16_rn(h) & 0x7FFFu);
-        }
+      for (int f = 0; f < 64; ++f) {
+        const float h = silu_clamped_product(__uint_as_float(v[f >> 5][f & 31]) * alpha,
+                                             __uint_as_float(v[2 + (f >> 5)][f & 31]) * alpha, p.gate_limit,
+                                             p.up_limit);
+        m = max(m, f32_to_bf16_rn(h) & 0x7FFFu);
       }
 #pragma unroll
       for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
       if (lane == 0 && m) atomicMax(&p.amax_bits[g], m << 16);
     } else {  // kEpiCombine
       const int tok = p.sorted_ids[row];
-      const float wgt = tok >= 0 ? p.row_w[row] * alpha : 0.f;
-      float* dst = p.acc + (int64_t)(tok >= 0 ? tok : 0) * p.H + (int64_t)nt * BN + half * (BN / 2);
-#pragma unroll 1
-      for (int c = 0; c < BN / 64; ++c) {
-        uint32_t r[32];
-        tmem_load_32(t_base + half * (BN / 2) + c * 32, r);
-        tmem_load_wait();
-        if (tok >= 0) {
+      if (tok >= 0) {
+        const float wgt = p.row_w[row] * alpha;
+        float* dst = p.acc + (int64_t)tok * p.H + (int64_t)nt * BN + half * (BN / 2);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + 4 * j),
-                      make_float4(__uint_as_float(r[4 * j]) * wgt, __uint_as_float(r[4 * j + 1]) * wgt,
-                                  __uint_as_float(r[4 * j + 2]) * wgt, __uint_as_float(r[4 * j + 3]) * wgt));
-        }
+                      make_float4(__uint_as_float(v[c][4 * j]) * wgt, __uint_as_float(v[c][4 * j + 1]) * wgt,
+                                  __uint_as_float(v[c][4 * j + 2]) * wgt, __uint_as_float(v[c][4 * j + 3]) * wgt));
       }
     }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(L.acc_empty));
-    acc_phase ^= 1u;
   }
 }
 
