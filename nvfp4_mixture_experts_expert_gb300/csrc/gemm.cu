@@ -16,9 +16,10 @@
 //   warp 0   TMA producer: per K-stage of 256 elements, one 128x128-byte A box,
 //            two 128x128-byte B boxes (SWIZZLE_128B) and the matching 512-byte
 //            scale tiles (plain bulk copies), into a 4-deep shared-memory ring.
-//   warp 1   TMEM allocator and MMA issuer: copies the scale tiles to TMEM
-//            (tcgen05.cp 32x128b.warpx4) and issues 4 MMAs of 128x256x64 per
-//            stage into a 128-lane x 256-column FP32 accumulator in TMEM.
+//   warp 1   TMEM allocator and MMA issuer: 4 MMAs of 128x256x64 per stage
+//            into a 128-lane x 256-column FP32 accumulator in TMEM.
+//   warp 10  scale copier: moves each stage's scale tiles into TMEM
+//            (tcgen05.cp 32x128b.warpx4) ahead of the MMAs that read them.
 //   warps 2-9 epilogue: each warp owns the 32 TMEM lanes of its quarter
 //            (warp % 4), i.e. 32 output rows, and one half of the tile's
 //            columns; it reads the accumulator with tcgen05.ld.
@@ -56,7 +57,8 @@ constexpr int TMEM_COLS = 512;
 constexpr int SF_COL0 = 256;         // scale columns start after the accumulator
 constexpr int SF_COLS_PER_STAGE = 48;  // 4 x (4 SFA + 8 SFB)
 constexpr int NUM_EPI_WARPS = 8;  // two per TMEM lane quarter, each owning half of the columns
-constexpr int NUM_THREADS = 64 + NUM_EPI_WARPS * 32;
+constexpr int COPIER_WARP = 2 + NUM_EPI_WARPS;
+constexpr int NUM_THREADS = 32 * (COPIER_WARP + 1);
 constexpr int MAX_GROUPS = 1024;
 static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
 static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
@@ -73,6 +75,8 @@ struct SmemLayout {
   uint64_t* acc_full;
   uint64_t* acc_empty;
   uint64_t* drain;
+  uint64_t* sf_full;     // [STAGES] scale tiles of a stage are in TMEM
+  uint64_t* drain_cp;    // copier's own drain on abort
   uint32_t* tmem_slot;
   int* abort_flag;
   int* offsets;
@@ -88,7 +92,9 @@ __device__ __forceinline__ SmemLayout carve(uint8_t* raw) {
   L.acc_full = L.empty + STAGES;
   L.acc_empty = L.acc_full + 1;
   L.drain = L.acc_empty + 1;
-  L.tmem_slot = reinterpret_cast<uint32_t*>(L.drain + 1);
+  L.sf_full = L.drain + 1;
+  L.drain_cp = L.sf_full + STAGES;
+  L.tmem_slot = reinterpret_cast<uint32_t*>(L.drain_cp + 1);
   L.abort_flag = reinterpret_cast<int*>(L.tmem_slot + 1);
   L.offsets = reinterpret_cast<int*>(L.abort_flag + 3);
   return L;
@@ -167,6 +173,44 @@ __device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total)
   }
 }
 
+// ------------------------------------------------------------------ scale copier
+// Copies each stage's scale tiles from shared memory into that stage's TMEM
+// columns and signals sf_full[stage].  Issuing these copies from their own
+// warp lets them overlap the MMA stream of the previous stages.  A stage's
+// TMEM columns are rewritten only after its shared-memory slot was refilled,
+// i.e. after the MMAs that read them committed.
+__device__ void copier_loop(const GemmArgs& p, const SmemLayout& L, int total, uint32_t tmem) {
+  volatile int* abort = L.abort_flag;
+  uint32_t stage = 0, phase = 0;
+  bool issued_any = false;
+  for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+    for (int kb = 0; kb < p.num_kb; ++kb) {
+      const int nmma = min(4, (p.K - kb * 256) / 64);
+      if (!wait_bounded(smem_u32(&L.full[stage]), phase, abort, p.status, p.timeout_ns)) break;
+      tc_fence_after();
+      const uint32_t sfa_s = smem_u32(L.stages + stage * STAGE_BYTES) + A_BYTES + B_BYTES;
+      const uint32_t sfb_s = sfa_s + SFA_BYTES;
+      const uint32_t sf_col = tmem + SF_COL0 + stage * SF_COLS_PER_STAGE;
+      for (int i = 0; i < nmma; ++i) {
+        tc_cp_sf(sf_col + 4 * i, smem_desc(sfa_s + 512 * i, 0, 128, 0));
+        tc_cp_sf(sf_col + 16 + 8 * i, smem_desc(sfb_s + 512 * i, 0, 128, 0));
+        tc_cp_sf(sf_col + 16 + 8 * i + 4, smem_desc(sfb_s + 2048 + 512 * i, 0, 128, 0));
+      }
+      issued_any = true;
+      tc_commit(smem_u32(&L.sf_full[stage]));
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  if (*abort && issued_any) {  // copies in flight must land before TMEM is freed
+    tc_commit(smem_u32(L.drain_cp));
+    volatile int no_abort = 0;
+    wait_bounded(smem_u32(L.drain_cp), 0, &no_abort, nullptr, p.timeout_ns);
+  }
+}
+
 // ------------------------------------------------------------------ MMA issuer
 __device__ void mma_loop(const GemmArgs& p, const SmemLayout& L, int total, uint32_t tmem) {
   volatile int* abort = L.abort_flag;
@@ -179,21 +223,15 @@ __device__ void mma_loop(const GemmArgs& p, const SmemLayout& L, int total, uint
     bool ok = true;
     for (int kb = 0; kb < p.num_kb; ++kb) {
       const int nmma = min(4, (p.K - kb * 256) / 64);
-      if (!wait_bounded(smem_u32(&L.full[stage]), phase, abort, p.status, p.timeout_ns)) {
+      // sf_full[stage] implies full[stage]: the copier waited for the stage's data first
+      if (!wait_bounded(smem_u32(&L.sf_full[stage]), phase, abort, p.status, p.timeout_ns)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t a_s = smem_u32(L.stages + stage * STAGE_BYTES);
       const uint32_t b_s = a_s + A_BYTES;
-      const uint32_t sfa_s = b_s + B_BYTES;
-      const uint32_t sfb_s = sfa_s + SFA_BYTES;
       const uint32_t sf_col = tmem + SF_COL0 + stage * SF_COLS_PER_STAGE;
-      for (int i = 0; i < nmma; ++i) {
-        tc_cp_sf(sf_col + 4 * i, smem_desc(sfa_s + 512 * i, 0, 128, 0));
-        tc_cp_sf(sf_col + 16 + 8 * i, smem_desc(sfb_s + 512 * i, 0, 128, 0));
-        tc_cp_sf(sf_col + 16 + 8 * i + 4, smem_desc(sfb_s + 2048 + 512 * i, 0, 128, 0));
-      }
       for (int i = 0; i < nmma; ++i) {
         const uint64_t ad = smem_desc(a_s + 32 * i, 16, 1024, 2);
         const uint64_t bd = smem_desc(b_s + 32 * i, 16, 1024, 2);
@@ -353,6 +391,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid
     mbar_init(smem_u32(L.acc_full), 1);
     mbar_init(smem_u32(L.acc_empty), NUM_EPI_WARPS);
     mbar_init(smem_u32(L.drain), 1);
+    mbar_init(smem_u32(L.drain_cp), 1);
+    for (int st = 0; st < STAGES; ++st) mbar_init(smem_u32(&L.sf_full[st]), 1);
     *L.abort_flag = 0;
     fence_mbar_init();
   }
@@ -375,8 +415,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid
     if (lane == 0) producer_loop(p, L, total);
   } else if (warp == 1) {
     if (lane == 0) mma_loop(p, L, total, tmem);
-  } else {
+  } else if (warp < COPIER_WARP) {
     epilogue_loop<EPI>(p, L, total, tmem);
+  } else {
+    if (lane == 0) copier_loop(p, L, total, tmem);
   }
   tc_fence_before();
   __syncthreads();
@@ -405,7 +447,7 @@ cudaError_t launch_one(const GemmArgs& a, int grid, cudaStream_t s) {
 }  // namespace
 
 size_t gemm_smem_bytes(int G) {
-  return 1024 + (size_t)STAGES * STAGE_BYTES + 8 * (2 * STAGES + 3) + 16 + 4 * (size_t)(G + 1) + 16;
+  return 1024 + (size_t)STAGES * STAGE_BYTES + 8 * (3 * STAGES + 4) + 16 + 4 * (size_t)(G + 1) + 16;
 }
 
 cudaError_t launch_gemm(int kind, const GemmArgs& args, int grid, cudaStream_t s) {
