@@ -82,6 +82,35 @@ int nvfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, int64_t
                    int64_t rows_padded, void* stream);
 
 /*
+ * nvfp4_quantize_no_alloc -- nvfp4_quantize with the global scale computed
+ * on the device (gs == NULL behaviour), for callers that cannot provide any
+ * scratch memory.  The method's pages have no counterpart of this call; it
+ * exists for hosts that own all device memory and offer no way to get a
+ * temporary buffer (a server with a pre-reserved pool, a plugin interface
+ * without a workspace argument), so neither they nor the library may call
+ * cudaMalloc.
+ *
+ * Same arguments and results as nvfp4_quantize with gs == NULL (gs_out
+ * receives 2688/amax per group), minus the workspace.  Instead, the partial
+ * maxima of the amax reduction live in a fixed array inside the library's
+ * device image (NVFP4_QUANTIZE_NO_ALLOC_MAX_GROUPS x 128 floats = 32 KB on
+ * every GPU that loads the library, held until the process exits).
+ *   - groups > NVFP4_QUANTIZE_NO_ALLOC_MAX_GROUPS is rejected with
+ *     NVFP4_ERR_UNSUPPORTED before anything is launched.
+ *   - The first call on a device looks up that array's device address (with
+ *     the device current) and caches it; make that first call before any
+ *     stream capture on the device.
+ *   - Nothing is allocated: no cudaMalloc / cudaFree, no allocating library call.
+ *   - Every call on a device shares the array.  Each call rewrites every slot
+ *     it reads, so no state survives from one call to the next, but calls
+ *     whose kernels overlap on the GPU race on it: keep them ordered on one
+ *     stream (or use nvfp4_quantize with your own workspace).
+ */
+#define NVFP4_QUANTIZE_NO_ALLOC_MAX_GROUPS 64
+int nvfp4_quantize_no_alloc(const void* x, int64_t rows, int64_t K, int64_t ld_x, int64_t group_stride_x, int groups,
+                            float* gs_out, void* fp4, void* sf, int64_t rows_padded, void* stream);
+
+/*
  * nvfp4_assemble_scales -- place per-group linear scales into 128-row padded
  * slots in the tile layout (vllm page: "Root cause of garbage output",
  * "Bug 9" multi-chunk slots, and the wish for an assembly call that takes a

@@ -64,6 +64,8 @@ _last_error = _sig("nvfp4_last_error", ctypes.c_char_p, [])
 _quantize_ws = _sig("nvfp4_quantize_workspace_size", c_size, [c_int])
 _quantize = _sig("nvfp4_quantize", c_int, [c_ptr, c_i64, c_i64, c_i64, c_i64, c_int, c_ptr, c_ptr, c_ptr, c_size,
                                            c_ptr, c_ptr, c_i64, c_ptr])
+_quantize_no_alloc = _sig("nvfp4_quantize_no_alloc", c_int, [c_ptr, c_i64, c_i64, c_i64, c_i64, c_int, c_ptr,
+                                                             c_ptr, c_ptr, c_i64, c_ptr])
 _assemble = _sig("nvfp4_assemble_scales", c_int, [c_ptr, c_i64, c_ptr, c_ptr, c_int, c_i64, c_ptr, c_ptr])
 _gemm = _sig("nvfp4_grouped_gemm", c_int, [c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_int, c_i64,
                                            c_i64, c_i64, c_ptr, c_i64, c_i64, c_ptr])
@@ -131,6 +133,13 @@ def nvfp4_quantize(x, rows, K, ld_x, group_stride_x, groups, gs, gs_out, workspa
                    rows_padded, stream=None):
     _check(_quantize(_p(x), rows, K, ld_x, group_stride_x, groups, _p(gs), _p(gs_out), _p(workspace),
                      workspace_bytes, _p(fp4), _p(sf), rows_padded, _stream(stream)))
+
+
+def nvfp4_quantize_no_alloc(x, rows, K, ld_x, group_stride_x, groups, gs_out, fp4, sf, rows_padded, stream=None):
+    """nvfp4_quantize with gs computed on the device and no workspace argument, for
+    callers that cannot allocate device memory (see include/nvfp4moe.h)."""
+    _check(_quantize_no_alloc(_p(x), rows, K, ld_x, group_stride_x, groups, _p(gs_out), _p(fp4), _p(sf),
+                              rows_padded, _stream(stream)))
 
 
 def nvfp4_assemble_scales(sf_linear, sf_cols, offsets, padded_offsets, groups, rows_capacity, sf_swizzled,

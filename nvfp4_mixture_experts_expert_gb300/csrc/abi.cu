@@ -116,6 +116,8 @@ inline void stage_mark(int i, cudaStream_t s) {
 
 }  // namespace
 
+void nvfp4::set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg ? msg : ""); }
+
 extern "C" {
 
 int nvfp4_version(void) { return 100; }

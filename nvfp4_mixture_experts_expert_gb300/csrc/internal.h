@@ -88,6 +88,9 @@ struct GemmArgs {
 };
 
 size_t gemm_smem_bytes(int G);
+
+// abi.cu: sets the text nvfp4_last_error() returns on the calling thread.
+void set_last_error(const char* msg);
 cudaError_t launch_gemm(int kind, const GemmArgs& args, int grid, cudaStream_t s);
 cudaError_t gemm_status_ptr(int** ptr);
 cudaError_t gemm_read_status(int* out, int reset);
