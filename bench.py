@@ -242,8 +242,8 @@ def run_ours(args, world, rank, local):
     barrier(world)
     ms = t_start.elapsed_time(t_end) / args.steps
     ms = max_over_ranks(ms, world)
-    names = ["route", "slot_scan", "slot_scatter", "gather_quantize", "l1_gemm_swiglu_quant", "l2_gemm_combine",
-             "finalize"]
+    names = ["route", "slot_scan", "slot_scatter", "gather_quantize", "l1_gemm_swiglu_quant", "l2_gemm_weighted",
+             "token_combine"]
     stages = {n: statistics.mean(ev[i].elapsed_time(ev[i + 1]) for ev in stage_events) for i, n in enumerate(names)}
 
     # ---- end to end through the C ABI with pinned host buffers
@@ -284,7 +284,7 @@ def run_ours(args, world, rank, local):
     l1_flops = 2.0 * A * H * (2 * I)
     l2_flops = 2.0 * A * I * H
     l1_tflops = l1_flops / (stages["l1_gemm_swiglu_quant"] * 1e-3) / 1e12
-    l2_tflops = l2_flops / (stages["l2_gemm_combine"] * 1e-3) / 1e12
+    l2_tflops = l2_flops / (stages["l2_gemm_weighted"] * 1e-3) / 1e12
     traffic = stored_traffic("l1_gemm_swiglu_quant_" + args.workload)
     roofline = {"kernel": "l1_gemm_swiglu_quant", "bound": "tensor", "achieved": round(l1_tflops, 1),
                 "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(l1_tflops / fp4_peak, 4),

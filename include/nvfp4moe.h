@@ -164,7 +164,8 @@ int nvfp4_grouped_gemm(const void* A, const void* SFA, const float* a_gs, const 
  *   G  = dq(quant(x_t, a1_gs[e])) . dq(W13[e])^T           (2I outputs)
  *   h  = bf16( silu(min(G[:I], gate_limit)) * clamp(G[I:], -up_limit, up_limit) )
  *   Y  = dq(quant(h, a2_gs[e])) . dq(W2[e])^T              (H outputs)
- *   out[t] += w * Y,   out is written as bf16.
+ *   out[t] = bf16( sum over its top_k experts, in order, of bf16(w * Y) ),
+ *   FP32 sum: deterministic (no atomics).
  *   hidden         device bf16 [T][H]
  *   router_logits  device f32 [T][E]
  *   w13            device u8 [E][2I][H/2]  (rows 0..I-1 gate, I..2I-1 up)
@@ -211,12 +212,13 @@ int nvfp4_moe_calibrate(const void* hidden, const float* router_logits, int64_t 
  *   tile_expert i32[cap/128], sorted_token_ids i32[cap] (-1 pad),
  *   row_weight f32[cap] (0 pad), inverse i32[A] (assignment -> row)
  *   a1 u8[cap][H/2], sfa1 u8[cap*H/16], a2 u8[cap][I/2], sfa2 u8[cap*I/16]
- *   acc f32[T][H] (combine accumulator), calib u32[2E] (calibration amax bits)
+ *   y bf16[cap][H] (routing-weighted L2 rows in slot order), calib u32[2E]
+ *   (calibration amax bits)
  * Only rows < P of the row-indexed buffers are defined after a call.
  */
 typedef struct {
   size_t topk_ids, topk_w, block_counts, counts, offsets, meta, tile_expert, sorted_token_ids, row_weight,
-      inverse, a1, sfa1, a2, sfa2, acc, calib, total;
+      inverse, a1, sfa1, a2, sfa2, y, calib, total;
   int64_t capacity;
   int64_t route_blocks;
 } nvfp4_moe_layout;
@@ -233,7 +235,7 @@ int nvfp4_device_status(int* status_out, int reset);
  * Optional per-stage timing of nvfp4_moe_forward: when set, the forward
  * records events[i] (cudaEvent_t) on its stream before stage i, i = 0..6, and
  * events[7] after the last stage (stages: route, slot scan, slot scatter,
- * gather+quantize, L1 GEMM, L2 GEMM, finalize).  n_events must be 8, or 0
+ * gather+quantize, L1 GEMM, L2 GEMM, token combine).  n_events must be 8, or 0
  * with events NULL to switch it off.  Process-wide; not thread-safe.
  */
 int nvfp4_moe_set_stage_events(void* const* events, int n_events);

@@ -47,7 +47,7 @@ class Nvfp4Error(RuntimeError):
 class MoeLayout(ctypes.Structure):
     _fields_ = [(n, c_size) for n in (
         "topk_ids", "topk_w", "block_counts", "counts", "offsets", "meta", "tile_expert",
-        "sorted_token_ids", "row_weight", "inverse", "a1", "sfa1", "a2", "sfa2", "acc", "calib", "total")] + [
+        "sorted_token_ids", "row_weight", "inverse", "a1", "sfa1", "a2", "sfa2", "y", "calib", "total")] + [
         ("capacity", c_i64), ("route_blocks", c_i64)]
 
 

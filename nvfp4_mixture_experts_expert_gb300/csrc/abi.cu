@@ -273,7 +273,7 @@ int nvfp4_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int E, int top_k
   out->sfa1 = take(cap * H / 16);
   out->a2 = take(cap * I / 2);
   out->sfa2 = take(cap * I / 16);
-  out->acc = take(T * H * 4);
+  out->y = take(cap * H * 2);
   out->calib = take((int64_t)2 * E * 4);
   out->total = off;
   out->capacity = cap;
@@ -332,7 +332,7 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
   uint8_t* sfa1 = ws + L.sfa1;
   uint8_t* a2 = ws + L.a2;
   uint8_t* sfa2 = ws + L.sfa2;
-  float* acc = (float*)(ws + L.acc);
+  uint16_t* ybuf = (uint16_t*)(ws + L.y);
   const int64_t cap = L.capacity;
 
   GemmArgs g1, g2;
@@ -377,8 +377,7 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
   g2.b_second_offset = 128;
   g2.b_tile_stride = 256;
   g2.sfb_group_bytes = H * (I / 16);
-  g2.n_major = 1;  // all CTAs on one 256-column slice of the combine accumulator at a time
-  g2.acc = acc;
+  g2.y = ybuf;
   g2.sorted_ids = sorted_ids;
   g2.row_w = row_w;
   g2.H = (int)H;
@@ -388,7 +387,7 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
   const int nb = (int)L.route_blocks;
   cudaError_t e;
   stage_mark(0, s);
-  if ((e = launch_route_topk(router_logits, T, E, top_k, ids, wts, bcnt, acc, H, s)) != cudaSuccess)
+  if ((e = launch_route_topk(router_logits, T, E, top_k, ids, wts, bcnt, s)) != cudaSuccess)
     return cuda_fail(e, "route launch");
   stage_mark(1, s);
   if ((e = launch_slot_scan(bcnt, nb, E, counts, offsets, meta, tile_expert, sorted_ids, row_w, nullptr, 0, s)) !=
@@ -410,8 +409,8 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
   if ((e = launch_gemm(kEpiCombine, g2, (int)(t2 < dev->sms ? t2 : dev->sms), s)) != cudaSuccess)
     return cuda_fail(e, "L2 launch");
   stage_mark(6, s);
-  if ((e = launch_finalize(acc, T * H, (uint16_t*)out, dev->sms, s)) != cudaSuccess)
-    return cuda_fail(e, "finalize launch");
+  if ((e = launch_token_combine(ybuf, inverse, T, H, top_k, (uint16_t*)out, s)) != cudaSuccess)
+    return cuda_fail(e, "combine launch");
   stage_mark(7, s);
   return NVFP4_OK;
 }
@@ -456,7 +455,6 @@ int nvfp4_moe_calibrate(const void* hidden, const float* router_logits, int64_t 
   int32_t* inverse = (int32_t*)(ws + L.inverse);
   uint8_t* a1 = ws + L.a1;
   uint8_t* sfa1 = ws + L.sfa1;
-  float* acc = (float*)(ws + L.acc);
   uint32_t* amax = (uint32_t*)(ws + L.calib);
   const int64_t cap = L.capacity;
   cudaError_t e;
@@ -492,7 +490,7 @@ int nvfp4_moe_calibrate(const void* hidden, const float* router_logits, int64_t 
   g1.status = dev->status;
   g1.timeout_ns = 2000000000ull;
   const int nb = (int)L.route_blocks;
-  if ((e = launch_route_topk(router_logits, T, E, top_k, ids, wts, bcnt, acc, H, s)) != cudaSuccess ||
+  if ((e = launch_route_topk(router_logits, T, E, top_k, ids, wts, bcnt, s)) != cudaSuccess ||
       (e = launch_slot_scan(bcnt, nb, E, counts, offsets, meta, tile_expert, sorted_ids, row_w, amax, 2 * E, s)) !=
           cudaSuccess ||
       (e = launch_slot_scatter(ids, wts, T, E, top_k, bcnt, offsets, sorted_ids, row_w, inverse, s)) !=

@@ -7,8 +7,9 @@
 //                    nibbles and tile-layout scales written for the L2 GEMM
 //                    (bridge.py page: fused SwiGLU epilogue; cutedsl page: gate
 //                    clamped before SiLU)
-//   kEpiCombine      MoE L2: out[token] += w_row * alpha * acc (FP32 red.add),
-//                    pad rows skipped (vllm page: scatter_add with zero-weight pads)
+//   kEpiCombine      MoE L2: Y[row] = bf16(w_row * alpha * acc) for real slot rows,
+//                    in slot order; the token combine then sums each token's
+//                    top_k rows (vllm page: scatter_add with zero-weight pads)
 //   kEpiSwigluAmax   MoE calibration: per-expert amax of the bf16 SwiGLU output
 //                    (vllm page: L2 global scale from the actual L1 output)
 //
@@ -27,8 +28,9 @@
 // boxes are the gate rows [n0, n0+128) and the up rows [I+n0, I+n0+128) of the
 // expert's W13, so gate and up of one output feature sit in the same TMEM lane
 // 128 columns apart, and the 16-wide requantization blocks are in-register.
-// Tiles are ordered m-tile major, n-tile minor; m-tiles map to groups through
-// the 128-aligned group offsets read from device memory (no host sync).
+// Tiles are ordered m-tile major, n-tile minor (n-major is available); m-tiles
+// map to groups through the 128-aligned group offsets read from device memory
+// (no host sync).
 // Every mbarrier wait is bounded (timeout -> device status word, abort, drain
 // of copies/MMAs in flight, TMEM freed, return).
 #include <cuda.h>
@@ -361,18 +363,20 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
 #pragma unroll
       for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
       if (lane == 0 && m) atomicMax(&p.amax_bits[g], m << 16);
-    } else {  // kEpiCombine
-      const int tok = p.sorted_ids[row];
-      if (tok >= 0) {
+    } else {  // kEpiCombine: routing-weighted rows, stored in slot order for the token combine
+      if (p.sorted_ids[row] >= 0) {
         const float wgt = p.row_w[row] * alpha;
-        float* dst = p.acc + (int64_t)tok * p.H + (int64_t)nt * BN + half * (BN / 2);
+        uint16_t* dst = p.y + row * p.H + (int64_t)nt * BN + half * (BN / 2);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            atomicAdd(reinterpret_cast<float4*>(dst + c * 32 + 4 * j),
-                      make_float4(__uint_as_float(v[c][4 * j]) * wgt, __uint_as_float(v[c][4 * j + 1]) * wgt,
-                                  __uint_as_float(v[c][4 * j + 2]) * wgt, __uint_as_float(v[c][4 * j + 3]) * wgt));
+          for (int j = 0; j < 16; ++j)
+            pk[j] = pack_bf16x2(__uint_as_float(v[c][2 * j]) * wgt, __uint_as_float(v[c][2 * j + 1]) * wgt);
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
       }
     }
   }

@@ -33,14 +33,16 @@ cudaError_t launch_gs_from_amax(const uint32_t* amax_bits, int n, float* gs, cud
 // ---------------------------------------------------------------- route.cu
 constexpr int kRouteTokensPerBlock = 64;
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
-                              int32_t* block_counts, float* acc, int64_t H, cudaStream_t s);
+                              int32_t* block_counts, cudaStream_t s);
 cudaError_t launch_slot_scan(int32_t* block_counts, int nblocks, int E, int32_t* counts, int32_t* offsets,
                              int32_t* meta, int32_t* tile_expert, int32_t* sorted_ids, float* row_w,
                              uint32_t* zero_words, int n_zero_words, cudaStream_t s);
 cudaError_t launch_slot_scatter(const int32_t* ids, const float* w, int64_t T, int E, int k,
                                 const int32_t* block_base, const int32_t* offsets, int32_t* sorted_ids,
                                 float* row_w, int32_t* inverse, cudaStream_t s);
-cudaError_t launch_finalize(const float* acc, int64_t n, uint16_t* out, int num_sms, cudaStream_t s);
+// out[t] = bf16( sum_j Y[inverse[t*k + j]] ), j ascending, FP32 sum.
+cudaError_t launch_token_combine(const uint16_t* y, const int32_t* inverse, int64_t T, int64_t H, int k,
+                                 uint16_t* out, cudaStream_t s);
 
 // ---------------------------------------------------------------- gemm.cu
 enum EpilogueKind { kEpiBf16 = 0, kEpiSwigluQuant = 1, kEpiCombine = 2, kEpiSwigluAmax = 3 };
@@ -77,7 +79,7 @@ struct GemmArgs {
   // kEpiSwigluAmax: per-group amax of h (float bits, atomicMax)
   uint32_t* amax_bits;
   // kEpiCombine
-  float* acc;
+  uint16_t* y;  // bf16 [rows][H], routing-weighted L2 rows in slot order
   const int32_t* sorted_ids;
   const float* row_w;
   int H;

@@ -5,7 +5,7 @@
 //  route_topk     one warp per token: top-k of the FP32 logits (ties -> lower
 //                 expert), weights = exp(l_j - l_max) / sum over the chosen
 //                 (softmax renormalised over the top-k); per-block expert
-//                 histogram in shared memory; zeroes the token's combine rows.
+//                 histogram in shared memory.
 //  slot_scan      one block: per-expert exclusive scan of the block histograms,
 //                 padded offsets (multiples of 128, multi-chunk experts --
 //                 vllm page "Bug 9"), the m-tile -> expert table, pad rows.
@@ -13,7 +13,8 @@
 //                 expert (ascending flat index t*k+j) via warp match/ballot,
 //                 giving the slot row; writes sorted_token_ids, row weights and
 //                 the inverse map.  Deterministic: no atomics decide a row.
-//  finalize       FP32 combine accumulator -> bf16 output.
+//  token_combine  out[t] = bf16(sum over the token's top_k rows of the
+//                 routing-weighted L2 output), rows in j order: deterministic.
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -29,7 +30,7 @@ constexpr int kRouteWarps = 8;
 
 __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
     const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ ids, float* __restrict__ w,
-    int32_t* __restrict__ block_counts, float* __restrict__ acc, int64_t H) {
+    int32_t* __restrict__ block_counts) {
   __shared__ int32_t hist[kMaxExperts];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
@@ -84,9 +85,6 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
         atomicAdd(&hist[sel_e[j]], 1);
       }
     }
-    // zero this token's combine accumulator row (H floats)
-    float4* row = reinterpret_cast<float4*>(acc + t * H);
-    for (int64_t i = lane; i < H / 4; i += 32) row[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) block_counts[(int64_t)blockIdx.x * E + e] = hist[e];
@@ -201,19 +199,37 @@ __global__ void __launch_bounds__(256) slot_scatter_kernel(const int32_t* __rest
   }
 }
 
-__global__ void finalize_kernel(const float4* __restrict__ acc, int64_t n4, uint2* __restrict__ out) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
-    const float4 v = acc[i];
-    out[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+// One 256-thread block per token; thread i owns 8 consecutive features per
+// 2048-feature stripe and adds the token's k rows (16-byte loads) in j order.
+__global__ void __launch_bounds__(256) token_combine_kernel(const uint16_t* __restrict__ y,
+                                                            const int32_t* __restrict__ inverse, int64_t H, int k,
+                                                            uint16_t* __restrict__ out) {
+  const int64_t t = blockIdx.x;
+  __shared__ int32_t rows[kMaxTopK];
+  if (threadIdx.x < k) rows[threadIdx.x] = inverse[t * k + threadIdx.x];
+  __syncthreads();
+  for (int64_t c = (int64_t)threadIdx.x * 8; c < H; c += (int64_t)blockDim.x * 8) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + (int64_t)rows[j] * H + c));
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] += bf16_lo(u[q]);
+        acc[2 * q + 1] += bf16_hi(u[q]);
+      }
+    }
+    *reinterpret_cast<uint4*>(out + t * H + c) = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                                           pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
   }
 }
 
 }  // namespace
 
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
-                              int32_t* block_counts, float* acc, int64_t H, cudaStream_t s) {
+                              int32_t* block_counts, cudaStream_t s) {
   const int64_t nb = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
-  route_topk_kernel<<<(unsigned)nb, kRouteWarps * 32, 0, s>>>(logits, T, E, k, ids, w, block_counts, acc, H);
+  route_topk_kernel<<<(unsigned)nb, kRouteWarps * 32, 0, s>>>(logits, T, E, k, ids, w, block_counts);
   return cudaGetLastError();
 }
 
@@ -234,13 +250,9 @@ cudaError_t launch_slot_scatter(const int32_t* ids, const float* w, int64_t T, i
   return cudaGetLastError();
 }
 
-cudaError_t launch_finalize(const float* acc, int64_t n, uint16_t* out, int num_sms, cudaStream_t s) {
-  const int64_t n4 = n / 4;
-  int64_t grid = (n4 + 255) / 256;
-  if (grid > (int64_t)num_sms * 8) grid = (int64_t)num_sms * 8;
-  if (grid < 1) grid = 1;
-  finalize_kernel<<<(unsigned)grid, 256, 0, s>>>(reinterpret_cast<const float4*>(acc), n4,
-                                                 reinterpret_cast<uint2*>(out));
+cudaError_t launch_token_combine(const uint16_t* y, const int32_t* inverse, int64_t T, int64_t H, int k,
+                                 uint16_t* out, cudaStream_t s) {
+  if (T > 0) token_combine_kernel<<<(unsigned)T, 256, 0, s>>>(y, inverse, H, k, out);
   return cudaGetLastError();
 }
 

@@ -33,11 +33,11 @@ def test_workspace_layout_is_consistent(binding):
     L = binding.nvfp4_moe_workspace_layout(T, H, I, E, k)
     assert L["capacity"] == 55296  # roundup(T*k + 127*E, 128)
     order = ["topk_ids", "topk_w", "block_counts", "counts", "offsets", "meta", "tile_expert",
-             "sorted_token_ids", "row_weight", "inverse", "a1", "sfa1", "a2", "sfa2", "acc"]
+             "sorted_token_ids", "row_weight", "inverse", "a1", "sfa1", "a2", "sfa2", "y", "calib"]
     offs = [L[n] for n in order]
     assert offs == sorted(offs) and all(o % 1024 == 0 for o in offs)
     assert L["sfa1"] - L["a1"] >= L["capacity"] * H // 2
-    assert L["total"] - L["acc"] >= T * H * 4
+    assert L["calib"] - L["y"] >= L["capacity"] * H * 2
     assert binding.nvfp4_moe_workspace_size(T, H, I, E, k) == L["total"]
 
 
