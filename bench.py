@@ -324,19 +324,26 @@ def decode_side_measurement(seed):
     def step():
         fwd(L["hidden"], L["logits"], w, L["a1"], L["a2"], GATE_LIMIT, UP_LIMIT, out=out)
 
+    from nvfp4_mixture_experts_expert_gb300 import binding as B
     for _ in range(5):
         step()
-    times = []
+    times, stage_times = [], []
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+    for ev in evs:  # materialise the CUDA events (torch creates them on first record)
+        ev.record()
+    torch.cuda.synchronize()
     for _ in range(20):
         flush.fill_(1)  # evict the weights from L2 between iterations
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record()
+        B.nvfp4_moe_set_stage_events(evs)
         step()
-        b.record()
+        B.nvfp4_moe_set_stage_events(None)
         torch.cuda.synchronize()
-        times.append(a.elapsed_time(b))
+        times.append(evs[0].elapsed_time(evs[7]))
+        stage_times.append([evs[i].elapsed_time(evs[i + 1]) for i in range(7)])
     ms = statistics.median(times)
+    names = ["route", "slot_scan", "slot_scatter", "gather_quantize", "l1_gemm_swiglu_quant", "l2_gemm_weighted",
+             "token_combine"]
+    stages = {n: round(statistics.median(st[i] for st in stage_times), 4) for i, n in enumerate(names)}
     counts = fwd.view("counts", torch.int32, L["E"]).cpu()
     active = [e for e in range(L["E"]) if int(counts[e]) > 0]
     H, I = L["H"], L["I"]
@@ -346,7 +353,8 @@ def decode_side_measurement(seed):
     return {"workload": workload_name("decode"), "ms_per_step": round(ms, 4),
             "tokens_per_s": round(L["T"] / (ms * 1e-3), 1), "active_experts": len(active),
             "weight_bytes": wbytes, "weight_stream_gbs": round(gbs, 1),
-            "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "l2": "flushed (512 MB write) before each step"}
+            "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "stages_ms": stages,
+            "l2": "flushed (512 MB write) before each step"}
 
 
 # --------------------------------------------------------------------------- CPU oracle (baseline / reference arm)

@@ -31,7 +31,7 @@ cudaError_t launch_gather_amax(const uint16_t* hidden, int64_t H, const int32_t*
 cudaError_t launch_gs_from_amax(const uint32_t* amax_bits, int n, float* gs, cudaStream_t s);
 
 // ---------------------------------------------------------------- route.cu
-constexpr int kRouteTokensPerBlock = 64;
+constexpr int kRouteTokensPerBlock = 16;
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
                               int32_t* block_counts, cudaStream_t s);
 cudaError_t launch_slot_scan(int32_t* block_counts, int nblocks, int E, int32_t* counts, int32_t* offsets,

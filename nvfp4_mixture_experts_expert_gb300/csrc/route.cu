@@ -3,10 +3,12 @@
 // offsets, no .item(), padding slots with zero weight).
 //
 //  route_topk     one warp per token: top-k of the FP32 logits (ties -> lower
-//                 expert), weights = exp(l_j - l_max) / sum over the chosen
+//                 expert) by packed (logit, expert) keys held in registers,
+//                 weights = exp(l_j - l_max) / sum over the chosen
 //                 (softmax renormalised over the top-k); per-block expert
 //                 histogram in shared memory.
-//  slot_scan      one block: per-expert exclusive scan of the block histograms,
+//  slot_scan      one block: per-expert exclusive scan of the (expert-major)
+//                 block histograms,
 //                 padded offsets (multiples of 128, multi-chunk experts --
 //                 vllm page "Bug 9"), the m-tile -> expert table, pad rows.
 //  slot_scatter   per block, the stable rank of each assignment inside its
@@ -28,6 +30,24 @@ constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
 constexpr int kRouteWarps = 8;
 
+// Order-preserving key of a (logit, expert) pair: larger logit first, equal
+// logits -> lower expert first.  Lanes with no expert get key 0, below every
+// real key (also below -inf logits).
+__device__ __forceinline__ uint64_t route_key(float v, int e) {
+  uint32_t u = __float_as_uint(v);
+  if (u == 0x80000000u) u = 0u;  // -0 ranks equal to +0
+  const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((uint64_t)ord << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)e);
+}
+__device__ __forceinline__ float key_value(uint64_t key) {
+  const uint32_t ord = (uint32_t)(key >> 32);
+  return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
+}
+__device__ __forceinline__ int key_expert(uint64_t key) { return (int)(0xFFFFFFFFu - (uint32_t)key); }
+
+// One warp per token, all selection state in registers: k rounds of a warp
+// arg-max over packed keys; then lane j < k computes exp(l_j - l_max) and the
+// warp sum gives the renormalised weights.
 __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
     const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ ids, float* __restrict__ w,
     int32_t* __restrict__ block_counts) {
@@ -37,57 +57,46 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
   __syncthreads();
   const int64_t t0 = (int64_t)blockIdx.x * kRouteTokensPerBlock;
   const int64_t t1 = min(T, t0 + kRouteTokensPerBlock);
+  const int per_lane = (E + 31) / 32;
   for (int64_t t = t0 + warp; t < t1; t += kRouteWarps) {
-    float v[kMaxExperts / 32];
+    uint64_t key[kMaxExperts / 32];
 #pragma unroll
     for (int i = 0; i < kMaxExperts / 32; ++i) {
       const int e = i * 32 + lane;
-      v[i] = e < E ? logits[t * E + e] : -INFINITY;
+      key[i] = (i < per_lane && e < E) ? route_key(__ldg(logits + t * E + e), e) : 0ull;
     }
-    uint32_t taken = 0;  // bit i: expert i*32+lane already chosen
-    float sel_l[kMaxTopK];
-    int sel_e[kMaxTopK];
-    for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int be = 0x7FFFFFFF;
+    uint64_t mine = 0ull;  // lane j keeps the j-th selected key
 #pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; ++i) {
-        const int e = i * 32 + lane;
-        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || be == 0x7FFFFFFF)) {
-          bv = v[i];
-          be = e;
-        }
-      }
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j >= k) break;
+      uint64_t best = 0ull;
+#pragma unroll
+      for (int i = 0; i < kMaxExperts / 32; ++i) best = key[i] > best ? key[i] : best;
 #pragma unroll
       for (int o = 16; o; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be) || be == 0x7FFFFFFF) {
-          if (oe != 0x7FFFFFFF) {
-            bv = ov;
-            be = oe;
-          }
-        }
+        const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+        best = other > best ? other : best;
       }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      sel_l[j] = bv;
-      sel_e[j] = be;
+#pragma unroll
+      for (int i = 0; i < kMaxExperts / 32; ++i)
+        if (key[i] == best) key[i] = 0ull;  // keys are unique: only the winner's lane matches
+      if (lane == j) mine = best;
     }
-    if (lane == 0) {
-      float z[kMaxTopK], sum = 0.f;
-      for (int j = 0; j < k; ++j) {
-        z[j] = expf(sel_l[j] - sel_l[0]);
-        sum += z[j];
-      }
-      for (int j = 0; j < k; ++j) {
-        ids[t * k + j] = sel_e[j];
-        w[t * k + j] = z[j] / sum;
-        atomicAdd(&hist[sel_e[j]], 1);
-      }
+    const uint64_t top = __shfl_sync(0xffffffffu, mine, 0);
+    const float z = lane < k ? expf(key_value(mine) - key_value(top)) : 0.f;
+    float sum = z;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane < k) {
+      const int e = key_expert(mine);
+      ids[t * k + lane] = e;
+      w[t * k + lane] = z / sum;
+      atomicAdd(&hist[e], 1);
     }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) block_counts[(int64_t)blockIdx.x * E + e] = hist[e];
+  // expert-major: block_counts[e][block]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) block_counts[(int64_t)e * gridDim.x + blockIdx.x] = hist[e];
 }
 
 __global__ void __launch_bounds__(1024) slot_scan_kernel(int32_t* __restrict__ block_counts, int nblocks, int E,
@@ -100,29 +109,40 @@ __global__ void __launch_bounds__(1024) slot_scan_kernel(int32_t* __restrict__ b
   __shared__ int32_t s_cnt[kMaxExperts];
   for (int i = threadIdx.x; i < n_zero_words; i += blockDim.x) zero_words[i] = 0u;
   __shared__ int32_t s_off[kMaxExperts + 1];
-  // one warp per expert: exclusive scan over the route blocks, in place
+  // one warp per expert: exclusive scan over the route blocks, in place, on the
+  // expert-major histograms; each lane loads kScanPerLane consecutive counts at
+  // once so the loads overlap instead of forming a dependent chain
+  constexpr int kScanPerLane = 16;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const int chunk = (nblocks + 31) / 32;  // consecutive blocks per lane
   for (int e = warp; e < E; e += nwarps) {
-    const int b0 = min(nblocks, lane * chunk), b1 = min(nblocks, b0 + chunk);
-    int local = 0;
-    for (int b = b0; b < b1; ++b) local += block_counts[(int64_t)b * E + e];
-    int incl = local;
+    int32_t* row = block_counts + (int64_t)e * nblocks;
+    int carry = 0;
+    for (int base = 0; base < nblocks; base += 32 * kScanPerLane) {
+      const int b0 = base + lane * kScanPerLane;
+      int v[kScanPerLane];
+      int local = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
+      for (int i = 0; i < kScanPerLane; ++i) {
+        v[i] = b0 + i < nblocks ? row[b0 + i] : 0;
+        local += v[i];
+      }
+      int incl = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+      }
+      int run = carry + incl - local;
+#pragma unroll
+      for (int i = 0; i < kScanPerLane; ++i) {
+        if (b0 + i < nblocks) row[b0 + i] = run;
+        run += v[i];
+      }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    int run = incl - local;
-    for (int b = b0; b < b1; ++b) {
-      const int c = block_counts[(int64_t)b * E + e];
-      block_counts[(int64_t)b * E + e] = run;
-      run += c;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
     if (lane == 0) {
-      s_cnt[e] = total;
-      counts[e] = total;
+      s_cnt[e] = carry;
+      counts[e] = carry;
     }
   }
   __syncthreads();
@@ -163,7 +183,7 @@ __global__ void __launch_bounds__(256) slot_scatter_kernel(const int32_t* __rest
   __shared__ int32_t warp_cnt[8][kMaxExperts];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    running[e] = block_base[(int64_t)blockIdx.x * E + e] + offsets[e];
+    running[e] = block_base[(int64_t)e * gridDim.x + blockIdx.x] + offsets[e];
 #pragma unroll
     for (int q = 0; q < 8; ++q) warp_cnt[q][e] = 0;
   }

@@ -134,3 +134,24 @@ def test_device_calibration_matches_oracle_scales():
     np.testing.assert_array_equal(host(a1), orc.a1_gs)
     np.testing.assert_allclose(host(a2), orc.a2_gs, rtol=1e-2)
     assert host(a1)[3] == 1.0 and host(a2)[3] == 1.0  # the expert with no rows
+
+
+def test_routing_ties_and_signed_zero_match_oracle():
+    """Exactly equal logits go to the lower expert; -0 and +0 rank as equal."""
+    import torch
+    wl = W.moe_workload(40, 256, 128, 40, 8, 5)
+    lg = wl.logits.copy()
+    lg[0, :] = 1.5                       # all tied
+    lg[1, 7] = lg[1, 3] = lg[1, 30] = 4.0  # a three-way tie at the top
+    lg[2, :] = 0.0
+    lg[2, 5] = -0.0
+    lg[2, 9] = -0.0                      # zeros of both signs
+    lg[3, 20:] = -np.inf                 # only 20 finite candidates
+    wl.logits = np.ascontiguousarray(lg, np.float32)
+    orc = OracleMoE(wl)
+    w, fwd, out = run_gpu(wl, orc)
+    ids = host(fwd.view("topk_ids", torch.int32, wl.T * wl.top_k)).reshape(wl.T, wl.top_k)
+    np.testing.assert_array_equal(ids, orc.ids)
+    assert ids[0].tolist() == list(range(8)) and ids[1, :3].tolist() == [3, 7, 30]
+    wts = host(fwd.view("topk_w", torch.float32, wl.T * wl.top_k)).reshape(wl.T, wl.top_k)
+    np.testing.assert_allclose(wts, orc.w, rtol=1e-6, atol=1e-7)
