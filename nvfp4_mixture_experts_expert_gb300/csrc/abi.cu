@@ -391,26 +391,26 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
   if ((e = launch_route_topk(router_logits, T, E, top_k, ids, wts, bcnt, s)) != cudaSuccess)
     return cuda_fail(e, "route launch");
   stage_mark(1, s);
-  if ((e = launch_slot_scan(bcnt, nb, E, counts, offsets, meta, tile_expert, sorted_ids, row_w, nullptr, 0, s)) !=
+  if ((e = launch_slot_scan(bcnt, nb, E, counts, offsets, meta, tile_expert, sorted_ids, row_w, nullptr, 0, s, true)) !=
       cudaSuccess)
     return cuda_fail(e, "slot scan launch");
   stage_mark(2, s);
-  if ((e = launch_slot_scatter(ids, wts, T, E, top_k, bcnt, offsets, sorted_ids, row_w, inverse, s)) !=
+  if ((e = launch_slot_scatter(ids, wts, T, E, top_k, bcnt, offsets, sorted_ids, row_w, inverse, s, true)) !=
       cudaSuccess)
     return cuda_fail(e, "slot scatter launch");
   stage_mark(3, s);
   if ((e = launch_gather_quantize((const uint16_t*)hidden, H, sorted_ids, tile_expert, meta, a1_gs, cap, a1, sfa1,
-                                  dev->sms, s)) != cudaSuccess)
+                                  dev->sms, s, true)) != cudaSuccess)
     return cuda_fail(e, "gather launch");
   stage_mark(4, s);
   const int64_t t1 = cap / 128 * g1.n_tiles, t2 = cap / 128 * g2.n_tiles;
-  if ((e = launch_gemm(kEpiSwigluQuant, g1, (int)(t1 < dev->sms ? t1 : dev->sms), s)) != cudaSuccess)
+  if ((e = launch_gemm(kEpiSwigluQuant, g1, (int)(t1 < dev->sms ? t1 : dev->sms), s, true)) != cudaSuccess)
     return cuda_fail(e, "L1 launch");
   stage_mark(5, s);
-  if ((e = launch_gemm(kEpiCombine, g2, (int)(t2 < dev->sms ? t2 : dev->sms), s)) != cudaSuccess)
+  if ((e = launch_gemm(kEpiCombine, g2, (int)(t2 < dev->sms ? t2 : dev->sms), s, true)) != cudaSuccess)
     return cuda_fail(e, "L2 launch");
   stage_mark(6, s);
-  if ((e = launch_token_combine(ybuf, inverse, T, H, top_k, (uint16_t*)out, s)) != cudaSuccess)
+  if ((e = launch_token_combine(ybuf, inverse, T, H, top_k, (uint16_t*)out, s, true)) != cudaSuccess)
     return cuda_fail(e, "combine launch");
   stage_mark(7, s);
   return NVFP4_OK;

@@ -387,6 +387,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid
   extern __shared__ uint8_t smem_raw[];
   const SmemLayout L = carve(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&L.full[s]), 1);
@@ -400,6 +401,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid
     *L.abort_flag = 0;
     fence_mbar_init();
   }
+  pdl_wait();  // everything below reads what earlier kernels wrote
   for (int i = threadIdx.x; i <= p.G; i += blockDim.x) L.offsets[i] = p.padded_offsets[i];
   if (warp == 1) {
     tmem_alloc(smem_u32(L.tmem_slot), TMEM_COLS);
@@ -433,7 +435,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid
 }
 
 template <int EPI>
-cudaError_t launch_one(const GemmArgs& a, int grid, cudaStream_t s) {
+cudaError_t launch_one(const GemmArgs& a, int grid, cudaStream_t s, bool pdl) {
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -444,8 +446,7 @@ cudaError_t launch_one(const GemmArgs& a, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  nvfp4_gemm_kernel<EPI><<<grid, NUM_THREADS, gemm_smem_bytes(a.G), s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(nvfp4_gemm_kernel<EPI>, dim3(grid), dim3(NUM_THREADS), gemm_smem_bytes(a.G), s, pdl, a);
 }
 
 }  // namespace
@@ -454,13 +455,13 @@ size_t gemm_smem_bytes(int G) {
   return 1024 + (size_t)STAGES * STAGE_BYTES + 8 * (3 * STAGES + 4) + 16 + 4 * (size_t)(G + 1) + 16;
 }
 
-cudaError_t launch_gemm(int kind, const GemmArgs& args, int grid, cudaStream_t s) {
+cudaError_t launch_gemm(int kind, const GemmArgs& args, int grid, cudaStream_t s, bool pdl) {
   if (args.G < 1 || args.G > MAX_GROUPS) return cudaErrorInvalidValue;
   switch (kind) {
-    case kEpiBf16: return launch_one<kEpiBf16>(args, grid, s);
-    case kEpiSwigluQuant: return launch_one<kEpiSwigluQuant>(args, grid, s);
-    case kEpiCombine: return launch_one<kEpiCombine>(args, grid, s);
-    case kEpiSwigluAmax: return launch_one<kEpiSwigluAmax>(args, grid, s);
+    case kEpiBf16: return launch_one<kEpiBf16>(args, grid, s, pdl);
+    case kEpiSwigluQuant: return launch_one<kEpiSwigluQuant>(args, grid, s, pdl);
+    case kEpiCombine: return launch_one<kEpiCombine>(args, grid, s, pdl);
+    case kEpiSwigluAmax: return launch_one<kEpiSwigluAmax>(args, grid, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -8,6 +8,24 @@
 
 namespace nvfp4 {
 
+// Launch with optional programmatic stream serialization (the kernel must call
+// pdl_wait() before touching global memory when pdl is set).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                          Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? at : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------- quant.cu
 // Per-group amax of bf16 rows into partial maxima, then gs = 2688/amax.
 constexpr int kAmaxBlocksPerGroup = 128;
@@ -22,7 +40,8 @@ cudaError_t launch_assemble_scales(const uint8_t* sf_linear, int64_t sf_cols, co
 // MoE: gather hidden rows into expert slots and quantize them (one slot row per thread group).
 cudaError_t launch_gather_quantize(const uint16_t* hidden, int64_t H, const int32_t* sorted_ids,
                                    const int32_t* tile_expert, const int32_t* meta, const float* a1_gs,
-                                   int64_t capacity, uint8_t* a1, uint8_t* sfa1, int num_sms, cudaStream_t s);
+                                   int64_t capacity, uint8_t* a1, uint8_t* sfa1, int num_sms, cudaStream_t s,
+                                   bool pdl = false);
 // Calibration: per-expert amax of the gathered hidden rows (as float bits, atomicMax
 // into a zeroed array), and gs = 2688/amax (1 for an empty / all-zero expert).
 cudaError_t launch_gather_amax(const uint16_t* hidden, int64_t H, const int32_t* sorted_ids,
@@ -36,13 +55,13 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int3
                               int32_t* block_counts, cudaStream_t s);
 cudaError_t launch_slot_scan(int32_t* block_counts, int nblocks, int E, int32_t* counts, int32_t* offsets,
                              int32_t* meta, int32_t* tile_expert, int32_t* sorted_ids, float* row_w,
-                             uint32_t* zero_words, int n_zero_words, cudaStream_t s);
+                             uint32_t* zero_words, int n_zero_words, cudaStream_t s, bool pdl = false);
 cudaError_t launch_slot_scatter(const int32_t* ids, const float* w, int64_t T, int E, int k,
                                 const int32_t* block_base, const int32_t* offsets, int32_t* sorted_ids,
-                                float* row_w, int32_t* inverse, cudaStream_t s);
+                                float* row_w, int32_t* inverse, cudaStream_t s, bool pdl = false);
 // out[t] = bf16( sum_j Y[inverse[t*k + j]] ), j ascending, FP32 sum.
 cudaError_t launch_token_combine(const uint16_t* y, const int32_t* inverse, int64_t T, int64_t H, int k,
-                                 uint16_t* out, cudaStream_t s);
+                                 uint16_t* out, cudaStream_t s, bool pdl = false);
 
 // ---------------------------------------------------------------- gemm.cu
 enum EpilogueKind { kEpiBf16 = 0, kEpiSwigluQuant = 1, kEpiCombine = 2, kEpiSwigluAmax = 3 };
@@ -93,7 +112,7 @@ size_t gemm_smem_bytes(int G);
 
 // abi.cu: sets the text nvfp4_last_error() returns on the calling thread.
 void set_last_error(const char* msg);
-cudaError_t launch_gemm(int kind, const GemmArgs& args, int grid, cudaStream_t s);
+cudaError_t launch_gemm(int kind, const GemmArgs& args, int grid, cudaStream_t s, bool pdl = false);
 cudaError_t gemm_status_ptr(int** ptr);
 cudaError_t gemm_read_status(int* out, int reset);
 

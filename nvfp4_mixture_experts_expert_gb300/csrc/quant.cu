@@ -11,6 +11,7 @@
 
 #include "internal.h"
 #include "nvfp4_format.cuh"
+#include "ptx.cuh"
 
 namespace nvfp4 {
 
@@ -165,6 +166,8 @@ __global__ void __launch_bounds__(256) gather_quantize_kernel(const uint16_t* __
                                                               const int32_t* __restrict__ meta,
                                                               const float* __restrict__ a1_gs, int64_t capacity,
                                                               uint8_t* __restrict__ a1, uint8_t* __restrict__ sfa1) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t chunks = H / 64;
   const int64_t P = meta[0];
   const int64_t total = min(P, capacity) * chunks;
@@ -260,12 +263,12 @@ cudaError_t launch_assemble_scales(const uint8_t* sf_linear, int64_t sf_cols, co
 
 cudaError_t launch_gather_quantize(const uint16_t* hidden, int64_t H, const int32_t* sorted_ids,
                                    const int32_t* tile_expert, const int32_t* meta, const float* a1_gs,
-                                   int64_t capacity, uint8_t* a1, uint8_t* sfa1, int num_sms, cudaStream_t s) {
+                                   int64_t capacity, uint8_t* a1, uint8_t* sfa1, int num_sms, cudaStream_t s,
+                                   bool pdl) {
   const int64_t items = capacity * (H / 64);
   const int grid = grid_for(items, 256, num_sms, 8);
-  gather_quantize_kernel<<<grid, 256, 0, s>>>(hidden, H, sorted_ids, tile_expert, meta, a1_gs, capacity, a1,
-                                              sfa1);
-  return cudaGetLastError();
+  return launch_kernel(gather_quantize_kernel, dim3(grid), dim3(256), 0, s, pdl, hidden, H, sorted_ids, tile_expert,
+                       meta, a1_gs, capacity, a1, sfa1);
 }
 
 cudaError_t launch_gather_amax(const uint16_t* hidden, int64_t H, const int32_t* sorted_ids,

@@ -21,6 +21,7 @@
 
 #include "internal.h"
 #include "nvfp4_format.cuh"
+#include "ptx.cuh"
 
 namespace nvfp4 {
 
@@ -51,6 +52,7 @@ __device__ __forceinline__ int key_expert(uint64_t key) { return (int)(0xFFFFFFF
 __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
     const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ ids, float* __restrict__ w,
     int32_t* __restrict__ block_counts) {
+  pdl_trigger();
   __shared__ int32_t hist[kMaxExperts];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
@@ -106,6 +108,8 @@ __global__ void __launch_bounds__(1024) slot_scan_kernel(int32_t* __restrict__ b
                                                          int32_t* __restrict__ sorted_ids,
                                                          float* __restrict__ row_w,
                                                          uint32_t* __restrict__ zero_words, int n_zero_words) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int32_t s_cnt[kMaxExperts];
   for (int i = threadIdx.x; i < n_zero_words; i += blockDim.x) zero_words[i] = 0u;
   __shared__ int32_t s_off[kMaxExperts + 1];
@@ -179,6 +183,8 @@ __global__ void __launch_bounds__(256) slot_scatter_kernel(const int32_t* __rest
                                                            const int32_t* __restrict__ offsets,
                                                            int32_t* __restrict__ sorted_ids,
                                                            float* __restrict__ row_w, int32_t* __restrict__ inverse) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int32_t running[kMaxExperts];
   __shared__ int32_t warp_cnt[8][kMaxExperts];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -224,6 +230,7 @@ __global__ void __launch_bounds__(256) slot_scatter_kernel(const int32_t* __rest
 __global__ void __launch_bounds__(256) token_combine_kernel(const uint16_t* __restrict__ y,
                                                             const int32_t* __restrict__ inverse, int64_t H, int k,
                                                             uint16_t* __restrict__ out) {
+  pdl_wait();
   const int64_t t = blockIdx.x;
   __shared__ int32_t rows[kMaxTopK];
   if (threadIdx.x < k) rows[threadIdx.x] = inverse[t * k + threadIdx.x];
@@ -255,25 +262,23 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int3
 
 cudaError_t launch_slot_scan(int32_t* block_counts, int nblocks, int E, int32_t* counts, int32_t* offsets,
                              int32_t* meta, int32_t* tile_expert, int32_t* sorted_ids, float* row_w,
-                             uint32_t* zero_words, int n_zero_words, cudaStream_t s) {
-  slot_scan_kernel<<<1, 1024, 0, s>>>(block_counts, nblocks, E, counts, offsets, meta, tile_expert, sorted_ids,
-                                      row_w, zero_words, n_zero_words);
-  return cudaGetLastError();
+                             uint32_t* zero_words, int n_zero_words, cudaStream_t s, bool pdl) {
+  return launch_kernel(slot_scan_kernel, dim3(1), dim3(1024), 0, s, pdl, block_counts, nblocks, E, counts, offsets,
+                       meta, tile_expert, sorted_ids, row_w, zero_words, n_zero_words);
 }
 
 cudaError_t launch_slot_scatter(const int32_t* ids, const float* w, int64_t T, int E, int k,
                                 const int32_t* block_base, const int32_t* offsets, int32_t* sorted_ids,
-                                float* row_w, int32_t* inverse, cudaStream_t s) {
+                                float* row_w, int32_t* inverse, cudaStream_t s, bool pdl) {
   const int64_t nb = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
-  slot_scatter_kernel<<<(unsigned)nb, 256, 0, s>>>(ids, w, T, E, k, block_base, offsets, sorted_ids, row_w,
-                                                   inverse);
-  return cudaGetLastError();
+  return launch_kernel(slot_scatter_kernel, dim3((unsigned)nb), dim3(256), 0, s, pdl, ids, w, T, E, k, block_base,
+                       offsets, sorted_ids, row_w, inverse);
 }
 
 cudaError_t launch_token_combine(const uint16_t* y, const int32_t* inverse, int64_t T, int64_t H, int k,
-                                 uint16_t* out, cudaStream_t s) {
-  if (T > 0) token_combine_kernel<<<(unsigned)T, 256, 0, s>>>(y, inverse, H, k, out);
-  return cudaGetLastError();
+                                 uint16_t* out, cudaStream_t s, bool pdl) {
+  if (T == 0) return cudaSuccess;
+  return launch_kernel(token_combine_kernel, dim3((unsigned)T), dim3(256), 0, s, pdl, y, inverse, H, k, out);
 }
 
 }  // namespace nvfp4
