@@ -151,6 +151,21 @@ int nvfp4_grouped_gemm(const void* A, const void* SFA, const float* a_gs, const 
                        void* stream);
 
 /*
+ * nvfp4_debug_gemm_stall -- failure-detection check of the GEMM pipeline
+ * (no counterpart on the pages; it exercises the bounded waits).
+ * Launches nvfp4_grouped_gemm's kernel on the given (valid) operands with its
+ * TMA producer switched off, so nothing ever fills the shared-memory ring:
+ * the consumers' waits give up after timeout_ms, the kernel records
+ * NVFP4_ERR_DEVICE_TIMEOUT in the device status word, frees its tensor
+ * memory and returns, leaving the context usable.  D is not written.
+ * Arguments as nvfp4_grouped_gemm (counts = NULL, group_stride_d = 0);
+ * 1 <= timeout_ms <= 10000.  Read the result with nvfp4_device_status().
+ */
+int nvfp4_debug_gemm_stall(const void* A, const void* SFA, const float* a_gs, const void* B, const void* SFB,
+                           const float* b_gs, const int32_t* padded_offsets, int groups, int64_t rows_capacity,
+                           int64_t N, int64_t K, void* D, int64_t ldd, int timeout_ms, void* stream);
+
+/*
  * nvfp4_moe_forward -- the NVFP4 mixture-of-experts FFN forward
  * (vllm page: the MoE runner -- 128-row slots, multi-chunk slots "Bug 9",
  * sorted_token_ids gather, quantize_activation_nvfp4 with calibrated global

@@ -69,6 +69,8 @@ _quantize_no_alloc = _sig("nvfp4_quantize_no_alloc", c_int, [c_ptr, c_i64, c_i64
 _assemble = _sig("nvfp4_assemble_scales", c_int, [c_ptr, c_i64, c_ptr, c_ptr, c_int, c_i64, c_ptr, c_ptr])
 _gemm = _sig("nvfp4_grouped_gemm", c_int, [c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_int, c_i64,
                                            c_i64, c_i64, c_ptr, c_i64, c_i64, c_ptr])
+_gemm_stall = _sig("nvfp4_debug_gemm_stall", c_int, [c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_int, c_i64,
+                                                      c_i64, c_i64, c_ptr, c_i64, c_int, c_ptr])
 _moe_ws = _sig("nvfp4_moe_workspace_size", c_size, [c_i64, c_i64, c_i64, c_int, c_int])
 _moe_layout = _sig("nvfp4_moe_workspace_layout", c_int, [c_i64, c_i64, c_i64, c_int, c_int,
                                                          ctypes.POINTER(MoeLayout)])
@@ -152,6 +154,12 @@ def nvfp4_grouped_gemm(A, SFA, a_gs, B, SFB, b_gs, padded_offsets, counts, group
                        group_stride_d, stream=None):
     _check(_gemm(_p(A), _p(SFA), _p(a_gs), _p(B), _p(SFB), _p(b_gs), _p(padded_offsets), _p(counts), groups,
                  rows_capacity, N, K, _p(D), ldd, group_stride_d, _stream(stream)))
+
+
+def nvfp4_debug_gemm_stall(A, SFA, a_gs, B, SFB, b_gs, padded_offsets, groups, rows_capacity, N, K, D, ldd,
+                           timeout_ms, stream=None):
+    _check(_gemm_stall(_p(A), _p(SFA), _p(a_gs), _p(B), _p(SFB), _p(b_gs), _p(padded_offsets), groups,
+                       rows_capacity, N, K, _p(D), ldd, timeout_ms, _stream(stream)))
 
 
 def nvfp4_moe_workspace_size(T, H, I, E, top_k):

@@ -119,6 +119,56 @@ inline void stage_mark(int i, cudaStream_t s) {
 
 void nvfp4::set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg ? msg : ""); }
 
+static int grouped_gemm_impl(const void* A, const void* SFA, const float* a_gs, const void* B, const void* SFB,
+                             const float* b_gs, const int32_t* padded_offsets, const int32_t* counts, int groups,
+                             int64_t rows_capacity, int64_t N, int64_t K, void* D, int64_t ldd,
+                             int64_t group_stride_d, void* stream, int debug_no_loads, uint64_t timeout_ns) {
+  g_err[0] = 0;
+  if (groups < 1 || groups > 1024) return fail(NVFP4_ERR_INVALID_ARG, "groups must be in [1, 1024]");
+  if (K <= 0 || K % 64) return fail(NVFP4_ERR_INVALID_ARG, "K must be a positive multiple of 64");
+  if (N <= 0 || N % 256) return fail(NVFP4_ERR_UNSUPPORTED, "N must be a positive multiple of 256");
+  if (rows_capacity < 0 || rows_capacity % 128) return fail(NVFP4_ERR_INVALID_ARG, "rows_capacity % 128 != 0");
+  if (ldd % 8 || group_stride_d % 8 || ldd < 0 || group_stride_d < 0)
+    return fail(NVFP4_ERR_INVALID_ARG, "ldd and group_stride_d must be non-negative multiples of 8");
+  if (!A || !SFA || !a_gs || !B || !SFB || !b_gs || !padded_offsets || !D)
+    return fail(NVFP4_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(A) || !aligned16(SFA) || !aligned16(B) || !aligned16(SFB) || !aligned16(D))
+    return fail(NVFP4_ERR_INVALID_ARG, "A, SFA, B, SFB and D must be 16-byte aligned");
+  if ((int64_t)groups * N > INT32_MAX || rows_capacity > INT32_MAX)
+    return fail(NVFP4_ERR_UNSUPPORTED, "row counts beyond 2^31");
+  DeviceInfo* dev = nullptr;
+  if (int rc = device_info(&dev)) return rc;
+  if (rows_capacity == 0) return NVFP4_OK;
+  GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  if (int rc = make_fp4_map(&a.tmap_a, A, rows_capacity, K)) return rc;
+  if (int rc = make_fp4_map(&a.tmap_b, B, (int64_t)groups * N, K)) return rc;
+  a.sfa = (const uint8_t*)SFA;
+  a.sfb = (const uint8_t*)SFB;
+  a.padded_offsets = padded_offsets;
+  a.counts = counts;
+  a.a_gs = a_gs;
+  a.b_gs = b_gs;
+  a.G = groups;
+  a.K = (int)K;
+  a.num_kb = (int)((K + 255) / 256);
+  a.b_rows_per_group = (int)N;
+  a.n_tiles = (int)(N / 256);
+  a.b_second_offset = 128;
+  a.b_tile_stride = 256;
+  a.sfb_group_bytes = N * (K / 16);
+  a.D = (uint16_t*)D;
+  a.ldd = ldd;
+  a.gstride_d = group_stride_d;
+  a.status = dev->status;
+  a.timeout_ns = timeout_ns;
+  a.debug_no_loads = debug_no_loads;
+  const int64_t max_tiles = rows_capacity / 128 * a.n_tiles;
+  const int grid = (int)(max_tiles < dev->sms ? max_tiles : dev->sms);
+  cudaError_t e = launch_gemm(kEpiBf16, a, grid, (cudaStream_t)stream);
+  return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "gemm launch");
+}
+
 extern "C" {
 
 int nvfp4_version(void) { return 100; }
@@ -201,49 +251,17 @@ int nvfp4_grouped_gemm(const void* A, const void* SFA, const float* a_gs, const 
                        const float* b_gs, const int32_t* padded_offsets, const int32_t* counts, int groups,
                        int64_t rows_capacity, int64_t N, int64_t K, void* D, int64_t ldd, int64_t group_stride_d,
                        void* stream) {
+  return grouped_gemm_impl(A, SFA, a_gs, B, SFB, b_gs, padded_offsets, counts, groups, rows_capacity, N, K, D, ldd,
+                           group_stride_d, stream, 0, 2000000000ull);
+}
+
+int nvfp4_debug_gemm_stall(const void* A, const void* SFA, const float* a_gs, const void* B, const void* SFB,
+                           const float* b_gs, const int32_t* padded_offsets, int groups, int64_t rows_capacity,
+                           int64_t N, int64_t K, void* D, int64_t ldd, int timeout_ms, void* stream) {
   g_err[0] = 0;
-  if (groups < 1 || groups > 1024) return fail(NVFP4_ERR_INVALID_ARG, "groups must be in [1, 1024]");
-  if (K <= 0 || K % 64) return fail(NVFP4_ERR_INVALID_ARG, "K must be a positive multiple of 64");
-  if (N <= 0 || N % 256) return fail(NVFP4_ERR_UNSUPPORTED, "N must be a positive multiple of 256");
-  if (rows_capacity < 0 || rows_capacity % 128) return fail(NVFP4_ERR_INVALID_ARG, "rows_capacity % 128 != 0");
-  if (ldd % 8 || group_stride_d % 8 || ldd < 0 || group_stride_d < 0)
-    return fail(NVFP4_ERR_INVALID_ARG, "ldd and group_stride_d must be non-negative multiples of 8");
-  if (!A || !SFA || !a_gs || !B || !SFB || !b_gs || !padded_offsets || !D)
-    return fail(NVFP4_ERR_INVALID_ARG, "null pointer");
-  if (!aligned16(A) || !aligned16(SFA) || !aligned16(B) || !aligned16(SFB) || !aligned16(D))
-    return fail(NVFP4_ERR_INVALID_ARG, "A, SFA, B, SFB and D must be 16-byte aligned");
-  if ((int64_t)groups * N > INT32_MAX || rows_capacity > INT32_MAX)
-    return fail(NVFP4_ERR_UNSUPPORTED, "row counts beyond 2^31");
-  DeviceInfo* dev = nullptr;
-  if (int rc = device_info(&dev)) return rc;
-  if (rows_capacity == 0) return NVFP4_OK;
-  GemmArgs a;
-  memset(&a, 0, sizeof(a));
-  if (int rc = make_fp4_map(&a.tmap_a, A, rows_capacity, K)) return rc;
-  if (int rc = make_fp4_map(&a.tmap_b, B, (int64_t)groups * N, K)) return rc;
-  a.sfa = (const uint8_t*)SFA;
-  a.sfb = (const uint8_t*)SFB;
-  a.padded_offsets = padded_offsets;
-  a.counts = counts;
-  a.a_gs = a_gs;
-  a.b_gs = b_gs;
-  a.G = groups;
-  a.K = (int)K;
-  a.num_kb = (int)((K + 255) / 256);
-  a.b_rows_per_group = (int)N;
-  a.n_tiles = (int)(N / 256);
-  a.b_second_offset = 128;
-  a.b_tile_stride = 256;
-  a.sfb_group_bytes = N * (K / 16);
-  a.D = (uint16_t*)D;
-  a.ldd = ldd;
-  a.gstride_d = group_stride_d;
-  a.status = dev->status;
-  a.timeout_ns = 2000000000ull;
-  const int64_t max_tiles = rows_capacity / 128 * a.n_tiles;
-  const int grid = (int)(max_tiles < dev->sms ? max_tiles : dev->sms);
-  cudaError_t e = launch_gemm(kEpiBf16, a, grid, (cudaStream_t)stream);
-  return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "gemm launch");
+  if (timeout_ms < 1 || timeout_ms > 10000) return fail(NVFP4_ERR_INVALID_ARG, "timeout_ms must be in [1, 10000]");
+  return grouped_gemm_impl(A, SFA, a_gs, B, SFB, b_gs, padded_offsets, nullptr, groups, rows_capacity, N, K, D, ldd,
+                           0, stream, 1, (uint64_t)timeout_ms * 1000000ull);
 }
 
 int nvfp4_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int E, int top_k, nvfp4_moe_layout* out) {

@@ -111,3 +111,25 @@ def test_gemm_device_status_is_clean():
     pb = make_problem([64], 256, 256, seed=2)
     run_gpu(pb)
     assert B.nvfp4_device_status(reset=False) == 0
+
+
+def test_stalled_pipeline_reports_timeout_and_context_survives():
+    """Failure detection without a fault: with the TMA producer switched off the
+    consumers' bounded waits run out, the kernel reports a device timeout,
+    frees its tensor memory and returns; the same process then runs a correct
+    GEMM with a clean status."""
+    import time
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import binding as B
+    pb = make_problem([128], 256, 256, seed=4)
+    B.nvfp4_device_status(reset=True)
+    D = torch.zeros((128, 256), dtype=torch.bfloat16, device="cuda")
+    t0 = time.time()
+    B.nvfp4_debug_gemm_stall(dev(pb["A"]), dev(pb["SFA"]), dev(pb["a_gs"]), dev(pb["B"]), dev(pb["SFB"]),
+                             dev(pb["b_gs"]), dev(pb["padded"]), 1, pb["cap"], 256, 256, D, 256, 200)
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 30
+    assert B.nvfp4_device_status(reset=True) == B.NVFP4_ERR_DEVICE_TIMEOUT
+    assert not D.any()  # nothing was stored
+    check(pb, run_gpu(pb))  # the context still works and the result is right
+    assert B.nvfp4_device_status() == 0
