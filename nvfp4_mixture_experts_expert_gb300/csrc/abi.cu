@@ -158,6 +158,7 @@ static int grouped_gemm_impl(const void* A, const void* SFA, const float* a_gs, 
   a.b_tile_stride = 256;
   a.sfb_group_bytes = N * (K / 16);
   a.D = (uint16_t*)D;
+  a.d_vec32 = (reinterpret_cast<uintptr_t>(D) & 31u) == 0 && ldd % 16 == 0 && group_stride_d % 16 == 0;
   a.ldd = ldd;
   a.gstride_d = group_stride_d;
   a.status = dev->status;
@@ -417,8 +418,8 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
       cudaSuccess)
     return cuda_fail(e, "slot scatter launch");
   stage_mark(3, s);
-  if ((e = launch_gather_quantize((const uint16_t*)hidden, H, sorted_ids, tile_expert, meta, a1_gs, cap, a1, sfa1,
-                                  dev->sms, s, true)) != cudaSuccess)
+  if ((e = launch_gather_quantize((const uint16_t*)hidden, H, T, top_k, ids, inverse, counts, offsets, E, a1_gs,
+                                  cap, a1, sfa1, s, true)) != cudaSuccess)
     return cuda_fail(e, "gather launch");
   stage_mark(4, s);
   const int64_t t1 = cap / 128 * g1.n_tiles, t2 = cap / 128 * g2.n_tiles;
@@ -517,8 +518,8 @@ int nvfp4_moe_calibrate(const void* hidden, const float* router_logits, int64_t 
       (e = launch_gather_amax((const uint16_t*)hidden, H, sorted_ids, tile_expert, meta, cap, amax, dev->sms, s)) !=
           cudaSuccess ||
       (e = launch_gs_from_amax(amax, E, a1_gs_out, s)) != cudaSuccess ||
-      (e = launch_gather_quantize((const uint16_t*)hidden, H, sorted_ids, tile_expert, meta, a1_gs_out, cap, a1,
-                                  sfa1, dev->sms, s)) != cudaSuccess)
+      (e = launch_gather_quantize((const uint16_t*)hidden, H, T, top_k, ids, inverse, counts, offsets, E,
+                                  a1_gs_out, cap, a1, sfa1, s)) != cudaSuccess)
     return cuda_fail(e, "calibration launch");
   const int64_t t1 = cap / 128 * g1.n_tiles;
   if ((e = launch_gemm(kEpiSwigluAmax, g1, (int)(t1 < dev->sms ? t1 : dev->sms), s)) != cudaSuccess ||

@@ -319,9 +319,14 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             pk[j] = pack_bf16x2(__uint_as_float(v[c][2 * j]) * alpha, __uint_as_float(v[c][2 * j + 1]) * alpha);
-          uint4* dst = reinterpret_cast<uint4*>(drow + c * 32);
+          if (p.d_vec32) {
+            st_global_v8(drow + c * 32, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+            st_global_v8(drow + c * 32 + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(drow + c * 32);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          }
         }
       }
     } else if constexpr (EPI == kEpiSwigluQuant) {
@@ -346,9 +351,9 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
         words[blk * 2 + 1] = hi;
       }
       const int64_t f0 = (int64_t)nt * 128 + half * 64;  // first output feature of this thread
-      uint4* dst = reinterpret_cast<uint4*>(p.q_out + row * (p.I / 2) + f0 / 2);
-      dst[0] = make_uint4(words[0], words[1], words[2], words[3]);
-      dst[1] = make_uint4(words[4], words[5], words[6], words[7]);
+      // workspace rows: 32-byte aligned (I/2 and f0/2 are multiples of 32 bytes)
+      st_global_v8(p.q_out + row * (p.I / 2) + f0 / 2, words[0], words[1], words[2], words[3], words[4], words[5],
+                   words[6], words[7]);
       *reinterpret_cast<uint32_t*>(p.q_sf + sf_offset(row, f0 / 16, p.I / 16)) = scales;
     } else if constexpr (EPI == kEpiSwigluAmax) {
       // calibration: amax of the bf16 SwiGLU output of this row's features
@@ -373,9 +378,9 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             pk[j] = pack_bf16x2(__uint_as_float(v[c][2 * j]) * wgt, __uint_as_float(v[c][2 * j + 1]) * wgt);
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) d4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          // workspace rows: 32-byte aligned (H is a multiple of 256)
+          st_global_v8(dst + c * 32, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+          st_global_v8(dst + c * 32 + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
         }
       }
     }

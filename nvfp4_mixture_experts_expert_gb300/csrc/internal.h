@@ -38,10 +38,10 @@ cudaError_t launch_assemble_scales(const uint8_t* sf_linear, int64_t sf_cols, co
                                    const int32_t* padded_offsets, int groups, int64_t rows_capacity,
                                    uint8_t* sf_swz, int num_sms, cudaStream_t s);
 // MoE: gather hidden rows into expert slots and quantize them (one slot row per thread group).
-cudaError_t launch_gather_quantize(const uint16_t* hidden, int64_t H, const int32_t* sorted_ids,
-                                   const int32_t* tile_expert, const int32_t* meta, const float* a1_gs,
-                                   int64_t capacity, uint8_t* a1, uint8_t* sfa1, int num_sms, cudaStream_t s,
-                                   bool pdl = false);
+cudaError_t launch_gather_quantize(const uint16_t* hidden, int64_t H, int64_t T, int top_k,
+                                   const int32_t* topk_ids, const int32_t* inverse, const int32_t* counts,
+                                   const int32_t* offsets, int E, const float* a1_gs, int64_t capacity, uint8_t* a1,
+                                   uint8_t* sfa1, cudaStream_t s, bool pdl = false);
 // Calibration: per-expert amax of the gathered hidden rows (as float bits, atomicMax
 // into a zeroed array), and gs = 2688/amax (1 for an empty / all-zero expert).
 cudaError_t launch_gather_amax(const uint16_t* hidden, int64_t H, const int32_t* sorted_ids,
@@ -88,6 +88,7 @@ struct GemmArgs {
   uint16_t* D;
   int64_t ldd;
   int64_t gstride_d;
+  int d_vec32;  // D, ldd and gstride_d allow 32-byte stores
   // kEpiSwigluQuant
   uint8_t* q_out;
   uint8_t* q_sf;

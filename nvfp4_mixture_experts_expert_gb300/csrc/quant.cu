@@ -2,11 +2,11 @@
 // quantization with scales written straight into the 128x4 tile layout,
 // scale assembly into 128-row padded slots, and the MoE gather+quantize.
 //
-// All kernels are HBM-bound streaming kernels: one thread owns 64
-// consecutive K elements of one row (4 blocks of 16 = one MMA K-step), so a
-// warp reads 4 KB of contiguous bf16 with 16-byte loads, writes 1 KB of
-// contiguous nibbles, and each thread writes its 4 scale codes as one
-// aligned 32-bit word of the tile layout.
+// All kernels are HBM-bound streaming kernels.  The strided quantizer gives
+// one thread 64 consecutive K elements of one row (4 blocks of 16 = one MMA
+// K-step) and writes its 4 scale codes as one aligned 32-bit word of the
+// tile layout.  The MoE gather gives one lane one 16-element block, so each
+// warp load and store is contiguous (see gather_quantize_kernel).
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -160,36 +160,166 @@ __global__ void assemble_scales_kernel(const uint8_t* __restrict__ lin, int64_t 
 }
 
 // ---------------------------------------------------------------- MoE gather + quantize
+// ---------------------------------------------------------------- MoE gather
+// Token-major gather + quantize of the L1 activations.  One warp owns one
+// (token, segment of up to kGatherChunks x 512 elements) item: lane l owns
+// the 16-element block at element 512*c + 16*l of each 512-element chunk c,
+// loads it once with one 32-byte access (the warp reads 1 KB contiguous),
+// and takes the block's max |x| from the bf16 bit patterns (x*gs rounds
+// monotonically in |x|, so max|x*gs| = fl(max|x| * gs)).  It then quantizes
+// the block for each of the token's top_k slot rows with that expert's
+// global scale: 8 bytes of nibbles per lane (256 contiguous bytes per warp)
+// and one 32-bit word of 4 block scales per group of 4 lanes.  The hidden row
+// is read from memory once instead of once per slot.  The trailing warps
+// write the pad rows of every expert's slot range as zero blocks.
+constexpr int kGatherChunks = 2;
+
+// One 16-element bf16 block (32 bytes): a single 32-byte load where the
+// address is 32-byte aligned, else two 16-byte loads (the entry points only
+// promise 16-byte alignment of the hidden states).
+template <bool kAligned32>
+__device__ __forceinline__ void ld_block32(const uint16_t* p, uint32_t (&w)[8]) {
+  if constexpr (kAligned32) {
+    asm("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+        : "l"(p));
+  } else {
+    const uint4 a = ldg_nc(p), b = ldg_nc(p + 8);
+    w[0] = a.x, w[1] = a.y, w[2] = a.z, w[3] = a.w, w[4] = b.x, w[5] = b.y, w[6] = b.z, w[7] = b.w;
+  }
+}
+
+// Packed pairs of FP32 values (element 2j in the low half, 2j+1 in the high
+// half), each half rounded exactly like its scalar operation.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// max |x| over the 16 bf16 values of a block, as an FP32 value.
+__device__ __forceinline__ float block_amax_bf16(const uint32_t (&w)[8]) {
+  uint32_t m = 0u;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) m = __vmaxu2(m, w[q] & 0x7FFF7FFFu);
+  return __uint_as_float(max(m & 0xFFFFu, m >> 16) << 16);
+}
+
+// Quantize one block of 16 bf16 values (raw bits) with global scale gs; the
+// same arithmetic as quant_block16, element pairs at a time.  tab[s] holds
+// (dec(s), RN(1/dec(s))) for every scale code s.
+__device__ __forceinline__ uint32_t quant_block16_bf16(const uint32_t (&w)[8], float amax, float gs, float rcp6,
+                                                       const float2* tab, uint32_t& lo, uint32_t& hi) {
+  lo = hi = 0u;
+  const float b = __fmul_rn(amax, gs);
+  if (!(b >= kUnderflowAmax)) return 0u;
+  // b / 6 with the same exact correction as the element quotients (6 is an E4M3 value)
+  const uint32_t s = e4m3_code(div_by_scale(fminf(b, 3.40282347e38f), 6.0f, rcp6));
+  const float2 dy = tab[s];
+  const uint64_t gs2 = f2_pack(gs, gs), y2 = f2_pack(dy.y, dy.y), nd2 = f2_pack(-dy.x, -dy.x);
+  uint32_t out[2] = {0u, 0u};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint64_t xs = f2_mul(f2_pack(bf16_lo(w[j]), bf16_hi(w[j])), gs2);
+    const uint64_t q0 = f2_mul(xs, y2);
+    const uint64_t r = f2_fma(q0, nd2, xs);
+    float ql, qh;
+    f2_unpack(f2_fma(r, y2, q0), ql, qh);
+    out[j >> 2] |= e2m1x2_code(ql, qh) << ((j & 3) * 8);
+  }
+  lo = drop_negative_zero(out[0]);
+  hi = drop_negative_zero(out[1]);
+  return s;
+}
+
+template <bool kAligned32>
 __global__ void __launch_bounds__(256) gather_quantize_kernel(const uint16_t* __restrict__ hidden, int64_t H,
-                                                              const int32_t* __restrict__ sorted_ids,
-                                                              const int32_t* __restrict__ tile_expert,
-                                                              const int32_t* __restrict__ meta,
+                                                              int64_t T, int top_k,
+                                                              const int32_t* __restrict__ topk_ids,
+                                                              const int32_t* __restrict__ inverse,
+                                                              const int32_t* __restrict__ counts,
+                                                              const int32_t* __restrict__ offsets, int E,
                                                               const float* __restrict__ a1_gs, int64_t capacity,
                                                               uint8_t* __restrict__ a1, uint8_t* __restrict__ sfa1) {
   pdl_trigger();
-  pdl_wait();
-  const int64_t chunks = H / 64;
-  const int64_t P = meta[0];
-  const int64_t total = min(P, capacity) * chunks;
-  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
-       it += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = it / chunks, c = it - r * chunks;
-    const int t = sorted_ids[r];
-    uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
-    uint32_t sc = 0;
-    if (t >= 0) {
-      const float gs = a1_gs[tile_expert[r >> 7]];
-      const uint16_t* src = hidden + (int64_t)t * H + c * 64;
-      uint4 raw[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) raw[j] = ldg_nc(src + j * 8);
-      sc = quant_chunk64(raw, gs, o0, o1);
-    }
-    uint4* dst = reinterpret_cast<uint4*>(a1 + r * (H / 2) + c * 32);
-    dst[0] = o0;
-    dst[1] = o1;
-    *reinterpret_cast<uint32_t*>(sfa1 + sf_offset(r, c * 4, H / 16)) = sc;
+  __shared__ float2 tab[128];
+  if (threadIdx.x < 128) {
+    const float d = e4m3_value(threadIdx.x);
+    tab[threadIdx.x] = make_float2(d, threadIdx.x ? __frcp_rn(d) : 0.f);
   }
+  __syncthreads();
+  pdl_wait();
+  const float rcp6 = __frcp_rn(6.0f);
+  const int lane = threadIdx.x & 31;
+  const int64_t item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t seg_elems = 512 * kGatherChunks;
+  const int64_t segs = (H + seg_elems - 1) / seg_elems;
+  const int64_t sf_cols = H / 16;
+  if (item < T * segs) {
+    const int64_t t = item / segs, e0 = (item - t * segs) * seg_elems;
+    uint32_t raw[kGatherChunks][8];
+    float amax[kGatherChunks];
+#pragma unroll
+    for (int c = 0; c < kGatherChunks; ++c) {
+      const int64_t el = e0 + c * 512 + lane * 16;
+      if (el < H) {
+        ld_block32<kAligned32>(hidden + t * H + el, raw[c]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) raw[c][q] = 0u;
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < kGatherChunks; ++c) amax[c] = block_amax_bf16(raw[c]);
+    int my_row = 0;
+    float my_gs = 1.f;
+    if (lane < top_k) {
+      my_row = inverse[t * top_k + lane];
+      my_gs = a1_gs[topk_ids[t * top_k + lane]];
+    }
+    for (int j = 0; j < top_k; ++j) {
+      const int64_t r = __shfl_sync(0xffffffffu, my_row, j);
+      const float gs = __shfl_sync(0xffffffffu, my_gs, j);
+      const bool row_ok = r >= 0 && r < capacity;
+#pragma unroll
+      for (int c = 0; c < kGatherChunks; ++c) {
+        const int64_t el = e0 + c * 512 + lane * 16;
+        uint32_t lo, hi;
+        const uint32_t sc = quant_block16_bf16(raw[c], amax[c], gs, rcp6, tab, lo, hi);
+        const uint32_t word = sc | (__shfl_down_sync(0xffffffffu, sc, 1) << 8) |
+                              (__shfl_down_sync(0xffffffffu, sc, 2) << 16) |
+                              (__shfl_down_sync(0xffffffffu, sc, 3) << 24);
+        if (row_ok && el < H) {
+          *reinterpret_cast<uint2*>(a1 + r * (H / 2) + el / 2) = make_uint2(lo, hi);
+          if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sfa1 + sf_offset(r, el / 16, sf_cols)) = word;
+        }
+      }
+    }
+    return;
+  }
+  // pad rows: item -> (expert, j-th row past the expert's last token)
+  const int64_t p = item - T * segs;
+  if (p >= (int64_t)E * 128) return;
+  const int e = (int)(p >> 7), j = (int)(p & 127);
+  const int64_t r = (int64_t)offsets[e] + counts[e] + j;
+  if (r >= offsets[e + 1] || r >= capacity) return;
+  for (int64_t b = lane * 16; b < H / 2; b += 32 * 16)
+    *reinterpret_cast<uint4*>(a1 + r * (H / 2) + b) = make_uint4(0u, 0u, 0u, 0u);
+  for (int64_t m = lane; m < sf_cols / 4; m += 32)
+    *reinterpret_cast<uint32_t*>(sfa1 + sf_offset(r, 4 * m, sf_cols)) = 0u;
 }
 
 // One warp per slot row: max |x| of the token's hidden row, folded into its
@@ -261,14 +391,17 @@ cudaError_t launch_assemble_scales(const uint8_t* sf_linear, int64_t sf_cols, co
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather_quantize(const uint16_t* hidden, int64_t H, const int32_t* sorted_ids,
-                                   const int32_t* tile_expert, const int32_t* meta, const float* a1_gs,
-                                   int64_t capacity, uint8_t* a1, uint8_t* sfa1, int num_sms, cudaStream_t s,
-                                   bool pdl) {
-  const int64_t items = capacity * (H / 64);
-  const int grid = grid_for(items, 256, num_sms, 8);
-  return launch_kernel(gather_quantize_kernel, dim3(grid), dim3(256), 0, s, pdl, hidden, H, sorted_ids, tile_expert,
-                       meta, a1_gs, capacity, a1, sfa1);
+cudaError_t launch_gather_quantize(const uint16_t* hidden, int64_t H, int64_t T, int top_k,
+                                   const int32_t* topk_ids, const int32_t* inverse, const int32_t* counts,
+                                   const int32_t* offsets, int E, const float* a1_gs, int64_t capacity, uint8_t* a1,
+                                   uint8_t* sfa1, cudaStream_t s, bool pdl) {
+  const int64_t segs = (H + 512 * kGatherChunks - 1) / (512 * kGatherChunks);
+  const int64_t warps = T * segs + (int64_t)E * 128;
+  const int64_t grid = (warps + 7) / 8;
+  auto* kernel = (reinterpret_cast<uintptr_t>(hidden) & 31u) == 0 ? gather_quantize_kernel<true>
+                                                                   : gather_quantize_kernel<false>;
+  return launch_kernel(kernel, dim3((unsigned)grid), dim3(256), 0, s, pdl, hidden, H, T, top_k, topk_ids, inverse,
+                       counts, offsets, E, a1_gs, capacity, a1, sfa1);
 }
 
 cudaError_t launch_gather_amax(const uint16_t* hidden, int64_t H, const int32_t* sorted_ids,

@@ -106,6 +106,24 @@ def test_gemm_identity_weight_returns_dequantized_activation():
     np.testing.assert_allclose(bf16_host(D), expect, rtol=2.0 ** -7, atol=0)  # at most one bf16 ulp
 
 
+def test_gemm_output_only_16_byte_aligned():
+    """D at a 16-byte (not 32-byte) offset with a row stride of N + 8 elements:
+    the epilogue keeps 16-byte stores there (32-byte stores need 32-byte rows)."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import binding as B
+    pb = make_problem([150], 256, 256, seed=7)
+    ldd = 256 + 8
+    buf = torch.full((8 + 256 * ldd,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    D = buf[8:]
+    assert D.data_ptr() % 32 == 16
+    B.nvfp4_grouped_gemm(dev(pb["A"]), dev(pb["SFA"]), dev(pb["a_gs"]), dev(pb["B"]), dev(pb["SFB"]),
+                         dev(pb["b_gs"]), dev(pb["padded"]), dev(pb["counts"]), 1, pb["cap"], 256, 256, D, ldd, 0)
+    torch.cuda.synchronize()
+    got = bf16_host(D[:150 * ldd].view(150, ldd))
+    check(pb, got[None, :, :256])
+    assert np.all(np.isnan(got[:, 256:]))  # the gap between rows is not written
+
+
 def test_gemm_device_status_is_clean():
     from nvfp4_mixture_experts_expert_gb300 import binding as B
     pb = make_problem([64], 256, 256, seed=2)

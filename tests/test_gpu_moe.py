@@ -111,6 +111,27 @@ def test_moe_edge_cases(case):
     check_all(wl, orc, *run_gpu(wl, orc))
 
 
+def test_moe_hidden_16_byte_aligned_and_half_chunk_rows():
+    """The gather reads each 16-element block with one 32-byte load only where
+    the hidden states are 32-byte aligned; a pointer that is 16-byte but not
+    32-byte aligned takes the two-load path.  H = 768 also leaves the last
+    512-element chunk of every row half filled."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    wl = W.moe_workload(70, 768, 256, 5, 3, 33)
+    orc = OracleMoE(wl)
+    flat = bf16_dev(wl.hidden).reshape(-1)
+    buf = torch.empty(flat.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    hidden = buf[8:].view(wl.T, wl.H)
+    hidden.copy_(flat.view(wl.T, wl.H))
+    assert hidden.data_ptr() % 32 == 16
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    fwd = api.MoEForward(wl.T, wl.H, wl.I, wl.E, wl.top_k)
+    out = fwd(hidden, dev(wl.logits), w, dev(orc.a1_gs), dev(orc.a2_gs), wl.gate_limit, wl.up_limit)
+    torch.cuda.synchronize()
+    check_all(wl, orc, w, fwd, out)
+
+
 def test_moe_zero_tokens_is_a_no_op():
     from nvfp4_mixture_experts_expert_gb300 import binding as B
     import torch
