@@ -246,6 +246,19 @@ int nvfp4_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int E, int top_k
  */
 int nvfp4_device_status(int* status_out, int reset);
 
+/* GEMM variant (process-wide; every GEMM above and the MoE forward).
+ *
+ * enable != 0: a cluster of two CTAs on two SMs computes each 256 x 256 output
+ * tile with the paired tensor-core instructions (tcgen05 cta_group::2); each
+ * SM stages half of the B tile, so it reads fewer operand bytes per MMA.
+ * enable == 0: one CTA per 128 x 256 tile.  Both variants compute every output
+ * element with the same arithmetic in the same order, so their results are
+ * bit-identical.  Default: disabled (the single-CTA variant is the faster of
+ * the two on the MoE layer).  Returns the previous setting (0 / 1).
+ * Not thread-safe with respect to launches issued concurrently from other
+ * host threads; no device work, no error. */
+int nvfp4_gemm_set_cta_pair(int enable);
+
 /*
  * Optional per-stage timing of nvfp4_moe_forward: when set, the forward
  * records events[i] (cudaEvent_t) on its stream before stage i, i = 0..6, and

@@ -165,8 +165,8 @@ static int grouped_gemm_impl(const void* A, const void* SFA, const float* a_gs, 
   a.timeout_ns = timeout_ns;
   a.debug_no_loads = debug_no_loads;
   const int64_t max_tiles = rows_capacity / 128 * a.n_tiles;
-  const int grid = (int)(max_tiles < dev->sms ? max_tiles : dev->sms);
-  cudaError_t e = launch_gemm(kEpiBf16, a, grid, (cudaStream_t)stream);
+  cudaError_t e = launch_gemm(kEpiBf16, a, (int)(max_tiles < INT32_MAX ? max_tiles : INT32_MAX), dev->sms,
+                              (cudaStream_t)stream);
   return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "gemm launch");
 }
 
@@ -423,10 +423,10 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
     return cuda_fail(e, "gather launch");
   stage_mark(4, s);
   const int64_t t1 = cap / 128 * g1.n_tiles, t2 = cap / 128 * g2.n_tiles;
-  if ((e = launch_gemm(kEpiSwigluQuant, g1, (int)(t1 < dev->sms ? t1 : dev->sms), s, true)) != cudaSuccess)
+  if ((e = launch_gemm(kEpiSwigluQuant, g1, (int)t1, dev->sms, s, true)) != cudaSuccess)
     return cuda_fail(e, "L1 launch");
   stage_mark(5, s);
-  if ((e = launch_gemm(kEpiCombine, g2, (int)(t2 < dev->sms ? t2 : dev->sms), s, true)) != cudaSuccess)
+  if ((e = launch_gemm(kEpiCombine, g2, (int)t2, dev->sms, s, true)) != cudaSuccess)
     return cuda_fail(e, "L2 launch");
   stage_mark(6, s);
   if ((e = launch_token_combine(ybuf, inverse, T, H, top_k, (uint16_t*)out, s, true)) != cudaSuccess)
@@ -522,11 +522,13 @@ int nvfp4_moe_calibrate(const void* hidden, const float* router_logits, int64_t 
                                   a1_gs_out, cap, a1, sfa1, s)) != cudaSuccess)
     return cuda_fail(e, "calibration launch");
   const int64_t t1 = cap / 128 * g1.n_tiles;
-  if ((e = launch_gemm(kEpiSwigluAmax, g1, (int)(t1 < dev->sms ? t1 : dev->sms), s)) != cudaSuccess ||
+  if ((e = launch_gemm(kEpiSwigluAmax, g1, (int)t1, dev->sms, s)) != cudaSuccess ||
       (e = launch_gs_from_amax(amax + E, E, a2_gs_out, s)) != cudaSuccess)
     return cuda_fail(e, "calibration launch");
   return NVFP4_OK;
 }
+
+int nvfp4_gemm_set_cta_pair(int enable) { return gemm_set_pair(enable != 0) ? 1 : 0; }
 
 int nvfp4_device_status(int* status_out, int reset) {
   g_err[0] = 0;

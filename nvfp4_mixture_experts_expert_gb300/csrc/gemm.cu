@@ -13,26 +13,44 @@
 //   kEpiSwigluAmax   MoE calibration: per-expert amax of the bf16 SwiGLU output
 //                    (vllm page: L2 global scale from the actual L1 output)
 //
-// Design (one CTA per SM, persistent over output tiles, warp-specialised):
-//   warp 0   TMA producer: per K-stage of 256 elements, one 128x128-byte A box,
-//            two 128x128-byte B boxes (SWIZZLE_128B) and the matching 512-byte
-//            scale tiles (plain bulk copies), into a 4-deep shared-memory ring.
-//   warp 1   TMEM allocator and MMA issuer: 4 MMAs of 128x256x64 per stage
-//            into a 128-lane x 256-column FP32 accumulator in TMEM.
-//   warp 10  scale copier: moves each stage's scale tiles into TMEM
-//            (tcgen05.cp 32x128b.warpx4) ahead of the MMAs that read them.
-//   warps 2-9 epilogue: each warp owns the 32 TMEM lanes of its quarter
+// Design (persistent over output tiles, warp-specialised, one CTA per SM):
+//   warp 0   TMA producer: per K-stage of 256 elements, the A box (128 rows x
+//            128 bytes), the B box(es) (SWIZZLE_128B) and the matching 512-byte
+//            scale tiles (plain bulk copies), into a shared-memory ring.
+//   warp 1   TMEM allocator and MMA issuer: 4 MMAs of K=64 per stage into a
+//            128-lane x 256-column FP32 accumulator in TMEM.
+//   warps 4-11 epilogue: each warp owns the 32 TMEM lanes of its quarter
 //            (warp % 4), i.e. 32 output rows, and one half of the tile's
 //            columns; it reads the accumulator with tcgen05.ld.
-// A tile is 128 rows x 256 MMA columns.  For the SwiGLU epilogue the two B
-// boxes are the gate rows [n0, n0+128) and the up rows [I+n0, I+n0+128) of the
-// expert's W13, so gate and up of one output feature sit in the same TMEM lane
-// 128 columns apart, and the 16-wide requantization blocks are in-register.
-// Tiles are ordered m-tile major, n-tile minor (n-major is available); m-tiles
-// map to groups through the 128-aligned group offsets read from device memory
-// (no host sync).
+//   warps 12-15 scale staging: shared memory -> TMEM scale columns with
+//            tcgen05.st, one warp per lane quarter (see sf_loop).
+//   Registers are re-balanced per warpgroup with setmaxnreg (the epilogue
+//   holds a 128-column accumulator row per thread).
+// Two variants:
+//   single   one CTA computes a 128 x 256 tile; 4-stage ring of 54 KB stages.
+//   pair     a cluster of two CTAs on two SMs computes a 256 x 256 tile with
+//            tcgen05 cta_group::2: each CTA holds 128 rows of A and one
+//            128-row half of the B tile (the gate or up half for SwiGLU) plus
+//            all of the stage's scale tiles, so an SM reads 8 KB of operands
+//            per 128x256x64 MMA instead of 12 KB; 5-stage ring of 38 KB stages.
+//            The leader CTA (rank 0) issues the MMAs; its commits are
+//            multicast to both CTAs' barriers.  The peer's scale warps arrive
+//            on the leader's sf_full (its operands have landed and its scales
+//            are in its TMEM); its epilogue warps release the accumulator on
+//            the leader's barrier.  An expert's m-tiles are paired in order;
+//            an odd last tile is paired with a copy of itself whose rows the
+//            peer does not store.
+// A tile is 128 (per CTA) rows x 256 MMA columns.  For the SwiGLU epilogue the
+// two B boxes are the gate rows [n0, n0+128) and the up rows [I+n0, I+n0+128)
+// of the expert's W13, so gate and up of one output feature sit in the same
+// TMEM lane 128 columns apart, and the 16-wide requantization blocks are
+// in-register.  Work units (m-tiles or m-tile pairs) are ordered unit major,
+// n-tile minor (n-major is available); units map to groups through the
+// 128-aligned group offsets read from device memory (no host sync).
 // Every mbarrier wait is bounded (timeout -> device status word, abort, drain
-// of copies/MMAs in flight, TMEM freed, return).
+// of copies/MMAs in flight, TMEM freed, return); in the pair variant every
+// CTA runs to the final cluster barrier before the collective TMEM release,
+// and each producer first waits for the leader's last multicast releases.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -49,21 +67,35 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK_BYTES = 128;  // 256 FP4 elements per stage
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK_BYTES;
-constexpr int B_BYTES = BN * BK_BYTES;
 constexpr int SFA_BYTES = 4 * 512;
 constexpr int SFB_BYTES = 8 * 512;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
 constexpr int TMEM_COLS = 512;
 constexpr int SF_COL0 = 256;         // scale columns start after the accumulator
 constexpr int SF_COLS_PER_STAGE = 48;  // 4 x (4 SFA + 8 SFB)
-constexpr int NUM_EPI_WARPS = 8;  // two per TMEM lane quarter, each owning half of the columns
-constexpr int COPIER_WARP = 2 + NUM_EPI_WARPS;
-constexpr int NUM_THREADS = 32 * (COPIER_WARP + 1);
+// Warp roles, by warpgroup (setmaxnreg re-balances registers per warpgroup):
+//   WG0  warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer (warps 2-3 idle)
+//   WG1-2 warps 4-11 epilogue: two per TMEM lane quarter, each owning half of the columns
+//   WG3  warps 12-15 scale staging: one per TMEM lane quarter
+constexpr int EPI_WARP0 = 4;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int SF_WARP0 = EPI_WARP0 + NUM_EPI_WARPS;
+constexpr int NUM_THREADS = 32 * (SF_WARP0 + 4);
+constexpr int REGS_LAUNCH = 128;  // per thread at launch (the kernel's register allocation)
+constexpr int REGS_SMALL = 72;    // WG0 and WG3 after setmaxnreg.dec
+constexpr int REGS_EPI = 184;     // WG1 and WG2 after setmaxnreg.inc
+static_assert(128 * (2 * REGS_SMALL + 2 * REGS_EPI) <= NUM_THREADS * REGS_LAUNCH,
+              "the register split must fit the launch allocation");
 constexpr int MAX_GROUPS = 1024;
-static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
-static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+
+template <bool PAIR>
+struct Cfg {
+  static constexpr int STAGES = PAIR ? 5 : 4;
+  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK_BYTES;  // B rows this CTA loads per stage
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+};
 
 // Instruction descriptor: E2M1 x E2M1, UE4M3 scales, K-major A and B, dense K=64.
 __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
@@ -78,28 +110,36 @@ struct SmemLayout {
   uint64_t* acc_empty;
   uint64_t* drain;
   uint64_t* sf_full;     // [STAGES] scale tiles of a stage are in TMEM
-  uint64_t* drain_cp;    // copier's own drain on abort
   uint32_t* tmem_slot;
   int* abort_flag;
-  int* offsets;
+  int* offsets;   // [G+1] padded row offsets
+  int* unit_off;  // [G+1] first work unit (m-tile or m-tile pair) of each group
 };
 
-__device__ __forceinline__ SmemLayout carve(uint8_t* raw) {
+template <bool PAIR>
+__device__ __forceinline__ SmemLayout carve(uint8_t* raw, int G) {
+  using C = Cfg<PAIR>;
   SmemLayout L;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   L.stages = base;
-  uint8_t* p = base + STAGES * STAGE_BYTES;
+  uint8_t* p = base + C::STAGES * C::STAGE_BYTES;
   L.full = reinterpret_cast<uint64_t*>(p);
-  L.empty = L.full + STAGES;
-  L.acc_full = L.empty + STAGES;
+  L.empty = L.full + C::STAGES;
+  L.sf_full = L.empty + C::STAGES;
+  L.acc_full = L.sf_full + C::STAGES;
   L.acc_empty = L.acc_full + 1;
   L.drain = L.acc_empty + 1;
-  L.sf_full = L.drain + 1;
-  L.drain_cp = L.sf_full + STAGES;
-  L.tmem_slot = reinterpret_cast<uint32_t*>(L.drain_cp + 1);
+  L.tmem_slot = reinterpret_cast<uint32_t*>(L.drain + 1);
   L.abort_flag = reinterpret_cast<int*>(L.tmem_slot + 1);
   L.offsets = reinterpret_cast<int*>(L.abort_flag + 3);
+  L.unit_off = L.offsets + G + 1;
   return L;
+}
+
+template <bool PAIR>
+constexpr size_t smem_bytes_for(int G) {
+  return 1024 + (size_t)Cfg<PAIR>::STAGES * Cfg<PAIR>::STAGE_BYTES + 8 * (3 * Cfg<PAIR>::STAGES + 4) + 16 +
+         8 * (size_t)(G + 1) + 16;
 }
 
 __device__ __forceinline__ int find_group(const int* off, int G, int row) {
@@ -111,147 +151,221 @@ __device__ __forceinline__ int find_group(const int* off, int G, int row) {
   return lo;
 }
 
-// Tile index -> (m-tile, n-tile).  m-major keeps consecutive CTAs on one
-// activation tile (and one expert's weights); n-major keeps every CTA on one
-// output column slice, which bounds the live part of a scattered output.
-__device__ __forceinline__ void decode_tile(int tile, int num_mtiles, int n_tiles, int n_major, int& mt, int& nt) {
-  if (n_major) {
-    nt = tile / num_mtiles;
-    mt = tile - nt * num_mtiles;
+// Work item -> (group, m-tile of this CTA, n-tile).  Unit-major order keeps
+// consecutive CTAs on one activation tile (and one expert's weights);
+// n-major keeps every CTA on one output column slice.  In the pair variant a
+// unit is two consecutive m-tiles of one group (rank 0 takes the first); the
+// second of an odd group's last pair does not exist (valid = false) and that
+// CTA reloads the first tile so every copy stays inside the operands.
+struct Work {
+  int g, mt, nt;
+  bool valid;
+};
+
+template <bool PAIR>
+__device__ __forceinline__ Work decode_work(const SmemLayout& L, const GemmArgs& p, int it, uint32_t rank) {
+  const int nu = L.unit_off[p.G];
+  int u, nt;
+  if (p.n_major) {
+    nt = it / nu;
+    u = it - nt * nu;
   } else {
-    mt = tile / n_tiles;
-    nt = tile - mt * n_tiles;
+    u = it / p.n_tiles;
+    nt = it - u * p.n_tiles;
   }
+  Work w;
+  w.g = find_group(L.unit_off, p.G, u);
+  w.nt = nt;
+  const int t0 = L.offsets[w.g] / BM, k = u - L.unit_off[w.g];
+  if constexpr (PAIR) {
+    const int mt = t0 + 2 * k + (int)rank;
+    w.valid = mt < L.offsets[w.g + 1] / BM;
+    w.mt = w.valid ? mt : mt - 1;
+  } else {
+    w.mt = t0 + k;
+    w.valid = true;
+  }
+  return w;
 }
 
 // ------------------------------------------------------------------ producer
-__device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total) {
+// Work items it = start, start + step, ... (step = CTAs, or CTA pairs).
+template <bool PAIR>
+__device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total, int start, int step,
+                              uint32_t rank) {
+  using C = Cfg<PAIR>;
   volatile int* abort = L.abort_flag;
-  int issued_parity[STAGES];
+  int issued_parity[C::STAGES];
 #pragma unroll
-  for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+  for (int s = 0; s < C::STAGES; ++s) issued_parity[s] = -1;
   uint32_t stage = 0, phase = 0;
+  bool ok = true;
   const int kt = p.K / 64;  // scale tiles per 128-row band
   if (!p.debug_no_loads) {
-    const int num_mtiles = L.offsets[p.G] / BM;
-    for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
-      int mt, nt;
-      decode_tile(tile, num_mtiles, p.n_tiles, p.n_major, mt, nt);
-      const int g = find_group(L.offsets, p.G, mt * BM);
-      const int b_r0 = nt * p.b_tile_stride;
+    for (int it = start; it < total && ok && !*abort; it += step) {
+      const Work w = decode_work<PAIR>(L, p, it, rank);
+      const int b_r0 = w.nt * p.b_tile_stride;
       const int b_r1 = b_r0 + p.b_second_offset;
-      const int64_t b_row0 = (int64_t)g * p.b_rows_per_group + b_r0;
-      const int64_t b_row1 = (int64_t)g * p.b_rows_per_group + b_r1;
-      const uint8_t* sfa = p.sfa + (int64_t)mt * kt * 512;
-      const uint8_t* sfb0 = p.sfb + g * p.sfb_group_bytes + (int64_t)(b_r0 >> 7) * kt * 512;
-      const uint8_t* sfb1 = p.sfb + g * p.sfb_group_bytes + (int64_t)(b_r1 >> 7) * kt * 512;
+      const int64_t b_row0 = (int64_t)w.g * p.b_rows_per_group + b_r0;
+      const int64_t b_row1 = (int64_t)w.g * p.b_rows_per_group + b_r1;
+      const uint8_t* sfa = p.sfa + (int64_t)w.mt * kt * 512;
+      const uint8_t* sfb0 = p.sfb + w.g * p.sfb_group_bytes + (int64_t)(b_r0 >> 7) * kt * 512;
+      const uint8_t* sfb1 = p.sfb + w.g * p.sfb_group_bytes + (int64_t)(b_r1 >> 7) * kt * 512;
       for (int kb = 0; kb < p.num_kb; ++kb) {
         const int nmma = min(4, (p.K - kb * 256) / 64);
-        if (!wait_bounded(smem_u32(&L.empty[stage]), phase ^ 1u, abort, p.status, p.timeout_ns)) break;
-        uint8_t* st = L.stages + stage * STAGE_BYTES;
+        if (!wait_bounded<PAIR>(smem_u32(&L.empty[stage]), phase ^ 1u, abort, p.status, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = L.stages + stage * C::STAGE_BYTES;
         const uint32_t bar = smem_u32(&L.full[stage]);
-        mbar_arrive_expect_tx(bar, A_BYTES + B_BYTES + 3 * nmma * 512);
-        tma_load_2d(smem_u32(st), &p.tmap_a, kb * BK_BYTES, mt * BM, bar);
-        tma_load_2d(smem_u32(st + A_BYTES), &p.tmap_b, kb * BK_BYTES, (int32_t)b_row0, bar);
-        tma_load_2d(smem_u32(st + A_BYTES + B_BYTES / 2), &p.tmap_b, kb * BK_BYTES, (int32_t)b_row1, bar);
-        bulk_load(smem_u32(st + A_BYTES + B_BYTES), sfa + kb * 2048, nmma * 512, bar);
-        bulk_load(smem_u32(st + A_BYTES + B_BYTES + SFA_BYTES), sfb0 + kb * 2048, nmma * 512, bar);
-        bulk_load(smem_u32(st + A_BYTES + B_BYTES + SFA_BYTES + 2048), sfb1 + kb * 2048, nmma * 512, bar);
+        mbar_arrive_expect_tx(bar, A_BYTES + C::B_BYTES + 3 * nmma * 512);
+        tma_load_2d(smem_u32(st), &p.tmap_a, kb * BK_BYTES, w.mt * BM, bar);
+        if constexpr (PAIR) {  // this CTA's half of the B tile
+          tma_load_2d(smem_u32(st + A_BYTES), &p.tmap_b, kb * BK_BYTES, (int32_t)(rank ? b_row1 : b_row0), bar);
+        } else {
+          tma_load_2d(smem_u32(st + A_BYTES), &p.tmap_b, kb * BK_BYTES, (int32_t)b_row0, bar);
+          tma_load_2d(smem_u32(st + A_BYTES + C::B_BYTES / 2), &p.tmap_b, kb * BK_BYTES, (int32_t)b_row1, bar);
+        }
+        uint8_t* sf_st = st + A_BYTES + C::B_BYTES;
+        bulk_load(smem_u32(sf_st), sfa + kb * 2048, nmma * 512, bar);
+        bulk_load(smem_u32(sf_st + SFA_BYTES), sfb0 + kb * 2048, nmma * 512, bar);
+        bulk_load(smem_u32(sf_st + SFA_BYTES + 2048), sfb1 + kb * 2048, nmma * 512, bar);
         issued_parity[stage] = (int)phase;
-        if (++stage == STAGES) {
+        if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
   }
-  if (*abort) {  // let copies already issued land before the CTA exits
+  if (*abort || !ok) {  // let copies already issued land before the CTA exits
 #pragma unroll
-    for (int s = 0; s < STAGES; ++s)
+    for (int s = 0; s < C::STAGES; ++s)
       if (issued_parity[s] >= 0) {
         volatile int no_abort = 0;
         wait_bounded(smem_u32(&L.full[s]), (uint32_t)issued_parity[s], &no_abort, nullptr, p.timeout_ns);
       }
-  }
-}
-
-// ------------------------------------------------------------------ scale copier
-// Copies each stage's scale tiles from shared memory into that stage's TMEM
-// columns and signals sf_full[stage].  Issuing these copies from their own
-// warp lets them overlap the MMA stream of the previous stages.  A stage's
-// TMEM columns are rewritten only after its shared-memory slot was refilled,
-// i.e. after the MMAs that read them committed.
-__device__ void copier_loop(const GemmArgs& p, const SmemLayout& L, int total, uint32_t tmem) {
-  volatile int* abort = L.abort_flag;
-  uint32_t stage = 0, phase = 0;
-  bool issued_any = false;
-  for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
-    for (int kb = 0; kb < p.num_kb; ++kb) {
-      const int nmma = min(4, (p.K - kb * 256) / 64);
-      if (!wait_bounded(smem_u32(&L.full[stage]), phase, abort, p.status, p.timeout_ns)) break;
-      tc_fence_after();
-      const uint32_t sfa_s = smem_u32(L.stages + stage * STAGE_BYTES) + A_BYTES + B_BYTES;
-      const uint32_t sfb_s = sfa_s + SFA_BYTES;
-      const uint32_t sf_col = tmem + SF_COL0 + stage * SF_COLS_PER_STAGE;
-      for (int i = 0; i < nmma; ++i) {
-        tc_cp_sf(sf_col + 4 * i, smem_desc(sfa_s + 512 * i, 0, 128, 0));
-        tc_cp_sf(sf_col + 16 + 8 * i, smem_desc(sfb_s + 512 * i, 0, 128, 0));
-        tc_cp_sf(sf_col + 16 + 8 * i + 4, smem_desc(sfb_s + 2048 + 512 * i, 0, 128, 0));
-      }
-      issued_any = true;
-      tc_commit(smem_u32(&L.sf_full[stage]));
-      if (++stage == STAGES) {
+  } else if constexpr (PAIR) {
+    // the leader's last multicast releases land in this CTA before it may exit
+    for (int i = 0; i < C::STAGES; ++i) {
+      if (!wait_bounded<true>(smem_u32(&L.empty[stage]), phase ^ 1u, abort, p.status, p.timeout_ns)) break;
+      if (++stage == C::STAGES) {
         stage = 0;
         phase ^= 1u;
       }
     }
   }
-  if (*abort && issued_any) {  // copies in flight must land before TMEM is freed
-    tc_commit(smem_u32(L.drain_cp));
-    volatile int no_abort = 0;
-    wait_bounded(smem_u32(L.drain_cp), 0, &no_abort, nullptr, p.timeout_ns);
-  }
 }
 
-// ------------------------------------------------------------------ MMA issuer
-__device__ void mma_loop(const GemmArgs& p, const SmemLayout& L, int total, uint32_t tmem) {
+// ------------------------------------------------------------------ scale staging
+// Warps 12-15 (one per TMEM lane quarter) move each stage's scale tiles from
+// shared memory into that stage's TMEM columns with tcgen05.st: lane l of the
+// warp for quarter q writes 16-byte line l of every 512-byte tile into TMEM
+// lane 32q + l, 4 columns per tile -- the layout the block-scaled MMA reads
+// (each quarter holds the same 32 lines; SFB tiles cover all N rows).  Two
+// store instructions per warp per stage replace 12 tcgen05.cp copies, which
+// would queue in the tensor pipe ahead of the MMAs.  A stage's columns are
+// rewritten only after its shared-memory slot was refilled, i.e. after the
+// MMAs that read them committed.  sf_full[stage] counts the 4 warps (8 in the
+// pair variant: the peer's warps arrive on the leader's barrier, which also
+// tells the leader that the peer's operands have landed).
+template <bool PAIR>
+__device__ void sf_loop(const GemmArgs& p, const SmemLayout& L, int total, int start, int step, uint32_t tmem,
+                        uint32_t rank) {
+  using C = Cfg<PAIR>;
   volatile int* abort = L.abort_flag;
-  const uint32_t idesc = idesc_nvf4(BM, BN);
-  uint32_t stage = 0, phase = 0, acc_phase = 0;
-  bool issued_any = false;
-  for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
-    if (!wait_bounded(smem_u32(L.acc_empty), acc_phase ^ 1u, abort, p.status, p.timeout_ns)) break;
-    tc_fence_after();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+  uint32_t stage = 0, phase = 0;
+  for (int it = start; it < total; it += step) {
     bool ok = true;
     for (int kb = 0; kb < p.num_kb; ++kb) {
-      const int nmma = min(4, (p.K - kb * 256) / 64);
-      // sf_full[stage] implies full[stage]: the copier waited for the stage's data first
-      if (!wait_bounded(smem_u32(&L.sf_full[stage]), phase, abort, p.status, p.timeout_ns)) {
+      int landed = 1;
+      if (lane == 0) landed = wait_bounded(smem_u32(&L.full[stage]), phase, abort, p.status, p.timeout_ns);
+      if (!__shfl_sync(0xffffffffu, landed, 0)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      const uint32_t a_s = smem_u32(L.stages + stage * STAGE_BYTES);
-      const uint32_t b_s = a_s + A_BYTES;
-      const uint32_t sf_col = tmem + SF_COL0 + stage * SF_COLS_PER_STAGE;
-      for (int i = 0; i < nmma; ++i) {
-        const uint64_t ad = smem_desc(a_s + 32 * i, 16, 1024, 2);
-        const uint64_t bd = smem_desc(b_s + 32 * i, 16, 1024, 2);
-        tc_mma_nvf4(tmem, ad, bd, idesc, sf_col + 4 * i, sf_col + 16 + 8 * i, (kb | i) != 0);
+      // columns of a stage: SFA of K-steps 0-3 (4 each), then per K-step the
+      // SFB tiles of B rows 0-127 and 128-255 (4 each); unused K-steps of a
+      // partial last stage carry stale scales that no MMA reads
+      const uint8_t* sf = L.stages + stage * C::STAGE_BYTES + A_BYTES + C::B_BYTES + 16 * lane;
+      uint32_t r[48];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 a = *reinterpret_cast<const uint4*>(sf + 512 * i);
+        const uint4 b0 = *reinterpret_cast<const uint4*>(sf + SFA_BYTES + 512 * i);
+        const uint4 b1 = *reinterpret_cast<const uint4*>(sf + SFA_BYTES + 2048 + 512 * i);
+        r[4 * i + 0] = a.x, r[4 * i + 1] = a.y, r[4 * i + 2] = a.z, r[4 * i + 3] = a.w;
+        r[16 + 8 * i + 0] = b0.x, r[16 + 8 * i + 1] = b0.y, r[16 + 8 * i + 2] = b0.z, r[16 + 8 * i + 3] = b0.w;
+        r[16 + 8 * i + 4] = b1.x, r[16 + 8 * i + 5] = b1.y, r[16 + 8 * i + 6] = b1.z, r[16 + 8 * i + 7] = b1.w;
       }
-      issued_any = true;
-      tc_commit(smem_u32(&L.empty[stage]));
-      if (++stage == STAGES) {
+      const uint32_t col = t_lane + SF_COL0 + stage * SF_COLS_PER_STAGE;
+      tmem_store_32(col, r);
+      tmem_store_16_hi(col + 32, r);
+      tmem_store_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (PAIR && rank) mbar_arrive_remote(mapa_shared(smem_u32(&L.sf_full[stage]), 0));
+        else mbar_arrive(smem_u32(&L.sf_full[stage]));
+      }
+      if (++stage == C::STAGES) {
         stage = 0;
         phase ^= 1u;
       }
     }
     if (!ok) break;
-    tc_commit(smem_u32(L.acc_full));
+  }
+}
+
+// ------------------------------------------------------------------ MMA issuer
+template <bool PAIR>
+__device__ void mma_loop(const GemmArgs& p, const SmemLayout& L, int total, int start, int step, uint32_t tmem) {
+  using C = Cfg<PAIR>;
+  volatile int* abort = L.abort_flag;
+  const uint32_t idesc = idesc_nvf4(PAIR ? 2 * BM : BM, BN);
+  uint32_t stage = 0, phase = 0, acc_phase = 0;
+  bool issued_any = false;
+  for (int it = start; it < total && !*abort; it += step) {
+    if (!wait_bounded<PAIR>(smem_u32(L.acc_empty), acc_phase ^ 1u, abort, p.status, p.timeout_ns)) break;
+    tc_fence_after();
+    bool ok = true;
+    for (int kb = 0; kb < p.num_kb; ++kb) {
+      const int nmma = min(4, (p.K - kb * 256) / 64);
+      // sf_full[stage] implies full[stage] (in both CTAs of a pair): the scale
+      // warps waited for the stage's data first
+      if (!wait_bounded<PAIR>(smem_u32(&L.sf_full[stage]), phase, abort, p.status, p.timeout_ns)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a_s = smem_u32(L.stages + stage * C::STAGE_BYTES);
+      const uint32_t b_s = a_s + A_BYTES;
+      const uint32_t sf_col = tmem + SF_COL0 + stage * SF_COLS_PER_STAGE;
+      for (int i = 0; i < nmma; ++i) {
+        const uint64_t ad = smem_desc(a_s + 32 * i, 16, 1024, 2);
+        const uint64_t bd = smem_desc(b_s + 32 * i, 16, 1024, 2);
+        if constexpr (PAIR) tc_mma_nvf4_pair(tmem, ad, bd, idesc, sf_col + 4 * i, sf_col + 16 + 8 * i, (kb | i) != 0);
+        else tc_mma_nvf4(tmem, ad, bd, idesc, sf_col + 4 * i, sf_col + 16 + 8 * i, (kb | i) != 0);
+      }
+      issued_any = true;
+      if constexpr (PAIR) tc_commit_pair_mc(smem_u32(&L.empty[stage]), 3);
+      else tc_commit(smem_u32(&L.empty[stage]));
+      if (++stage == C::STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) break;
+    if constexpr (PAIR) tc_commit_pair_mc(smem_u32(L.acc_full), 3);
+    else tc_commit(smem_u32(L.acc_full));
     acc_phase ^= 1u;
   }
   if (*abort && issued_any) {  // every MMA / copy issued must finish before TMEM is freed
-    tc_commit(smem_u32(L.drain));
+    if constexpr (PAIR) tc_commit_pair(smem_u32(L.drain));
+    else tc_commit(smem_u32(L.drain));
     volatile int no_abort = 0;
     wait_bounded(smem_u32(L.drain), 0, &no_abort, nullptr, p.timeout_ns);
   }
@@ -267,19 +381,21 @@ __device__ __forceinline__ float silu_clamped_product(float g, float u, float gl
 // Each epilogue thread first copies its 128 accumulator columns (one row)
 // from TMEM into registers and releases the accumulator, so the MMAs of the
 // next tile overlap all of the epilogue arithmetic and stores below.
-template <int EPI>
-__device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total, uint32_t tmem) {
+template <int EPI, bool PAIR>
+__device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total, int start, int step, uint32_t tmem,
+                              uint32_t rank) {
   volatile int* abort = L.abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;        // TMEM lanes this warp may access
-  const int half = (warp - 2) >> 2;    // which half of the tile's columns it owns
+  const int half = (warp - EPI_WARP0) >> 2;  // which half of the tile's columns it owns
   const int row_in_tile = quarter * 32 + lane;
   const uint32_t t_base = tmem + ((uint32_t)(quarter * 32) << 16);
-  const int num_mtiles = L.offsets[p.G] / BM;
+  // the accumulator is released on the leader's barrier (remote for the peer)
+  const uint32_t acc_empty = PAIR && rank ? mapa_shared(smem_u32(L.acc_empty), 0) : smem_u32(L.acc_empty);
   uint32_t acc_phase = 0;
-  for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+  for (int it = start; it < total; it += step) {
     int ok = 1;
-    if (lane == 0) ok = wait_bounded(smem_u32(L.acc_full), acc_phase, abort, p.status, p.timeout_ns);
+    if (lane == 0) ok = wait_bounded<PAIR>(smem_u32(L.acc_full), acc_phase, abort, p.status, p.timeout_ns);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) break;
     __syncwarp();
@@ -299,13 +415,16 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
     tmem_load_wait();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(L.acc_empty));
+    if (lane == 0) {
+      if (PAIR && rank) mbar_arrive_remote(acc_empty);
+      else mbar_arrive(acc_empty);
+    }
     acc_phase ^= 1u;
 
-    int mt, nt;
-    decode_tile(tile, num_mtiles, p.n_tiles, p.n_major, mt, nt);
-    const int g = find_group(L.offsets, p.G, mt * BM);
-    const int64_t row = (int64_t)mt * BM + row_in_tile;
+    const Work w = decode_work<PAIR>(L, p, it, rank);
+    if (!w.valid) continue;  // the pair's second tile does not exist: nothing to store
+    const int g = w.g, nt = w.nt;
+    const int64_t row = (int64_t)w.mt * BM + row_in_tile;
     const float alpha = 1.0f / (p.a_gs[g] * p.b_gs[g]);
 
     if constexpr (EPI == kEpiBf16) {
@@ -387,86 +506,214 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
   }
 }
 
-template <int EPI>
+template <int EPI, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid_constant__ GemmArgs p) {
+  using C = Cfg<PAIR>;
   extern __shared__ uint8_t smem_raw[];
-  const SmemLayout L = carve(smem_raw);
+  const SmemLayout L = carve<PAIR>(smem_raw, p.G);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   pdl_trigger();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(smem_u32(&L.full[s]), 1);
       mbar_init(smem_u32(&L.empty[s]), 1);
+      mbar_init(smem_u32(&L.sf_full[s]), PAIR ? 8 : 4);  // scale warps of this CTA (and of the peer)
     }
     mbar_init(smem_u32(L.acc_full), 1);
-    mbar_init(smem_u32(L.acc_empty), NUM_EPI_WARPS);
+    mbar_init(smem_u32(L.acc_empty), PAIR ? 2 * NUM_EPI_WARPS : NUM_EPI_WARPS);
     mbar_init(smem_u32(L.drain), 1);
-    mbar_init(smem_u32(L.drain_cp), 1);
-    for (int st = 0; st < STAGES; ++st) mbar_init(smem_u32(&L.sf_full[st]), 1);
     *L.abort_flag = 0;
     fence_mbar_init();
   }
   pdl_wait();  // everything below reads what earlier kernels wrote
   for (int i = threadIdx.x; i <= p.G; i += blockDim.x) L.offsets[i] = p.padded_offsets[i];
-  if (warp == 1) {
-    tmem_alloc(smem_u32(L.tmem_slot), TMEM_COLS);
-    tmem_relinquish();
-  }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&p.tmap_a);
-    prefetch_tmap(&p.tmap_b);
+  __syncthreads();
+  if (warp == 0) {  // work units per group (m-tiles, or pairs of m-tiles), exclusive prefix
+    int carry = 0;
+    for (int base = 0; base < p.G; base += 32) {
+      const int g = base + lane;
+      int c = 0;
+      if (g < p.G) {
+        const int tiles = (L.offsets[g + 1] - L.offsets[g]) / BM;
+        c = PAIR ? (tiles + 1) >> 1 : tiles;
+      }
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+      }
+      if (g < p.G) L.unit_off[g] = carry + incl - c;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      L.unit_off[p.G] = carry;
+      prefetch_tmap(&p.tmap_a);
+      prefetch_tmap(&p.tmap_b);
+    }
+  } else if (warp == 1) {
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(L.tmem_slot), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(L.tmem_slot), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // both CTAs' barriers initialised, TMEM allocated
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *L.tmem_slot;
-  const int total = (L.offsets[p.G] / BM) * p.n_tiles;
+  const int total = L.unit_off[p.G] * p.n_tiles;
+  const int start = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
-  if (warp == 0) {
-    if (lane == 0) producer_loop(p, L, total);
-  } else if (warp == 1) {
-    if (lane == 0) mma_loop(p, L, total, tmem);
-  } else if (warp < COPIER_WARP) {
-    epilogue_loop<EPI>(p, L, total, tmem);
+  // each warpgroup changes its register budget first thing in its own branch
+  if (warp < EPI_WARP0) {
+    regs_dec<REGS_SMALL>();
+    if (warp == 0) {
+      if (lane == 0) producer_loop<PAIR>(p, L, total, start, step, rank);
+    } else if (warp == 1) {
+      if (lane == 0 && rank == 0) mma_loop<PAIR>(p, L, total, start, step, tmem);
+    }
+  } else if (warp < SF_WARP0) {
+    regs_inc<REGS_EPI>();
+    epilogue_loop<EPI, PAIR>(p, L, total, start, step, tmem, rank);
   } else {
-    if (lane == 0) copier_loop(p, L, total, tmem);
+    regs_dec<REGS_SMALL>();
+    sf_loop<PAIR>(p, L, total, start, step, tmem, rank);
   }
+  __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // no CTA frees TMEM or exits while its peer may still touch it
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, TMEM_COLS);
+    else tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
-template <int EPI>
-cudaError_t launch_one(const GemmArgs& a, int grid, cudaStream_t s, bool pdl) {
+// Raises the kernel's dynamic shared-memory limit (once per device).
+// Also checks that the kernel was allocated exactly REGS_LAUNCH registers per
+// thread: setmaxnreg.inc waits for registers the other warpgroups release,
+// and the split above is sized for that allocation (a smaller one would make
+// the increase wait for ever), so the kernel is never launched otherwise.
+template <int EPI, bool PAIR>
+cudaError_t configure(int dev) {
   static int configured_device = -1;
+  if (configured_device == dev) return cudaSuccess;
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, nvfp4_gemm_kernel<EPI, PAIR>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != REGS_LAUNCH || fa.maxThreadsPerBlock < NUM_THREADS) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(nvfp4_gemm_kernel<EPI, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_bytes_for<PAIR>(MAX_GROUPS));
+  if (e == cudaSuccess) configured_device = dev;
+  return e;
+}
+
+// Largest number of co-resident CTA pairs for one kernel instance (cached per
+// device); 0 when pairs cannot be launched.
+template <int EPI>
+int max_pairs(int dev) {
+  static int cached_dev = -1, cached = 0;
+  if (cached_dev == dev) return cached;
+  if (configure<EPI, true>(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem_bytes_for<true>(MAX_GROUPS);
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel<EPI, true>, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cached_dev = dev;
+  cached = n;
+  return n;
+}
+
+// grid = number of CTAs (single) or of CTA pairs (pair).
+template <int EPI, bool PAIR>
+cudaError_t launch_one(const GemmArgs& a, int grid, cudaStream_t s, bool pdl) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const size_t smem = gemm_smem_bytes(MAX_GROUPS);
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(nvfp4_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
+  if ((e = configure<EPI, PAIR>(dev)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(PAIR ? 2 * grid : grid);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem_bytes_for<PAIR>(a.G);
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  int n = 0;
+  if (PAIR) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = 2;
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
   }
-  return launch_kernel(nvfp4_gemm_kernel<EPI>, dim3(grid), dim3(NUM_THREADS), gemm_smem_bytes(a.G), s, pdl, a);
+  if (pdl) {
+    at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = n ? at : nullptr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel<EPI, PAIR>, a);
+}
+
+template <int EPI>
+cudaError_t launch_kind(const GemmArgs& a, int units_upper, int num_sms, cudaStream_t s, bool pdl) {
+  if (gemm_pair_enabled()) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const int pairs = max_pairs<EPI>(dev);
+    if (pairs > 0) {
+      const int want = (units_upper + 1) / 2;
+      return launch_one<EPI, true>(a, want < pairs ? (want < 1 ? 1 : want) : pairs, s, pdl);
+    }
+  }
+  return launch_one<EPI, false>(a, units_upper < num_sms ? (units_upper < 1 ? 1 : units_upper) : num_sms, s, pdl);
 }
 
 }  // namespace
 
-size_t gemm_smem_bytes(int G) {
-  return 1024 + (size_t)STAGES * STAGE_BYTES + 8 * (3 * STAGES + 4) + 16 + 4 * (size_t)(G + 1) + 16;
+size_t gemm_smem_bytes(int G) { return smem_bytes_for<false>(G); }
+
+namespace {
+bool g_gemm_pair = false;
 }
 
-cudaError_t launch_gemm(int kind, const GemmArgs& args, int grid, cudaStream_t s, bool pdl) {
+bool gemm_pair_enabled() { return g_gemm_pair; }
+bool gemm_set_pair(bool enable) {
+  const bool prev = g_gemm_pair;
+  g_gemm_pair = enable;
+  return prev;
+}
+
+cudaError_t launch_gemm(int kind, const GemmArgs& args, int units_upper, int num_sms, cudaStream_t s, bool pdl) {
   if (args.G < 1 || args.G > MAX_GROUPS) return cudaErrorInvalidValue;
   switch (kind) {
-    case kEpiBf16: return launch_one<kEpiBf16>(args, grid, s, pdl);
-    case kEpiSwigluQuant: return launch_one<kEpiSwigluQuant>(args, grid, s, pdl);
-    case kEpiCombine: return launch_one<kEpiCombine>(args, grid, s, pdl);
-    case kEpiSwigluAmax: return launch_one<kEpiSwigluAmax>(args, grid, s, pdl);
+    case kEpiBf16: return launch_kind<kEpiBf16>(args, units_upper, num_sms, s, pdl);
+    case kEpiSwigluQuant: return launch_kind<kEpiSwigluQuant>(args, units_upper, num_sms, s, pdl);
+    case kEpiCombine: return launch_kind<kEpiCombine>(args, units_upper, num_sms, s, pdl);
+    case kEpiSwigluAmax: return launch_kind<kEpiSwigluAmax>(args, units_upper, num_sms, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

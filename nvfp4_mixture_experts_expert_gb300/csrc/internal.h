@@ -113,7 +113,13 @@ size_t gemm_smem_bytes(int G);
 
 // abi.cu: sets the text nvfp4_last_error() returns on the calling thread.
 void set_last_error(const char* msg);
-cudaError_t launch_gemm(int kind, const GemmArgs& args, int grid, cudaStream_t s, bool pdl = false);
+// units_upper: an upper bound on the work items (128-row m-tiles x n-tiles);
+// the grid is sized from it and from the SM count / co-resident CTA pairs.
+cudaError_t launch_gemm(int kind, const GemmArgs& args, int units_upper, int num_sms, cudaStream_t s,
+                        bool pdl = false);
+// Whether GEMMs run as CTA pairs (cta_group::2) or single CTAs; set returns the previous choice.
+bool gemm_pair_enabled();
+bool gemm_set_pair(bool enable);
 cudaError_t gemm_status_ptr(int** ptr);
 cudaError_t gemm_read_status(int* out, int reset);
 

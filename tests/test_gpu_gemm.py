@@ -69,15 +69,39 @@ def check(pb, D):
         assert np.all(np.abs(got - ref) <= tol), (g, np.max(np.abs(got - ref) - tol))
 
 
+@pytest.fixture(params=[True, False], ids=["pair", "single"])
+def cta_pair(request):
+    """Runs the test with the paired-CTA GEMM (cta_group::2) and with one CTA per tile."""
+    from nvfp4_mixture_experts_expert_gb300 import binding as B
+    prev = B.nvfp4_gemm_set_cta_pair(request.param)
+    yield request.param
+    B.nvfp4_gemm_set_cta_pair(prev)
+
+
 @pytest.mark.parametrize("counts,N,K", [
-    ([128], 256, 256),               # one tile, one K stage
-    ([100, 0, 260], 512, 320),       # ragged groups, an empty group, partial last K stage
+    ([128], 256, 256),               # one tile, one K stage (a pair whose second tile does not exist)
+    ([100, 0, 260], 512, 320),       # ragged groups, an empty group, partial last K stage, odd tile counts
     ([37, 129], 256, 128),           # K = 128: a single half stage
     ([300], 768, 1024),              # several tiles and K stages
+    ([256, 384, 1, 640], 256, 512),  # even and odd tile counts side by side
 ])
-def test_grouped_gemm_matches_oracle(counts, N, K):
+def test_grouped_gemm_matches_oracle(counts, N, K, cta_pair):
     pb = make_problem(counts, N, K, seed=sum(counts) + N + K)
     check(pb, run_gpu(pb))
+
+
+def test_pair_and_single_cta_gemm_are_bit_identical():
+    from nvfp4_mixture_experts_expert_gb300 import binding as B
+    pb = make_problem([300, 0, 129, 640, 5], 512, 768, seed=11)
+    prev = B.nvfp4_gemm_set_cta_pair(True)
+    try:
+        d_pair = run_gpu(pb)
+        B.nvfp4_gemm_set_cta_pair(False)
+        d_single = run_gpu(pb)
+    finally:
+        B.nvfp4_gemm_set_cta_pair(prev)
+    for g, c in enumerate(pb["counts"]):
+        np.testing.assert_array_equal(d_pair[g, :c], d_single[g, :c])
 
 
 def test_gemm_rows_beyond_counts_are_not_written():
@@ -131,7 +155,7 @@ def test_gemm_device_status_is_clean():
     assert B.nvfp4_device_status(reset=False) == 0
 
 
-def test_stalled_pipeline_reports_timeout_and_context_survives():
+def test_stalled_pipeline_reports_timeout_and_context_survives(cta_pair):
     """Failure detection without a fault: with the TMA producer switched off the
     consumers' bounded waits run out, the kernel reports a device timeout,
     frees its tensor memory and returns; the same process then runs a correct

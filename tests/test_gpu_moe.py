@@ -132,6 +132,35 @@ def test_moe_hidden_16_byte_aligned_and_half_chunk_rows():
     check_all(wl, orc, w, fwd, out)
 
 
+def test_moe_pair_and_single_cta_gemms_are_bit_identical():
+    """The MoE forward with the paired-CTA GEMMs and with single-CTA GEMMs:
+    identical L2 inputs (SwiGLU + requantization epilogue) and outputs
+    (routing-weighted combine epilogue), bit for bit."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api, binding as B
+    wl = W.moe_workload(300, 512, 256, 5, 3, 41, logit_bias_std=1.5)
+    orc = OracleMoE(wl)
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    fwd = api.MoEForward(wl.T, wl.H, wl.I, wl.E, wl.top_k)
+    res = {}
+    prev = B.nvfp4_gemm_set_cta_pair(True)
+    try:
+        for pair in (True, False):
+            B.nvfp4_gemm_set_cta_pair(pair)
+            out = fwd(bf16_dev(wl.hidden), dev(wl.logits), w, dev(orc.a1_gs), dev(orc.a2_gs), wl.gate_limit,
+                      wl.up_limit)
+            torch.cuda.synchronize()
+            P = int(host(fwd.view("meta", torch.int32, 1))[0])
+            res[pair] = (host(out.view(torch.int16)), host(fwd.view("a2", torch.uint8, P * wl.I // 2)),
+                         host(fwd.view("sfa2", torch.uint8, P * wl.I // 16)))
+    finally:
+        B.nvfp4_gemm_set_cta_pair(prev)
+    counts = orc.meta["counts"]
+    assert (np.asarray(counts) > 128).any() and ((np.asarray(counts) + 127) // 128 % 2 == 1).any()
+    for a, b in zip(res[True], res[False]):
+        np.testing.assert_array_equal(a, b)
+
+
 def test_moe_zero_tokens_is_a_no_op():
     from nvfp4_mixture_experts_expert_gb300 import binding as B
     import torch
