@@ -248,16 +248,21 @@ int nvfp4_device_status(int* status_out, int reset);
 
 /* GEMM variant (process-wide; every GEMM above and the MoE forward).
  *
- * enable != 0: a cluster of two CTAs on two SMs computes each 256 x 256 output
+ * A "pair" GEMM runs a cluster of two CTAs on two SMs per 256 x 256 output
  * tile with the paired tensor-core instructions (tcgen05 cta_group::2); each
- * SM stages half of the B tile, so it reads fewer operand bytes per MMA.
- * enable == 0: one CTA per 128 x 256 tile.  Both variants compute every output
- * element with the same arithmetic in the same order, so their results are
- * bit-identical.  Default: disabled (the single-CTA variant is the faster of
- * the two on the MoE layer).  Returns the previous setting (0 / 1).
- * Not thread-safe with respect to launches issued concurrently from other
- * host threads; no device work, no error. */
-int nvfp4_gemm_set_cta_pair(int enable);
+ * SM stages half of the B tile, so it reads fewer operand bytes per MMA, and
+ * the routing-weighted L2 epilogue stores through shared-memory staging.  A
+ * "single" GEMM runs one CTA per 128 x 256 tile.  Both compute every output
+ * element with the same arithmetic in the same order: results are
+ * bit-identical.
+ *   mode 0  single CTAs for every GEMM
+ *   mode 1  pairs for every GEMM with at most 256 groups
+ *   mode 2  pairs for the MoE L2 GEMM only (default; measured fastest)
+ * prev_mode (may be null) receives the previous mode.  Returns NVFP4_OK, or
+ * NVFP4_ERR_INVALID_ARG (mode unchanged) for a mode outside 0..2.  Not
+ * thread-safe with respect to launches issued concurrently from other host
+ * threads; no device work. */
+int nvfp4_gemm_set_cta_pair(int mode, int* prev_mode);
 
 /*
  * Optional per-stage timing of nvfp4_moe_forward: when set, the forward

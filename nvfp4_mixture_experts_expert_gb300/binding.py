@@ -82,7 +82,7 @@ _moe_calibrate = _sig("nvfp4_moe_calibrate", c_int, [c_ptr, c_ptr, c_i64, c_i64,
                                                      c_ptr])
 _device_status = _sig("nvfp4_device_status", c_int, [ctypes.POINTER(c_int), c_int])
 _stage_events = _sig("nvfp4_moe_set_stage_events", c_int, [ctypes.POINTER(c_ptr), c_int])
-_gemm_set_cta_pair = _sig("nvfp4_gemm_set_cta_pair", c_int, [c_int])
+_gemm_set_cta_pair = _sig("nvfp4_gemm_set_cta_pair", c_int, [c_int, ctypes.POINTER(c_int)])
 
 
 def _p(t):
@@ -193,9 +193,12 @@ def nvfp4_device_status(reset=False):
     return st.value
 
 
-def nvfp4_gemm_set_cta_pair(enable):
-    """Select the paired-CTA (True) or single-CTA (False) GEMM; returns the previous choice."""
-    return bool(_gemm_set_cta_pair(1 if enable else 0))
+def nvfp4_gemm_set_cta_pair(mode):
+    """GEMM variant: 0 / False single CTAs, 1 / True CTA pairs, 2 pairs for the MoE L2
+    GEMM only (default).  Returns the previous mode."""
+    prev = c_int(-1)
+    _check(_gemm_set_cta_pair(int(mode), ctypes.byref(prev)))
+    return prev.value
 
 
 def nvfp4_moe_set_stage_events(events):

@@ -528,7 +528,13 @@ int nvfp4_moe_calibrate(const void* hidden, const float* router_logits, int64_t 
   return NVFP4_OK;
 }
 
-int nvfp4_gemm_set_cta_pair(int enable) { return gemm_set_pair(enable != 0) ? 1 : 0; }
+int nvfp4_gemm_set_cta_pair(int mode, int* prev_mode) {
+  g_err[0] = 0;
+  if (mode < 0 || mode > 2) return fail(NVFP4_ERR_INVALID_ARG, "mode must be 0, 1 or 2");
+  const int prev = gemm_set_pair_mode(mode);
+  if (prev_mode) *prev_mode = prev;
+  return NVFP4_OK;
+}
 
 int nvfp4_device_status(int* status_out, int reset) {
   g_err[0] = 0;

@@ -87,12 +87,15 @@ constexpr int REGS_EPI = 184;     // WG1 and WG2 after setmaxnreg.inc
 static_assert(128 * (2 * REGS_SMALL + 2 * REGS_EPI) <= NUM_THREADS * REGS_LAUNCH,
               "the register split must fit the launch allocation");
 constexpr int MAX_GROUPS = 1024;
+constexpr int MAX_GROUPS_PAIR = 256;        // the pair variant's shared memory also holds the staging buffers
+constexpr int EPI_STAGE_BYTES = 32 * 128;   // per epilogue warp (pair): 32 rows x 64 bf16 columns
 
 template <bool PAIR>
 struct Cfg {
   static constexpr int STAGES = PAIR ? 5 : 4;
   static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK_BYTES;  // B rows this CTA loads per stage
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int EPI_BYTES = PAIR ? NUM_EPI_WARPS * EPI_STAGE_BYTES : 0;
   static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
 };
@@ -104,6 +107,7 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
 
 struct SmemLayout {
   uint8_t* stages;
+  uint8_t* epi_stage;  // pair variant: per-warp output staging for coalesced stores
   uint64_t* full;
   uint64_t* empty;
   uint64_t* acc_full;
@@ -122,7 +126,8 @@ __device__ __forceinline__ SmemLayout carve(uint8_t* raw, int G) {
   SmemLayout L;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   L.stages = base;
-  uint8_t* p = base + C::STAGES * C::STAGE_BYTES;
+  L.epi_stage = base + C::STAGES * C::STAGE_BYTES;
+  uint8_t* p = L.epi_stage + C::EPI_BYTES;
   L.full = reinterpret_cast<uint64_t*>(p);
   L.empty = L.full + C::STAGES;
   L.sf_full = L.empty + C::STAGES;
@@ -138,8 +143,8 @@ __device__ __forceinline__ SmemLayout carve(uint8_t* raw, int G) {
 
 template <bool PAIR>
 constexpr size_t smem_bytes_for(int G) {
-  return 1024 + (size_t)Cfg<PAIR>::STAGES * Cfg<PAIR>::STAGE_BYTES + 8 * (3 * Cfg<PAIR>::STAGES + 4) + 16 +
-         8 * (size_t)(G + 1) + 16;
+  return 1024 + (size_t)Cfg<PAIR>::STAGES * Cfg<PAIR>::STAGE_BYTES + Cfg<PAIR>::EPI_BYTES +
+         8 * (3 * Cfg<PAIR>::STAGES + 4) + 16 + 8 * (size_t)(G + 1) + 16;
 }
 
 __device__ __forceinline__ int find_group(const int* off, int G, int row) {
@@ -213,7 +218,7 @@ __device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total,
       const uint8_t* sfb1 = p.sfb + w.g * p.sfb_group_bytes + (int64_t)(b_r1 >> 7) * kt * 512;
       for (int kb = 0; kb < p.num_kb; ++kb) {
         const int nmma = min(4, (p.K - kb * 256) / 64);
-        if (!wait_bounded<PAIR>(smem_u32(&L.empty[stage]), phase ^ 1u, abort, p.status, p.timeout_ns)) {
+        if (!wait_bounded(smem_u32(&L.empty[stage]), phase ^ 1u, abort, p.status, p.timeout_ns)) {
           ok = false;
           break;
         }
@@ -249,7 +254,7 @@ __device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total,
   } else if constexpr (PAIR) {
     // the leader's last multicast releases land in this CTA before it may exit
     for (int i = 0; i < C::STAGES; ++i) {
-      if (!wait_bounded<true>(smem_u32(&L.empty[stage]), phase ^ 1u, abort, p.status, p.timeout_ns)) break;
+      if (!wait_bounded(smem_u32(&L.empty[stage]), phase ^ 1u, abort, p.status, p.timeout_ns)) break;
       if (++stage == C::STAGES) {
         stage = 0;
         phase ^= 1u;
@@ -329,14 +334,14 @@ __device__ void mma_loop(const GemmArgs& p, const SmemLayout& L, int total, int 
   uint32_t stage = 0, phase = 0, acc_phase = 0;
   bool issued_any = false;
   for (int it = start; it < total && !*abort; it += step) {
-    if (!wait_bounded<PAIR>(smem_u32(L.acc_empty), acc_phase ^ 1u, abort, p.status, p.timeout_ns)) break;
+    if (!wait_bounded(smem_u32(L.acc_empty), acc_phase ^ 1u, abort, p.status, p.timeout_ns)) break;
     tc_fence_after();
     bool ok = true;
     for (int kb = 0; kb < p.num_kb; ++kb) {
       const int nmma = min(4, (p.K - kb * 256) / 64);
       // sf_full[stage] implies full[stage] (in both CTAs of a pair): the scale
       // warps waited for the stage's data first
-      if (!wait_bounded<PAIR>(smem_u32(&L.sf_full[stage]), phase, abort, p.status, p.timeout_ns)) {
+      if (!wait_bounded(smem_u32(&L.sf_full[stage]), phase, abort, p.status, p.timeout_ns)) {
         ok = false;
         break;
       }
@@ -395,7 +400,7 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
   uint32_t acc_phase = 0;
   for (int it = start; it < total; it += step) {
     int ok = 1;
-    if (lane == 0) ok = wait_bounded<PAIR>(smem_u32(L.acc_full), acc_phase, abort, p.status, p.timeout_ns);
+    if (lane == 0) ok = wait_bounded(smem_u32(L.acc_full), acc_phase, abort, p.status, p.timeout_ns);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) break;
     __syncwarp();
@@ -450,22 +455,37 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
       }
     } else if constexpr (EPI == kEpiSwigluQuant) {
       // output features [nt*128 + half*64, +64) of one row = 4 quantization blocks
+      // (pairs of features per instruction where the arithmetic allows it;
+      // every value is rounded exactly as by the scalar operations)
       const float qgs = p.q_gs[g];
+      const float rcp6 = __frcp_rn(6.0f);
+      const uint64_t alpha2 = f2_pack(alpha, alpha), qgs2 = f2_pack(qgs, qgs);
       uint32_t scales = 0;
       uint32_t words[8];
 #pragma unroll
       for (int blk = 0; blk < 4; ++blk) {
-        float xs[16];
+        uint64_t xs2[8];
+        float b = 0.f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int f = blk * 16 + i;
-          const float h = silu_clamped_product(__uint_as_float(v[f >> 5][f & 31]) * alpha,
-                                               __uint_as_float(v[2 + (f >> 5)][f & 31]) * alpha, p.gate_limit,
-                                               p.up_limit);
-          xs[i] = __fmul_rn(__uint_as_float(f32_to_bf16_rn(h) << 16), qgs);
+        for (int q = 0; q < 8; ++q) {
+          const int f = blk * 16 + 2 * q;  // features f, f+1: same 32-column load
+          float g0, g1, u0, u1;
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(v[f >> 5][f & 31]), __uint_as_float(v[f >> 5][(f & 31) + 1])),
+                           alpha2),
+                    g0, g1);
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(v[2 + (f >> 5)][f & 31]),
+                                   __uint_as_float(v[2 + (f >> 5)][(f & 31) + 1])),
+                           alpha2),
+                    u0, u1);
+          const uint32_t hb = pack_bf16x2(silu_clamped_product(g0, u0, p.gate_limit, p.up_limit),
+                                          silu_clamped_product(g1, u1, p.gate_limit, p.up_limit));
+          xs2[q] = f2_mul(f2_pack(bf16_lo(hb), bf16_hi(hb)), qgs2);
+          float x0, x1;
+          f2_unpack(xs2[q], x0, x1);
+          b = fmaxf(b, fmaxf(fabsf(x0), fabsf(x1)));
         }
         uint32_t lo, hi;
-        scales |= quant_block16(xs, lo, hi) << (8 * blk);
+        scales |= quant_block16_pairs(xs2, b, rcp6, lo, hi) << (8 * blk);
         words[blk * 2] = lo;
         words[blk * 2 + 1] = hi;
       }
@@ -487,6 +507,37 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
 #pragma unroll
       for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
       if (lane == 0 && m) atomicMax(&p.amax_bits[g], m << 16);
+    } else if constexpr (PAIR) {  // kEpiCombine through the warp's staging buffer
+      // Routing-weighted rows in slot order for the token combine; pad rows
+      // carry weight 0 and are written as zeros (nothing reads them).  Each
+      // 64-column chunk goes through 4 KB of shared memory (16-byte units
+      // XOR-swizzled by row, conflict-free both ways) so every store
+      // instruction writes 4 whole 128-byte row segments.
+      uint8_t* buf = L.epi_stage + (warp - EPI_WARP0) * EPI_STAGE_BYTES;
+      const float wgt = p.row_w[row] * alpha;
+      uint16_t* ybase = p.y + ((int64_t)w.mt * BM + quarter * 32) * p.H + (int64_t)nt * BN + half * (BN / 2);
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          pk[j] = pack_bf16x2(__uint_as_float(v[2 * c2][2 * j]) * wgt, __uint_as_float(v[2 * c2][2 * j + 1]) * wgt);
+          pk[16 + j] = pack_bf16x2(__uint_as_float(v[2 * c2 + 1][2 * j]) * wgt,
+                                   __uint_as_float(v[2 * c2 + 1][2 * j + 1]) * wgt);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(buf + lane * 128 + ((u ^ (lane & 7)) << 4)) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = i * 4 + (lane >> 3), u = lane & 7;
+          const uint4 val = *reinterpret_cast<const uint4*>(buf + r * 128 + ((u ^ (r & 7)) << 4));
+          *reinterpret_cast<uint4*>(ybase + (int64_t)r * p.H + c2 * 64 + u * 8) = val;
+        }
+        __syncwarp();
+      }
     } else {  // kEpiCombine: routing-weighted rows, stored in slot order for the token combine
       if (p.sorted_ids[row] >= 0) {
         const float wgt = p.row_w[row] * alpha;
@@ -610,7 +661,7 @@ cudaError_t configure(int dev) {
   if (e != cudaSuccess) return e;
   if (fa.numRegs != REGS_LAUNCH || fa.maxThreadsPerBlock < NUM_THREADS) return cudaErrorInvalidConfiguration;
   e = cudaFuncSetAttribute(nvfp4_gemm_kernel<EPI, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem_bytes_for<PAIR>(MAX_GROUPS));
+                           (int)smem_bytes_for<PAIR>(PAIR ? MAX_GROUPS_PAIR : MAX_GROUPS));
   if (e == cudaSuccess) configured_device = dev;
   return e;
 }
@@ -628,7 +679,7 @@ int max_pairs(int dev) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);
   cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = smem_bytes_for<true>(MAX_GROUPS);
+  cfg.dynamicSmemBytes = smem_bytes_for<true>(MAX_GROUPS_PAIR);
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = 2;
@@ -679,7 +730,7 @@ cudaError_t launch_one(const GemmArgs& a, int grid, cudaStream_t s, bool pdl) {
 
 template <int EPI>
 cudaError_t launch_kind(const GemmArgs& a, int units_upper, int num_sms, cudaStream_t s, bool pdl) {
-  if (gemm_pair_enabled()) {
+  if (gemm_pair_enabled(EPI) && a.G <= MAX_GROUPS_PAIR) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -697,13 +748,18 @@ cudaError_t launch_kind(const GemmArgs& a, int units_upper, int num_sms, cudaStr
 size_t gemm_smem_bytes(int G) { return smem_bytes_for<false>(G); }
 
 namespace {
-bool g_gemm_pair = false;
+int g_gemm_pair_mode = 2;
 }
 
-bool gemm_pair_enabled() { return g_gemm_pair; }
-bool gemm_set_pair(bool enable) {
-  const bool prev = g_gemm_pair;
-  g_gemm_pair = enable;
+// Mode 2 pairs only the routing-weighted L2 epilogue, whose output stores go
+// through the pair variant's staging buffers; the SwiGLU L1 GEMM measured
+// faster as single CTAs.
+bool gemm_pair_enabled(int kind) {
+  return g_gemm_pair_mode == 1 || (g_gemm_pair_mode == 2 && kind == kEpiCombine);
+}
+int gemm_set_pair_mode(int mode) {
+  const int prev = g_gemm_pair_mode;
+  g_gemm_pair_mode = mode;
   return prev;
 }
 

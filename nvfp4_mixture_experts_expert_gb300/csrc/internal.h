@@ -117,9 +117,11 @@ void set_last_error(const char* msg);
 // the grid is sized from it and from the SM count / co-resident CTA pairs.
 cudaError_t launch_gemm(int kind, const GemmArgs& args, int units_upper, int num_sms, cudaStream_t s,
                         bool pdl = false);
-// Whether GEMMs run as CTA pairs (cta_group::2) or single CTAs; set returns the previous choice.
-bool gemm_pair_enabled();
-bool gemm_set_pair(bool enable);
+// Whether a GEMM with this epilogue runs as CTA pairs (cta_group::2) or single
+// CTAs.  Mode: 0 single, 1 pair, 2 pair for the routing-weighted L2 epilogue
+// only; set returns the previous mode.
+bool gemm_pair_enabled(int kind);
+int gemm_set_pair_mode(int mode);
 cudaError_t gemm_status_ptr(int** ptr);
 cudaError_t gemm_read_status(int* out, int reset);
 

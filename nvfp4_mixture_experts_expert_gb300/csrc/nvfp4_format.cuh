@@ -89,6 +89,53 @@ __device__ __forceinline__ uint32_t quant_block16(const float (&xs)[16], uint32_
   return s;
 }
 
+// Packed pairs of FP32 values (element 2j in the low half, 2j+1 in the high
+// half), each half rounded exactly like its scalar operation.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// quant_block16 on 8 packed pairs of already globally-scaled values, the
+// block maximum b given: the same arithmetic, two elements per instruction
+// where it can be (b / 6 through the same exact quotient, 6 being an E4M3
+// value; rcp6 = RN(1/6)).
+__device__ __forceinline__ uint32_t quant_block16_pairs(const uint64_t (&xs2)[8], float b, float rcp6, uint32_t& lo,
+                                                        uint32_t& hi) {
+  lo = hi = 0u;
+  if (!(b >= kUnderflowAmax)) return 0u;
+  const uint32_t s = e4m3_code(div_by_scale(fminf(b, 3.40282347e38f), 6.0f, rcp6));
+  const float d = e4m3_value(s);
+  const float y = __frcp_rn(d);
+  const uint64_t y2 = f2_pack(y, y), nd2 = f2_pack(-d, -d);
+  uint32_t out[2] = {0u, 0u};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint64_t q0 = f2_mul(xs2[j], y2);
+    const uint64_t r = f2_fma(q0, nd2, xs2[j]);
+    float ql, qh;
+    f2_unpack(f2_fma(r, y2, q0), ql, qh);
+    out[j >> 2] |= e2m1x2_code(ql, qh) << ((j & 3) * 8);
+  }
+  lo = drop_negative_zero(out[0]);
+  hi = drop_negative_zero(out[1]);
+  return s;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 

@@ -138,9 +138,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-// Arrive on an mbarrier in another CTA of the cluster (address from mapa_shared).
+// Arrive on an mbarrier in another CTA of the cluster (address from
+// mapa_shared).  Default (CTA-scope release) semantics: what the arrival
+// publishes is TMEM and TMA-written shared memory, ordered by the tcgen05
+// fences and the barrier phase, not generic stores; a cluster-scope release
+// would add a memory barrier to every stage.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05

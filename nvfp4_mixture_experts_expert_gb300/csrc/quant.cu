@@ -189,27 +189,6 @@ __device__ __forceinline__ void ld_block32(const uint16_t* p, uint32_t (&w)[8]) 
   }
 }
 
-// Packed pairs of FP32 values (element 2j in the low half, 2j+1 in the high
-// half), each half rounded exactly like its scalar operation.
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-
 // max |x| over the 16 bf16 values of a block, as an FP32 value.
 __device__ __forceinline__ float block_amax_bf16(const uint32_t (&w)[8]) {
   uint32_t m = 0u;

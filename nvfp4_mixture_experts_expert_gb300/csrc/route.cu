@@ -8,9 +8,10 @@
 //                 (softmax renormalised over the top-k); per-block expert
 //                 histogram in shared memory.
 //  slot_scan      one block: per-expert exclusive scan of the (expert-major)
-//                 block histograms,
-//                 padded offsets (multiples of 128, multi-chunk experts --
-//                 vllm page "Bug 9"), the m-tile -> expert table, pad rows.
+//                 block histograms (a warp per expert), padded offsets
+//                 (multiples of 128, multi-chunk experts -- vllm page "Bug 9")
+//                 by a warp scan, the m-tile -> expert table (a thread per
+//                 m-tile), pad rows.
 //  slot_scatter   per block, the stable rank of each assignment inside its
 //                 expert (ascending flat index t*k+j) via warp match/ballot,
 //                 giving the slot row; writes sorted_token_ids, row weights and
@@ -46,9 +47,14 @@ __device__ __forceinline__ float key_value(uint64_t key) {
 }
 __device__ __forceinline__ int key_expert(uint64_t key) { return (int)(0xFFFFFFFFu - (uint32_t)key); }
 
-// One warp per token, all selection state in registers: k rounds of a warp
-// arg-max over packed keys; then lane j < k computes exp(l_j - l_max) and the
-// warp sum gives the renormalised weights.
+// One warp per token, all selection state in registers (NK keys per lane,
+// expert e in lane e % 32, slot e / 32).  Each of the k rounds takes the
+// lane-local best key and two warp reductions: the max of the logit bits,
+// then, among lanes holding that logit, the max of the low (inverted
+// expert) bits, i.e. the lowest expert.  Lane j keeps the j-th selection;
+// then lane j < k computes exp(l_j - l_max) and the warp sum gives the
+// renormalised weights.
+template <int NK>
 __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
     const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ ids, float* __restrict__ w,
     int32_t* __restrict__ block_counts) {
@@ -59,30 +65,27 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
   __syncthreads();
   const int64_t t0 = (int64_t)blockIdx.x * kRouteTokensPerBlock;
   const int64_t t1 = min(T, t0 + kRouteTokensPerBlock);
-  const int per_lane = (E + 31) / 32;
   for (int64_t t = t0 + warp; t < t1; t += kRouteWarps) {
-    uint64_t key[kMaxExperts / 32];
+    uint64_t key[NK];
 #pragma unroll
-    for (int i = 0; i < kMaxExperts / 32; ++i) {
+    for (int i = 0; i < NK; ++i) {
       const int e = i * 32 + lane;
-      key[i] = (i < per_lane && e < E) ? route_key(__ldg(logits + t * E + e), e) : 0ull;
+      key[i] = e < E ? route_key(__ldg(logits + t * E + e), e) : 0ull;
     }
     uint64_t mine = 0ull;  // lane j keeps the j-th selected key
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) {
       if (j >= k) break;
-      uint64_t best = 0ull;
+      uint64_t best = key[0];
 #pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; ++i) best = key[i] > best ? key[i] : best;
+      for (int i = 1; i < NK; ++i) best = key[i] > best ? key[i] : best;
+      const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32));
+      const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32) == hi ? (uint32_t)best : 0u);
+      const uint64_t win = ((uint64_t)hi << 32) | lo;
 #pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
-        best = other > best ? other : best;
-      }
-#pragma unroll
-      for (int i = 0; i < kMaxExperts / 32; ++i)
-        if (key[i] == best) key[i] = 0ull;  // keys are unique: only the winner's lane matches
-      if (lane == j) mine = best;
+      for (int i = 0; i < NK; ++i)
+        if (key[i] == win) key[i] = 0ull;  // keys are unique: only the winner's lane matches
+      if (lane == j) mine = win;
     }
     const uint64_t top = __shfl_sync(0xffffffffu, mine, 0);
     const float z = lane < k ? expf(key_value(mine) - key_value(top)) : 0.f;
@@ -150,22 +153,40 @@ __global__ void __launch_bounds__(1024) slot_scan_kernel(int32_t* __restrict__ b
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (warp == 0) {  // padded offsets: exclusive scan of the 128-rounded counts
     int off = 0;
-    for (int e = 0; e < E; ++e) {
-      s_off[e] = off;
-      off += (s_cnt[e] + 127) / 128 * 128;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int c = e < E ? (s_cnt[e] + 127) / 128 * 128 : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+      }
+      if (e < E) s_off[e] = off + incl - c;
+      off += __shfl_sync(0xffffffffu, incl, 31);
     }
-    s_off[E] = off;
-    meta[0] = off;
-    meta[1] = off / 128;
-    meta[2] = 0;
-    meta[3] = 0;
+    if (lane == 0) {
+      s_off[E] = off;
+      meta[0] = off;
+      meta[1] = off / 128;
+      meta[2] = 0;
+      meta[3] = 0;
+    }
   }
   __syncthreads();
   for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = s_off[e];
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    for (int mt = s_off[e] / 128; mt < s_off[e + 1] / 128; ++mt) tile_expert[mt] = e;
+  // m-tile -> expert: the last expert whose slot range starts at or before the tile
+  for (int mt = threadIdx.x; mt < s_off[E] / 128; mt += blockDim.x) {
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_off[mid] <= mt * 128) lo = mid;
+      else hi = mid;
+    }
+    tile_expert[mt] = lo;
+  }
   // pad rows of every slot: token -1, weight 0
   for (int i = threadIdx.x; i < E * 128; i += blockDim.x) {
     const int e = i >> 7, j = i & 127;
@@ -256,7 +277,11 @@ __global__ void __launch_bounds__(256) token_combine_kernel(const uint16_t* __re
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
                               int32_t* block_counts, cudaStream_t s) {
   const int64_t nb = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
-  route_topk_kernel<<<(unsigned)nb, kRouteWarps * 32, 0, s>>>(logits, T, E, k, ids, w, block_counts);
+  const dim3 grid((unsigned)nb), block(kRouteWarps * 32);
+  if (E <= 32) route_topk_kernel<1><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, block_counts);
+  else if (E <= 64) route_topk_kernel<2><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, block_counts);
+  else if (E <= 128) route_topk_kernel<4><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, block_counts);
+  else route_topk_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, block_counts);
   return cudaGetLastError();
 }
 

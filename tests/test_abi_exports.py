@@ -71,3 +71,18 @@ def test_gemm_and_moe_reject_unsupported_shapes(binding):
         binding.nvfp4_moe_forward(16, 16, 4, 256, 128, 4, 2, 16, 16, 16, 16, 16, 16, 16, 16, 10.0, 10.0,
                                   256, 10, 16, stream=0)
     assert ei.value.status == binding.NVFP4_ERR_WORKSPACE
+
+
+def test_gemm_variant_mode_setter(binding):
+    """Host-only: the default mode pairs only the L2 GEMM (2); set returns the
+    previous mode; an out-of-range mode is refused and leaves the mode alone."""
+    prev = binding.nvfp4_gemm_set_cta_pair(0)
+    try:
+        assert prev == 2
+        assert binding.nvfp4_gemm_set_cta_pair(1) == 0
+        with pytest.raises(binding.Nvfp4Error) as ei:
+            binding.nvfp4_gemm_set_cta_pair(3)
+        assert ei.value.status == binding.NVFP4_ERR_INVALID_ARG
+        assert binding.nvfp4_gemm_set_cta_pair(1) == 1
+    finally:
+        binding.nvfp4_gemm_set_cta_pair(prev)
