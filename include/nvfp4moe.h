@@ -257,7 +257,8 @@ int nvfp4_device_status(int* status_out, int reset);
  * bit-identical.
  *   mode 0  single CTAs for every GEMM
  *   mode 1  pairs for every GEMM with at most 256 groups
- *   mode 2  pairs for the MoE L2 GEMM only (default; measured fastest)
+ *   mode 2  pairs for the MoE L2 GEMM when T * top_k >= 256 * E (experts
+ *           average two or more 128-row tiles); single otherwise (default)
  * prev_mode (may be null) receives the previous mode.  Returns NVFP4_OK, or
  * NVFP4_ERR_INVALID_ARG (mode unchanged) for a mode outside 0..2.  Not
  * thread-safe with respect to launches issued concurrently from other host

@@ -401,6 +401,7 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
   g2.sorted_ids = sorted_ids;
   g2.row_w = row_w;
   g2.H = (int)H;
+  g2.pair_hint = T * top_k >= (int64_t)256 * E;  // experts average two or more m-tiles
   g2.status = dev->status;
   g2.timeout_ns = 2000000000ull;
 

@@ -730,7 +730,7 @@ cudaError_t launch_one(const GemmArgs& a, int grid, cudaStream_t s, bool pdl) {
 
 template <int EPI>
 cudaError_t launch_kind(const GemmArgs& a, int units_upper, int num_sms, cudaStream_t s, bool pdl) {
-  if (gemm_pair_enabled(EPI) && a.G <= MAX_GROUPS_PAIR) {
+  if (gemm_pair_enabled(EPI, a.pair_hint != 0) && a.G <= MAX_GROUPS_PAIR) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -752,10 +752,10 @@ int g_gemm_pair_mode = 2;
 }
 
 // Mode 2 pairs only the routing-weighted L2 epilogue, whose output stores go
-// through the pair variant's staging buffers; the SwiGLU L1 GEMM measured
-// faster as single CTAs.
-bool gemm_pair_enabled(int kind) {
-  return g_gemm_pair_mode == 1 || (g_gemm_pair_mode == 2 && kind == kEpiCombine);
+// through the pair variant's staging buffers, and only for large batches; the
+// SwiGLU L1 GEMM measured faster as single CTAs.
+bool gemm_pair_enabled(int kind, bool hint) {
+  return g_gemm_pair_mode == 1 || (g_gemm_pair_mode == 2 && kind == kEpiCombine && hint);
 }
 int gemm_set_pair_mode(int mode) {
   const int prev = g_gemm_pair_mode;

@@ -89,6 +89,7 @@ struct GemmArgs {
   int64_t ldd;
   int64_t gstride_d;
   int d_vec32;  // D, ldd and gstride_d allow 32-byte stores
+  int pair_hint;  // mode 2: the caller expects most groups to span at least two m-tiles
   // kEpiSwigluQuant
   uint8_t* q_out;
   uint8_t* q_sf;
@@ -119,8 +120,10 @@ cudaError_t launch_gemm(int kind, const GemmArgs& args, int units_upper, int num
                         bool pdl = false);
 // Whether a GEMM with this epilogue runs as CTA pairs (cta_group::2) or single
 // CTAs.  Mode: 0 single, 1 pair, 2 pair for the routing-weighted L2 epilogue
-// only; set returns the previous mode.
-bool gemm_pair_enabled(int kind);
+// when the caller's hint says most groups span at least two m-tiles (a group
+// of one m-tile would leave half of its pair idle); set returns the previous
+// mode.
+bool gemm_pair_enabled(int kind, bool hint);
 int gemm_set_pair_mode(int mode);
 cudaError_t gemm_status_ptr(int** ptr);
 cudaError_t gemm_read_status(int* out, int reset);
