@@ -117,35 +117,39 @@ __global__ void __launch_bounds__(1024) slot_scan_kernel(int32_t* __restrict__ b
   for (int i = threadIdx.x; i < n_zero_words; i += blockDim.x) zero_words[i] = 0u;
   __shared__ int32_t s_off[kMaxExperts + 1];
   // one warp per expert: exclusive scan over the route blocks, in place, on the
-  // expert-major histograms; each lane loads kScanPerLane consecutive counts at
-  // once so the loads overlap instead of forming a dependent chain
+  // expert-major histograms.  Lane l takes entries l, l+32, ... of each
+  // 512-entry chunk, so every load and store instruction covers one 128-byte
+  // line; the chunk's 16 columns are scanned across the warp one after the
+  // other (independent shuffle chains, a running carry).
   constexpr int kScanPerLane = 16;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   for (int e = warp; e < E; e += nwarps) {
     int32_t* row = block_counts + (int64_t)e * nblocks;
     int carry = 0;
     for (int base = 0; base < nblocks; base += 32 * kScanPerLane) {
-      const int b0 = base + lane * kScanPerLane;
       int v[kScanPerLane];
-      int local = 0;
 #pragma unroll
       for (int i = 0; i < kScanPerLane; ++i) {
-        v[i] = b0 + i < nblocks ? row[b0 + i] : 0;
-        local += v[i];
+        const int b = base + i * 32 + lane;
+        v[i] = b < nblocks ? row[b] : 0;
       }
-      int incl = local;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int x = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += x;
-      }
-      int run = carry + incl - local;
 #pragma unroll
       for (int i = 0; i < kScanPerLane; ++i) {
-        if (b0 + i < nblocks) row[b0 + i] = run;
-        run += v[i];
+        int incl = v[i];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int x = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += x;
+        }
+        const int excl = carry + incl - v[i];
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+        v[i] = excl;
       }
-      carry += __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+      for (int i = 0; i < kScanPerLane; ++i) {
+        const int b = base + i * 32 + lane;
+        if (b < nblocks) row[b] = v[i];
+      }
     }
     if (lane == 0) {
       s_cnt[e] = carry;
