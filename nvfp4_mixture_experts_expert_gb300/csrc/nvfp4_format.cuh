@@ -48,6 +48,22 @@ __device__ __forceinline__ uint32_t e2m1x2_code(float lo, float hi) {
   return r;
 }
 
+// Eight E2M1 codes in one word: element 2j in the low nibble of byte j
+// (four paired conversions into byte registers, packed by one move).
+__device__ __forceinline__ uint32_t e2m1x8_word(float q0, float q1, float q2, float q3, float q4, float q5, float q6,
+                                                float q7) {
+  uint32_t w;
+  asm("{\n.reg .b8 b0, b1, b2, b3;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      "mov.b32 %0, {b0, b1, b2, b3};\n}"
+      : "=r"(w)
+      : "f"(q0), "f"(q1), "f"(q2), "f"(q3), "f"(q4), "f"(q5), "f"(q6), "f"(q7));
+  return w;
+}
+
 // Clear the sign bit of every nibble whose magnitude bits are zero (-0 -> 0).
 __device__ __forceinline__ uint32_t drop_negative_zero(uint32_t w) {
   const uint32_t mag = w & 0x77777777u;
@@ -80,12 +96,11 @@ __device__ __forceinline__ uint32_t quant_block16(const float (&xs)[16], uint32_
   const uint32_t s = e4m3_code(__fdiv_rn(b, 6.0f));
   const float d = e4m3_value(s);
   const float y = __frcp_rn(d);
-  uint32_t w[2] = {0u, 0u};
+  float q[16];
 #pragma unroll
-  for (int j = 0; j < 8; ++j)
-    w[j >> 2] |= e2m1x2_code(div_by_scale(xs[2 * j], d, y), div_by_scale(xs[2 * j + 1], d, y)) << ((j & 3) * 8);
-  lo = drop_negative_zero(w[0]);
-  hi = drop_negative_zero(w[1]);
+  for (int i = 0; i < 16; ++i) q[i] = div_by_scale(xs[i], d, y);
+  lo = drop_negative_zero(e2m1x8_word(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]));
+  hi = drop_negative_zero(e2m1x8_word(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]));
   return s;
 }
 
@@ -122,17 +137,15 @@ __device__ __forceinline__ uint32_t quant_block16_pairs(const uint64_t (&xs2)[8]
   const float d = e4m3_value(s);
   const float y = __frcp_rn(d);
   const uint64_t y2 = f2_pack(y, y), nd2 = f2_pack(-d, -d);
-  uint32_t out[2] = {0u, 0u};
+  float q[16];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const uint64_t q0 = f2_mul(xs2[j], y2);
     const uint64_t r = f2_fma(q0, nd2, xs2[j]);
-    float ql, qh;
-    f2_unpack(f2_fma(r, y2, q0), ql, qh);
-    out[j >> 2] |= e2m1x2_code(ql, qh) << ((j & 3) * 8);
+    f2_unpack(f2_fma(r, y2, q0), q[2 * j], q[2 * j + 1]);
   }
-  lo = drop_negative_zero(out[0]);
-  hi = drop_negative_zero(out[1]);
+  lo = drop_negative_zero(e2m1x8_word(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]));
+  hi = drop_negative_zero(e2m1x8_word(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]));
   return s;
 }
 

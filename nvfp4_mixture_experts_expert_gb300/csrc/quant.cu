@@ -209,18 +209,16 @@ __device__ __forceinline__ uint32_t quant_block16_bf16(const uint32_t (&w)[8], f
   const uint32_t s = e4m3_code(div_by_scale(fminf(b, 3.40282347e38f), 6.0f, rcp6));
   const float2 dy = tab[s];
   const uint64_t gs2 = f2_pack(gs, gs), y2 = f2_pack(dy.y, dy.y), nd2 = f2_pack(-dy.x, -dy.x);
-  uint32_t out[2] = {0u, 0u};
+  float q[16];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const uint64_t xs = f2_mul(f2_pack(bf16_lo(w[j]), bf16_hi(w[j])), gs2);
     const uint64_t q0 = f2_mul(xs, y2);
     const uint64_t r = f2_fma(q0, nd2, xs);
-    float ql, qh;
-    f2_unpack(f2_fma(r, y2, q0), ql, qh);
-    out[j >> 2] |= e2m1x2_code(ql, qh) << ((j & 3) * 8);
+    f2_unpack(f2_fma(r, y2, q0), q[2 * j], q[2 * j + 1]);
   }
-  lo = drop_negative_zero(out[0]);
-  hi = drop_negative_zero(out[1]);
+  lo = drop_negative_zero(e2m1x8_word(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]));
+  hi = drop_negative_zero(e2m1x8_word(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]));
   return s;
 }
 

@@ -39,3 +39,12 @@ def test_e2m1_pair_conversion_lane_order(probe):
     bad = ctypes.c_uint(999)
     assert probe.run_e2m1_pair_probe(vals.ctypes.data_as(ctypes.c_void_p), len(vals), ctypes.byref(bad)) == 0
     assert bad.value == 0
+
+
+def test_e2m1_word_pack_byte_order(probe):
+    rng = np.random.default_rng(9)
+    grid = np.array([0.0, 0.25, 0.5, 0.75, 1.0, 1.25, 1.75, 2.5, 3.0, 3.5, 5.0, 6.0, 7.0], np.float32)
+    vals = np.concatenate([grid, -grid, rng.uniform(-8, 8, 4000).astype(np.float32)])
+    bad = ctypes.c_uint(999)
+    assert probe.run_e2m1_word_probe(vals.ctypes.data_as(ctypes.c_void_p), len(vals), ctypes.byref(bad)) == 0
+    assert bad.value == 0
