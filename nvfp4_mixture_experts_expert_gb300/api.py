@@ -130,3 +130,70 @@ class MoEForward:
         off = self.layout[name]
         nbytes = count * torch.empty((), dtype=dtype).element_size()
         return self.workspace[off:off + nbytes].view(dtype)
+
+
+class HostPipeline:
+    """Streams batches from pinned host memory through one MoEForward.
+
+    submit(h_hidden, h_logits, h_out) enqueues, for one batch, the host->device
+    copy of its hidden states and router logits, the forward, and the
+    device->host copy of its output, on three CUDA streams with two device
+    buffer sets: the upload of batch i+1 and the download of batch i-1 overlap
+    the forward of batch i (the forwards themselves run in order on one stream,
+    sharing the forward's workspace).  Host tensors must be pinned; a batch's
+    h_out is complete once the event submit() returned has completed (or after
+    synchronize()).  Copies are plain cudaMemcpyAsync through torch; no
+    arithmetic happens here."""
+
+    def __init__(self, fwd: MoEForward, weights: MoEWeights, a1_gs, a2_gs, gate_limit=10.0, up_limit=10.0,
+                 device=None):
+        device = torch.device(device) if device is not None else a1_gs.device
+        self.fwd, self.w, self.a1_gs, self.a2_gs = fwd, weights, a1_gs, a2_gs
+        self.gate_limit, self.up_limit = gate_limit, up_limit
+        T, H, E = fwd.T, fwd.H, fwd.E
+        self.d_hidden = [torch.empty((T, H), dtype=torch.bfloat16, device=device) for _ in range(2)]
+        self.d_logits = [torch.empty((T, E), dtype=torch.float32, device=device) for _ in range(2)]
+        self.d_out = [torch.empty((T, H), dtype=torch.bfloat16, device=device) for _ in range(2)]
+        self.s_in = torch.cuda.Stream(device=device)
+        self.s_comp = torch.cuda.Stream(device=device)
+        self.s_out = torch.cuda.Stream(device=device)
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]    # batch's inputs are on the device
+        self.ev_comp = [torch.cuda.Event() for _ in range(2)]  # batch's forward has finished
+        self.ev_out = [torch.cuda.Event() for _ in range(2)]   # batch's output is on the host
+        self.count = 0
+        cur = torch.cuda.current_stream(device)  # weights / scales made there come first
+        for st in (self.s_in, self.s_comp, self.s_out):
+            st.wait_stream(cur)
+
+    @property
+    def h2d_bytes(self):
+        return self.d_hidden[0].numel() * 2 + self.d_logits[0].numel() * 4
+
+    @property
+    def d2h_bytes(self):
+        return self.d_out[0].numel() * 2
+
+    def submit(self, h_hidden, h_logits, h_out):
+        b = self.count & 1
+        # buffer set b was last read by the forward of batch count-2 (inputs)
+        # and by the download of batch count-2 (output)
+        self.s_in.wait_event(self.ev_comp[b])
+        with torch.cuda.stream(self.s_in):
+            self.d_hidden[b].copy_(h_hidden, non_blocking=True)
+            self.d_logits[b].copy_(h_logits, non_blocking=True)
+        self.ev_in[b].record(self.s_in)
+        self.s_comp.wait_event(self.ev_in[b])
+        self.s_comp.wait_event(self.ev_out[b])
+        self.fwd(self.d_hidden[b], self.d_logits[b], self.w, self.a1_gs, self.a2_gs, self.gate_limit,
+                 self.up_limit, out=self.d_out[b], stream=self.s_comp)
+        self.ev_comp[b].record(self.s_comp)
+        self.s_out.wait_event(self.ev_comp[b])
+        with torch.cuda.stream(self.s_out):
+            h_out.copy_(self.d_out[b], non_blocking=True)
+        self.ev_out[b].record(self.s_out)
+        self.count += 1
+        return self.ev_out[b]
+
+    def synchronize(self):
+        for s in (self.s_in, self.s_comp, self.s_out):
+            s.synchronize()

@@ -161,6 +161,35 @@ def test_moe_pair_and_single_cta_gemms_are_bit_identical():
         np.testing.assert_array_equal(a, b)
 
 
+def test_host_pipeline_matches_direct_forward():
+    """Three batches streamed from pinned host memory (uploads and downloads
+    overlapping the forwards) give the same outputs, bit for bit, as direct
+    forwards of the same batches."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    wl = W.moe_workload(200, 512, 256, 6, 2, 51)
+    orc = OracleMoE(wl)
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    a1, a2 = dev(orc.a1_gs), dev(orc.a2_gs)
+    fwd = api.MoEForward(wl.T, wl.H, wl.I, wl.E, wl.top_k)
+    rng = np.random.default_rng(5)
+    batches = []
+    for i in range(3):
+        h = bf16_dev(wl.hidden) * (1.0 + 0.25 * i)
+        lg = dev(wl.logits + rng.standard_normal(wl.logits.shape).astype(np.float32))
+        batches.append((h, lg))
+    direct = [host(fwd(h, lg, w, a1, a2, wl.gate_limit, wl.up_limit).view(torch.int16)) for h, lg in batches]
+    torch.cuda.synchronize()
+    pipe = api.HostPipeline(fwd, w, a1, a2, wl.gate_limit, wl.up_limit)
+    h_in = [(h.cpu().pin_memory(), lg.cpu().pin_memory()) for h, lg in batches]
+    h_out = [torch.empty((wl.T, wl.H), dtype=torch.bfloat16).pin_memory() for _ in batches]
+    for (hh, hl), ho in zip(h_in, h_out):
+        pipe.submit(hh, hl, ho)
+    pipe.synchronize()
+    for got, ref in zip(h_out, direct):
+        np.testing.assert_array_equal(got.view(torch.int16).numpy(), ref)
+
+
 def test_moe_zero_tokens_is_a_no_op():
     from nvfp4_mixture_experts_expert_gb300 import binding as B
     import torch
