@@ -190,6 +190,39 @@ def test_host_pipeline_matches_direct_forward():
         np.testing.assert_array_equal(got.view(torch.int16).numpy(), ref)
 
 
+def test_forward_captured_in_a_cuda_graph_replays_bit_exactly():
+    """The forward (7 kernels with programmatic dependent launch, no host
+    synchronisation) captured into a CUDA graph: replays on new inputs written
+    into the same buffers give the eager results bit for bit."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    wl = W.moe_workload(300, 512, 256, 6, 2, 61, logit_bias_std=1.0)
+    orc = OracleMoE(wl)
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    a1, a2 = dev(orc.a1_gs), dev(orc.a2_gs)
+    fwd = api.MoEForward(wl.T, wl.H, wl.I, wl.E, wl.top_k)
+    hidden, logits = bf16_dev(wl.hidden), dev(wl.logits)
+    out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
+    fwd(hidden, logits, w, a1, a2, wl.gate_limit, wl.up_limit, out=out)  # eager call first
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fwd(hidden, logits, w, a1, a2, wl.gate_limit, wl.up_limit, out=out, stream=s)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(3)
+    for i in range(2):
+        new_h = bf16_dev(wl.hidden) * (1.5 - 0.5 * i)
+        new_l = dev(wl.logits + rng.standard_normal(wl.logits.shape).astype(np.float32))
+        ref = fwd(new_h, new_l, w, a1, a2, wl.gate_limit, wl.up_limit).clone()
+        hidden.copy_(new_h)
+        logits.copy_(new_l)
+        g.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(host(out.view(torch.int16)), host(ref.view(torch.int16)))
+
+
 def test_moe_zero_tokens_is_a_no_op():
     from nvfp4_mixture_experts_expert_gb300 import binding as B
     import torch

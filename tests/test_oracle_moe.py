@@ -230,3 +230,62 @@ def test_tiny_workload_exercises_forced_blocks():
     under = (b > 0) & (b < 6 * 2.0 ** -9)
     assert zero_blocks.sum() >= 40 and under.sum() >= 10
     assert np.all(s.reshape(-1)[zero_blocks | under] == 0)
+
+
+# ----------------------------------------------------------------- expert parallelism (R17)
+
+def test_remap_global_ids_hand_example():
+    # 8 local experts starting at global id 16: [16, 24) are local
+    ids = np.array([[16, 23], [15, 24], [40, 17]])
+    w = np.array([[0.7, 0.3], [0.6, 0.4], [0.9, 0.1]])
+    loc, lw = O.remap_global_ids(ids, w, 16, 8)
+    assert loc.tolist() == [[0, 7], [-1, -1], [-1, 1]]
+    assert lw.tolist() == [[0.7, 0.3], [0.0, 0.0], [0.0, 0.1]]  # kept, not renormalised
+
+
+def test_sort_slots_skips_non_local_assignments():
+    ids = np.array([[1, -1], [0, 1], [-1, -1], [1, 0]])
+    w = np.arange(8, dtype=np.float64).reshape(4, 2) + 1
+    m = O.sort_slots(ids, w, 2)
+    assert m["counts"].tolist() == [2, 3]
+    assert m["offsets"].tolist() == [0, 128, 256]
+    # non-local assignments have no row; the rest keep ascending flat order per expert
+    assert m["inverse"].tolist() == [128, -1, 0, 129, -1, -1, 130, 1]
+    assert m["sorted_token_ids"][[0, 1, 128, 129, 130]].tolist() == [1, 3, 0, 1, 3]
+    assert m["row_weight"][[0, 1, 128, 129, 130]].tolist() == [3.0, 8.0, 1.0, 4.0, 7.0]
+    assert (m["sorted_token_ids"][2:128] == -1).all() and (m["row_weight"][2:128] == 0).all()
+
+
+def test_routed_forward_all_local_equals_logit_forward():
+    wl, hidden, w13, w2, w13q, w2q, a1, a2 = small_layer()
+    ids, w = O.route(wl.logits, wl.top_k)
+    gids, gw = O.remap_global_ids(ids + 100, w, 100, w13q[0].shape[0])
+    a = O.moe_forward(hidden, wl.logits, wl.top_k, w13q, w2q, a1, a2, 10.0, 10.0)
+    b = O.moe_forward_routed(hidden, gids, gw, w13q, w2q, a1, a2, 10.0, 10.0)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_routed_forward_equals_per_assignment_brute_force():
+    """Each local assignment's token through its expert alone (rows are
+    independent in every step), weighted and summed; non-local assignments and
+    tokens with none local contribute exactly zero."""
+    wl, hidden, w13, w2, w13q, w2q, a1, a2 = small_layer(T=40, E=5, k=3)
+    E = w13q[0].shape[0]
+    rng = np.random.default_rng(7)
+    T, k = hidden.shape[0], 3
+    gids = rng.integers(0, 12, (T, k))  # 12 global experts, local ones are [4, 9)
+    gids[5] = [0, 1, 11]               # a token with no local expert
+    gw = rng.uniform(0.1, 1.0, (T, k))
+    ids, w = O.remap_global_ids(gids, gw, 4, E)
+    out, inter = O.moe_forward_routed(hidden, ids, w, w13q, w2q, a1, a2, 10.0, 10.0, return_intermediates=True)
+    acc = np.zeros(hidden.shape)
+    for t in range(T):
+        for j in range(k):
+            e = int(ids[t, j])
+            if e < 0:
+                continue
+            h = O.expert_l1(hidden[t:t + 1], a1[e], w13q[0][e], w13q[1][e], w13q[2][e], 10.0, 10.0)
+            acc[t] += w[t, j] * O.expert_l2(h, a2[e], w2q[0][e], w2q[1][e], w2q[2][e])[0]
+    np.testing.assert_allclose(inter["acc"], acc, rtol=1e-12, atol=1e-12)
+    assert not out[5].any()
+    assert (ids == -1).any() and (ids >= 0).any()
