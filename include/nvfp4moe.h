@@ -200,6 +200,28 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
                       float gate_limit, float up_limit, void* workspace, size_t workspace_bytes, void* out,
                       void* stream);
 
+/* The same forward with expert parallelism: routing comes from the model's
+ * router as global top-k ids (vllm page, "Root cause of CUDA_ERROR_ASSERT
+ * index out of bounds", fixes 1-2: experts_start_idx; global ids remapped to
+ * local ids; non-local experts' weights zeroed).
+ *
+ *   topk_ids      device int32 [T][top_k], global expert ids (any value)
+ *   topk_weights  device f32 [T][top_k], the router's weights, used as given
+ *   experts_start global id of local expert 0; global id g is local expert
+ *                 g - experts_start when that lies in [0, E)
+ * An assignment to a non-local expert gets weight 0, no slot row and no
+ * work; a token with none local gets a zero output row.  The workspace size
+ * and layout are those of nvfp4_moe_forward (the topk arrays there hold the
+ * local ids, -1 for non-local, and the weights actually used).  All other
+ * arguments, checks and errors as nvfp4_moe_forward; router_logits is not
+ * used.  Asynchronous, no allocation, no host synchronisation. */
+int nvfp4_moe_forward_routed(const void* hidden, const int32_t* topk_ids, const float* topk_weights,
+                             int32_t experts_start, int64_t T, int64_t H, int64_t I, int E, int top_k,
+                             const void* w13, const void* w13_sf, const float* w13_gs, const void* w2,
+                             const void* w2_sf, const float* w2_gs, const float* a1_gs, const float* a2_gs,
+                             float gate_limit, float up_limit, void* workspace, size_t workspace_bytes, void* out,
+                             void* stream);
+
 /*
  * nvfp4_moe_calibrate -- per-expert activation global scales from sample data
  * (vllm page: compute_activation_global_scales -- L1 scale from the gathered

@@ -117,6 +117,18 @@ class MoEForward:
                             self.workspace, self.ws_bytes, out, stream)
         return out
 
+    def routed(self, hidden, topk_ids, topk_weights, experts_start, w: MoEWeights, a1_gs, a2_gs, gate_limit=10.0,
+               up_limit=10.0, out=None, stream=None):
+        """Forward with expert parallelism: global top-k ids (int32 [T, k]) and weights
+        (f32 [T, k]) from the model's router; this layer holds experts
+        [experts_start, experts_start + E)."""
+        if out is None:
+            out = torch.empty((self.T, self.H), dtype=torch.bfloat16, device=hidden.device)
+        B.nvfp4_moe_forward_routed(hidden, topk_ids, topk_weights, experts_start, self.T, self.H, self.I, self.E,
+                                   self.top_k, w.w13, w.w13_sf, w.w13_gs, w.w2, w.w2_sf, w.w2_gs, a1_gs, a2_gs,
+                                   gate_limit, up_limit, self.workspace, self.ws_bytes, out, stream)
+        return out
+
     def calibrate(self, hidden, logits, w: MoEWeights, gate_limit=10.0, up_limit=10.0, stream=None):
         """Per-expert activation global scales (a1_gs, a2_gs) from this batch."""
         a1 = torch.empty(self.E, dtype=torch.float32, device=hidden.device)

@@ -307,11 +307,20 @@ size_t nvfp4_moe_workspace_size(int64_t T, int64_t H, int64_t I, int E, int top_
   return L.total;
 }
 
-int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T, int64_t H, int64_t I, int E,
-                      int top_k, const void* w13, const void* w13_sf, const float* w13_gs, const void* w2,
-                      const void* w2_sf, const float* w2_gs, const float* a1_gs, const float* a2_gs,
-                      float gate_limit, float up_limit, void* workspace, size_t workspace_bytes, void* out,
-                      void* stream) {
+namespace {
+// Routing source of a forward: the router's logits over the local experts, or
+// (expert parallelism) the model router's global top-k ids and weights.
+struct Routing {
+  const float* logits;
+  const int32_t* topk_ids;
+  const float* topk_w;
+  int32_t experts_start;
+};
+
+int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H, int64_t I, int E, int top_k,
+                     const void* w13, const void* w13_sf, const float* w13_gs, const void* w2, const void* w2_sf,
+                     const float* w2_gs, const float* a1_gs, const float* a2_gs, float gate_limit, float up_limit,
+                     void* workspace, size_t workspace_bytes, void* out, void* stream) {
   g_err[0] = 0;
   if (T < 0) return fail(NVFP4_ERR_INVALID_ARG, "T must be >= 0");
   if (H <= 0 || H % 256) return fail(NVFP4_ERR_UNSUPPORTED, "H must be a positive multiple of 256");
@@ -322,11 +331,11 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
   nvfp4_moe_layout L;
   if (int rc = nvfp4_moe_workspace_layout(T, H, I, E, top_k, &L)) return rc;
   if (T == 0) return NVFP4_OK;
-  if (!hidden || !router_logits || !w13 || !w13_sf || !w13_gs || !w2 || !w2_sf || !w2_gs || !a1_gs || !a2_gs ||
-      !out)
+  if (!hidden || !w13 || !w13_sf || !w13_gs || !w2 || !w2_sf || !w2_gs || !a1_gs || !a2_gs || !out ||
+      (rt.logits ? false : (!rt.topk_ids || !rt.topk_w)))
     return fail(NVFP4_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(hidden) || !aligned16(w13) || !aligned16(w13_sf) || !aligned16(w2) || !aligned16(w2_sf) ||
-      !aligned16(out) || !aligned16(router_logits))
+      !aligned16(out) || (rt.logits && !aligned16(rt.logits)))
     return fail(NVFP4_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   if (!workspace || workspace_bytes < L.total)
     return fail(NVFP4_ERR_WORKSPACE, "workspace of %zu bytes needed, got %zu", L.total, workspace_bytes);
@@ -408,8 +417,9 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
   const int nb = (int)L.route_blocks;
   cudaError_t e;
   stage_mark(0, s);
-  if ((e = launch_route_topk(router_logits, T, E, top_k, ids, wts, bcnt, s)) != cudaSuccess)
-    return cuda_fail(e, "route launch");
+  e = rt.logits ? launch_route_topk(rt.logits, T, E, top_k, ids, wts, bcnt, s)
+                : launch_route_external(rt.topk_ids, rt.topk_w, rt.experts_start, T, E, top_k, ids, wts, bcnt, s);
+  if (e != cudaSuccess) return cuda_fail(e, "route launch");
   stage_mark(1, s);
   if ((e = launch_slot_scan(bcnt, nb, E, counts, offsets, meta, tile_expert, sorted_ids, row_w, nullptr, 0, s, true)) !=
       cudaSuccess)
@@ -434,6 +444,31 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
     return cuda_fail(e, "combine launch");
   stage_mark(7, s);
   return NVFP4_OK;
+}
+
+}  // namespace
+
+int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T, int64_t H, int64_t I, int E,
+                      int top_k, const void* w13, const void* w13_sf, const float* w13_gs, const void* w2,
+                      const void* w2_sf, const float* w2_gs, const float* a1_gs, const float* a2_gs,
+                      float gate_limit, float up_limit, void* workspace, size_t workspace_bytes, void* out,
+                      void* stream) {
+  if (T > 0 && !router_logits) return fail(NVFP4_ERR_INVALID_ARG, "null pointer");
+  const Routing rt{router_logits, nullptr, nullptr, 0};
+  return moe_forward_impl(hidden, rt, T, H, I, E, top_k, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, a1_gs, a2_gs,
+                          gate_limit, up_limit, workspace, workspace_bytes, out, stream);
+}
+
+int nvfp4_moe_forward_routed(const void* hidden, const int32_t* topk_ids, const float* topk_weights,
+                             int32_t experts_start, int64_t T, int64_t H, int64_t I, int E, int top_k,
+                             const void* w13, const void* w13_sf, const float* w13_gs, const void* w2,
+                             const void* w2_sf, const float* w2_gs, const float* a1_gs, const float* a2_gs,
+                             float gate_limit, float up_limit, void* workspace, size_t workspace_bytes, void* out,
+                             void* stream) {
+  if (T > 0 && (!topk_ids || !topk_weights)) return fail(NVFP4_ERR_INVALID_ARG, "null pointer");
+  const Routing rt{nullptr, topk_ids, topk_weights, experts_start};
+  return moe_forward_impl(hidden, rt, T, H, I, E, top_k, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, a1_gs, a2_gs,
+                          gate_limit, up_limit, workspace, workspace_bytes, out, stream);
 }
 
 int nvfp4_moe_calibrate(const void* hidden, const float* router_logits, int64_t T, int64_t H, int64_t I, int E,

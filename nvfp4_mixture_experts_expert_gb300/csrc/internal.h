@@ -53,6 +53,9 @@ cudaError_t launch_gs_from_amax(const uint32_t* amax_bits, int n, float* gs, cud
 constexpr int kRouteTokensPerBlock = 16;
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
                               int32_t* block_counts, cudaStream_t s);
+// Expert-parallel routing from given global top-k ids / weights (see route.cu).
+cudaError_t launch_route_external(const int32_t* topk_ids, const float* topk_w, int32_t start, int64_t T, int E,
+                                  int k, int32_t* ids, float* w, int32_t* block_counts, cudaStream_t s);
 cudaError_t launch_slot_scan(int32_t* block_counts, int nblocks, int E, int32_t* counts, int32_t* offsets,
                              int32_t* meta, int32_t* tile_expert, int32_t* sorted_ids, float* row_w,
                              uint32_t* zero_words, int n_zero_words, cudaStream_t s, bool pdl = false);

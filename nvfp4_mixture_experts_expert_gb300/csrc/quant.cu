@@ -264,8 +264,9 @@ __global__ void __launch_bounds__(256) gather_quantize_kernel(const uint16_t* __
     int my_row = 0;
     float my_gs = 1.f;
     if (lane < top_k) {
-      my_row = inverse[t * top_k + lane];
-      my_gs = a1_gs[topk_ids[t * top_k + lane]];
+      my_row = inverse[t * top_k + lane];  // -1: not a local expert (no row)
+      const int e = topk_ids[t * top_k + lane];
+      my_gs = e >= 0 ? a1_gs[e] : 1.f;
     }
     for (int j = 0; j < top_k; ++j) {
       const int64_t r = __shfl_sync(0xffffffffu, my_row, j);

@@ -16,6 +16,8 @@
 //                 expert (ascending flat index t*k+j) via warp match/ballot,
 //                 giving the slot row; writes sorted_token_ids, row weights and
 //                 the inverse map.  Deterministic: no atomics decide a row.
+//  route_external expert-parallel routing from the caller's global top-k ids
+//                 (remap to local, weight 0 / no row for other ranks' experts).
 //  token_combine  out[t] = bf16(sum over the token's top_k rows of the
 //                 routing-weighted L2 output), rows in j order: deterministic.
 #include <cuda_runtime.h>
@@ -101,6 +103,31 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
   }
   __syncthreads();
   // expert-major: block_counts[e][block]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) block_counts[(int64_t)e * gridDim.x + blockIdx.x] = hist[e];
+}
+
+// Expert-parallel routing: the caller's top-k ids are global; global id g is
+// local expert g - start when that lies in [0, E), else the assignment is not
+// local (id -1, weight 0, no slot row).  vllm page, "Root cause of
+// CUDA_ERROR_ASSERT index out of bounds", fixes 1-2.  Same block histograms
+// as route_topk_kernel.
+__global__ void __launch_bounds__(kRouteWarps * 32) route_external_kernel(
+    const int32_t* __restrict__ topk_ids, const float* __restrict__ topk_w, int32_t start, int64_t T, int E, int k,
+    int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ block_counts) {
+  pdl_trigger();
+  __shared__ int32_t hist[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int64_t f0 = (int64_t)blockIdx.x * kRouteTokensPerBlock * k;
+  const int64_t f1 = min(T, (int64_t)(blockIdx.x + 1) * kRouteTokensPerBlock) * k;
+  for (int64_t f = f0 + threadIdx.x; f < f1; f += blockDim.x) {
+    const int64_t e = (int64_t)topk_ids[f] - start;
+    const bool local = e >= 0 && e < E;
+    ids[f] = local ? (int32_t)e : -1;
+    w[f] = local ? topk_w[f] : 0.f;
+    if (local) atomicAdd(&hist[e], 1);
+  }
+  __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) block_counts[(int64_t)e * gridDim.x + blockIdx.x] = hist[e];
 }
 
@@ -225,11 +252,13 @@ __global__ void __launch_bounds__(256) slot_scatter_kernel(const int32_t* __rest
     const int64_t f = base + threadIdx.x;
     const bool valid = f < f1;
     const int e = valid ? ids[f] : -1;
+    const bool local = e >= 0;  // -1: an expert-parallel assignment to another rank
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
-    if (valid && rank == 0) warp_cnt[warp][e] = __popc(peers);
+    if (local && rank == 0) warp_cnt[warp][e] = __popc(peers);
     __syncthreads();
-    if (valid) {
+    if (valid && !local) inverse[f] = -1;
+    if (local) {
       int pre = running[e] + rank;
       for (int q = 0; q < warp; ++q) pre += warp_cnt[q][e];
       sorted_ids[pre] = (int32_t)(f / k);
@@ -263,6 +292,7 @@ __global__ void __launch_bounds__(256) token_combine_kernel(const uint16_t* __re
   for (int64_t c = (int64_t)threadIdx.x * 8; c < H; c += (int64_t)blockDim.x * 8) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < k; ++j) {
+      if (rows[j] < 0) continue;  // not a local expert: contributes nothing
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + (int64_t)rows[j] * H + c));
       const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -286,6 +316,14 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int3
   else if (E <= 64) route_topk_kernel<2><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, block_counts);
   else if (E <= 128) route_topk_kernel<4><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, block_counts);
   else route_topk_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, block_counts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_external(const int32_t* topk_ids, const float* topk_w, int32_t start, int64_t T, int E,
+                                  int k, int32_t* ids, float* w, int32_t* block_counts, cudaStream_t s) {
+  const int64_t nb = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
+  route_external_kernel<<<(unsigned)nb, kRouteWarps * 32, 0, s>>>(topk_ids, topk_w, start, T, E, k, ids, w,
+                                                                   block_counts);
   return cudaGetLastError();
 }
 

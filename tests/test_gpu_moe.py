@@ -223,6 +223,79 @@ def test_forward_captured_in_a_cuda_graph_replays_bit_exactly():
         np.testing.assert_array_equal(host(out.view(torch.int16)), host(ref.view(torch.int16)))
 
 
+def _routed_case(T=150, H=512, I=256, E=6, k=3, n_global=16, start=4, seed=71):
+    wl = W.moe_workload(T, H, I, E, k, seed)
+    orc = OracleMoE(wl)
+    rng = np.random.default_rng(seed)
+    gids = rng.integers(0, n_global, (T, k)).astype(np.int32)
+    gids[7] = [0, 1, n_global - 1]      # no local expert
+    gids[8] = [start, start + E - 1, start - 1]  # both ends of the local range and one below
+    gw = rng.uniform(0.05, 1.0, (T, k)).astype(np.float32)
+    return wl, orc, gids, gw, start
+
+
+def test_routed_forward_matches_oracle():
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    wl, orc, gids, gw, start = _routed_case()
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.top_k
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    fwd = api.MoEForward(T, H, I, E, k)
+    out = fwd.routed(bf16_dev(wl.hidden), dev(gids), dev(gw), start, w, dev(orc.a1_gs), dev(orc.a2_gs),
+                     wl.gate_limit, wl.up_limit)
+    torch.cuda.synchronize()
+    ids, wts = O.remap_global_ids(gids, gw.astype(np.float64), start, E)
+    m = O.sort_slots(ids, wts, E)
+    A, P = T * k, m["P"]
+    np.testing.assert_array_equal(host(fwd.view("topk_ids", torch.int32, A)).reshape(T, k), ids)
+    np.testing.assert_array_equal(host(fwd.view("topk_w", torch.float32, A)).reshape(T, k), wts.astype(np.float32))
+    np.testing.assert_array_equal(host(fwd.view("counts", torch.int32, E)), m["counts"])
+    np.testing.assert_array_equal(host(fwd.view("offsets", torch.int32, E + 1)), m["offsets"])
+    np.testing.assert_array_equal(host(fwd.view("sorted_token_ids", torch.int32, P)), m["sorted_token_ids"])
+    np.testing.assert_array_equal(host(fwd.view("inverse", torch.int32, A)), m["inverse"])
+    hidden = W.bf16_bits_to_f32(wl.hidden)
+    ref = O.moe_forward_routed(hidden, ids, wts.astype(np.float32).astype(np.float64), orc.w13q, orc.w2q,
+                               orc.a1_gs, orc.a2_gs, wl.gate_limit, wl.up_limit)
+    got = bf16_host(out)
+    assert not got[7].any()  # no local expert: zero row
+    rf, cs = rel_frob(got, ref), cosine(got, ref)
+    assert rf <= 2e-2 and cs >= 0.999, (rf, cs)
+
+
+def test_routed_forward_with_the_forward_own_routing_is_bit_identical():
+    """The routing the logit forward computed on the device, shifted to global
+    ids, gives the routed forward the logit forward's output bit for bit."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    wl = W.moe_workload(200, 512, 256, 6, 2, 73, logit_bias_std=1.0)
+    orc = OracleMoE(wl)
+    T, k = wl.T, wl.top_k
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    fwd = api.MoEForward(wl.T, wl.H, wl.I, wl.E, k)
+    a1, a2 = dev(orc.a1_gs), dev(orc.a2_gs)
+    ref = fwd(bf16_dev(wl.hidden), dev(wl.logits), w, a1, a2, wl.gate_limit, wl.up_limit).clone()
+    ids = fwd.view("topk_ids", torch.int32, T * k).clone() + 37
+    wts = fwd.view("topk_w", torch.float32, T * k).clone()
+    out = fwd.routed(bf16_dev(wl.hidden), ids, wts, 37, w, a1, a2, wl.gate_limit, wl.up_limit)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host(out.view(torch.int16)), host(ref.view(torch.int16)))
+
+
+def test_routed_forward_with_no_local_expert_is_zero():
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    wl, orc, gids, gw, start = _routed_case(T=40, seed=75)
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    fwd = api.MoEForward(wl.T, wl.H, wl.I, wl.E, wl.top_k)
+    out = torch.full((wl.T, wl.H), 1.0, dtype=torch.bfloat16, device="cuda")
+    far = np.full_like(gids, start + wl.E + 3)
+    fwd.routed(bf16_dev(wl.hidden), dev(far), dev(gw), start, w, dev(orc.a1_gs), dev(orc.a2_gs), wl.gate_limit,
+               wl.up_limit, out=out)
+    torch.cuda.synchronize()
+    assert not bf16_host(out).any()
+    assert host(fwd.view("meta", torch.int32, 1))[0] == 0
+
+
 def test_moe_zero_tokens_is_a_no_op():
     from nvfp4_mixture_experts_expert_gb300 import binding as B
     import torch
