@@ -41,7 +41,7 @@ notes):
   R12 activation global scales are inputs (calibrated beforehand).
   R13 W13 rows 0..I-1 are gate, rows I..2I-1 are up.
   R14 weights are K-major [N][K/2] per expert.
-  R17 expert parallelism: top-k ids from the model's router are global; the
+  R18 expert parallelism: top-k ids from the model's router are global; the
       local expert of global id g is g - experts_start when that lies in
       [0, E), else the assignment is not local: it gets weight 0, occupies
       no slot row and contributes nothing; local assignments keep the
@@ -289,7 +289,7 @@ def sort_slots(ids, weights, num_experts, row_align=128):
     ids = np.asarray(ids, dtype=np.int64)
     T, k = ids.shape
     flat = ids.reshape(-1)
-    local = flat >= 0  # R17: non-local assignments (-1) get no row; inverse -1
+    local = flat >= 0  # R18: non-local assignments (-1) get no row; inverse -1
     counts = np.bincount(flat[local], minlength=num_experts).astype(np.int64)
     padded = (counts + row_align - 1) // row_align * row_align
     offsets = np.concatenate([[0], np.cumsum(padded)]).astype(np.int64)
@@ -374,7 +374,7 @@ def expert_l2(h, a2_gs, w2_nib, w2_s, w2_gs):
 
 
 def remap_global_ids(topk_ids, topk_weights, experts_start, num_experts):
-    """R17, [vllm] "Root cause of CUDA_ERROR_ASSERT index out of bounds"
+    """R18, [vllm] "Root cause of CUDA_ERROR_ASSERT index out of bounds"
     paragraph (fixes 1-2: experts_start_idx; remap global -> local ids and
     zero the weights of non-local experts): local id g - start where it lies
     in [0, E), else -1 with weight 0."""
@@ -400,7 +400,7 @@ def moe_forward(hidden, logits, top_k, w13q, w2q, a1_gs, a2_gs,
 def moe_forward_routed(hidden, ids, w, w13q, w2q, a1_gs, a2_gs,
                        gate_limit=10.0, up_limit=10.0, return_intermediates=False):
     """The MoE forward from given routing: local expert ids [T,k] (-1 = not
-    local, R17) and weights [T,k]; otherwise as moe_forward."""
+    local, R18) and weights [T,k]; otherwise as moe_forward."""
     hidden = np.asarray(hidden, dtype=np.float32)
     T, H = hidden.shape
     E = w13q[0].shape[0]

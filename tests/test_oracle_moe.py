@@ -232,7 +232,7 @@ def test_tiny_workload_exercises_forced_blocks():
     assert np.all(s.reshape(-1)[zero_blocks | under] == 0)
 
 
-# ----------------------------------------------------------------- expert parallelism (R17)
+# ----------------------------------------------------------------- expert parallelism (R18)
 
 def test_remap_global_ids_hand_example():
     # 8 local experts starting at global id 16: [16, 24) are local
