@@ -347,6 +347,99 @@ def run_ours(args, world, rank, local):
     return res, L
 
 
+def linear_side_measurement(seed):
+    """The dense NVFP4 linear (M=2048, K=3584, N=6144) and the grouped linear
+    (G=8, T=2048, D=2048 -> R=1024, strided (T,G,D) in, (T,G,R) out): amax ->
+    global scale -> quantization of the activations, then the block-scaled
+    GEMM; weights quantized once beforehand.  L2 flushed before each step
+    (these inputs fit in L2)."""
+    import numpy as np
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api, binding as B
+    from nvfp4_mixture_experts_expert_gb300 import workloads as W
+    peaks = measured_peaks()
+    fp4_peak = peaks["bf16_tflops_sustained"] * FP4_OVER_BF16
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+
+    def bf16(bits):
+        return torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).cuda()
+
+    def timed(fn, gemm_ev):
+        for _ in range(3):
+            fn()
+        tot, gem = [], []
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        for _ in range(20):
+            flush.fill_(1)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            tot.append(a.elapsed_time(b))
+            gem.append(gemm_ev[0].elapsed_time(gemm_ev[1]))
+        return statistics.median(tot), statistics.median(gem)
+
+    res = {}
+    # dense linear
+    wl = W.dense_gemm(seed)
+    M, N, K = wl.M, wl.N, wl.K
+    a = bf16(wl.a)
+    fb, sfb, gb = api.quantize(bf16(wl.b))
+    fa = torch.empty((M, K // 2), dtype=torch.uint8, device="cuda")
+    sfa = torch.empty(M * K // 16, dtype=torch.uint8, device="cuda")
+    ga = torch.empty(1, dtype=torch.float32, device="cuda")
+    wsb = B.nvfp4_quantize_workspace_size(1)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    offs = torch.tensor([0, M], dtype=torch.int32, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def dense():
+        B.nvfp4_quantize(a, M, K, K, 0, 1, None, ga, ws, wsb, fa, sfa, M)
+        ev[0].record()
+        B.nvfp4_grouped_gemm(fa, sfa, ga, fb, sfb, gb, offs, None, 1, M, N, K, D, N, 0)
+        ev[1].record()
+
+    ms, gms = timed(dense, ev)
+    flops = 2.0 * M * N * K
+    res["dense_linear"] = {"workload": "NVFP4 linear M=2048 K=3584 N=6144 (activation quantized per call)",
+                           "ms_per_call": round(ms, 4), "gemm_ms": round(gms, 4),
+                           "gemm_tflops": round(flops / (gms * 1e-3) / 1e12, 1),
+                           "gemm_frac_fp4": round(flops / (gms * 1e-3) / 1e12 / fp4_peak, 4)}
+    # grouped linear
+    gl = W.grouped_linear(seed)
+    T, G, Dd, R = gl.T, gl.G, gl.D, gl.R
+    x = bf16(gl.x)
+    fw, sfw, gw = api.quantize_expert_weights(bf16(gl.w), gs=torch.from_numpy(gl.w_gs).cuda())
+    fx = torch.empty((G * T, Dd // 2), dtype=torch.uint8, device="cuda")
+    sfx = torch.empty(G * T * Dd // 16, dtype=torch.uint8, device="cuda")
+    gx = torch.empty(G, dtype=torch.float32, device="cuda")
+    wsg = B.nvfp4_quantize_workspace_size(G)
+    wsx = torch.empty(wsg, dtype=torch.uint8, device="cuda")
+    out = torch.empty((T, G, R), dtype=torch.bfloat16, device="cuda")
+    goffs = torch.arange(G + 1, dtype=torch.int32, device="cuda") * T
+    gcnt = torch.full((G,), T, dtype=torch.int32, device="cuda")
+
+    def grouped():
+        B.nvfp4_quantize(x, T, Dd, G * Dd, Dd, G, None, gx, wsx, wsg, fx, sfx, T)
+        ev[0].record()
+        B.nvfp4_grouped_gemm(fx, sfx, gx, fw, sfw, gw, goffs, gcnt, G, G * T, R, Dd, out, G * R, R)
+        ev[1].record()
+
+    ms, gms = timed(grouped, ev)
+    flops = 2.0 * G * T * R * Dd
+    gbytes = G * T * Dd * (1 / 2 + 1 / 16) + G * R * Dd * (1 / 2 + 1 / 16) + G * T * R * 2
+    res["grouped_linear"] = {"workload": "NVFP4 grouped linear G=8 T=2048 D=2048 R=1024, strided (T,G,D) -> (T,G,R)",
+                             "ms_per_call": round(ms, 4), "gemm_ms": round(gms, 4),
+                             "gemm_tflops": round(flops / (gms * 1e-3) / 1e12, 1),
+                             "gemm_frac_fp4": round(flops / (gms * 1e-3) / 1e12 / fp4_peak, 4),
+                             "gemm_gbs": round(gbytes / (gms * 1e-3) / 1e9, 1),
+                             "gemm_frac_hbm": round(gbytes / (gms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+    res["l2"] = "flushed (512 MB write) before each call"
+    return res
+
+
 def decode_side_measurement(seed):
     """Decode-size forward (T=128, E=32): HBM-bound weight streaming."""
     import torch
@@ -503,7 +596,7 @@ def main():
     res, _ = run_ours(args, world, rank, local)
     if rank == 0:
         if not args.no_extras and world == 1:
-            res["extra"] = {"decode": decode_side_measurement(args.seed)}
+            res["extra"] = {"decode": decode_side_measurement(args.seed), "linear": linear_side_measurement(args.seed)}
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline(args.workload, args.seed)
         print(json.dumps(res), flush=True)

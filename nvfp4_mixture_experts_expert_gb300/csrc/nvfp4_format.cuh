@@ -83,27 +83,6 @@ __device__ __forceinline__ float div_by_scale(float x, float d, float y) {
   return __fmaf_rn(r, y, q0);
 }
 
-// Quantize one block of 16 already globally-scaled values.  Returns the
-// scale code; writes 8 packed bytes (element 2j in the low nibble of byte j).
-__device__ __forceinline__ uint32_t quant_block16(const float (&xs)[16], uint32_t& lo, uint32_t& hi) {
-  float b = 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) b = fmaxf(b, fabsf(xs[i]));
-  if (!(b >= kUnderflowAmax)) {
-    lo = hi = 0u;
-    return 0u;
-  }
-  const uint32_t s = e4m3_code(__fdiv_rn(b, 6.0f));
-  const float d = e4m3_value(s);
-  const float y = __frcp_rn(d);
-  float q[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) q[i] = div_by_scale(xs[i], d, y);
-  lo = drop_negative_zero(e2m1x8_word(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]));
-  hi = drop_negative_zero(e2m1x8_word(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]));
-  return s;
-}
-
 // Packed pairs of FP32 values (element 2j in the low half, 2j+1 in the high
 // half), each half rounded exactly like its scalar operation.
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
@@ -125,10 +104,11 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
   return r;
 }
 
-// quant_block16 on 8 packed pairs of already globally-scaled values, the
-// block maximum b given: the same arithmetic, two elements per instruction
-// where it can be (b / 6 through the same exact quotient, 6 being an E4M3
-// value; rcp6 = RN(1/6)).
+// Quantize one block of 16 already globally-scaled values given as 8 packed
+// pairs, with the block maximum b given.  Returns the scale code; writes 8
+// packed bytes (element 2j in the low nibble of byte j).  b / 6 and every
+// x' / dec(scale) are the correctly rounded quotients (div_by_scale; 6 is an
+// E4M3 value; rcp6 = RN(1/6)), two elements per instruction where possible.
 __device__ __forceinline__ uint32_t quant_block16_pairs(const uint64_t (&xs2)[8], float b, float rcp6, uint32_t& lo,
                                                         uint32_t& hi) {
   lo = hi = 0u;

@@ -2,11 +2,10 @@
 // quantization with scales written straight into the 128x4 tile layout,
 // scale assembly into 128-row padded slots, and the MoE gather+quantize.
 //
-// All kernels are HBM-bound streaming kernels.  The strided quantizer gives
-// one thread 64 consecutive K elements of one row (4 blocks of 16 = one MMA
-// K-step) and writes its 4 scale codes as one aligned 32-bit word of the
-// tile layout.  The MoE gather gives one lane one 16-element block, so each
-// warp load and store is contiguous (see gather_quantize_kernel).
+// All kernels are streaming kernels.  The quantizers give one lane one
+// 16-element block, so each warp load and store is contiguous, and write 4
+// scale codes per aligned 32-bit word of the tile layout (see
+// gather_quantize_kernel and quantize_kernel).
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -19,34 +18,6 @@ namespace {
 
 __device__ __forceinline__ uint4 ldg_nc(const uint16_t* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
-}
-
-// Quantize 64 bf16 values (8 x uint4 of raw bits) with global scale gs.
-// Writes 32 packed bytes and returns 4 scale codes (column c in byte c).
-__device__ __forceinline__ uint32_t quant_chunk64(const uint4 (&raw)[8], float gs, uint4& o0, uint4& o1) {
-  uint32_t sc = 0, w[8];
-#pragma unroll
-  for (int blk = 0; blk < 4; ++blk) {
-    float xs[16];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const uint4 v = raw[blk * 2 + j];
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        xs[j * 8 + q * 2 + 0] = __fmul_rn(bf16_lo(u[q]), gs);
-        xs[j * 8 + q * 2 + 1] = __fmul_rn(bf16_hi(u[q]), gs);
-      }
-    }
-    uint32_t lo, hi;
-    const uint32_t s = quant_block16(xs, lo, hi);
-    w[blk * 2] = lo;
-    w[blk * 2 + 1] = hi;
-    sc |= s << (8 * blk);
-  }
-  o0 = make_uint4(w[0], w[1], w[2], w[3]);
-  o1 = make_uint4(w[4], w[5], w[6], w[7]);
-  return sc;
 }
 
 // ---------------------------------------------------------------- amax
@@ -88,39 +59,6 @@ __global__ void group_gs_kernel(const float* __restrict__ partial, int nb, int g
   float a = 0.f;
   for (int i = 0; i < nb; ++i) a = fmaxf(a, partial[(int64_t)g * nb + i]);
   gs[g] = a > 0.f ? __fdiv_rn(kGsNumerator, a) : 1.0f;
-}
-
-// ---------------------------------------------------------------- quantize
-__global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
-                                                       int64_t ld_x, int64_t gstride_x, int groups,
-                                                       const float* __restrict__ gs, float* __restrict__ gs_copy,
-                                                       uint8_t* __restrict__ fp4, uint8_t* __restrict__ sf,
-                                                       int64_t rows_padded) {
-  const int64_t chunks = K / 64;
-  const int64_t per_group = rows_padded * chunks;
-  const int64_t total = per_group * groups;
-  if (gs_copy && blockIdx.x == 0)
-    for (int i = threadIdx.x; i < groups; i += blockDim.x) gs_copy[i] = gs[i];
-  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
-       it += (int64_t)gridDim.x * blockDim.x) {
-    const int g = (int)(it / per_group);
-    const int64_t rem = it - (int64_t)g * per_group;
-    const int64_t r = rem / chunks, c = rem - r * chunks;
-    const int64_t orow = (int64_t)g * rows_padded + r;
-    uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0;
-    uint32_t sc = 0;
-    if (r < rows) {
-      const uint16_t* src = x + (int64_t)g * gstride_x + r * ld_x + c * 64;
-      uint4 raw[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) raw[j] = ldg_nc(src + j * 8);
-      sc = quant_chunk64(raw, gs[g], o0, o1);
-    }
-    uint4* dst = reinterpret_cast<uint4*>(fp4 + orow * (K / 2) + c * 32);
-    dst[0] = o0;
-    dst[1] = o1;
-    *reinterpret_cast<uint32_t*>(sf + sf_offset(orow, c * 4, K / 16)) = sc;
-  }
 }
 
 // ---------------------------------------------------------------- scale assembly
@@ -198,7 +136,7 @@ __device__ __forceinline__ float block_amax_bf16(const uint32_t (&w)[8]) {
 }
 
 // Quantize one block of 16 bf16 values (raw bits) with global scale gs; the
-// same arithmetic as quant_block16, element pairs at a time.  tab[s] holds
+// same arithmetic as quant_block16_pairs, with the scale pair from a table: tab[s] holds
 // (dec(s), RN(1/dec(s))) for every scale code s.
 __device__ __forceinline__ uint32_t quant_block16_bf16(const uint32_t (&w)[8], float amax, float gs, float rcp6,
                                                        const float2* tab, uint32_t& lo, uint32_t& hi) {
@@ -300,6 +238,60 @@ __global__ void __launch_bounds__(256) gather_quantize_kernel(const uint16_t* __
     *reinterpret_cast<uint32_t*>(sfa1 + sf_offset(r, 4 * m, sf_cols)) = 0u;
 }
 
+// ---------------------------------------------------------------- quantize
+// Strided groups of rows -> NVFP4 (rows [rows, rows_padded) of every group are
+// zero blocks).  Same layout as the MoE gather: one warp per (group, row,
+// 1024-element segment), lane l owns the 16-element block at 512*c + 16*l of
+// the segment's two chunks, one 32-byte load per block, 8 bytes of nibbles
+// per lane and a 32-bit scale word per 4 lanes.  K is a multiple of 64, so the
+// 4 lanes of a scale word are all inside or all outside the row.
+template <bool kAligned32>
+__global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
+                                                       int64_t ld_x, int64_t gstride_x, int groups,
+                                                       const float* __restrict__ gs, float* __restrict__ gs_copy,
+                                                       uint8_t* __restrict__ fp4, uint8_t* __restrict__ sf,
+                                                       int64_t rows_padded) {
+  __shared__ float2 tab[128];
+  if (threadIdx.x < 128) {
+    const float d = e4m3_value(threadIdx.x);
+    tab[threadIdx.x] = make_float2(d, threadIdx.x ? __frcp_rn(d) : 0.f);
+  }
+  __syncthreads();
+  if (gs_copy && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < groups; i += blockDim.x) gs_copy[i] = gs[i];
+  const float rcp6 = __frcp_rn(6.0f);
+  const int lane = threadIdx.x & 31;
+  const int64_t segs = (K + 1023) / 1024;
+  const int64_t per_group = rows_padded * segs;
+  const int64_t items = per_group * groups;
+  const int64_t sf_cols = K / 16;
+  for (int64_t item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); item < items;
+       item += (int64_t)gridDim.x * (blockDim.x >> 5)) {
+    const int64_t g = item / per_group;
+    const int64_t rem = item - g * per_group;
+    const int64_t r = rem / segs, e0 = (rem - r * segs) * 1024;
+    const int64_t orow = g * rows_padded + r;
+    const float gsv = gs[g];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int64_t el = e0 + c * 512 + lane * 16;
+      uint32_t lo = 0u, hi = 0u, sc = 0u;
+      if (r < rows && el < K) {
+        uint32_t raw[8];
+        ld_block32<kAligned32>(x + g * gstride_x + r * ld_x + el, raw);
+        sc = quant_block16_bf16(raw, block_amax_bf16(raw), gsv, rcp6, tab, lo, hi);
+      }
+      const uint32_t word = sc | (__shfl_down_sync(0xffffffffu, sc, 1) << 8) |
+                            (__shfl_down_sync(0xffffffffu, sc, 2) << 16) |
+                            (__shfl_down_sync(0xffffffffu, sc, 3) << 24);
+      if (el < K) {
+        *reinterpret_cast<uint2*>(fp4 + orow * (K / 2) + el / 2) = make_uint2(lo, hi);
+        if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(orow, el / 16, sf_cols)) = word;
+      }
+    }
+  }
+}
+
 // One warp per slot row: max |x| of the token's hidden row, folded into its
 // expert's amax with an order-independent atomicMax on the float bits.
 __global__ void __launch_bounds__(256) gather_amax_kernel(const uint16_t* __restrict__ hidden, int64_t H,
@@ -352,9 +344,13 @@ cudaError_t launch_group_amax(const uint16_t* x, int64_t rows, int64_t K, int64_
 cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, int64_t ld_x, int64_t gstride_x,
                             int groups, const float* gs, float* gs_copy, uint8_t* fp4, uint8_t* sf,
                             int64_t rows_padded, int num_sms, cudaStream_t s) {
-  const int64_t items = rows_padded * (K / 64) * groups;
-  const int grid = grid_for(items, 256, num_sms, 8);
-  quantize_kernel<<<grid, 256, 0, s>>>(x, rows, K, ld_x, gstride_x, groups, gs, gs_copy, fp4, sf, rows_padded);
+  const int64_t warps = rows_padded * ((K + 1023) / 1024) * groups;
+  const int grid = grid_for(warps * 32, 256, num_sms, 8);
+  const bool a32 = (reinterpret_cast<uintptr_t>(x) & 31u) == 0 && ld_x % 16 == 0 && gstride_x % 16 == 0;
+  if (a32) quantize_kernel<true><<<grid, 256, 0, s>>>(x, rows, K, ld_x, gstride_x, groups, gs, gs_copy, fp4, sf,
+                                                      rows_padded);
+  else quantize_kernel<false><<<grid, 256, 0, s>>>(x, rows, K, ld_x, gstride_x, groups, gs, gs_copy, fp4, sf,
+                                                   rows_padded);
   return cudaGetLastError();
 }
 
