@@ -426,6 +426,18 @@ def moe_forward_routed(hidden, ids, w, w13q, w2q, a1_gs, a2_gs,
     return out
 
 
+def shared_expert_forward(hidden, w13q, w2q, a1_gs, a2_gs, gate_limit=10.0, up_limit=10.0):
+    """The shared expert: one NVFP4 SwiGLU FFN over every token, no routing
+    ([cutedsl] "CuTeDSLSharedExpertRunner: num_groups=1 GEMM, no
+    scatter/routing" and the fused L1+SiLU+L2 paragraph).  w13q / w2q hold one
+    expert: (nibbles [1,2I,H], scales, gs [1]); a1_gs / a2_gs scalars.
+    Returns bf16 values as FP32 [T, H]."""
+    hidden = np.asarray(hidden, dtype=np.float32)
+    h = expert_l1(hidden, a1_gs, w13q[0][0], w13q[1][0], w13q[2][0], gate_limit, up_limit)
+    Y = expert_l2(h, a2_gs, w2q[0][0], w2q[1][0], w2q[2][0])
+    return bf16_round(Y.astype(np.float32))
+
+
 def calibrate_activation_scales(hidden, logits, top_k, w13q, gate_limit=10.0, up_limit=10.0,
                                 row_limit=None):
     """[vllm] "compute_activation_global_scales" paragraphs: per local expert,

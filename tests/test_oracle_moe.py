@@ -289,3 +289,14 @@ def test_routed_forward_equals_per_assignment_brute_force():
     np.testing.assert_allclose(inter["acc"], acc, rtol=1e-12, atol=1e-12)
     assert not out[5].any()
     assert (ids == -1).any() and (ids >= 0).any()
+
+
+# ----------------------------------------------------------------- shared expert
+
+def test_shared_expert_equals_one_expert_top1_moe():
+    """With one expert and top_k = 1 every routing weight is exactly 1, so the
+    routed layer and the shared-expert FFN compute the same thing."""
+    wl, hidden, w13, w2, w13q, w2q, a1, a2 = small_layer(T=70, E=1, k=1)
+    moe = O.moe_forward(hidden, wl.logits, 1, w13q, w2q, a1, a2, 10.0, 10.0)
+    ffn = O.shared_expert_forward(hidden, w13q, w2q, a1[0], a2[0], 10.0, 10.0)
+    np.testing.assert_array_equal(moe, ffn)
