@@ -222,6 +222,27 @@ int nvfp4_moe_forward_routed(const void* hidden, const int32_t* topk_ids, const 
                              float gate_limit, float up_limit, void* workspace, size_t workspace_bytes, void* out,
                              void* stream);
 
+/* Shared expert: one NVFP4 SwiGLU FFN applied to every token, no routing
+ * (cutedsl page: "CuTeDSLSharedExpertRunner: num_groups=1 GEMM, no
+ * scatter/routing", the fused L1+SiLU+L2 pipeline, rows padded to 128 for the
+ * scale layout, all buffers pre-allocated).
+ *
+ *   out[t] = bf16( L2( requant( SwiGLU( L1( quant(hidden[t]) ) ) ) ) )
+ * with the arithmetic of nvfp4_moe_forward for one expert and weight 1.
+ *   hidden   bf16 [T][H];  out bf16 [T][H] (only its T rows are written)
+ *   w13      [2I][H/2] nibbles (gate rows 0..I-1, up rows I..2I-1), w13_sf
+ *            tile-layout scales [2I*H/16], w13_gs f32[1]; w2 [H][I/2], w2_sf,
+ *            w2_gs f32[1]; a1_gs / a2_gs f32[1] activation global scales
+ *   workspace device scratch of nvfp4_shared_expert_workspace_size(T, H, I)
+ *            bytes, 256-byte aligned
+ * H a multiple of 256, I of 128; T = 0 is a no-op.  Errors as
+ * nvfp4_moe_forward.  Asynchronous, no allocation, no host synchronisation. */
+size_t nvfp4_shared_expert_workspace_size(int64_t T, int64_t H, int64_t I);
+int nvfp4_shared_expert_forward(const void* hidden, int64_t T, int64_t H, int64_t I, const void* w13,
+                                const void* w13_sf, const float* w13_gs, const void* w2, const void* w2_sf,
+                                const float* w2_gs, const float* a1_gs, const float* a2_gs, float gate_limit,
+                                float up_limit, void* workspace, size_t workspace_bytes, void* out, void* stream);
+
 /*
  * nvfp4_moe_calibrate -- per-expert activation global scales from sample data
  * (vllm page: compute_activation_global_scales -- L1 scale from the gathered

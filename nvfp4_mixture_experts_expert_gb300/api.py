@@ -144,6 +144,24 @@ class MoEForward:
         return self.workspace[off:off + nbytes].view(dtype)
 
 
+class SharedExpertForward:
+    """The shared expert's NVFP4 SwiGLU FFN over every token (no routing), with
+    its workspace; weights are one expert of quantize_moe_weights (E = 1)."""
+
+    def __init__(self, T, H, I, device="cuda"):
+        self.T, self.H, self.I = T, H, I
+        self.ws_bytes = max(B.nvfp4_shared_expert_workspace_size(T, H, I), 256)
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+
+    def __call__(self, hidden, w: MoEWeights, a1_gs, a2_gs, gate_limit=10.0, up_limit=10.0, out=None, stream=None):
+        if out is None:
+            out = torch.empty((self.T, self.H), dtype=torch.bfloat16, device=hidden.device)
+        B.nvfp4_shared_expert_forward(hidden, self.T, self.H, self.I, w.w13, w.w13_sf, w.w13_gs, w.w2, w.w2_sf,
+                                      w.w2_gs, a1_gs, a2_gs, gate_limit, up_limit, self.workspace, self.ws_bytes,
+                                      out, stream)
+        return out
+
+
 class HostPipeline:
     """Streams batches from pinned host memory through one MoEForward.
 

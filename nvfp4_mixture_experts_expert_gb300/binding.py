@@ -81,6 +81,10 @@ _moe_forward_routed = _sig("nvfp4_moe_forward_routed", c_int, [c_ptr, c_ptr, c_p
                                                                c_i64, c_int, c_int, c_ptr, c_ptr, c_ptr, c_ptr,
                                                                c_ptr, c_ptr, c_ptr, c_ptr, c_float, c_float, c_ptr,
                                                                c_size, c_ptr, c_ptr])
+_se_ws = _sig("nvfp4_shared_expert_workspace_size", c_size, [c_i64, c_i64, c_i64])
+_se_forward = _sig("nvfp4_shared_expert_forward", c_int, [c_ptr, c_i64, c_i64, c_i64, c_ptr, c_ptr, c_ptr, c_ptr,
+                                                          c_ptr, c_ptr, c_ptr, c_ptr, c_float, c_float, c_ptr,
+                                                          c_size, c_ptr, c_ptr])
 _moe_calibrate = _sig("nvfp4_moe_calibrate", c_int, [c_ptr, c_ptr, c_i64, c_i64, c_i64, c_int, c_int, c_ptr,
                                                      c_ptr, c_ptr, c_float, c_float, c_ptr, c_size, c_ptr, c_ptr,
                                                      c_ptr])
@@ -191,6 +195,17 @@ def nvfp4_moe_forward_routed(hidden, topk_ids, topk_weights, experts_start, T, H
                                _p(w13), _p(w13_sf), _p(w13_gs), _p(w2), _p(w2_sf), _p(w2_gs), _p(a1_gs),
                                _p(a2_gs), gate_limit, up_limit, _p(workspace), workspace_bytes, _p(out),
                                _stream(stream)))
+
+
+def nvfp4_shared_expert_workspace_size(T, H, I):
+    return int(_se_ws(T, H, I))
+
+
+def nvfp4_shared_expert_forward(hidden, T, H, I, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, a1_gs, a2_gs, gate_limit,
+                                up_limit, workspace, workspace_bytes, out, stream=None):
+    _check(_se_forward(_p(hidden), T, H, I, _p(w13), _p(w13_sf), _p(w13_gs), _p(w2), _p(w2_sf), _p(w2_gs),
+                       _p(a1_gs), _p(a2_gs), gate_limit, up_limit, _p(workspace), workspace_bytes, _p(out),
+                       _stream(stream)))
 
 
 def nvfp4_moe_calibrate(hidden, router_logits, T, H, I, E, top_k, w13, w13_sf, w13_gs, gate_limit, up_limit,

@@ -471,6 +471,124 @@ int nvfp4_moe_forward_routed(const void* hidden, const int32_t* topk_ids, const 
                           gate_limit, up_limit, workspace, workspace_bytes, out, stream);
 }
 
+// ------------------------------------------------------------------ shared expert
+namespace {
+struct SharedExpertLayout {
+  size_t a1, sfa1, a2, sfa2, total;
+  int64_t rows;  // T rounded up to 128
+};
+SharedExpertLayout shared_expert_layout(int64_t T, int64_t H, int64_t I) {
+  SharedExpertLayout L;
+  L.rows = round_up(T > 0 ? T : 1, 128);
+  size_t off = 0;
+  auto take = [&](int64_t bytes) {
+    const size_t at = off;
+    off = (size_t)round_up((int64_t)off + bytes, 1024);
+    return at;
+  };
+  L.a1 = take(L.rows * H / 2);
+  L.sfa1 = take(L.rows * H / 16);
+  L.a2 = take(L.rows * I / 2);
+  L.sfa2 = take(L.rows * I / 16);
+  L.total = off;
+  return L;
+}
+}  // namespace
+
+size_t nvfp4_shared_expert_workspace_size(int64_t T, int64_t H, int64_t I) {
+  if (T < 0 || H <= 0 || I <= 0) return 0;
+  return shared_expert_layout(T, H, I).total;
+}
+
+int nvfp4_shared_expert_forward(const void* hidden, int64_t T, int64_t H, int64_t I, const void* w13,
+                                const void* w13_sf, const float* w13_gs, const void* w2, const void* w2_sf,
+                                const float* w2_gs, const float* a1_gs, const float* a2_gs, float gate_limit,
+                                float up_limit, void* workspace, size_t workspace_bytes, void* out, void* stream) {
+  g_err[0] = 0;
+  if (T < 0) return fail(NVFP4_ERR_INVALID_ARG, "T must be >= 0");
+  if (H <= 0 || H % 256) return fail(NVFP4_ERR_UNSUPPORTED, "H must be a positive multiple of 256");
+  if (I <= 0 || I % 128) return fail(NVFP4_ERR_UNSUPPORTED, "I must be a positive multiple of 128");
+  if (!(gate_limit > 0.f) || !(up_limit > 0.f)) return fail(NVFP4_ERR_INVALID_ARG, "limits must be positive");
+  if (T == 0) return NVFP4_OK;
+  if (!hidden || !w13 || !w13_sf || !w13_gs || !w2 || !w2_sf || !w2_gs || !a1_gs || !a2_gs || !out)
+    return fail(NVFP4_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(hidden) || !aligned16(w13) || !aligned16(w13_sf) || !aligned16(w2) || !aligned16(w2_sf) ||
+      !aligned16(out))
+    return fail(NVFP4_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  const SharedExpertLayout L = shared_expert_layout(T, H, I);
+  if (!workspace || workspace_bytes < L.total)
+    return fail(NVFP4_ERR_WORKSPACE, "workspace of %zu bytes needed, got %zu", L.total, workspace_bytes);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(NVFP4_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (L.rows > INT32_MAX || 2 * I > INT32_MAX) return fail(NVFP4_ERR_UNSUPPORTED, "row counts beyond 2^31");
+  DeviceInfo* dev = nullptr;
+  if (int rc = device_info(&dev)) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* ws = (uint8_t*)workspace;
+  uint8_t* a1 = ws + L.a1;
+  uint8_t* sfa1 = ws + L.sfa1;
+  uint8_t* a2 = ws + L.a2;
+  uint8_t* sfa2 = ws + L.sfa2;
+  GemmArgs g1, g2;
+  memset(&g1, 0, sizeof(g1));
+  memset(&g2, 0, sizeof(g2));
+  if (int rc = make_fp4_map(&g1.tmap_a, a1, L.rows, H)) return rc;
+  if (int rc = make_fp4_map(&g1.tmap_b, w13, 2 * I, H)) return rc;
+  if (int rc = make_fp4_map(&g2.tmap_a, a2, L.rows, I)) return rc;
+  if (int rc = make_fp4_map(&g2.tmap_b, w2, H, I)) return rc;
+  // L1: one group, SwiGLU + requantization into A2 (gate rows 0..I-1, up rows I..2I-1)
+  g1.sfa = sfa1;
+  g1.sfb = (const uint8_t*)w13_sf;
+  g1.a_gs = a1_gs;
+  g1.b_gs = w13_gs;
+  g1.G = 1;
+  g1.host_rows = (int)L.rows;
+  g1.K = (int)H;
+  g1.num_kb = (int)((H + 255) / 256);
+  g1.b_rows_per_group = (int)(2 * I);
+  g1.n_tiles = (int)(I / 128);
+  g1.b_second_offset = (int)I;
+  g1.b_tile_stride = 128;
+  g1.sfb_group_bytes = 2 * I * (H / 16);
+  g1.q_out = a2;
+  g1.q_sf = sfa2;
+  g1.q_gs = a2_gs;
+  g1.I = (int)I;
+  g1.gate_limit = gate_limit;
+  g1.up_limit = up_limit;
+  g1.status = dev->status;
+  g1.timeout_ns = 2000000000ull;
+  // L2: one group, bf16 rows straight into out (rows >= T not stored)
+  g2.sfa = sfa2;
+  g2.sfb = (const uint8_t*)w2_sf;
+  g2.a_gs = a2_gs;
+  g2.b_gs = w2_gs;
+  g2.G = 1;
+  g2.host_rows = (int)L.rows;
+  g2.host_count = (int)T;
+  g2.K = (int)I;
+  g2.num_kb = (int)((I + 255) / 256);
+  g2.b_rows_per_group = (int)H;
+  g2.n_tiles = (int)(H / 256);
+  g2.b_second_offset = 128;
+  g2.b_tile_stride = 256;
+  g2.sfb_group_bytes = H * (I / 16);
+  g2.D = (uint16_t*)out;
+  g2.ldd = H;
+  g2.d_vec32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
+  g2.status = dev->status;
+  g2.timeout_ns = 2000000000ull;
+  cudaError_t e;
+  if ((e = launch_quantize((const uint16_t*)hidden, T, H, H, 0, 1, a1_gs, nullptr, a1, sfa1, L.rows, dev->sms, s)) !=
+      cudaSuccess)
+    return cuda_fail(e, "quantize launch");
+  const int64_t t1 = L.rows / 128 * g1.n_tiles, t2 = L.rows / 128 * g2.n_tiles;
+  if ((e = launch_gemm(kEpiSwigluQuant, g1, (int)t1, dev->sms, s, true)) != cudaSuccess)
+    return cuda_fail(e, "L1 launch");
+  if ((e = launch_gemm(kEpiBf16, g2, (int)t2, dev->sms, s, true)) != cudaSuccess) return cuda_fail(e, "L2 launch");
+  return NVFP4_OK;
+}
+
 int nvfp4_moe_calibrate(const void* hidden, const float* router_logits, int64_t T, int64_t H, int64_t I, int E,
                         int top_k, const void* w13, const void* w13_sf, const float* w13_gs, float gate_limit,
                         float up_limit, void* workspace, size_t workspace_bytes, float* a1_gs_out, float* a2_gs_out,

@@ -434,7 +434,7 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
 
     if constexpr (EPI == kEpiBf16) {
       const int64_t i_local = row - L.offsets[g];
-      const bool valid = p.counts ? i_local < p.counts[g] : true;
+      const bool valid = p.counts ? i_local < p.counts[g] : (p.host_count <= 0 || i_local < p.host_count);
       if (valid) {
         uint16_t* drow = p.D + g * p.gstride_d + i_local * p.ldd + (int64_t)nt * BN + half * (BN / 2);
 #pragma unroll
@@ -578,7 +578,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid
     fence_mbar_init();
   }
   pdl_wait();  // everything below reads what earlier kernels wrote
-  for (int i = threadIdx.x; i <= p.G; i += blockDim.x) L.offsets[i] = p.padded_offsets[i];
+  if (p.host_rows > 0) {  // one group of host-known size
+    if (threadIdx.x == 0) {
+      L.offsets[0] = 0;
+      L.offsets[1] = p.host_rows;
+    }
+  } else {
+    for (int i = threadIdx.x; i <= p.G; i += blockDim.x) L.offsets[i] = p.padded_offsets[i];
+  }
   __syncthreads();
   if (warp == 0) {  // work units per group (m-tiles, or pairs of m-tiles), exclusive prefix
     int carry = 0;

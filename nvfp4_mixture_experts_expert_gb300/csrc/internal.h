@@ -93,6 +93,11 @@ struct GemmArgs {
   int64_t gstride_d;
   int d_vec32;  // D, ldd and gstride_d allow 32-byte stores
   int pair_hint;  // mode 2: the caller expects most groups to span at least two m-tiles
+  // One group whose sizes the host knows (no device metadata): host_rows > 0
+  // replaces padded_offsets by [0, host_rows]; host_count > 0 (kEpiBf16, no
+  // counts array) keeps rows at or beyond it from being stored.
+  int host_rows;
+  int host_count;
   // kEpiSwigluQuant
   uint8_t* q_out;
   uint8_t* q_sf;
