@@ -436,6 +436,29 @@ def linear_side_measurement(seed):
                              "gemm_frac_fp4": round(flops / (gms * 1e-3) / 1e12 / fp4_peak, 4),
                              "gemm_gbs": round(gbytes / (gms * 1e-3) / 1e9, 1),
                              "gemm_frac_hbm": round(gbytes / (gms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+    # shared expert: the same SwiGLU FFN on every token (one group, no routing)
+    swl = W.moe_workload(8192, 4096, 2048, 1, 1, seed, with_weights=False)
+    rng = np.random.default_rng(seed + 1)
+    w13 = torch.from_numpy((rng.standard_normal((1, 4096, 4096), dtype=np.float32) * np.float32(0.02))).cuda()
+    w2 = torch.from_numpy((rng.standard_normal((1, 4096, 2048), dtype=np.float32) * np.float32(0.02))).cuda()
+    sw = api.quantize_moe_weights(w13.to(torch.bfloat16), w2.to(torch.bfloat16))
+    sh = bf16(swl.hidden)
+    one = torch.ones(1, dtype=torch.float32, device="cuda")
+    a1s = torch.full((1,), 2688.0 / float(sh.abs().max()), dtype=torch.float32, device="cuda")
+    se = api.SharedExpertForward(8192, 4096, 2048)
+    sout = torch.empty((8192, 4096), dtype=torch.bfloat16, device="cuda")
+    se_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def shared():
+        se_ev[0].record()
+        se(sh, sw, a1s, one * 200.0, GATE_LIMIT, UP_LIMIT, out=sout)  # fixed L2 scale: timing only
+        se_ev[1].record()
+
+    ms, _ = timed(shared, se_ev)
+    flops = 2.0 * 8192 * 4096 * 2048 * 3
+    res["shared_expert"] = {"workload": "shared-expert NVFP4 SwiGLU FFN T=8192 H=4096 I=2048 (quantize + L1 + L2)",
+                            "ms_per_call": round(ms, 4), "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+                            "frac_fp4": round(flops / (ms * 1e-3) / 1e12 / fp4_peak, 4)}
     res["l2"] = "flushed (512 MB write) before each call"
     return res
 
