@@ -206,6 +206,7 @@ __global__ void __launch_bounds__(256) gather_quantize_kernel(const uint16_t* __
       const int e = topk_ids[t * top_k + lane];
       my_gs = e >= 0 ? a1_gs[e] : 1.f;
     }
+#pragma unroll 2  // two slots' blocks in flight per lane (independent dependency chains)
     for (int j = 0; j < top_k; ++j) {
       const int64_t r = __shfl_sync(0xffffffffu, my_row, j);
       const float gs = __shfl_sync(0xffffffffu, my_gs, j);
