@@ -287,12 +287,20 @@ __global__ void __launch_bounds__(256) token_combine_kernel(const uint16_t* __re
   pdl_wait();
   const int64_t t = blockIdx.x;
   __shared__ int32_t rows[kMaxTopK];
-  if (threadIdx.x < k) rows[threadIdx.x] = inverse[t * k + threadIdx.x];
+  __shared__ int n_rows;
+  if (threadIdx.x == 0) {  // the token's local rows in j order (non-local ones contribute nothing)
+    int n = 0;
+    for (int j = 0; j < k; ++j) {
+      const int r = inverse[t * k + j];
+      if (r >= 0) rows[n++] = r;
+    }
+    n_rows = n;
+  }
   __syncthreads();
+  const int n = n_rows;
   for (int64_t c = (int64_t)threadIdx.x * 8; c < H; c += (int64_t)blockDim.x * 8) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      if (rows[j] < 0) continue;  // not a local expert: contributes nothing
+    for (int j = 0; j < n; ++j) {
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + (int64_t)rows[j] * H + c));
       const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
