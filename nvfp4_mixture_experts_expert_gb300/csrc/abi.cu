@@ -417,17 +417,25 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
   const int nb = (int)L.route_blocks;
   cudaError_t e;
   stage_mark(0, s);
-  e = rt.logits ? launch_route_topk(rt.logits, T, E, top_k, ids, wts, bcnt, s)
-                : launch_route_external(rt.topk_ids, rt.topk_w, rt.experts_start, T, E, top_k, ids, wts, bcnt, s);
-  if (e != cudaSuccess) return cuda_fail(e, "route launch");
-  stage_mark(1, s);
-  if ((e = launch_slot_scan(bcnt, nb, E, counts, offsets, meta, tile_expert, sorted_ids, row_w, nullptr, 0, s, true)) !=
-      cudaSuccess)
-    return cuda_fail(e, "slot scan launch");
-  stage_mark(2, s);
-  if ((e = launch_slot_scatter(ids, wts, T, E, top_k, bcnt, offsets, sorted_ids, row_w, inverse, s, true)) !=
-      cudaSuccess)
-    return cuda_fail(e, "slot scatter launch");
+  if (T <= kSmallRouteTokens) {  // one block: routing, offsets and slots without launch boundaries
+    if ((e = launch_route_small(rt.logits, rt.topk_ids, rt.topk_w, rt.experts_start, T, E, top_k, ids, wts, counts,
+                                offsets, meta, tile_expert, sorted_ids, row_w, inverse, s)) != cudaSuccess)
+      return cuda_fail(e, "route launch");
+    stage_mark(1, s);
+    stage_mark(2, s);
+  } else {
+    e = rt.logits ? launch_route_topk(rt.logits, T, E, top_k, ids, wts, bcnt, s)
+                  : launch_route_external(rt.topk_ids, rt.topk_w, rt.experts_start, T, E, top_k, ids, wts, bcnt, s);
+    if (e != cudaSuccess) return cuda_fail(e, "route launch");
+    stage_mark(1, s);
+    if ((e = launch_slot_scan(bcnt, nb, E, counts, offsets, meta, tile_expert, sorted_ids, row_w, nullptr, 0, s,
+                              true)) != cudaSuccess)
+      return cuda_fail(e, "slot scan launch");
+    stage_mark(2, s);
+    if ((e = launch_slot_scatter(ids, wts, T, E, top_k, bcnt, offsets, sorted_ids, row_w, inverse, s, true)) !=
+        cudaSuccess)
+      return cuda_fail(e, "slot scatter launch");
+  }
   stage_mark(3, s);
   if ((e = launch_gather_quantize((const uint16_t*)hidden, H, T, top_k, ids, inverse, counts, offsets, E, a1_gs,
                                   cap, a1, sfa1, s, true)) != cudaSuccess)

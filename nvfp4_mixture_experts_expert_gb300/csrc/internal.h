@@ -56,6 +56,13 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int3
 // Expert-parallel routing from given global top-k ids / weights (see route.cu).
 cudaError_t launch_route_external(const int32_t* topk_ids, const float* topk_w, int32_t start, int64_t T, int E,
                                   int k, int32_t* ids, float* w, int32_t* block_counts, cudaStream_t s);
+// Small batches: routing (logits, or external ids when logits is null),
+// offsets, tile table, pad rows and slot permutation in one block.
+constexpr int64_t kSmallRouteTokens = 256;
+cudaError_t launch_route_small(const float* logits, const int32_t* ext_ids, const float* ext_w, int32_t start,
+                               int64_t T, int E, int k, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                               int32_t* meta, int32_t* tile_expert, int32_t* sorted_ids, float* row_w,
+                               int32_t* inverse, cudaStream_t s);
 cudaError_t launch_slot_scan(int32_t* block_counts, int nblocks, int E, int32_t* counts, int32_t* offsets,
                              int32_t* meta, int32_t* tile_expert, int32_t* sorted_ids, float* row_w,
                              uint32_t* zero_words, int n_zero_words, cudaStream_t s, bool pdl = false);

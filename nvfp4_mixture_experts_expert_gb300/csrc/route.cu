@@ -57,6 +57,43 @@ __device__ __forceinline__ int key_expert(uint64_t key) { return (int)(0xFFFFFFF
 // then lane j < k computes exp(l_j - l_max) and the warp sum gives the
 // renormalised weights.
 template <int NK>
+__device__ __forceinline__ void route_token(const float* __restrict__ logits, int64_t t, int E, int k, int lane,
+                                            int32_t* __restrict__ ids, float* __restrict__ w, int32_t* hist) {
+  uint64_t key[NK];
+#pragma unroll
+  for (int i = 0; i < NK; ++i) {
+    const int e = i * 32 + lane;
+    key[i] = e < E ? route_key(__ldg(logits + t * E + e), e) : 0ull;
+  }
+  uint64_t mine = 0ull;  // lane j keeps the j-th selected key
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    if (j >= k) break;
+    uint64_t best = key[0];
+#pragma unroll
+    for (int i = 1; i < NK; ++i) best = key[i] > best ? key[i] : best;
+    const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32));
+    const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32) == hi ? (uint32_t)best : 0u);
+    const uint64_t win = ((uint64_t)hi << 32) | lo;
+#pragma unroll
+    for (int i = 0; i < NK; ++i)
+      if (key[i] == win) key[i] = 0ull;  // keys are unique: only the winner's lane matches
+    if (lane == j) mine = win;
+  }
+  const uint64_t top = __shfl_sync(0xffffffffu, mine, 0);
+  const float z = lane < k ? expf(key_value(mine) - key_value(top)) : 0.f;
+  float sum = z;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane < k) {
+    const int e = key_expert(mine);
+    ids[t * k + lane] = e;
+    w[t * k + lane] = z / sum;
+    atomicAdd(&hist[e], 1);
+  }
+}
+
+template <int NK>
 __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
     const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ ids, float* __restrict__ w,
     int32_t* __restrict__ block_counts) {
@@ -67,40 +104,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
   __syncthreads();
   const int64_t t0 = (int64_t)blockIdx.x * kRouteTokensPerBlock;
   const int64_t t1 = min(T, t0 + kRouteTokensPerBlock);
-  for (int64_t t = t0 + warp; t < t1; t += kRouteWarps) {
-    uint64_t key[NK];
-#pragma unroll
-    for (int i = 0; i < NK; ++i) {
-      const int e = i * 32 + lane;
-      key[i] = e < E ? route_key(__ldg(logits + t * E + e), e) : 0ull;
-    }
-    uint64_t mine = 0ull;  // lane j keeps the j-th selected key
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-      if (j >= k) break;
-      uint64_t best = key[0];
-#pragma unroll
-      for (int i = 1; i < NK; ++i) best = key[i] > best ? key[i] : best;
-      const uint32_t hi = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32));
-      const uint32_t lo = __reduce_max_sync(0xffffffffu, (uint32_t)(best >> 32) == hi ? (uint32_t)best : 0u);
-      const uint64_t win = ((uint64_t)hi << 32) | lo;
-#pragma unroll
-      for (int i = 0; i < NK; ++i)
-        if (key[i] == win) key[i] = 0ull;  // keys are unique: only the winner's lane matches
-      if (lane == j) mine = win;
-    }
-    const uint64_t top = __shfl_sync(0xffffffffu, mine, 0);
-    const float z = lane < k ? expf(key_value(mine) - key_value(top)) : 0.f;
-    float sum = z;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane < k) {
-      const int e = key_expert(mine);
-      ids[t * k + lane] = e;
-      w[t * k + lane] = z / sum;
-      atomicAdd(&hist[e], 1);
-    }
-  }
+  for (int64_t t = t0 + warp; t < t1; t += kRouteWarps) route_token<NK>(logits, t, E, k, lane, ids, w, hist);
   __syncthreads();
   // expert-major: block_counts[e][block]
   for (int e = threadIdx.x; e < E; e += blockDim.x) block_counts[(int64_t)e * gridDim.x + blockIdx.x] = hist[e];
@@ -314,6 +318,120 @@ __global__ void __launch_bounds__(256) token_combine_kernel(const uint16_t* __re
   }
 }
 
+// Small batches (T <= kSmallRouteTokens): routing, padded offsets, tile
+// table, pad rows and the stable slot permutation in one block of 32 warps,
+// phase after phase (the same arithmetic as route_topk / route_external,
+// slot_scan and slot_scatter, without their launch boundaries).
+constexpr int kSmallWarps = 32;
+
+template <int NK>
+__global__ void __launch_bounds__(kSmallWarps * 32) route_small_kernel(
+    const float* __restrict__ logits, const int32_t* __restrict__ ext_ids, const float* __restrict__ ext_w,
+    int32_t start, int64_t T, int E, int k, int32_t* __restrict__ ids, float* __restrict__ w,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ meta,
+    int32_t* __restrict__ tile_expert, int32_t* __restrict__ sorted_ids, float* __restrict__ row_w,
+    int32_t* __restrict__ inverse) {
+  pdl_trigger();
+  __shared__ int32_t hist[kMaxExperts];
+  __shared__ int32_t s_off[kMaxExperts + 1];
+  __shared__ int32_t running[kMaxExperts];
+  __shared__ int32_t warp_cnt[kSmallWarps][kMaxExperts];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t A = T * k;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  // phase 1: routing and per-expert counts
+  if (logits) {
+    for (int64_t t = warp; t < T; t += kSmallWarps) route_token<NK>(logits, t, E, k, lane, ids, w, hist);
+  } else {
+    for (int64_t f = threadIdx.x; f < A; f += blockDim.x) {
+      const int64_t e = (int64_t)ext_ids[f] - start;
+      const bool local = e >= 0 && e < E;
+      ids[f] = local ? (int32_t)e : -1;
+      w[f] = local ? ext_w[f] : 0.f;
+      if (local) atomicAdd(&hist[e], 1);
+    }
+  }
+  __syncthreads();
+  // phase 2: padded offsets (multiples of 128), tile table, pad rows
+  if (warp == 0) {
+    int off = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int c = e < E ? (hist[e] + 127) / 128 * 128 : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+      }
+      if (e < E) s_off[e] = off + incl - c;
+      off += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      s_off[E] = off;
+      meta[0] = off;
+      meta[1] = off / 128;
+      meta[2] = 0;
+      meta[3] = 0;
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = s_off[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    counts[e] = hist[e];
+    running[e] = s_off[e];
+  }
+  for (int mt = threadIdx.x; mt < s_off[E] / 128; mt += blockDim.x) {
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_off[mid] <= mt * 128) lo = mid;
+      else hi = mid;
+    }
+    tile_expert[mt] = lo;
+  }
+  for (int i = threadIdx.x; i < E * 128; i += blockDim.x) {
+    const int e = i >> 7, j = i & 127;
+    const int r = s_off[e] + hist[e] + j;
+    if (r < s_off[e + 1]) {
+      sorted_ids[r] = -1;
+      row_w[r] = 0.f;
+    }
+  }
+  for (int i = threadIdx.x; i < kSmallWarps * E; i += blockDim.x) warp_cnt[i / E][i % E] = 0;
+  __syncthreads();
+  // phase 3: stable rank of every assignment inside its expert (ascending flat index)
+  for (int64_t base = 0; base < A; base += blockDim.x) {
+    const int64_t f = base + threadIdx.x;
+    const bool valid = f < A;
+    const int e = valid ? ids[f] : -1;
+    const bool local = e >= 0;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (local && rank == 0) warp_cnt[warp][e] = __popc(peers);
+    __syncthreads();
+    if (valid && !local) inverse[f] = -1;
+    if (local) {
+      int pre = running[e] + rank;
+      for (int q = 0; q < warp; ++q) pre += warp_cnt[q][e];
+      sorted_ids[pre] = (int32_t)(f / k);
+      row_w[pre] = w[f];
+      inverse[f] = pre;
+    }
+    __syncthreads();
+    for (int x = threadIdx.x; x < E; x += blockDim.x) {
+      int add = 0;
+      for (int q = 0; q < kSmallWarps; ++q) {
+        add += warp_cnt[q][x];
+        warp_cnt[q][x] = 0;
+      }
+      running[x] += add;
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
@@ -332,6 +450,26 @@ cudaError_t launch_route_external(const int32_t* topk_ids, const float* topk_w, 
   const int64_t nb = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
   route_external_kernel<<<(unsigned)nb, kRouteWarps * 32, 0, s>>>(topk_ids, topk_w, start, T, E, k, ids, w,
                                                                    block_counts);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_small(const float* logits, const int32_t* ext_ids, const float* ext_w, int32_t start,
+                               int64_t T, int E, int k, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                               int32_t* meta, int32_t* tile_expert, int32_t* sorted_ids, float* row_w,
+                               int32_t* inverse, cudaStream_t s) {
+  const dim3 grid(1), block(kSmallWarps * 32);
+  if (!logits || E <= 32)
+    route_small_kernel<1><<<grid, block, 0, s>>>(logits, ext_ids, ext_w, start, T, E, k, ids, w, counts, offsets,
+                                                 meta, tile_expert, sorted_ids, row_w, inverse);
+  else if (E <= 64)
+    route_small_kernel<2><<<grid, block, 0, s>>>(logits, ext_ids, ext_w, start, T, E, k, ids, w, counts, offsets,
+                                                 meta, tile_expert, sorted_ids, row_w, inverse);
+  else if (E <= 128)
+    route_small_kernel<4><<<grid, block, 0, s>>>(logits, ext_ids, ext_w, start, T, E, k, ids, w, counts, offsets,
+                                                 meta, tile_expert, sorted_ids, row_w, inverse);
+  else
+    route_small_kernel<8><<<grid, block, 0, s>>>(logits, ext_ids, ext_w, start, T, E, k, ids, w, counts, offsets,
+                                                 meta, tile_expert, sorted_ids, row_w, inverse);
   return cudaGetLastError();
 }
 

@@ -262,6 +262,30 @@ def test_routed_forward_matches_oracle():
     assert rf <= 2e-2 and cs >= 0.999, (rf, cs)
 
 
+def test_routed_forward_matches_oracle_multi_block_routing():
+    """T above the single-block routing limit: the routing, scan and scatter
+    kernels of large batches, on external ids."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    wl, orc, gids, gw, start = _routed_case(T=600, seed=77)
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.top_k
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    fwd = api.MoEForward(T, H, I, E, k)
+    out = fwd.routed(bf16_dev(wl.hidden), dev(gids), dev(gw), start, w, dev(orc.a1_gs), dev(orc.a2_gs),
+                     wl.gate_limit, wl.up_limit)
+    torch.cuda.synchronize()
+    ids, wts = O.remap_global_ids(gids, gw.astype(np.float64), start, E)
+    m = O.sort_slots(ids, wts, E)
+    np.testing.assert_array_equal(host(fwd.view("offsets", torch.int32, E + 1)), m["offsets"])
+    np.testing.assert_array_equal(host(fwd.view("sorted_token_ids", torch.int32, m["P"])), m["sorted_token_ids"])
+    np.testing.assert_array_equal(host(fwd.view("inverse", torch.int32, T * k)), m["inverse"])
+    ref = O.moe_forward_routed(W.bf16_bits_to_f32(wl.hidden), ids, wts.astype(np.float32).astype(np.float64),
+                               orc.w13q, orc.w2q, orc.a1_gs, orc.a2_gs, wl.gate_limit, wl.up_limit)
+    got = bf16_host(out)
+    rf, cs = rel_frob(got, ref), cosine(got, ref)
+    assert rf <= 2e-2 and cs >= 0.999, (rf, cs)
+
+
 def test_routed_forward_with_the_forward_own_routing_is_bit_identical():
     """The routing the logit forward computed on the device, shifted to global
     ids, gives the routed forward the logit forward's output bit for bit."""
