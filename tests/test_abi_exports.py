@@ -86,3 +86,34 @@ def test_gemm_variant_mode_setter(binding):
         assert binding.nvfp4_gemm_set_cta_pair(1) == 1
     finally:
         binding.nvfp4_gemm_set_cta_pair(prev)
+
+
+def test_routed_and_shared_expert_entries_check_arguments_on_host(binding):
+    # routed forward: ids / weights required, sizes as the logit forward
+    with pytest.raises(binding.Nvfp4Error) as ei:
+        binding.nvfp4_moe_forward_routed(16, None, 16, 0, 4, 256, 128, 4, 2, 16, 16, 16, 16, 16, 16, 16, 16, 10.0,
+                                         10.0, 256, 1 << 30, 16, stream=0)
+    assert ei.value.status == binding.NVFP4_ERR_INVALID_ARG
+    with pytest.raises(binding.Nvfp4Error) as ei:
+        binding.nvfp4_moe_forward_routed(16, 16, 16, 0, 4, 300, 128, 4, 2, 16, 16, 16, 16, 16, 16, 16, 16, 10.0,
+                                         10.0, 256, 1 << 30, 16, stream=0)
+    assert ei.value.status == binding.NVFP4_ERR_UNSUPPORTED
+    # shared expert: H % 256, I % 128, workspace size and alignment
+    with pytest.raises(binding.Nvfp4Error) as ei:
+        binding.nvfp4_shared_expert_forward(16, 4, 300, 128, 16, 16, 16, 16, 16, 16, 16, 16, 10.0, 10.0, 256,
+                                            1 << 30, 16, stream=0)
+    assert ei.value.status == binding.NVFP4_ERR_UNSUPPORTED
+    need = binding.nvfp4_shared_expert_workspace_size(4, 256, 128)
+    assert need > 0
+    with pytest.raises(binding.Nvfp4Error) as ei:
+        binding.nvfp4_shared_expert_forward(16, 4, 256, 128, 16, 16, 16, 16, 16, 16, 16, 16, 10.0, 10.0, 256,
+                                            need - 1, 16, stream=0)
+    assert ei.value.status == binding.NVFP4_ERR_WORKSPACE
+    with pytest.raises(binding.Nvfp4Error) as ei:
+        binding.nvfp4_shared_expert_forward(16, 4, 256, 128, 16, 16, 16, 16, 16, 16, 16, 16, 10.0, 10.0, 16,
+                                            need, 16, stream=0)
+    assert ei.value.status == binding.NVFP4_ERR_INVALID_ARG  # workspace not 256-byte aligned
+    with pytest.raises(binding.Nvfp4Error) as ei:
+        binding.nvfp4_shared_expert_forward(16, 4, 256, 128, 16, 16, 16, 16, 16, 16, 16, 16, -1.0, 10.0, 256,
+                                            need, 16, stream=0)
+    assert ei.value.status == binding.NVFP4_ERR_INVALID_ARG  # limits must be positive
