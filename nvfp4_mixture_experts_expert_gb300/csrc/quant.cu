@@ -23,6 +23,8 @@ __device__ __forceinline__ uint4 ldg_nc(const uint16_t* p) {
 // ---------------------------------------------------------------- amax
 __global__ void group_amax_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ld_x,
                                   int64_t gstride_x, float* __restrict__ partial) {
+  pdl_trigger();
+  pdl_wait();
   const int g = blockIdx.y;
   const int nb = gridDim.x;
   const int64_t vec_per_row = K / 8;
@@ -54,6 +56,8 @@ __global__ void group_amax_kernel(const uint16_t* __restrict__ x, int64_t rows, 
 
 // gs = 2688 / amax (IEEE division), 1 when the group is all zero.
 __global__ void group_gs_kernel(const float* __restrict__ partial, int nb, int groups, float* __restrict__ gs) {
+  pdl_trigger();
+  pdl_wait();
   const int g = blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= groups) return;
   float a = 0.f;
@@ -252,12 +256,14 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
                                                        const float* __restrict__ gs, float* __restrict__ gs_copy,
                                                        uint8_t* __restrict__ fp4, uint8_t* __restrict__ sf,
                                                        int64_t rows_padded) {
+  pdl_trigger();
   __shared__ float2 tab[128];
   if (threadIdx.x < 128) {
     const float d = e4m3_value(threadIdx.x);
     tab[threadIdx.x] = make_float2(d, threadIdx.x ? __frcp_rn(d) : 0.f);
   }
   __syncthreads();
+  pdl_wait();  // the global scales may come from the amax kernels just before
   if (gs_copy && blockIdx.x == 0)
     for (int i = threadIdx.x; i < groups; i += blockDim.x) gs_copy[i] = gs[i];
   const float rcp6 = __frcp_rn(6.0f);
@@ -337,9 +343,10 @@ int grid_for(int64_t items, int threads, int num_sms, int per_sm) {
 cudaError_t launch_group_amax(const uint16_t* x, int64_t rows, int64_t K, int64_t ld_x, int64_t gstride_x,
                               int groups, float* partial, float* gs_out, cudaStream_t s) {
   dim3 grid(kAmaxBlocksPerGroup, groups);
-  group_amax_kernel<<<grid, 256, 0, s>>>(x, rows, K, ld_x, gstride_x, partial);
-  group_gs_kernel<<<(groups + 127) / 128, 128, 0, s>>>(partial, kAmaxBlocksPerGroup, groups, gs_out);
-  return cudaGetLastError();
+  cudaError_t e = launch_kernel(group_amax_kernel, grid, dim3(256), 0, s, true, x, rows, K, ld_x, gstride_x, partial);
+  if (e != cudaSuccess) return e;
+  return launch_kernel(group_gs_kernel, dim3((groups + 127) / 128), dim3(128), 0, s, true, (const float*)partial,
+                       (int)kAmaxBlocksPerGroup, groups, gs_out);
 }
 
 cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, int64_t ld_x, int64_t gstride_x,
@@ -348,11 +355,9 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, int64_t 
   const int64_t warps = rows_padded * ((K + 1023) / 1024) * groups;
   const int grid = grid_for(warps * 32, 256, num_sms, 8);
   const bool a32 = (reinterpret_cast<uintptr_t>(x) & 31u) == 0 && ld_x % 16 == 0 && gstride_x % 16 == 0;
-  if (a32) quantize_kernel<true><<<grid, 256, 0, s>>>(x, rows, K, ld_x, gstride_x, groups, gs, gs_copy, fp4, sf,
-                                                      rows_padded);
-  else quantize_kernel<false><<<grid, 256, 0, s>>>(x, rows, K, ld_x, gstride_x, groups, gs, gs_copy, fp4, sf,
-                                                   rows_padded);
-  return cudaGetLastError();
+  auto* kernel = a32 ? quantize_kernel<true> : quantize_kernel<false>;
+  return launch_kernel(kernel, dim3(grid), dim3(256), 0, s, true, x, rows, K, ld_x, gstride_x, groups, gs, gs_copy,
+                       fp4, sf, rows_padded);
 }
 
 cudaError_t launch_assemble_scales(const uint8_t* sf_linear, int64_t sf_cols, const int32_t* offsets,
