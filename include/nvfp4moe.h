@@ -187,6 +187,15 @@ int nvfp4_debug_gemm_stall(const void* A, const void* SFA, const float* a_gs, co
  *   w13_sf         device u8 [E][2I*H/16]  (tile layout per expert)
  *   w2             device u8 [E][H][I/2],  w2_sf device u8 [E][H*I/16]
  *   w13_gs, w2_gs, a1_gs, a2_gs   device f32[E] global (encode) scales
+ *   a2_gs may be NULL: the L2 activation scales are then taken from this
+ *                  batch (vllm page: the L2 scale from the actual L1 output;
+ *                  cutedsl page: a BF16 L1 output when no calibrated L2 scale
+ *                  exists): a2_gs[e] = 2688 / amax(h of expert e's rows), 1
+ *                  when that is 0.  L1 writes h in bf16 into the workspace's y
+ *                  region with that amax, a quantize pass reads it back, and
+ *                  the scales used are left in the workspace (calib region,
+ *                  f32 at byte offset 4E).  Same results, bit for bit, as a
+ *                  call given those scales.
  *   workspace      device scratch of nvfp4_moe_workspace_size(...) bytes, 256-aligned;
  *                  it also holds every intermediate (see nvfp4_moe_workspace_layout).
  *   out            device bf16 [T][H]
@@ -270,8 +279,10 @@ int nvfp4_moe_calibrate(const void* hidden, const float* router_logits, int64_t 
  *   tile_expert i32[cap/128], sorted_token_ids i32[cap] (-1 pad),
  *   row_weight f32[cap] (0 pad), inverse i32[A] (assignment -> row)
  *   a1 u8[cap][H/2], sfa1 u8[cap*H/16], a2 u8[cap][I/2], sfa2 u8[cap*I/16]
- *   y bf16[cap][H] (routing-weighted L2 rows in slot order), calib u32[2E]
- *   (calibration amax bits)
+ *   y bf16[cap][max(H, I)] (routing-weighted L2 rows in slot order, row
+ *   stride H; with a2_gs NULL first the bf16 L1 output, row stride I),
+ *   calib u32[2E] (calibration amax bits; with a2_gs NULL, E amax words of
+ *   the L1 output, then the E L2 global scales as f32)
  * Only rows < P of the row-indexed buffers are defined after a call.
  */
 typedef struct {

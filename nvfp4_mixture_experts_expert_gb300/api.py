@@ -110,6 +110,8 @@ class MoEForward:
 
     def __call__(self, hidden, logits, w: MoEWeights, a1_gs, a2_gs, gate_limit=10.0, up_limit=10.0, out=None,
                  stream=None):
+        """a2_gs None: each expert's L2 activation scale is taken from this
+        batch's own L1 output (read back with batch_l2_scales())."""
         if out is None:
             out = torch.empty((self.T, self.H), dtype=torch.bfloat16, device=hidden.device)
         B.nvfp4_moe_forward(hidden, logits, self.T, self.H, self.I, self.E, self.top_k, w.w13, w.w13_sf,
@@ -136,6 +138,11 @@ class MoEForward:
         B.nvfp4_moe_calibrate(hidden, logits, self.T, self.H, self.I, self.E, self.top_k, w.w13, w.w13_sf,
                               w.w13_gs, gate_limit, up_limit, self.workspace, self.ws_bytes, a1, a2, stream)
         return a1, a2
+
+    def batch_l2_scales(self):
+        """The L2 global scales the last call with a2_gs None used (f32 [E])."""
+        off = self.layout["calib"] + 4 * self.E
+        return self.workspace[off:off + 4 * self.E].view(torch.float32)
 
     def view(self, name, dtype, count):
         """A view of one intermediate of the last call (see nvfp4_moe_workspace_layout)."""

@@ -293,7 +293,7 @@ int nvfp4_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int E, int top_k
   out->sfa1 = take(cap * H / 16);
   out->a2 = take(cap * I / 2);
   out->sfa2 = take(cap * I / 16);
-  out->y = take(cap * H * 2);
+  out->y = take(cap * (H > I ? H : I) * 2);  // also the bf16 L1 output when L2 scales come from the batch
   out->calib = take((int64_t)2 * E * 4);
   out->total = off;
   out->capacity = cap;
@@ -331,7 +331,7 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
   nvfp4_moe_layout L;
   if (int rc = nvfp4_moe_workspace_layout(T, H, I, E, top_k, &L)) return rc;
   if (T == 0) return NVFP4_OK;
-  if (!hidden || !w13 || !w13_sf || !w13_gs || !w2 || !w2_sf || !w2_gs || !a1_gs || !a2_gs || !out ||
+  if (!hidden || !w13 || !w13_sf || !w13_gs || !w2 || !w2_sf || !w2_gs || !a1_gs || !out ||
       (rt.logits ? false : (!rt.topk_ids || !rt.topk_w)))
     return fail(NVFP4_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(hidden) || !aligned16(w13) || !aligned16(w13_sf) || !aligned16(w2) || !aligned16(w2_sf) ||
@@ -363,6 +363,11 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
   uint8_t* sfa2 = ws + L.sfa2;
   uint16_t* ybuf = (uint16_t*)(ws + L.y);
   const int64_t cap = L.capacity;
+  // No L2 scales given: L1 stores its bf16 SwiGLU output (in the y region)
+  // and per-expert amax, and a quantize pass derives the scales from them.
+  const bool batch_l2_scale = a2_gs == nullptr;
+  uint32_t* l2_amax = (uint32_t*)(ws + L.calib);
+  float* l2_gs = (float*)(ws + L.calib) + E;
 
   GemmArgs g1, g2;
   memset(&g1, 0, sizeof(g1));
@@ -387,6 +392,11 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
   g1.q_out = a2;
   g1.q_sf = sfa2;
   g1.q_gs = a2_gs;
+  if (batch_l2_scale) {
+    g1.D = ybuf;
+    g1.ldd = I;
+    g1.amax_bits = l2_amax;
+  }
   g1.I = (int)I;
   g1.gate_limit = gate_limit;
   g1.up_limit = up_limit;
@@ -396,7 +406,7 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
   g2.sfa = sfa2;
   g2.sfb = (const uint8_t*)w2_sf;
   g2.padded_offsets = offsets;
-  g2.a_gs = a2_gs;
+  g2.a_gs = batch_l2_scale ? l2_gs : a2_gs;
   g2.b_gs = w2_gs;
   g2.G = E;
   g2.K = (int)I;
@@ -417,6 +427,8 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
   const int nb = (int)L.route_blocks;
   cudaError_t e;
   stage_mark(0, s);
+  if (batch_l2_scale && (e = cudaMemsetAsync(l2_amax, 0, (size_t)E * 4, s)) != cudaSuccess)
+    return cuda_fail(e, "amax reset");
   if (T <= kSmallRouteTokens) {  // one block: routing, offsets and slots without launch boundaries
     if ((e = launch_route_small(rt.logits, rt.topk_ids, rt.topk_w, rt.experts_start, T, E, top_k, ids, wts, counts,
                                 offsets, meta, tile_expert, sorted_ids, row_w, inverse, s)) != cudaSuccess)
@@ -442,8 +454,12 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
     return cuda_fail(e, "gather launch");
   stage_mark(4, s);
   const int64_t t1 = cap / 128 * g1.n_tiles, t2 = cap / 128 * g2.n_tiles;
-  if ((e = launch_gemm(kEpiSwigluQuant, g1, (int)t1, dev->sms, s, true)) != cudaSuccess)
+  if ((e = launch_gemm(batch_l2_scale ? kEpiSwigluAmax : kEpiSwigluQuant, g1, (int)t1, dev->sms, s, true)) !=
+      cudaSuccess)
     return cuda_fail(e, "L1 launch");
+  if (batch_l2_scale && (e = launch_slot_quantize(ybuf, I, meta, tile_expert, cap, l2_amax, E, l2_gs, a2, sfa2,
+                                                  dev->sms, s, true)) != cudaSuccess)
+    return cuda_fail(e, "L2 activation quantize launch");
   stage_mark(5, s);
   if ((e = launch_gemm(kEpiCombine, g2, (int)t2, dev->sms, s, true)) != cudaSuccess)
     return cuda_fail(e, "L2 launch");

@@ -11,7 +11,9 @@
 //                    in slot order; the token combine then sums each token's
 //                    top_k rows (vllm page: scatter_add with zero-weight pads)
 //   kEpiSwigluAmax   MoE calibration: per-expert amax of the bf16 SwiGLU output
-//                    (vllm page: L2 global scale from the actual L1 output)
+//                    (vllm page: L2 global scale from the actual L1 output);
+//                    optionally stores that bf16 output (forward with L2
+//                    scales taken from the batch, cutedsl page's BF16 L1 output)
 //
 // Design (persistent over output tiles, warp-specialised, one CTA per SM):
 //   warp 0   TMA producer: per K-stage of 256 elements, the A box (128 rows x
@@ -506,14 +508,29 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
                    words[6], words[7]);
       *reinterpret_cast<uint32_t*>(p.q_sf + sf_offset(row, f0 / 16, p.I / 16)) = scales;
     } else if constexpr (EPI == kEpiSwigluAmax) {
-      // calibration: amax of the bf16 SwiGLU output of this row's features
+      // amax of the bf16 SwiGLU output of this row's 64 features; with D set,
+      // the bf16 values themselves too (row-major, ldd elements per row)
       uint32_t m = 0;
+      uint32_t hw[32];
 #pragma unroll
-      for (int f = 0; f < 64; ++f) {
-        const float h = silu_clamped_product(__uint_as_float(v[f >> 5][f & 31]) * alpha,
-                                             __uint_as_float(v[2 + (f >> 5)][f & 31]) * alpha, p.gate_limit,
-                                             p.up_limit);
-        m = max(m, f32_to_bf16_rn(h) & 0x7FFFu);
+      for (int q = 0; q < 32; ++q) {
+        const int f = 2 * q;  // features f, f+1: same 32-column load
+        const float h0 = silu_clamped_product(__uint_as_float(v[f >> 5][f & 31]) * alpha,
+                                              __uint_as_float(v[2 + (f >> 5)][f & 31]) * alpha, p.gate_limit,
+                                              p.up_limit);
+        const float h1 = silu_clamped_product(__uint_as_float(v[f >> 5][(f & 31) + 1]) * alpha,
+                                              __uint_as_float(v[2 + (f >> 5)][(f & 31) + 1]) * alpha, p.gate_limit,
+                                              p.up_limit);
+        hw[q] = pack_bf16x2(h0, h1);
+        m = max(m, max(hw[q] & 0x7FFFu, (hw[q] >> 16) & 0x7FFFu));
+      }
+      if (p.D) {
+        // 32-byte aligned: the caller passes a 32-byte aligned D and ldd a multiple of 16
+        uint16_t* drow = p.D + row * p.ldd + (int64_t)nt * 128 + half * 64;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          st_global_v8(drow + c * 16, hw[8 * c], hw[8 * c + 1], hw[8 * c + 2], hw[8 * c + 3], hw[8 * c + 4],
+                       hw[8 * c + 5], hw[8 * c + 6], hw[8 * c + 7]);
       }
 #pragma unroll
       for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));

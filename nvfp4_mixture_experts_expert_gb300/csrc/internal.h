@@ -48,6 +48,12 @@ cudaError_t launch_gather_amax(const uint16_t* hidden, int64_t H, const int32_t*
                                const int32_t* tile_expert, const int32_t* meta, int64_t capacity,
                                uint32_t* amax_bits, int num_sms, cudaStream_t s);
 cudaError_t launch_gs_from_amax(const uint32_t* amax_bits, int n, float* gs, cudaStream_t s);
+// MoE L2 activations with global scales from the batch: slot rows of the bf16
+// SwiGLU output h [capacity, K] quantized with gs = 2688/amax of their expert
+// (amax as float bits); gs_out receives the E global scales.
+cudaError_t launch_slot_quantize(const uint16_t* h, int64_t K, const int32_t* meta, const int32_t* tile_expert,
+                                 int64_t capacity, const uint32_t* amax_bits, int E, float* gs_out, uint8_t* fp4,
+                                 uint8_t* sf, int num_sms, cudaStream_t s, bool pdl = false);
 
 // ---------------------------------------------------------------- route.cu
 constexpr int kRouteTokensPerBlock = 16;

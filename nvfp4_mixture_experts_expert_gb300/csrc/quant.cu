@@ -325,11 +325,66 @@ __global__ void __launch_bounds__(256) gather_amax_kernel(const uint16_t* __rest
   }
 }
 
+// gs = 2688 / amax (IEEE division) from amax float bits; 1 for amax 0.
+__device__ __forceinline__ float gs_of_amax_bits(uint32_t bits) {
+  const float a = __uint_as_float(bits);
+  return a > 0.f ? __fdiv_rn(kGsNumerator, a) : 1.0f;
+}
+
 __global__ void gs_from_amax_kernel(const uint32_t* __restrict__ amax_bits, int n, float* __restrict__ gs) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
-  const float a = __uint_as_float(amax_bits[i]);
-  gs[i] = a > 0.f ? __fdiv_rn(kGsNumerator, a) : 1.0f;
+  gs[i] = gs_of_amax_bits(amax_bits[i]);
+}
+
+// L2 activations with global scales taken from the batch: slot rows [0, P) of
+// the bf16 SwiGLU output h [capacity, K] (row-major, 32-byte aligned rows) ->
+// NVFP4 nibbles and tile-layout scales, each row with its expert's
+// gs = 2688 / amax(h of that expert).  Block 0 also stores the E global scales
+// (the L2 GEMM's alpha needs them).  Warp layout as quantize_kernel.
+__global__ void __launch_bounds__(256) slot_quantize_kernel(const uint16_t* __restrict__ h, int64_t K,
+                                                            const int32_t* __restrict__ meta,
+                                                            const int32_t* __restrict__ tile_expert,
+                                                            int64_t capacity, const uint32_t* __restrict__ amax_bits,
+                                                            int E, float* __restrict__ gs_out,
+                                                            uint8_t* __restrict__ fp4, uint8_t* __restrict__ sf) {
+  pdl_trigger();
+  __shared__ float2 tab[128];
+  if (threadIdx.x < 128) {
+    const float d = e4m3_value(threadIdx.x);
+    tab[threadIdx.x] = make_float2(d, threadIdx.x ? __frcp_rn(d) : 0.f);
+  }
+  __syncthreads();
+  pdl_wait();  // h, the amax words and the slot table come from the kernels before
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < E; i += blockDim.x) gs_out[i] = gs_of_amax_bits(amax_bits[i]);
+  const float rcp6 = __frcp_rn(6.0f);
+  const int lane = threadIdx.x & 31;
+  const int64_t P = min((int64_t)meta[0], capacity);
+  const int64_t segs = (K + 1023) / 1024;
+  const int64_t sf_cols = K / 16;
+  for (int64_t item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); item < P * segs;
+       item += (int64_t)gridDim.x * (blockDim.x >> 5)) {
+    const int64_t r = item / segs, e0 = (item - r * segs) * 1024;
+    const float gsv = gs_of_amax_bits(amax_bits[tile_expert[r >> 7]]);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int64_t el = e0 + c * 512 + lane * 16;
+      uint32_t lo = 0u, hi = 0u, sc = 0u;
+      if (el < K) {
+        uint32_t raw[8];
+        ld_block32<true>(h + r * K + el, raw);
+        sc = quant_block16_bf16(raw, block_amax_bf16(raw), gsv, rcp6, tab, lo, hi);
+      }
+      const uint32_t word = sc | (__shfl_down_sync(0xffffffffu, sc, 1) << 8) |
+                            (__shfl_down_sync(0xffffffffu, sc, 2) << 16) |
+                            (__shfl_down_sync(0xffffffffu, sc, 3) << 24);
+      if (el < K) {
+        *reinterpret_cast<uint2*>(fp4 + r * (K / 2) + el / 2) = make_uint2(lo, hi);
+        if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(r, el / 16, sf_cols)) = word;
+      }
+    }
+  }
 }
 
 int grid_for(int64_t items, int threads, int num_sms, int per_sm) {
@@ -395,6 +450,14 @@ cudaError_t launch_gather_amax(const uint16_t* hidden, int64_t H, const int32_t*
 cudaError_t launch_gs_from_amax(const uint32_t* amax_bits, int n, float* gs, cudaStream_t s) {
   gs_from_amax_kernel<<<(n + 127) / 128, 128, 0, s>>>(amax_bits, n, gs);
   return cudaGetLastError();
+}
+
+cudaError_t launch_slot_quantize(const uint16_t* h, int64_t K, const int32_t* meta, const int32_t* tile_expert,
+                                 int64_t capacity, const uint32_t* amax_bits, int E, float* gs_out, uint8_t* fp4,
+                                 uint8_t* sf, int num_sms, cudaStream_t s, bool pdl) {
+  const int grid = grid_for(capacity * ((K + 1023) / 1024) * 32, 256, num_sms, 8);
+  return launch_kernel(slot_quantize_kernel, dim3(grid), dim3(256), 0, s, pdl, h, K, meta, tile_expert, capacity,
+                       amax_bits, E, gs_out, fp4, sf);
 }
 
 }  // namespace nvfp4

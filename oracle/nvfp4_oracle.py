@@ -46,6 +46,10 @@ notes):
       [0, E), else the assignment is not local: it gets weight 0, occupies
       no slot row and contributes nothing; local assignments keep the
       router's weights (no renormalisation after the drop).
+  R19 L2 scales from the batch: when no calibrated L2 activation scale is
+      given, expert e's L2 global scale is 2688 / amax of its own bf16 L1
+      output h in this forward (1 when that amax is 0); h is quantized with it
+      exactly as with a given scale.
 """
 from __future__ import annotations
 
@@ -400,7 +404,10 @@ def moe_forward(hidden, logits, top_k, w13q, w2q, a1_gs, a2_gs,
 def moe_forward_routed(hidden, ids, w, w13q, w2q, a1_gs, a2_gs,
                        gate_limit=10.0, up_limit=10.0, return_intermediates=False):
     """The MoE forward from given routing: local expert ids [T,k] (-1 = not
-    local, R18) and weights [T,k]; otherwise as moe_forward."""
+    local, R18) and weights [T,k]; otherwise as moe_forward.
+    a2_gs None (R19): each expert's L2 global scale is 2688/amax of its own
+    bf16 L1 output in this batch ([vllm] "L2 gs from the actual L1 GEMM
+    output"; [cutedsl] BF16 L1 output when no calibrated L2 scale exists)."""
     hidden = np.asarray(hidden, dtype=np.float32)
     T, H = hidden.shape
     E = w13q[0].shape[0]
@@ -416,10 +423,11 @@ def moe_forward_routed(hidden, ids, w, w13q, w2q, a1_gs, a2_gs,
         toks = meta["sorted_token_ids"][lo:lo + n]
         h = expert_l1(hidden[toks], a1_gs[e], w13q[0][e], w13q[1][e], w13q[2][e],
                       gate_limit, up_limit)
-        Y = expert_l2(h, a2_gs[e], w2q[0][e], w2q[1][e], w2q[2][e])
+        a2e = global_scale(np.max(np.abs(h))) if a2_gs is None else a2_gs[e]
+        Y = expert_l2(h, a2e, w2q[0][e], w2q[1][e], w2q[2][e])
         np.add.at(acc, toks, meta["row_weight"][lo:lo + n, None] * Y)
         if return_intermediates:
-            inter[e] = dict(h=h, Y=Y, toks=toks)
+            inter[e] = dict(h=h, Y=Y, toks=toks, a2_gs=a2e)
     out = bf16_round(acc.astype(np.float32))
     if return_intermediates:
         return out, dict(ids=ids, w=w, meta=meta, experts=inter, acc=acc)

@@ -364,3 +364,60 @@ def test_routing_ties_and_signed_zero_match_oracle():
     assert ids[0].tolist() == list(range(8)) and ids[1, :3].tolist() == [3, 7, 30]
     wts = host(fwd.view("topk_w", torch.float32, wl.T * wl.top_k)).reshape(wl.T, wl.top_k)
     np.testing.assert_allclose(wts, orc.w, rtol=1e-6, atol=1e-7)
+
+
+# ----------------------------------------------------------------- L2 scales from the batch
+
+@pytest.mark.parametrize("T,H,I,E,k,dead", [(120, 512, 256, 6, 2, (3,)), (700, 256, 512, 5, 3, ())])
+def test_batch_l2_scales_match_oracle(T, H, I, E, k, dead):
+    """a2_gs NULL: the L1 GEMM stores bf16 h and per-expert amax, a quantize
+    pass derives each expert's L2 scale.  Small and multi-block routing; an
+    expert with no rows (scale 1); I > H (the bf16 h rows are wider than the
+    output rows they share the workspace region with)."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    wl = W.moe_workload(T, H, I, E, k, 91, dead_experts=dead)
+    orc = OracleMoE(wl)
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    fwd = api.MoEForward(T, H, I, E, k)
+    out = fwd(bf16_dev(wl.hidden), dev(wl.logits), w, dev(orc.a1_gs), None, wl.gate_limit, wl.up_limit)
+    torch.cuda.synchronize()
+    ref, inter = O.moe_forward(orc.hidden, wl.logits, k, orc.w13q, orc.w2q, orc.a1_gs, None, wl.gate_limit,
+                               wl.up_limit, return_intermediates=True)
+    scales = host(fwd.batch_l2_scales())
+    want = np.ones(E, np.float32)
+    for e, d in inter["experts"].items():
+        want[e] = d["a2_gs"]
+    for e in dead:
+        assert scales[e] == 1.0
+    # amax of h from FP32 (kernel) vs FP64 (oracle) accumulation: one bf16 step at most
+    np.testing.assert_allclose(scales, want, rtol=8e-3)
+    assert np.mean(scales == want) >= 0.5
+    got = bf16_host(out)
+    rf, cs = rel_frob(got, ref), cosine(got, ref)
+    assert rf <= 2e-2 and cs >= 0.999, (rf, cs)
+
+
+@pytest.mark.parametrize("T", [100, 600])
+def test_batch_l2_scales_bit_identical_to_the_same_scales_given(T):
+    """The forward with a2_gs NULL and the forward given the scales it derived
+    produce the same L2 activations and the same output, bit for bit (the
+    separate quantize pass and the fused L1 requantization round alike)."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    wl = W.moe_workload(T, 512, 256, 6, 2, 93, logit_bias_std=1.0)
+    orc = OracleMoE(wl)
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    fwd = api.MoEForward(wl.T, wl.H, wl.I, wl.E, wl.top_k)
+    hidden, logits, a1 = bf16_dev(wl.hidden), dev(wl.logits), dev(orc.a1_gs)
+    out_dyn = fwd(hidden, logits, w, a1, None, wl.gate_limit, wl.up_limit)
+    torch.cuda.synchronize()
+    P = orc.meta["P"]
+    a2_dyn = fwd.view("a2", torch.uint8, P * wl.I // 2).clone()
+    sf_dyn = fwd.view("sfa2", torch.uint8, P * wl.I // 16).clone()
+    scales = fwd.batch_l2_scales().clone()
+    out_giv = fwd(hidden, logits, w, a1, scales, wl.gate_limit, wl.up_limit)
+    torch.cuda.synchronize()
+    assert torch.equal(fwd.view("a2", torch.uint8, P * wl.I // 2), a2_dyn)
+    assert torch.equal(fwd.view("sfa2", torch.uint8, P * wl.I // 16), sf_dyn)
+    assert torch.equal(out_dyn, out_giv)

@@ -300,3 +300,59 @@ def test_shared_expert_equals_one_expert_top1_moe():
     moe = O.moe_forward(hidden, wl.logits, 1, w13q, w2q, a1, a2, 10.0, 10.0)
     ffn = O.shared_expert_forward(hidden, w13q, w2q, a1[0], a2[0], 10.0, 10.0)
     np.testing.assert_array_equal(moe, ffn)
+
+
+# ----------------------------------------------------------------- L2 scales from the batch (R19)
+
+def test_batch_l2_scales_match_brute_force_per_expert_amax():
+    """a2_gs None: each expert's L2 scale is 2688/amax of the bf16 SwiGLU
+    output of exactly the tokens routed to it.  The scales are rebuilt here
+    from the brute-force routing (no slots) and fed to the dense brute-force
+    layer."""
+    wl, hidden, w13, w2, w13q, w2q, a1, _ = small_layer(T=40, H=64, I=32, E=5, k=2, seed=21)
+    E, I, k = 5, 32, 2
+    ids, _ = brute_route(wl.logits, k)
+    a2 = np.ones(E, np.float32)
+    for e in range(E):
+        rows = [t for t in range(wl.T) if e in ids[t]]
+        if not rows:
+            continue
+        A = O.dequant_blocks(*O.quantize_blocks(hidden[rows], a1[e])) / np.float64(a1[e])
+        B = O.dequant_blocks(w13q[0][e], w13q[1][e]) / np.float64(w13q[2][e])
+        G = A @ B.T
+        g = np.minimum(G[:, :I], 10.0)
+        u = np.clip(G[:, I:], -10.0, 10.0)
+        h = O.bf16_round((g / (1 + np.exp(-g)) * u).astype(np.float32))
+        amax = np.float32(np.abs(h).max())
+        if amax > 0:
+            a2[e] = np.float32(2688.0) / amax
+    out = O.moe_forward(hidden, wl.logits, k, w13q, w2q, a1, None, 10.0, 10.0)
+    ref = dense_brute_moe(hidden, wl.logits, k, w13q, w2q, a1, a2, 10.0, 10.0)
+    np.testing.assert_allclose(out, ref, rtol=1e-2, atol=1e-6)
+    assert np.mean(out != ref) < 0.01
+
+
+def test_batch_l2_scales_put_each_experts_amax_on_the_top_code():
+    """With the scale taken from the expert's own amax, the largest |h| maps to
+    2688 = 6 * 448: its block gets the largest finite E4M3 scale (448, code
+    0x7E) and it gets the largest E2M1 magnitude (6, code 7)."""
+    wl, hidden, w13, w2, w13q, w2q, a1, _ = small_layer(T=60, H=64, I=32, E=4, k=2, seed=22)
+    _, inter = O.moe_forward(hidden, wl.logits, 2, w13q, w2q, a1, None, 10.0, 10.0,
+                             return_intermediates=True)
+    assert len(inter["experts"]) >= 3
+    for e, d in inter["experts"].items():
+        h = d["h"]
+        nib, s = O.quantize_blocks(h, d["a2_gs"])
+        r, c = np.unravel_index(np.argmax(np.abs(h)), h.shape)
+        assert s[r, c // 16] == 0x7E
+        assert (nib[r, c] & 7) == 7
+        assert s.max() == 0x7E
+
+
+def test_batch_l2_scales_equal_calibrated_scales_forward():
+    """The calibration entry computes the same per-expert amax over the same
+    rows, so a forward given the calibrated L2 scales is the same forward."""
+    wl, hidden, w13, w2, w13q, w2q, a1, a2 = small_layer(T=50, H=64, I=32, E=5, k=2, seed=23)
+    dyn = O.moe_forward(hidden, wl.logits, 2, w13q, w2q, a1, None, 10.0, 10.0)
+    cal = O.moe_forward(hidden, wl.logits, 2, w13q, w2q, a1, a2, 10.0, 10.0)
+    np.testing.assert_array_equal(dyn, cal)
