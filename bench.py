@@ -491,30 +491,56 @@ def decode_side_measurement(seed):
     fwd, w = L["fwd"], L["w"]
     out = torch.empty((L["T"], L["H"]), dtype=torch.bfloat16, device="cuda")
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    flush_rd = torch.ones(256 * 1024 * 1024 // 4, dtype=torch.int32, device="cuda")
 
-    def step():
-        fwd(L["hidden"], L["logits"], w, L["a1"], L["a2"], GATE_LIMIT, UP_LIMIT, out=out)
+    def flush_l2():
+        # evict the weights: write 512 MB, then read 256 MB so that the lines
+        # left in L2 are clean (no write-back traffic lands in the timed step)
+        flush.fill_(1)
+        flush_rd.max()
+
+    def step(stream=None):
+        fwd(L["hidden"], L["logits"], w, L["a1"], L["a2"], GATE_LIMIT, UP_LIMIT, out=out, stream=stream)
 
     from nvfp4_mixture_experts_expert_gb300 import binding as B
     for _ in range(5):
         step()
-    times, stage_times = [], []
+    times, stage_times, graph_times = [], [], []
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     for _ in range(20):
-        flush.fill_(1)  # evict the weights from L2 between iterations
+        flush_l2()
         a.record()
         step()
         b.record()
         torch.cuda.synchronize()
         times.append(a.elapsed_time(b))
     ms = statistics.median(times)
+    # the same step replayed from a CUDA graph (no host launch work in the step)
+    cur = torch.cuda.current_stream()
+    g_stream = torch.cuda.Stream()
+    g_stream.wait_stream(cur)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=g_stream):
+        step(stream=g_stream)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    for _ in range(20):
+        flush_l2()
+        a.record()
+        graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        graph_times.append(a.elapsed_time(b))
+    graph_ms = statistics.median(graph_times)
+    del graph
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
     for ev in evs:  # materialise the CUDA events (torch creates them on first record)
         ev.record()
     torch.cuda.synchronize()
     for _ in range(10):  # separate pass: per-stage events (they serialise the kernels)
-        flush.fill_(1)
+        flush_l2()
         B.nvfp4_moe_set_stage_events(evs)
         step()
         B.nvfp4_moe_set_stage_events(None)
@@ -532,8 +558,12 @@ def decode_side_measurement(seed):
     return {"workload": workload_name("decode"), "ms_per_step": round(ms, 4),
             "tokens_per_s": round(L["T"] / (ms * 1e-3), 1), "active_experts": len(active),
             "weight_bytes": wbytes, "weight_stream_gbs": round(gbs, 1),
-            "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "stages_ms": stages,
-            "l2": "flushed (512 MB write) before each step"}
+            "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+            "cuda_graph": {"ms_per_step": round(graph_ms, 4),
+                           "weight_stream_gbs": round(wbytes / (graph_ms * 1e-3) / 1e9, 1),
+                           "hbm_frac": round(wbytes / (graph_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
+            "stages_ms": stages,
+            "l2": "flushed before each step (512 MB write, then 256 MB read: clean lines left)"}
 
 
 # --------------------------------------------------------------------------- CPU oracle (baseline / reference arm)
