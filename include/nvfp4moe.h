@@ -283,7 +283,9 @@ int nvfp4_moe_calibrate(const void* hidden, const float* router_logits, int64_t 
  *   stride H; with a2_gs NULL first the bf16 L1 output, row stride I),
  *   calib u32[2E] (calibration amax bits; with a2_gs NULL, E amax words of
  *   the L1 output, then the E L2 global scales as f32)
- * Only rows < P of the row-indexed buffers are defined after a call.
+ * Only rows < P of the row-indexed buffers are defined after a call; the
+ * pad rows of a1 hold zero block scales (every value exactly 0) and
+ * unspecified nibble bytes.
  */
 typedef struct {
   size_t topk_ids, topk_w, block_counts, counts, offsets, meta, tile_expert, sorted_token_ids, row_weight,

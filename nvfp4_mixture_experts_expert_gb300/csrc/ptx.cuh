@@ -138,6 +138,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
+// 32-bit load from the shared memory of another CTA of the cluster (address
+// from mapa_shared).
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
 // Arrive on an mbarrier in another CTA of the cluster (address from
 // mapa_shared).  Default (CTA-scope release) semantics: what the arrival
 // publishes is TMEM and TMA-written shared memory, ordered by the tcgen05

@@ -113,7 +113,9 @@ __global__ void assemble_scales_kernel(const uint8_t* __restrict__ lin, int64_t 
 // global scale: 8 bytes of nibbles per lane (256 contiguous bytes per warp)
 // and one 32-bit word of 4 block scales per group of 4 lanes.  The hidden row
 // is read from memory once instead of once per slot.  The trailing warps
-// write the pad rows of every expert's slot range as zero blocks.
+// give the pad rows of every expert's slot range zero block scales, which
+// makes every value in them exactly 0 whatever their nibble bytes hold
+// (E2M1 codes are all finite); the nibble bytes are not written.
 constexpr int kGatherChunks = 2;
 
 // One 16-element bf16 block (32 bytes): a single 32-byte load where the
@@ -237,8 +239,6 @@ __global__ void __launch_bounds__(256) gather_quantize_kernel(const uint16_t* __
   const int e = (int)(p >> 7), j = (int)(p & 127);
   const int64_t r = (int64_t)offsets[e] + counts[e] + j;
   if (r >= offsets[e + 1] || r >= capacity) return;
-  for (int64_t b = lane * 16; b < H / 2; b += 32 * 16)
-    *reinterpret_cast<uint4*>(a1 + r * (H / 2) + b) = make_uint4(0u, 0u, 0u, 0u);
   for (int64_t m = lane; m < sf_cols / 4; m += 32)
     *reinterpret_cast<uint32_t*>(sfa1 + sf_offset(r, 4 * m, sf_cols)) = 0u;
 }

@@ -303,10 +303,16 @@ __global__ void __launch_bounds__(256) token_combine_kernel(const uint16_t* __re
   __syncthreads();
   const int n = n_rows;
   for (int64_t c = (int64_t)threadIdx.x * 8; c < H; c += (int64_t)blockDim.x * 8) {
+    // all of the token's rows in flight at once, then summed in j order
+    uint4 v[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j)
+      if (j < n) v[j] = __ldg(reinterpret_cast<const uint4*>(y + (int64_t)rows[j] * H + c));
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < n; ++j) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + (int64_t)rows[j] * H + c));
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j >= n) break;
+      const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         acc[2 * q] += bf16_lo(u[q]);
@@ -319,32 +325,42 @@ __global__ void __launch_bounds__(256) token_combine_kernel(const uint16_t* __re
 }
 
 // Small batches (T <= kSmallRouteTokens): routing, padded offsets, tile
-// table, pad rows and the stable slot permutation in one block of 32 warps,
-// phase after phase (the same arithmetic as route_topk / route_external,
-// slot_scan and slot_scatter, without their launch boundaries).
+// table, pad rows and the stable slot permutation in one launch of a cluster
+// of kSmallCtas CTAs (the same arithmetic as route_topk / route_external,
+// slot_scan and slot_scatter, without their launch boundaries).  CTA r routes
+// tokens [32r, 32r + 32), a warp per token; the CTAs read each other's
+// per-expert counts through distributed shared memory, so each knows the
+// totals (padded offsets) and how many rows of every expert the lower-ranked
+// CTAs' tokens take (its first slot per expert), and ranks its own
+// assignments from there.
 constexpr int kSmallWarps = 32;
+constexpr int kSmallCtas = 8;
+static_assert(kSmallWarps * kSmallCtas == kSmallRouteTokens, "one token per warp");
 
 template <int NK>
-__global__ void __launch_bounds__(kSmallWarps * 32) route_small_kernel(
+__global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallWarps * 32) route_small_kernel(
     const float* __restrict__ logits, const int32_t* __restrict__ ext_ids, const float* __restrict__ ext_w,
     int32_t start, int64_t T, int E, int k, int32_t* __restrict__ ids, float* __restrict__ w,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ meta,
     int32_t* __restrict__ tile_expert, int32_t* __restrict__ sorted_ids, float* __restrict__ row_w,
     int32_t* __restrict__ inverse) {
   pdl_trigger();
-  __shared__ int32_t hist[kMaxExperts];
+  __shared__ int32_t hist[kMaxExperts];     // this CTA's tokens' rows per expert
+  __shared__ int32_t total[kMaxExperts];    // all CTAs' rows per expert
   __shared__ int32_t s_off[kMaxExperts + 1];
-  __shared__ int32_t running[kMaxExperts];
+  __shared__ int32_t running[kMaxExperts];  // next slot of this CTA per expert
   __shared__ int32_t warp_cnt[kSmallWarps][kMaxExperts];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t A = T * k;
+  const uint32_t rank = cluster_ctarank();
+  const int64_t t0 = (int64_t)rank * kSmallWarps, t1 = min(T, t0 + kSmallWarps);
+  const int64_t f0 = t0 * k, f1 = t1 > t0 ? t1 * k : f0;  // this CTA's assignments
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
-  // phase 1: routing and per-expert counts
+  // phase 1: routing of this CTA's tokens and their per-expert counts
   if (logits) {
-    for (int64_t t = warp; t < T; t += kSmallWarps) route_token<NK>(logits, t, E, k, lane, ids, w, hist);
+    if (t0 + warp < t1) route_token<NK>(logits, t0 + warp, E, k, lane, ids, w, hist);
   } else {
-    for (int64_t f = threadIdx.x; f < A; f += blockDim.x) {
+    for (int64_t f = f0 + threadIdx.x; f < f1; f += blockDim.x) {
       const int64_t e = (int64_t)ext_ids[f] - start;
       const bool local = e >= 0 && e < E;
       ids[f] = local ? (int32_t)e : -1;
@@ -352,13 +368,27 @@ __global__ void __launch_bounds__(kSmallWarps * 32) route_small_kernel(
       if (local) atomicAdd(&hist[e], 1);
     }
   }
+  cluster_sync_all();  // every CTA's counts are final
+  // phase 2: totals and this CTA's first slot per expert (rows of the
+  // lower-ranked CTAs come first: ascending flat index), padded offsets
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const uint32_t a = smem_u32(&hist[e]);
+    int sum = 0, below = 0;
+#pragma unroll
+    for (int q = 0; q < kSmallCtas; ++q) {
+      const int c = (int)ld_shared_cluster_u32(mapa_shared(a, (uint32_t)q));
+      sum += c;
+      below += q < (int)rank ? c : 0;
+    }
+    total[e] = sum;
+    running[e] = below;
+  }
   __syncthreads();
-  // phase 2: padded offsets (multiples of 128), tile table, pad rows
   if (warp == 0) {
     int off = 0;
     for (int base = 0; base < E; base += 32) {
       const int e = base + lane;
-      const int c = e < E ? (hist[e] + 127) / 128 * 128 : 0;
+      const int c = e < E ? (total[e] + 127) / 128 * 128 : 0;
       int incl = c;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -370,30 +400,33 @@ __global__ void __launch_bounds__(kSmallWarps * 32) route_small_kernel(
     }
     if (lane == 0) {
       s_off[E] = off;
-      meta[0] = off;
-      meta[1] = off / 128;
-      meta[2] = 0;
-      meta[3] = 0;
+      if (rank == 0) {
+        meta[0] = off;
+        meta[1] = off / 128;
+        meta[2] = 0;
+        meta[3] = 0;
+      }
     }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = s_off[e];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    counts[e] = hist[e];
-    running[e] = s_off[e];
-  }
-  for (int mt = threadIdx.x; mt < s_off[E] / 128; mt += blockDim.x) {
-    int lo = 0, hi = E;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_off[mid] <= mt * 128) lo = mid;
-      else hi = mid;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) running[e] += s_off[e];
+  if (rank == 0) {
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) offsets[e] = s_off[e];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) counts[e] = total[e];
+    for (int mt = threadIdx.x; mt < s_off[E] / 128; mt += blockDim.x) {
+      int lo = 0, hi = E;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_off[mid] <= mt * 128) lo = mid;
+        else hi = mid;
+      }
+      tile_expert[mt] = lo;
     }
-    tile_expert[mt] = lo;
   }
-  for (int i = threadIdx.x; i < E * 128; i += blockDim.x) {
+  // pad rows, spread over the cluster
+  for (int i = (int)rank * blockDim.x + threadIdx.x; i < E * 128; i += kSmallCtas * blockDim.x) {
     const int e = i >> 7, j = i & 127;
-    const int r = s_off[e] + hist[e] + j;
+    const int r = s_off[e] + total[e] + j;
     if (r < s_off[e + 1]) {
       sorted_ids[r] = -1;
       row_w[r] = 0.f;
@@ -401,19 +434,19 @@ __global__ void __launch_bounds__(kSmallWarps * 32) route_small_kernel(
   }
   for (int i = threadIdx.x; i < kSmallWarps * E; i += blockDim.x) warp_cnt[i / E][i % E] = 0;
   __syncthreads();
-  // phase 3: stable rank of every assignment inside its expert (ascending flat index)
-  for (int64_t base = 0; base < A; base += blockDim.x) {
+  // phase 3: stable rank of every assignment of this CTA inside its expert
+  for (int64_t base = f0; base < f1; base += blockDim.x) {
     const int64_t f = base + threadIdx.x;
-    const bool valid = f < A;
+    const bool valid = f < f1;
     const int e = valid ? ids[f] : -1;
     const bool local = e >= 0;
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    if (local && rank == 0) warp_cnt[warp][e] = __popc(peers);
+    const int rk = __popc(peers & ((1u << lane) - 1u));
+    if (local && rk == 0) warp_cnt[warp][e] = __popc(peers);
     __syncthreads();
     if (valid && !local) inverse[f] = -1;
     if (local) {
-      int pre = running[e] + rank;
+      int pre = running[e] + rk;
       for (int q = 0; q < warp; ++q) pre += warp_cnt[q][e];
       sorted_ids[pre] = (int32_t)(f / k);
       row_w[pre] = w[f];
@@ -430,6 +463,7 @@ __global__ void __launch_bounds__(kSmallWarps * 32) route_small_kernel(
     }
     __syncthreads();
   }
+  cluster_sync_all();  // no CTA leaves while another may still read its counts
 }
 
 }  // namespace
@@ -457,7 +491,7 @@ cudaError_t launch_route_small(const float* logits, const int32_t* ext_ids, cons
                                int64_t T, int E, int k, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
                                int32_t* meta, int32_t* tile_expert, int32_t* sorted_ids, float* row_w,
                                int32_t* inverse, cudaStream_t s) {
-  const dim3 grid(1), block(kSmallWarps * 32);
+  const dim3 grid(kSmallCtas), block(kSmallWarps * 32);  // one cluster
   if (!logits || E <= 32)
     route_small_kernel<1><<<grid, block, 0, s>>>(logits, ext_ids, ext_w, start, T, E, k, ids, w, counts, offsets,
                                                  meta, tile_expert, sorted_ids, row_w, inverse);

@@ -52,7 +52,9 @@ def check_all(wl, orc, w, fwd, out, check_a2=True):
     np.testing.assert_allclose(host(fwd.view("row_weight", torch.float32, P)), m["row_weight"], rtol=1e-6, atol=1e-7)
     # gathered + quantized L1 activations
     a1_ref, sfa1_ref = orc.slot_activations()
-    np.testing.assert_array_equal(host(fwd.view("a1", torch.uint8, P * H // 2)).reshape(P, H // 2), a1_ref)
+    real = m["sorted_token_ids"] >= 0  # pad rows: zero scales, nibble bytes unspecified
+    np.testing.assert_array_equal(host(fwd.view("a1", torch.uint8, P * H // 2)).reshape(P, H // 2)[real],
+                                  a1_ref[real])
     np.testing.assert_array_equal(host(fwd.view("sfa1", torch.uint8, P * H // 16)), sfa1_ref)
     # end to end
     ref, inter = orc.forward()
