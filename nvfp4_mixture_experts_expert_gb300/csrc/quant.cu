@@ -102,7 +102,6 @@ __global__ void assemble_scales_kernel(const uint8_t* __restrict__ lin, int64_t 
 }
 
 // ---------------------------------------------------------------- MoE gather + quantize
-// ---------------------------------------------------------------- MoE gather
 // Token-major gather + quantize of the L1 activations.  One warp owns one
 // (token, segment of up to kGatherChunks x 512 elements) item: lane l owns
 // the 16-element block at element 512*c + 16*l of each 512-element chunk c,
@@ -116,6 +115,8 @@ __global__ void assemble_scales_kernel(const uint8_t* __restrict__ lin, int64_t 
 // give the pad rows of every expert's slot range zero block scales, which
 // makes every value in them exactly 0 whatever their nibble bytes hold
 // (E2M1 codes are all finite); the nibble bytes are not written.
+// Large batches take 2 chunks (1,024 elements) per warp; batches of at most
+// kSmallRouteTokens tokens take 1, for twice the warps on few tokens.
 constexpr int kGatherChunks = 2;
 
 // One 16-element bf16 block (32 bytes): a single 32-byte load where the
@@ -166,7 +167,7 @@ __device__ __forceinline__ uint32_t quant_block16_bf16(const uint32_t (&w)[8], f
   return s;
 }
 
-template <bool kAligned32>
+template <bool kAligned32, int kChunks>
 __global__ void __launch_bounds__(256) gather_quantize_kernel(const uint16_t* __restrict__ hidden, int64_t H,
                                                               int64_t T, int top_k,
                                                               const int32_t* __restrict__ topk_ids,
@@ -186,15 +187,15 @@ __global__ void __launch_bounds__(256) gather_quantize_kernel(const uint16_t* __
   const float rcp6 = __frcp_rn(6.0f);
   const int lane = threadIdx.x & 31;
   const int64_t item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int64_t seg_elems = 512 * kGatherChunks;
+  const int64_t seg_elems = 512 * kChunks;
   const int64_t segs = (H + seg_elems - 1) / seg_elems;
   const int64_t sf_cols = H / 16;
   if (item < T * segs) {
     const int64_t t = item / segs, e0 = (item - t * segs) * seg_elems;
-    uint32_t raw[kGatherChunks][8];
-    float amax[kGatherChunks];
+    uint32_t raw[kChunks][8];
+    float amax[kChunks];
 #pragma unroll
-    for (int c = 0; c < kGatherChunks; ++c) {
+    for (int c = 0; c < kChunks; ++c) {
       const int64_t el = e0 + c * 512 + lane * 16;
       if (el < H) {
         ld_block32<kAligned32>(hidden + t * H + el, raw[c]);
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(256) gather_quantize_kernel(const uint16_t* __
       }
     }
 #pragma unroll
-    for (int c = 0; c < kGatherChunks; ++c) amax[c] = block_amax_bf16(raw[c]);
+    for (int c = 0; c < kChunks; ++c) amax[c] = block_amax_bf16(raw[c]);
     int my_row = 0;
     float my_gs = 1.f;
     if (lane < top_k) {
@@ -218,7 +219,7 @@ __global__ void __launch_bounds__(256) gather_quantize_kernel(const uint16_t* __
       const float gs = __shfl_sync(0xffffffffu, my_gs, j);
       const bool row_ok = r >= 0 && r < capacity;
 #pragma unroll
-      for (int c = 0; c < kGatherChunks; ++c) {
+      for (int c = 0; c < kChunks; ++c) {
         const int64_t el = e0 + c * 512 + lane * 16;
         uint32_t lo, hi;
         const uint32_t sc = quant_block16_bf16(raw[c], amax[c], gs, rcp6, tab, lo, hi);
@@ -430,11 +431,14 @@ cudaError_t launch_gather_quantize(const uint16_t* hidden, int64_t H, int64_t T,
                                    const int32_t* topk_ids, const int32_t* inverse, const int32_t* counts,
                                    const int32_t* offsets, int E, const float* a1_gs, int64_t capacity, uint8_t* a1,
                                    uint8_t* sfa1, cudaStream_t s, bool pdl) {
-  const int64_t segs = (H + 512 * kGatherChunks - 1) / (512 * kGatherChunks);
+  const int chunks = T <= kSmallRouteTokens ? 1 : kGatherChunks;
+  const int64_t segs = (H + 512 * chunks - 1) / (512 * chunks);
   const int64_t warps = T * segs + (int64_t)E * 128;
   const int64_t grid = (warps + 7) / 8;
-  auto* kernel = (reinterpret_cast<uintptr_t>(hidden) & 31u) == 0 ? gather_quantize_kernel<true>
-                                                                   : gather_quantize_kernel<false>;
+  const bool a32 = (reinterpret_cast<uintptr_t>(hidden) & 31u) == 0;
+  auto* kernel = chunks == 1 ? (a32 ? gather_quantize_kernel<true, 1> : gather_quantize_kernel<false, 1>)
+                             : (a32 ? gather_quantize_kernel<true, kGatherChunks>
+                                    : gather_quantize_kernel<false, kGatherChunks>);
   return launch_kernel(kernel, dim3((unsigned)grid), dim3(256), 0, s, pdl, hidden, H, T, top_k, topk_ids, inverse,
                        counts, offsets, E, a1_gs, capacity, a1, sfa1);
 }
