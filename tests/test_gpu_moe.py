@@ -423,3 +423,89 @@ def test_batch_l2_scales_bit_identical_to_the_same_scales_given(T):
     assert torch.equal(fwd.view("a2", torch.uint8, P * wl.I // 2), a2_dyn)
     assert torch.equal(fwd.view("sfa2", torch.uint8, P * wl.I // 16), sf_dyn)
     assert torch.equal(out_dyn, out_giv)
+
+
+# ----------------------------------------------------------------- routing at the small/large batch boundary
+
+@pytest.mark.parametrize("T", [1, 31, 33, 255, 256, 257])
+def test_routing_metadata_bit_exact_around_the_cluster_path(T):
+    """Batches of at most 256 tokens route in one cluster of 8 CTAs of 32
+    tokens each (distributed-shared-memory counts); 257 takes the three-kernel
+    path.  Ids, weights, counts, offsets, slot order and inverse map match the
+    oracle exactly at the CTA boundaries (1, 31, 33 tokens: empty and partial
+    CTAs; 255, 256: the last CTA partial and full), and the output matches."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    wl = W.moe_workload(T, 256, 128, 9, 3, 500 + T, logit_bias_std=1.0)
+    orc = OracleMoE(wl)
+    w, fwd, out = run_gpu(wl, orc)
+    k, E = wl.top_k, wl.E
+    A = T * k
+    m = orc.meta
+    P = m["P"]
+    np.testing.assert_array_equal(host(fwd.view("topk_ids", torch.int32, A)).reshape(T, k), orc.ids)
+    np.testing.assert_array_equal(host(fwd.view("counts", torch.int32, E)), m["counts"])
+    np.testing.assert_array_equal(host(fwd.view("offsets", torch.int32, E + 1)), m["offsets"])
+    assert host(fwd.view("meta", torch.int32, 2)).tolist() == [P, P // 128]
+    np.testing.assert_array_equal(host(fwd.view("sorted_token_ids", torch.int32, P)), m["sorted_token_ids"])
+    np.testing.assert_array_equal(host(fwd.view("inverse", torch.int32, A)), m["inverse"])
+    tiles = np.searchsorted(m["offsets"], np.arange(P // 128) * 128, side="right") - 1
+    np.testing.assert_array_equal(host(fwd.view("tile_expert", torch.int32, P // 128)), tiles)
+    ref, _ = orc.forward()
+    got = bf16_host(out)
+    rf, cs = rel_frob(got, ref), cosine(got, ref)
+    assert rf <= 2e-2 and cs >= 0.999, (rf, cs)
+
+
+@pytest.mark.parametrize("T", [40, 250])
+def test_routed_forward_on_the_cluster_path_matches_oracle(T):
+    """External global ids through the cluster routing (non-local experts
+    dropped inside each CTA), with the L2 scales taken from the batch."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    wl, orc, gids, gw, start = _routed_case(T=T, seed=80 + T)
+    Tn, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.top_k
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    fwd = api.MoEForward(Tn, H, I, E, k)
+    out = fwd.routed(bf16_dev(wl.hidden), dev(gids), dev(gw), start, w, dev(orc.a1_gs), None,
+                     wl.gate_limit, wl.up_limit)
+    torch.cuda.synchronize()
+    ids, wts = O.remap_global_ids(gids, gw.astype(np.float64), start, E)
+    m = O.sort_slots(ids, wts, E)
+    np.testing.assert_array_equal(host(fwd.view("sorted_token_ids", torch.int32, m["P"])), m["sorted_token_ids"])
+    np.testing.assert_array_equal(host(fwd.view("inverse", torch.int32, Tn * k)), m["inverse"])
+    ref = O.moe_forward_routed(W.bf16_bits_to_f32(wl.hidden), ids, wts.astype(np.float32).astype(np.float64),
+                               orc.w13q, orc.w2q, orc.a1_gs, None, wl.gate_limit, wl.up_limit)
+    got = bf16_host(out)
+    assert not got[7].any()
+    rf, cs = rel_frob(got, ref), cosine(got, ref)
+    assert rf <= 2e-2 and cs >= 0.999, (rf, cs)
+
+
+def test_batch_l2_scale_forward_replays_from_a_cuda_graph():
+    """The forward with a2_gs NULL (an amax reset, the bf16 L1 output and the
+    quantize pass) captured in a CUDA graph replays bit-exactly."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    wl = W.moe_workload(300, 512, 256, 6, 2, 62, logit_bias_std=1.0)
+    orc = OracleMoE(wl)
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    a1 = dev(orc.a1_gs)
+    fwd = api.MoEForward(wl.T, wl.H, wl.I, wl.E, wl.top_k)
+    hidden, logits = bf16_dev(wl.hidden), dev(wl.logits)
+    out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
+    fwd(hidden, logits, w, a1, None, wl.gate_limit, wl.up_limit, out=out)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fwd(hidden, logits, w, a1, None, wl.gate_limit, wl.up_limit, out=out, stream=s)
+    torch.cuda.synchronize()
+    for i in range(2):
+        new_h = bf16_dev(wl.hidden) * (2.0 - 0.75 * i)
+        ref = fwd(new_h, logits, w, a1, None, wl.gate_limit, wl.up_limit).clone()
+        hidden.copy_(new_h)
+        g.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(host(out.view(torch.int16)), host(ref.view(torch.int16)))
