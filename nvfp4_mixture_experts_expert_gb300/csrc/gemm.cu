@@ -413,7 +413,9 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
   uint32_t acc_phase = 0;
   for (int it = start; it < total; it += step) {
     int ok = 1;
-    if (lane == 0) ok = wait_bounded(smem_u32(L.acc_full), acc_phase, abort, p.status, p.timeout_ns);
+    // off the critical path (the accumulator is released right after its
+    // load): poll with short sleeps rather than spinning beside the MMA warp
+    if (lane == 0) ok = wait_bounded_backoff(smem_u32(L.acc_full), acc_phase, abort, p.status, p.timeout_ns, 200);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) break;
     __syncwarp();
