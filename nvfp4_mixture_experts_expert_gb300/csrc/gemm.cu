@@ -412,6 +412,18 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
   const uint32_t acc_empty = PAIR && rank ? mapa_shared(smem_u32(L.acc_empty), 0) : smem_u32(L.acc_empty);
   uint32_t acc_phase = 0;
   for (int it = start; it < total; it += step) {
+    // the tile and its per-tile parameters, loaded while the MMAs run
+    const Work w = decode_work<PAIR>(L, p, it, rank);
+    const int g = w.g, nt = w.nt;
+    const int64_t row = (int64_t)w.mt * BM + row_in_tile;
+    const float gs_a = p.a_gs[g], gs_b = p.b_gs[g];
+    float tile_param = 0.f;  // SwiGLU requant: the L2 activation scale; combine: the row's weight
+    int row_id = 0;          // single-CTA combine: the row's token (-1: pad row)
+    if constexpr (EPI == kEpiSwigluQuant) tile_param = p.q_gs[g];
+    if constexpr (EPI == kEpiCombine) {
+      tile_param = p.row_w[row];
+      if constexpr (!PAIR) row_id = p.sorted_ids[row];
+    }
     int ok = 1;
     // off the critical path (the accumulator is released right after its
     // load): poll with short sleeps rather than spinning beside the MMA warp
@@ -441,11 +453,8 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
     }
     acc_phase ^= 1u;
 
-    const Work w = decode_work<PAIR>(L, p, it, rank);
     if (!w.valid) continue;  // the pair's second tile does not exist: nothing to store
-    const int g = w.g, nt = w.nt;
-    const int64_t row = (int64_t)w.mt * BM + row_in_tile;
-    const float alpha = 1.0f / (p.a_gs[g] * p.b_gs[g]);
+    const float alpha = 1.0f / (gs_a * gs_b);
 
     if constexpr (EPI == kEpiBf16) {
       const int64_t i_local = row - L.offsets[g];
@@ -472,7 +481,7 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
       // output features [nt*128 + half*64, +64) of one row = 4 quantization blocks
       // (pairs of features per instruction where the arithmetic allows it;
       // every value is rounded exactly as by the scalar operations)
-      const float qgs = p.q_gs[g];
+      const float qgs = tile_param;
       const float rcp6 = __frcp_rn(6.0f);
       const uint64_t alpha2 = f2_pack(alpha, alpha), qgs2 = f2_pack(qgs, qgs);
       uint32_t scales = 0;
@@ -544,7 +553,7 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
       // XOR-swizzled by row, conflict-free both ways) so every store
       // instruction writes 4 whole 128-byte row segments.
       uint8_t* buf = L.epi_stage + (warp - EPI_WARP0) * EPI_STAGE_BYTES;
-      const float wgt = p.row_w[row] * alpha;
+      const float wgt = tile_param * alpha;
       uint16_t* ybase = p.y + ((int64_t)w.mt * BM + quarter * 32) * p.H + (int64_t)nt * BN + half * (BN / 2);
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
@@ -569,8 +578,8 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
         __syncwarp();
       }
     } else {  // kEpiCombine: routing-weighted rows, stored in slot order for the token combine
-      if (p.sorted_ids[row] >= 0) {
-        const float wgt = p.row_w[row] * alpha;
+      if (row_id >= 0) {
+        const float wgt = tile_param * alpha;
         uint16_t* dst = p.y + row * p.H + (int64_t)nt * BN + half * (BN / 2);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
