@@ -7,7 +7,6 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
-#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
