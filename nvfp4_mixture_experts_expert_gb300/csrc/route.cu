@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
+  pdl_wait();  // the logits may come from the kernel just before
   const int64_t t0 = (int64_t)blockIdx.x * kRouteTokensPerBlock;
   const int64_t t1 = min(T, t0 + kRouteTokensPerBlock);
   for (int64_t t = t0 + warp; t < t1; t += kRouteWarps) route_token<NK>(logits, t, E, k, lane, ids, w, hist);
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_external_kernel(
   __shared__ int32_t hist[kMaxExperts];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
+  pdl_wait();  // the ids may come from the kernel just before
   const int64_t f0 = (int64_t)blockIdx.x * kRouteTokensPerBlock * k;
   const int64_t f1 = min(T, (int64_t)(blockIdx.x + 1) * kRouteTokensPerBlock) * k;
   for (int64_t f = f0 + threadIdx.x; f < f1; f += blockDim.x) {
@@ -356,6 +358,7 @@ __global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallWarps
   const int64_t f0 = t0 * k, f1 = t1 > t0 ? t1 * k : f0;  // this CTA's assignments
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
+  pdl_wait();  // the logits or ids may come from the kernel just before
   // phase 1: routing of this CTA's tokens and their per-expert counts
   if (logits) {
     if (t0 + warp < t1) route_token<NK>(logits, t0 + warp, E, k, lane, ids, w, hist);
@@ -452,6 +455,7 @@ __global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallWarps
       row_w[pre] = w[f];
       inverse[f] = pre;
     }
+    if (base + (int64_t)blockDim.x >= f1) break;  // last pass: the running starts are not needed again
     __syncthreads();
     for (int x = threadIdx.x; x < E; x += blockDim.x) {
       int add = 0;
@@ -472,39 +476,29 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int3
                               int32_t* block_counts, cudaStream_t s) {
   const int64_t nb = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
   const dim3 grid((unsigned)nb), block(kRouteWarps * 32);
-  if (E <= 32) route_topk_kernel<1><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, block_counts);
-  else if (E <= 64) route_topk_kernel<2><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, block_counts);
-  else if (E <= 128) route_topk_kernel<4><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, block_counts);
-  else route_topk_kernel<8><<<grid, block, 0, s>>>(logits, T, E, k, ids, w, block_counts);
-  return cudaGetLastError();
+  auto* kernel = E <= 32 ? route_topk_kernel<1> : E <= 64 ? route_topk_kernel<2> : E <= 128 ? route_topk_kernel<4>
+                                                                                            : route_topk_kernel<8>;
+  return launch_kernel(kernel, grid, block, 0, s, true, logits, T, E, k, ids, w, block_counts);
 }
 
 cudaError_t launch_route_external(const int32_t* topk_ids, const float* topk_w, int32_t start, int64_t T, int E,
                                   int k, int32_t* ids, float* w, int32_t* block_counts, cudaStream_t s) {
   const int64_t nb = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
-  route_external_kernel<<<(unsigned)nb, kRouteWarps * 32, 0, s>>>(topk_ids, topk_w, start, T, E, k, ids, w,
-                                                                   block_counts);
-  return cudaGetLastError();
+  return launch_kernel(route_external_kernel, dim3((unsigned)nb), dim3(kRouteWarps * 32), 0, s, true, topk_ids, topk_w,
+                       start, T, E, k, ids, w, block_counts);
 }
 
 cudaError_t launch_route_small(const float* logits, const int32_t* ext_ids, const float* ext_w, int32_t start,
                                int64_t T, int E, int k, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
                                int32_t* meta, int32_t* tile_expert, int32_t* sorted_ids, float* row_w,
                                int32_t* inverse, cudaStream_t s) {
-  const dim3 grid(kSmallCtas), block(kSmallWarps * 32);  // one cluster
-  if (!logits || E <= 32)
-    route_small_kernel<1><<<grid, block, 0, s>>>(logits, ext_ids, ext_w, start, T, E, k, ids, w, counts, offsets,
-                                                 meta, tile_expert, sorted_ids, row_w, inverse);
-  else if (E <= 64)
-    route_small_kernel<2><<<grid, block, 0, s>>>(logits, ext_ids, ext_w, start, T, E, k, ids, w, counts, offsets,
-                                                 meta, tile_expert, sorted_ids, row_w, inverse);
-  else if (E <= 128)
-    route_small_kernel<4><<<grid, block, 0, s>>>(logits, ext_ids, ext_w, start, T, E, k, ids, w, counts, offsets,
-                                                 meta, tile_expert, sorted_ids, row_w, inverse);
-  else
-    route_small_kernel<8><<<grid, block, 0, s>>>(logits, ext_ids, ext_w, start, T, E, k, ids, w, counts, offsets,
-                                                 meta, tile_expert, sorted_ids, row_w, inverse);
-  return cudaGetLastError();
+  auto* kernel = (!logits || E <= 32) ? route_small_kernel<1>
+                 : E <= 64            ? route_small_kernel<2>
+                 : E <= 128           ? route_small_kernel<4>
+                                      : route_small_kernel<8>;
+  // one cluster (the kernel's compile-time cluster shape)
+  return launch_kernel(kernel, dim3(kSmallCtas), dim3(kSmallWarps * 32), 0, s, true, logits, ext_ids, ext_w, start,
+                       T, E, k, ids, w, counts, offsets, meta, tile_expert, sorted_ids, row_w, inverse);
 }
 
 cudaError_t launch_slot_scan(int32_t* block_counts, int nblocks, int E, int32_t* counts, int32_t* offsets,
