@@ -509,3 +509,36 @@ def test_batch_l2_scale_forward_replays_from_a_cuda_graph():
         g.replay()
         torch.cuda.synchronize()
         np.testing.assert_array_equal(host(out.view(torch.int16)), host(ref.view(torch.int16)))
+
+
+@pytest.mark.parametrize("T,E,k", [(200, 256, 8), (600, 100, 4), (120, 65, 2)])
+def test_many_experts_match_oracle(T, E, k):
+    """Many experts: 256 (eight 32-expert key slots per lane in the routing,
+    the cluster path, the most groups the CTA-pair GEMM takes), 100 on the
+    multi-block path and 65 just past two key slots.  Routing metadata
+    bit-exact, output within the end-to-end tolerance."""
+    import torch
+    wl = W.moe_workload(T, 256, 128, E, k, 900 + E, logit_bias_std=0.5)
+    orc = OracleMoE(wl)
+    w, fwd, out = run_gpu(wl, orc)
+    A, m = T * k, orc.meta
+    P = m["P"]
+    np.testing.assert_array_equal(host(fwd.view("topk_ids", torch.int32, A)).reshape(T, k), orc.ids)
+    np.testing.assert_allclose(host(fwd.view("topk_w", torch.float32, A)).reshape(T, k), orc.w, rtol=1e-6, atol=1e-7)
+    np.testing.assert_array_equal(host(fwd.view("offsets", torch.int32, E + 1)), m["offsets"])
+    np.testing.assert_array_equal(host(fwd.view("sorted_token_ids", torch.int32, P)), m["sorted_token_ids"])
+    np.testing.assert_array_equal(host(fwd.view("inverse", torch.int32, A)), m["inverse"])
+    ref, _ = orc.forward()
+    got = bf16_host(out)
+    rf, cs = rel_frob(got, ref), cosine(got, ref)
+    assert rf <= 2e-2 and cs >= 0.999, (rf, cs)
+    if E == 256:  # the CTA-pair GEMMs at their largest group count give the same bits
+        from nvfp4_mixture_experts_expert_gb300 import binding as B
+        prev = B.nvfp4_gemm_set_cta_pair(True)
+        try:
+            out2 = fwd(bf16_dev(wl.hidden), dev(wl.logits), w, dev(orc.a1_gs), dev(orc.a2_gs), wl.gate_limit,
+                       wl.up_limit)
+            torch.cuda.synchronize()
+        finally:
+            B.nvfp4_gemm_set_cta_pair(prev)
+        np.testing.assert_array_equal(host(out2.view(torch.int16)), host(out.view(torch.int16)))
