@@ -436,13 +436,11 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
     // other kinds: columns [half*128, +128).
     uint32_t v[4][32];
     if constexpr (EPI == kEpiSwigluQuant || EPI == kEpiSwigluAmax) {
-      tmem_load_32(t_base + half * 64, v[0]);
-      tmem_load_32(t_base + half * 64 + 32, v[1]);
-      tmem_load_32(t_base + 128 + half * 64, v[2]);
-      tmem_load_32(t_base + 128 + half * 64 + 32, v[3]);
-    } else {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_load_32(t_base + half * 128 + c * 32, v[c]);
+      tmem_load_64(t_base + half * 64, v[0], v[1]);
+      tmem_load_64(t_base + 128 + half * 64, v[2], v[3]);
+    } else {  // (a 128-column load needs more registers than the kernel is compiled with)
+      tmem_load_64(t_base + half * 128, v[0], v[1]);
+      tmem_load_64(t_base + half * 128 + 64, v[2], v[3]);
     }
     tmem_load_wait();
     tc_fence_before();
