@@ -396,6 +396,21 @@ __device__ __forceinline__ float silu_clamped_product(float g, float u, float gl
   return g * sig * u;
 }
 
+// The same for two features at once (packed pairs, each half rounded exactly
+// as the scalar form: bit-identical results with fewer instructions).
+__device__ __forceinline__ void silu_clamped_product2(float g0, float g1, float u0, float u1, float gl, float ul,
+                                                      float& h0, float& h1) {
+  g0 = fminf(g0, gl);
+  g1 = fminf(g1, gl);
+  u0 = fminf(fmaxf(u0, -ul), ul);
+  u1 = fminf(fmaxf(u1, -ul), ul);
+  const uint64_t g2 = f2_pack(g0, g1);
+  float t0, t1;
+  f2_unpack(f2_mul(g2, f2_pack(0.5f, 0.5f)), t0, t1);
+  const uint64_t sig2 = f2_fma(f2_pack(0.5f, 0.5f), f2_pack(tanh_approx(t0), tanh_approx(t1)), f2_pack(0.5f, 0.5f));
+  f2_unpack(f2_mul(f2_mul(g2, sig2), f2_pack(u0, u1)), h0, h1);
+}
+
 // Each epilogue thread first copies its 128 accumulator columns (one row)
 // from TMEM into registers and releases the accumulator, so the MMAs of the
 // next tile overlap all of the epilogue arithmetic and stores below.
@@ -499,8 +514,9 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
                                    __uint_as_float(v[2 + (f >> 5)][(f & 31) + 1])),
                            alpha2),
                     u0, u1);
-          const uint32_t hb = pack_bf16x2(silu_clamped_product(g0, u0, p.gate_limit, p.up_limit),
-                                          silu_clamped_product(g1, u1, p.gate_limit, p.up_limit));
+          float h0, h1;
+          silu_clamped_product2(g0, g1, u0, u1, p.gate_limit, p.up_limit, h0, h1);
+          const uint32_t hb = pack_bf16x2(h0, h1);
           xs2[q] = f2_mul(f2_pack(bf16_lo(hb), bf16_hi(hb)), qgs2);
           float x0, x1;
           f2_unpack(xs2[q], x0, x1);
