@@ -379,6 +379,13 @@ __device__ void mma_loop(const GemmArgs& p, const SmemLayout& L, int total, int 
 }
 
 // ------------------------------------------------------------------ epilogues
+// bf16 pair of two accumulator words each multiplied by s (one packed multiply).
+__device__ __forceinline__ uint32_t scaled_bf16x2(uint32_t a, uint32_t b, uint64_t s2) {
+  float x0, x1;
+  f2_unpack(f2_mul(f2_pack(__uint_as_float(a), __uint_as_float(b)), s2), x0, x1);
+  return pack_bf16x2(x0, x1);
+}
+
 __device__ __forceinline__ float tanh_approx(float x) {
   float r;
   asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
@@ -470,6 +477,7 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
     const float alpha = 1.0f / (gs_a * gs_b);
 
     if constexpr (EPI == kEpiBf16) {
+      const uint64_t alpha2 = f2_pack(alpha, alpha);
       const int64_t i_local = row - L.offsets[g];
       const bool valid = p.counts ? i_local < p.counts[g] : (p.host_count <= 0 || i_local < p.host_count);
       if (valid) {
@@ -479,7 +487,7 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            pk[j] = pack_bf16x2(__uint_as_float(v[c][2 * j]) * alpha, __uint_as_float(v[c][2 * j + 1]) * alpha);
+            pk[j] = scaled_bf16x2(v[c][2 * j], v[c][2 * j + 1], alpha2);
           if (p.d_vec32) {
             st_global_v8(drow + c * 32, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
             st_global_v8(drow + c * 32 + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
@@ -568,15 +576,15 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
       // instruction writes 4 whole 128-byte row segments.
       uint8_t* buf = L.epi_stage + (warp - EPI_WARP0) * EPI_STAGE_BYTES;
       const float wgt = tile_param * alpha;
+      const uint64_t wgt2 = f2_pack(wgt, wgt);
       uint16_t* ybase = p.y + ((int64_t)w.mt * BM + quarter * 32) * p.H + (int64_t)nt * BN + half * (BN / 2);
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
         uint32_t pk[32];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          pk[j] = pack_bf16x2(__uint_as_float(v[2 * c2][2 * j]) * wgt, __uint_as_float(v[2 * c2][2 * j + 1]) * wgt);
-          pk[16 + j] = pack_bf16x2(__uint_as_float(v[2 * c2 + 1][2 * j]) * wgt,
-                                   __uint_as_float(v[2 * c2 + 1][2 * j + 1]) * wgt);
+          pk[j] = scaled_bf16x2(v[2 * c2][2 * j], v[2 * c2][2 * j + 1], wgt2);
+          pk[16 + j] = scaled_bf16x2(v[2 * c2 + 1][2 * j], v[2 * c2 + 1][2 * j + 1], wgt2);
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u)
@@ -594,13 +602,14 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
     } else {  // kEpiCombine: routing-weighted rows, stored in slot order for the token combine
       if (row_id >= 0) {
         const float wgt = tile_param * alpha;
+        const uint64_t wgt2 = f2_pack(wgt, wgt);
         uint16_t* dst = p.y + row * p.H + (int64_t)nt * BN + half * (BN / 2);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            pk[j] = pack_bf16x2(__uint_as_float(v[c][2 * j]) * wgt, __uint_as_float(v[c][2 * j + 1]) * wgt);
+            pk[j] = scaled_bf16x2(v[c][2 * j], v[c][2 * j + 1], wgt2);
           // workspace rows: 32-byte aligned (H is a multiple of 256)
           st_global_v8(dst + c * 32, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
           st_global_v8(dst + c * 32 + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
