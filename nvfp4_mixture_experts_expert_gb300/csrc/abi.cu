@@ -100,6 +100,23 @@ int make_fp4_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K) {
   return NVFP4_OK;
 }
 
+// bf16 matrix [rows][cols] (row stride cols elements); box 64 columns (128 bytes)
+// x 32 rows, 128-byte swizzle: the staging layout of the routing-weighted L2
+// epilogue's bulk stores.
+int make_bf16_store_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return NVFP4_OK;
+}
+
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 int64_t moe_capacity(int64_t T, int E, int k) {
@@ -375,6 +392,7 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
   if (int rc = make_fp4_map(&g1.tmap_b, w13, (int64_t)E * 2 * I, H)) return rc;
   if (int rc = make_fp4_map(&g2.tmap_a, a2, cap, I)) return rc;
   if (int rc = make_fp4_map(&g2.tmap_b, w2, (int64_t)E * H, I)) return rc;
+  if (int rc = make_bf16_store_map(&g2.tmap_y, ybuf, cap, H)) return rc;
   g1.sfa = sfa1;
   g1.sfb = (const uint8_t*)w13_sf;
   g1.padded_offsets = offsets;

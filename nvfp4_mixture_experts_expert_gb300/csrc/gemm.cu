@@ -571,13 +571,14 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
     } else if constexpr (PAIR) {  // kEpiCombine through the warp's staging buffer
       // Routing-weighted rows in slot order for the token combine; pad rows
       // carry weight 0 and are written as zeros (nothing reads them).  Each
-      // 64-column chunk goes through 4 KB of shared memory (16-byte units
-      // XOR-swizzled by row, conflict-free both ways) so every store
-      // instruction writes 4 whole 128-byte row segments.
+      // 64-column chunk of the warp's 32 rows goes through its 4 KB of shared
+      // memory in the 128-byte-swizzled layout (16-byte unit u of row r at
+      // unit u ^ (r % 8): conflict-free) and leaves with one bulk tensor
+      // store; the buffer is rewritten once that store has read it.
       uint8_t* buf = L.epi_stage + (warp - EPI_WARP0) * EPI_STAGE_BYTES;
       const float wgt = tile_param * alpha;
       const uint64_t wgt2 = f2_pack(wgt, wgt);
-      uint16_t* ybase = p.y + ((int64_t)w.mt * BM + quarter * 32) * p.H + (int64_t)nt * BN + half * (BN / 2);
+      const int32_t y_row = (int32_t)(w.mt * BM + quarter * 32), y_col = nt * BN + half * (BN / 2);
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
         uint32_t pk[32];
@@ -586,18 +587,18 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
           pk[j] = scaled_bf16x2(v[2 * c2][2 * j], v[2 * c2][2 * j + 1], wgt2);
           pk[16 + j] = scaled_bf16x2(v[2 * c2 + 1][2 * j], v[2 * c2 + 1][2 * j + 1], wgt2);
         }
+        if (lane == 0) bulk_wait_read_all();  // the previous store from this buffer has read it
+        __syncwarp();
 #pragma unroll
         for (int u = 0; u < 8; ++u)
           *reinterpret_cast<uint4*>(buf + lane * 128 + ((u ^ (lane & 7)) << 4)) =
               make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        fence_proxy_async_smem();
         __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = i * 4 + (lane >> 3), u = lane & 7;
-          const uint4 val = *reinterpret_cast<const uint4*>(buf + r * 128 + ((u ^ (r & 7)) << 4));
-          *reinterpret_cast<uint4*>(ybase + (int64_t)r * p.H + c2 * 64 + u * 8) = val;
+        if (lane == 0) {
+          tma_store_2d(&p.tmap_y, smem_u32(buf), y_col + c2 * 64, y_row);
+          bulk_commit();
         }
-        __syncwarp();
       }
     } else {  // kEpiCombine: routing-weighted rows, stored in slot order for the token combine
       if (row_id >= 0) {
@@ -616,6 +617,10 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
         }
       }
     }
+  }
+  if constexpr (PAIR && EPI == kEpiCombine) {
+    if (lane == 0) bulk_wait_all();  // the warp's bulk stores are complete before its CTA exits
+    __syncwarp();
   }
 }
 

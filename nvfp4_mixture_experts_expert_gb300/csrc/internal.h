@@ -85,6 +85,7 @@ enum EpilogueKind { kEpiBf16 = 0, kEpiSwigluQuant = 1, kEpiCombine = 2, kEpiSwig
 struct GemmArgs {
   CUtensorMap tmap_a;  // A: [rows][K/2] bytes, box 128 B x 128 rows, 128-byte swizzle
   CUtensorMap tmap_b;  // B: [G * b_rows_per_group][K/2] bytes, same box
+  CUtensorMap tmap_y;  // kEpiCombine, pair variant: y as bf16 [rows][H], box 64 x 32, 128-byte swizzle
   const uint8_t* sfa;  // tile-layout scales of A (rows x K/16)
   const uint8_t* sfb;  // tile-layout scales of B, sfb_group_bytes per group
   const int32_t* padded_offsets;  // [G+1]

@@ -107,6 +107,23 @@ __device__ __forceinline__ bool wait_bounded_backoff(uint32_t bar, uint32_t pari
 }
 
 // ------------------------------------------------------------------ TMA
+// Bulk tensor store of one box from shared memory (bulk-group completion),
+// the group commit, and the waits for the group's shared-memory reads / full
+// completion.  The writing threads make their shared-memory stores visible to
+// the copy engine with fence_proxy_async_smem() first.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
                                             uint32_t bar) {
   asm volatile(
