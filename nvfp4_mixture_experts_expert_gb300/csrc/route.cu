@@ -290,6 +290,7 @@ __global__ void __launch_bounds__(256) slot_scatter_kernel(const int32_t* __rest
 __global__ void __launch_bounds__(256) token_combine_kernel(const uint16_t* __restrict__ y,
                                                             const int32_t* __restrict__ inverse, int64_t H, int k,
                                                             uint16_t* __restrict__ out) {
+  pdl_trigger();  // the next forward's first kernel may start its prologue
   pdl_wait();
   const int64_t t = blockIdx.x;
   __shared__ int32_t rows[kMaxTopK];
