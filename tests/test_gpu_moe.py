@@ -542,3 +542,36 @@ def test_many_experts_match_oracle(T, E, k):
         finally:
             B.nvfp4_gemm_set_cta_pair(prev)
         np.testing.assert_array_equal(host(out2.view(torch.int16)), host(out.view(torch.int16)))
+
+
+def test_small_batch_forward_replays_from_a_cuda_graph():
+    """Small batches (the routing cluster launch, programmatic dependent launch
+    from the first kernel) captured in a CUDA graph: replays on new inputs
+    give the eager results bit for bit."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    wl = W.moe_workload(100, 512, 256, 8, 4, 63, logit_bias_std=0.5)
+    orc = OracleMoE(wl)
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    a1, a2 = dev(orc.a1_gs), dev(orc.a2_gs)
+    fwd = api.MoEForward(wl.T, wl.H, wl.I, wl.E, wl.top_k)
+    hidden, logits = bf16_dev(wl.hidden), dev(wl.logits)
+    out = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
+    fwd(hidden, logits, w, a1, a2, wl.gate_limit, wl.up_limit, out=out)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fwd(hidden, logits, w, a1, a2, wl.gate_limit, wl.up_limit, out=out, stream=s)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    for i in range(3):
+        new_h = bf16_dev(wl.hidden) * (1.25 - 0.25 * i)
+        new_l = dev(wl.logits + rng.standard_normal(wl.logits.shape).astype(np.float32))
+        ref = fwd(new_h, new_l, w, a1, a2, wl.gate_limit, wl.up_limit).clone()
+        hidden.copy_(new_h)
+        logits.copy_(new_l)
+        g.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(host(out.view(torch.int16)), host(ref.view(torch.int16)))
