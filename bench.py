@@ -30,7 +30,6 @@ import os
 import statistics
 import subprocess
 import sys
-import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -103,17 +102,18 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
+        import threading
         self.proc = None
-        self.path = None
+        self.lines = []
         try:
-            fd, self.path = tempfile.mkstemp(suffix=".csv")
-            os.close(fd)
-            self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "50"],
-                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        self.reader = threading.Thread(target=lambda: self.lines.extend(self.proc.stdout), daemon=True)
+        self.reader.start()
 
     def stop(self):
         if self.proc is None:
@@ -123,14 +123,12 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        self.fh.close()
+        self.reader.join(timeout=5)
         rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) == 8:
-                    rows.append(parts)
-        os.unlink(self.path)
+        for line in list(self.lines):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 8:
+                rows.append(parts)
         if not rows:
             return None
         sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
