@@ -5,7 +5,6 @@ conversion puts the first element in the low nibble."""
 import ctypes
 import os
 import subprocess
-import tempfile
 
 import numpy as np
 import pytest
@@ -19,7 +18,9 @@ CSRC = os.path.join(os.path.dirname(HERE), "nvfp4_mixture_experts_expert_gb300",
 @pytest.fixture(scope="module")
 def probe():
     import torch  # noqa: F401  (initialises the CUDA context the probe shares)
-    out = os.path.join(tempfile.mkdtemp(), "fp_probe.so")
+    build = os.path.join(HERE, "probes", "_build")  # git-ignored, beside the probe source
+    os.makedirs(build, exist_ok=True)
+    out = os.path.join(build, "fp_probe.so")
     subprocess.run(["nvcc", "-gencode=arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-shared",
                     "-Xcompiler", "-fPIC", "-I", CSRC, os.path.join(HERE, "probes", "fp_probe.cu"), "-o", out],
                    check=True, capture_output=True)
