@@ -292,7 +292,9 @@ __global__ void __launch_bounds__(256) token_combine_kernel(const uint16_t* __re
                                                             uint16_t* __restrict__ out) {
   pdl_trigger();  // the next forward's first kernel may start its prologue
   pdl_wait();
+  // gridDim.y blocks share a token's columns (several per token for small batches)
   const int64_t t = blockIdx.x;
+  const int64_t c0 = H * blockIdx.y / gridDim.y, c1 = H * (blockIdx.y + 1) / gridDim.y;
   __shared__ int32_t rows[kMaxTopK];
   __shared__ int n_rows;
   if (threadIdx.x == 0) {  // the token's local rows in j order (non-local ones contribute nothing)
@@ -305,7 +307,7 @@ __global__ void __launch_bounds__(256) token_combine_kernel(const uint16_t* __re
   }
   __syncthreads();
   const int n = n_rows;
-  for (int64_t c = (int64_t)threadIdx.x * 8; c < H; c += (int64_t)blockDim.x * 8) {
+  for (int64_t c = c0 + (int64_t)threadIdx.x * 8; c < c1; c += (int64_t)blockDim.x * 8) {
     // all of the token's rows in flight at once, then summed in j order
     uint4 v[kMaxTopK];
 #pragma unroll
@@ -520,7 +522,9 @@ cudaError_t launch_slot_scatter(const int32_t* ids, const float* w, int64_t T, i
 cudaError_t launch_token_combine(const uint16_t* y, const int32_t* inverse, int64_t T, int64_t H, int k,
                                  uint16_t* out, cudaStream_t s, bool pdl) {
   if (T == 0) return cudaSuccess;
-  return launch_kernel(token_combine_kernel, dim3((unsigned)T), dim3(256), 0, s, pdl, y, inverse, H, k, out);
+  // small batches: 4 blocks per token (column quarters, multiples of 8) for more loads in flight
+  const unsigned split = T <= kSmallRouteTokens && H % 32 == 0 ? 4u : 1u;
+  return launch_kernel(token_combine_kernel, dim3((unsigned)T, split), dim3(256), 0, s, pdl, y, inverse, H, k, out);
 }
 
 }  // namespace nvfp4
