@@ -470,7 +470,7 @@ __global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallWarps
     }
     __syncthreads();
   }
-  cluster_sync_all();  // no CTA leaves while another may still read its counts
+  cluster_sync_relaxed();  // no CTA leaves while another may still read its counts
 }
 
 }  // namespace
