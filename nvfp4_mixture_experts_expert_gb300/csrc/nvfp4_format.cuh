@@ -132,12 +132,6 @@ __device__ __forceinline__ uint32_t quant_block16_pairs(const uint64_t (&xs2)[8]
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// FP32 -> bf16 bits, round to nearest even (finite inputs).
-__device__ __forceinline__ uint32_t f32_to_bf16_rn(float f) {
-  uint16_t h;
-  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(f));
-  return h;
-}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
