@@ -113,6 +113,67 @@ def test_moe_edge_cases(case):
     check_all(wl, orc, *run_gpu(wl, orc))
 
 
+def _forced_routing(wl, first, second=None):
+    """Overwrite the router logits so that token t takes expert first[t] (and
+    second[t] next, for top_k 2) by a wide margin; the rest stays random."""
+    lg = wl.logits.astype(np.float32).copy()
+    t = np.arange(wl.T)
+    lg[t, first] += np.float32(40.0)
+    if second is not None:
+        lg[t, second] += np.float32(20.0)
+    wl.logits = lg
+    return wl
+
+
+def test_moe_experts_with_exactly_128_and_129_rows():
+    """Expert 0 fills exactly one m-tile, expert 1 spills one row into a second
+    tile, expert 2 takes 300 rows (three tiles, the last ragged), expert 3 43."""
+    wl = W.moe_workload(300, 256, 128, 5, 2, 41)
+    first = np.where(np.arange(300) < 128, 0, np.where(np.arange(300) < 257, 1, 2))
+    second = np.where(np.arange(300) < 257, 2, 3)
+    _forced_routing(wl, first, second)
+    orc = OracleMoE(wl)
+    assert orc.meta["counts"].tolist() == [128, 129, 300, 43, 0]
+    check_all(wl, orc, *run_gpu(wl, orc))
+
+
+@pytest.mark.parametrize("k", [1, 2])
+def test_moe_all_tokens_on_one_expert(k):
+    """Every token's first choice is expert 2 (and, for top_k 2, its second
+    choice expert 0): the other experts get no row."""
+    wl = W.moe_workload(200, 256, 128, 4, k, 43)
+    _forced_routing(wl, np.full(200, 2), np.zeros(200, np.int64) if k == 2 else None)
+    orc = OracleMoE(wl)
+    assert orc.meta["counts"].tolist() == ([0, 0, 200, 0] if k == 1 else [200, 0, 200, 0])
+    check_all(wl, orc, *run_gpu(wl, orc))
+
+
+def test_moe_all_zero_hidden_states():
+    """All-zero input: calibration gives every scale 1 (the amax == 0 rule),
+    the gathered activations are all zero codes and the output is exactly 0."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    wl = W.moe_workload(90, 256, 128, 4, 2, 47)
+    wl.hidden = np.zeros_like(wl.hidden)
+    orc = OracleMoE(wl)
+    assert np.all(orc.a1_gs == 1) and np.all(orc.a2_gs == 1)
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    fwd = api.MoEForward(wl.T, wl.H, wl.I, wl.E, wl.top_k)
+    a1, a2 = fwd.calibrate(bf16_dev(wl.hidden), dev(wl.logits), w, wl.gate_limit, wl.up_limit)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host(a1), orc.a1_gs)
+    np.testing.assert_array_equal(host(a2), orc.a2_gs)
+    out = fwd(bf16_dev(wl.hidden), dev(wl.logits), w, a1, a2, wl.gate_limit, wl.up_limit)
+    torch.cuda.synchronize()
+    assert not host(out.view(torch.int16)).any()  # +0.0 everywhere
+    ref, _ = orc.forward()
+    assert not ref.any()
+    P = orc.meta["P"]
+    real = orc.meta["sorted_token_ids"] >= 0
+    assert not host(fwd.view("a1", torch.uint8, P * wl.H // 2)).reshape(P, -1)[real].any()
+    assert not host(fwd.view("sfa1", torch.uint8, P * wl.H // 16)).any()
+
+
 def test_moe_hidden_16_byte_aligned_and_half_chunk_rows():
     """The gather reads each 16-element block with one 32-byte load only where
     the hidden states are 32-byte aligned; a pointer that is 16-byte but not

@@ -75,6 +75,20 @@ def test_forced_range_includes_values_plain_rounding_keeps():
     assert int(s[0, 0]) == 0 and int(nib[0, 0]) == 0
 
 
+def test_block_exactly_at_the_underflow_threshold_is_kept():
+    # amax = 6 * 2^-9: b/6 = 2^-9 is the smallest E4M3 subnormal (code 0x01), the
+    # block survives and its maximum maps to E2M1 6.0 (code 7); the next FP32
+    # value below the threshold is forced to zero.
+    t = np.float32(6 * 2.0 ** -9)
+    x = np.zeros((2, 16), np.float32)
+    x[0, 0], x[0, 1] = t, -t / np.float32(2)
+    x[1, 0] = np.nextafter(t, np.float32(0))
+    nib, s = O.quantize_blocks(x, np.float32(1))
+    assert int(s[0, 0]) == 0x01
+    assert int(nib[0, 0]) == 0x7 and int(nib[0, 1]) == 0xD  # -3.0 = sign bit | code 5
+    assert int(s[1, 0]) == 0 and not nib[1].any()
+
+
 def test_scale_applies_per_row():
     rng = np.random.default_rng(5)
     x = rng.standard_normal((3, 32)).astype(np.float32)
