@@ -56,9 +56,12 @@ __device__ __forceinline__ int key_expert(uint64_t key) { return (int)(0xFFFFFFF
 // expert) bits, i.e. the lowest expert.  Lane j keeps the j-th selection;
 // then lane j < k computes exp(l_j - l_max) and the warp sum gives the
 // renormalised weights.
+// s_ids / s_w (may be null): shared-memory copies of the token's k ids and
+// weights, at [lane] of the given base.
 template <int NK>
 __device__ __forceinline__ void route_token(const float* __restrict__ logits, int64_t t, int E, int k, int lane,
-                                            int32_t* __restrict__ ids, float* __restrict__ w, int32_t* hist) {
+                                            int32_t* __restrict__ ids, float* __restrict__ w, int32_t* hist,
+                                            int32_t* s_ids = nullptr, float* s_w = nullptr) {
   uint64_t key[NK];
 #pragma unroll
   for (int i = 0; i < NK; ++i) {
@@ -87,8 +90,13 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, in
   for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   if (lane < k) {
     const int e = key_expert(mine);
+    const float wt = z / sum;
     ids[t * k + lane] = e;
-    w[t * k + lane] = z / sum;
+    w[t * k + lane] = wt;
+    if (s_ids) {
+      s_ids[lane] = e;
+      s_w[lane] = wt;
+    }
     atomicAdd(&hist[e], 1);
   }
 }
@@ -355,6 +363,8 @@ __global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallWarps
   __shared__ int32_t s_off[kMaxExperts + 1];
   __shared__ int32_t running[kMaxExperts];  // next slot of this CTA per expert
   __shared__ int32_t warp_cnt[kSmallWarps][kMaxExperts];
+  __shared__ int32_t s_ids[kSmallWarps * kMaxTopK];  // this CTA's assignments, flat index - f0
+  __shared__ float s_w[kSmallWarps * kMaxTopK];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t rank = cluster_ctarank();
   const int64_t t0 = (int64_t)rank * kSmallWarps, t1 = min(T, t0 + kSmallWarps);
@@ -364,13 +374,18 @@ __global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallWarps
   pdl_wait();  // the logits or ids may come from the kernel just before
   // phase 1: routing of this CTA's tokens and their per-expert counts
   if (logits) {
-    if (t0 + warp < t1) route_token<NK>(logits, t0 + warp, E, k, lane, ids, w, hist);
+    if (t0 + warp < t1)
+      route_token<NK>(logits, t0 + warp, E, k, lane, ids, w, hist, s_ids + warp * k, s_w + warp * k);
   } else {
     for (int64_t f = f0 + threadIdx.x; f < f1; f += blockDim.x) {
       const int64_t e = (int64_t)ext_ids[f] - start;
       const bool local = e >= 0 && e < E;
-      ids[f] = local ? (int32_t)e : -1;
-      w[f] = local ? ext_w[f] : 0.f;
+      const int32_t id = local ? (int32_t)e : -1;
+      const float wt = local ? ext_w[f] : 0.f;
+      ids[f] = id;
+      w[f] = wt;
+      s_ids[f - f0] = id;
+      s_w[f - f0] = wt;
       if (local) atomicAdd(&hist[e], 1);
     }
   }
@@ -390,6 +405,9 @@ __global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallWarps
     running[e] = below;
   }
   __syncthreads();
+  // the remote reads above have completed (their values are stored): this
+  // CTA's part of the closing rendezvous, awaited just before it exits
+  cluster_arrive_relaxed();
   if (warp == 0) {
     int off = 0;
     for (int base = 0; base < E; base += 32) {
@@ -444,7 +462,7 @@ __global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallWarps
   for (int64_t base = f0; base < f1; base += blockDim.x) {
     const int64_t f = base + threadIdx.x;
     const bool valid = f < f1;
-    const int e = valid ? ids[f] : -1;
+    const int e = valid ? s_ids[f - f0] : -1;
     const bool local = e >= 0;
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
     const int rk = __popc(peers & ((1u << lane) - 1u));
@@ -455,7 +473,7 @@ __global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallWarps
       int pre = running[e] + rk;
       for (int q = 0; q < warp; ++q) pre += warp_cnt[q][e];
       sorted_ids[pre] = (int32_t)(f / k);
-      row_w[pre] = w[f];
+      row_w[pre] = s_w[f - f0];
       inverse[f] = pre;
     }
     if (base + (int64_t)blockDim.x >= f1) break;  // last pass: the running starts are not needed again
@@ -470,7 +488,7 @@ __global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallWarps
     }
     __syncthreads();
   }
-  cluster_sync_relaxed();  // no CTA leaves while another may still read its counts
+  cluster_wait();  // no CTA leaves while another may still read its counts
 }
 
 }  // namespace
