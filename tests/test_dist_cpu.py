@@ -43,3 +43,55 @@ def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(1.25, 1) == 1.25
     assert bench.whole_job_throughput(128, 1, 0.5) == pytest.approx(256000.0)
+
+
+def _ep_layer():
+    """One small seeded layer, the same on every rank: 6 experts, top-3."""
+    import numpy as np
+    from oracle import nvfp4_oracle as O
+    from nvfp4_mixture_experts_expert_gb300 import workloads as W
+    wl = W.moe_workload(40, 64, 32, 6, 3, 19)
+    hidden = W.bf16_bits_to_f32(wl.hidden)
+    w13q = O.quantize_expert_weights(W.bf16_bits_to_f32(wl.w13))
+    w2q = O.quantize_expert_weights(W.bf16_bits_to_f32(wl.w2))
+    a1, a2 = O.calibrate_activation_scales(hidden, wl.logits, wl.top_k, w13q)
+    ids, w = O.route(wl.logits, wl.top_k)
+    return np, O, wl, hidden, w13q, w2q, a1, a2, ids, w
+
+
+def _ep_worker(rank, world, port, out):
+    """Rank r holds experts [3r, 3r + 3) and runs the routed forward on the
+    global top-k; the partial sums meet in an all-reduce."""
+    import torch
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    np, O, wl, hidden, w13q, w2q, a1, a2, ids, w = _ep_layer()
+    per = wl.E // world
+    lo = rank * per
+    loc_ids, loc_w = O.remap_global_ids(ids, w, lo, per)
+    sl = slice(lo, lo + per)
+    part = tuple(x[sl] for x in w13q[:2]) + (w13q[2][sl],)
+    part2 = tuple(x[sl] for x in w2q[:2]) + (w2q[2][sl],)
+    _, inter = O.moe_forward_routed(hidden, loc_ids, loc_w, part, part2, a1[sl], a2[sl], return_intermediates=True)
+    acc = torch.from_numpy(inter["acc"].copy())
+    dist.all_reduce(acc)
+    out[rank] = acc.numpy().tolist()
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_expert_parallel_partial_sums_add_up_to_the_whole_layer():
+    """Two gloo ranks, each with half of the experts: the sum of their routed
+    forwards' FP64 accumulators equals the single-process layer's."""
+    import numpy as np
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        out = m.dict()
+        mp.start_processes(_ep_worker, args=(2, _free_port(), out), nprocs=2, join=True, start_method="spawn")
+        res = dict(out)
+    np_, O, wl, hidden, w13q, w2q, a1, a2, ids, w = _ep_layer()
+    _, whole = O.moe_forward_routed(hidden, ids, w, w13q, w2q, a1, a2, return_intermediates=True)
+    for r in (0, 1):
+        np.testing.assert_allclose(np.array(res[r]), whole["acc"], rtol=1e-12, atol=1e-15)
+    assert np.abs(whole["acc"]).max() > 0
