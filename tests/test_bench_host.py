@@ -1,0 +1,79 @@
+"""Host logic of bench.py that needs no GPU: the clock sampler's parsing of
+nvidia-smi output (fed by a fake nvidia-smi on PATH), the stored-traffic
+lookup that goes stale when the GEMM source changes, the whole-job value and
+the peak denominators."""
+import json
+import os
+import stat
+import time
+
+import pytest
+
+import bench
+
+FAKE_SMI = """#!/bin/sh
+cat <<'EOF'
+2070, 2070, 1200.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active
+1965, 2070, 1390.1, 0x0000000000000004, Not Active, Not Active, Not Active, Active
+2040, 2070, 1385.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active
+[N/A], 2070, [N/A], [N/A], [N/A], [N/A], [N/A], [N/A]
+garbage line
+EOF
+exec sleep 30
+"""
+
+
+def test_clock_sampler_parses_samples_and_reasons(tmp_path, monkeypatch):
+    smi = tmp_path / "nvidia-smi"
+    smi.write_text(FAKE_SMI)
+    smi.chmod(smi.stat().st_mode | stat.S_IEXEC)
+    monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
+    s = bench.ClockSampler(0)
+    time.sleep(0.5)
+    t0 = time.time()
+    r = s.stop()
+    assert time.time() - t0 < 10  # the sampler process is stopped, not awaited
+    assert r["samples"] == 4  # the malformed line is dropped, the N/A row kept
+    assert r["sm_mhz"] == 2040.0  # median of the three numeric SM clocks
+    assert r["sm_max_mhz"] == 2070.0
+    assert r["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_sampler_without_nvidia_smi_reports_nothing(tmp_path, monkeypatch):
+    monkeypatch.setenv("PATH", str(tmp_path))
+    assert bench.ClockSampler(0).stop() is None
+
+
+def _fake_root(tmp_path, gemm_src, stored_sha):
+    csrc = tmp_path / "nvfp4_mixture_experts_expert_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "gemm.cu").write_bytes(gemm_src)
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(
+        {"l1_gemm_swiglu_quant_prefill": {"bytes_per_launch": 123, "gemm_cu_sha256_16": stored_sha}}))
+    return str(tmp_path)
+
+
+def test_stored_traffic_only_for_the_source_it_was_measured_on(tmp_path, monkeypatch):
+    import hashlib
+    src = b"// kernel source\n"
+    sha = hashlib.sha256(src).hexdigest()[:16]
+    monkeypatch.setattr(bench, "ROOT", _fake_root(tmp_path / "a", src, sha))
+    assert bench.stored_traffic("l1_gemm_swiglu_quant_prefill") == 123
+    assert bench.stored_traffic("l1_gemm_swiglu_quant_decode") is None  # never measured
+    monkeypatch.setattr(bench, "ROOT", _fake_root(tmp_path / "b", src + b"// changed\n", sha))
+    assert bench.stored_traffic("l1_gemm_swiglu_quant_prefill") is None
+
+
+def test_measured_peaks_and_fallback(tmp_path, monkeypatch):
+    p = bench.measured_peaks()
+    assert p["source"] == "measured" and p["hbm_gbs"] > 1000 and p["bf16_tflops_sustained"] > 100
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    f = bench.measured_peaks()
+    assert f["source"] == "fallback" and f["hbm_gbs"] == 6800.0
+
+
+def test_whole_job_value_and_workload_names():
+    assert bench.whole_job_throughput(8192, 4, 1.0) == pytest.approx(8192 * 4 / 1e-3)
+    assert "T=8192" in bench.workload_name("prefill") and "E=48" in bench.workload_name("prefill")
+    assert "T=128" in bench.workload_name("decode") and "E=32" in bench.workload_name("decode")
