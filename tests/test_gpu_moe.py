@@ -148,6 +148,22 @@ def test_moe_all_tokens_on_one_expert(k):
     check_all(wl, orc, *run_gpu(wl, orc))
 
 
+def test_moe_swiglu_clamps_active():
+    """Limits small enough that a fifth of the gate values and a third of the
+    up values are clamped in the L1 epilogue (gate from above only, before
+    the SiLU; up on both sides)."""
+    wl = W.moe_workload(150, 256, 128, 5, 2, 49)
+    wl.gate_limit, wl.up_limit = 0.25, 0.3
+    orc = OracleMoE(wl)
+    ref, inter = orc.forward()
+    e = next(iter(inter["experts"]))
+    toks = inter["experts"][e]["toks"]
+    G = O.dequant_blocks(*O.quantize_blocks(orc.hidden[toks], orc.a1_gs[e])) / orc.a1_gs[e] @ \
+        (O.dequant_blocks(orc.w13q[0][e], orc.w13q[1][e]) / orc.w13q[2][e]).T
+    assert np.mean(G[:, :wl.I] > wl.gate_limit) > 0.15 and np.mean(np.abs(G[:, wl.I:]) > wl.up_limit) > 0.15
+    check_all(wl, orc, *run_gpu(wl, orc))
+
+
 def test_moe_all_zero_hidden_states():
     """All-zero input: calibration gives every scale 1 (the amax == 0 rule),
     the gathered activations are all zero codes and the output is exactly 0."""

@@ -167,6 +167,28 @@ def test_sparse_moe_equals_dense_brute_force():
     assert np.mean(out != ref) < 0.01
 
 
+def test_swiglu_clamps_the_gate_from_above_before_silu_and_up_on_both_sides():
+    """SiLU written out with math.exp, bf16 rounding by torch.  Limits 2 (gate)
+    and 10 (up) make each wrong reading visible: clamping after the SiLU,
+    clamping the gate from below too, or leaving up unclamped."""
+    import math
+    import torch
+    silu = lambda x: x / (1.0 + math.exp(-x))
+    g = np.array([12.0, -20.0, 3.0, 0.5, 2.0])
+    u = np.array([0.75, 1.0, -15.0, 12.0, -3.0])
+    want = [silu(2.0) * 0.75,   # gate clamped to 2 first
+            silu(-20.0) * 1.0,  # no lower clamp on the gate
+            silu(2.0) * -10.0,  # gate 3 -> 2, up -15 -> -10
+            silu(0.5) * 10.0,   # up 12 -> 10
+            silu(2.0) * -3.0]   # at the limit: unchanged
+    want = torch.tensor(want, dtype=torch.float32).to(torch.bfloat16).float().numpy()
+    got = O.swiglu(g, u, 2.0, 10.0)
+    np.testing.assert_array_equal(got, want)
+    # the readings it rules out give other values
+    assert got[0] != min(silu(12.0), 2.0) * 0.75
+    assert abs(got[1]) < 1e-7 and abs(silu(-2.0)) > 0.2
+
+
 def test_single_expert_top1_is_a_dense_swiglu_ffn():
     wl = W.moe_workload(20, 64, 32, 1, 1, 3)
     hidden = W.bf16_bits_to_f32(wl.hidden)
