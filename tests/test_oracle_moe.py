@@ -378,3 +378,40 @@ def test_batch_l2_scales_equal_calibrated_scales_forward():
     dyn = O.moe_forward(hidden, wl.logits, 2, w13q, w2q, a1, None, 10.0, 10.0)
     cal = O.moe_forward(hidden, wl.logits, 2, w13q, w2q, a1, a2, 10.0, 10.0)
     np.testing.assert_array_equal(dyn, cal)
+
+
+# ----------------------------------------------------------------- slot layout cases from the pages
+
+def _slot_cases():
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "slot_offsets.json")) as f:
+        return json.load(f)["cases"]
+
+
+def test_page_offsets_example_gets_whole_chunks_and_scale_rows():
+    """Counts [500, 524] (the page's offsets [0, 500, 1024]): expert 0 gets four
+    whole 128-row chunks, so all 500 of its scale rows sit where the GEMM reads
+    them, and its 12 pad rows carry zero scales."""
+    case = _slot_cases()[0]
+    counts = case["counts"]
+    ids = np.concatenate([np.full(c, e) for e, c in enumerate(counts)]).astype(np.int32)[:, None]
+    m = O.sort_slots(ids, np.ones(ids.shape), len(counts))
+    assert m["counts"].tolist() == counts
+    assert m["offsets"].tolist() == case["padded_offsets"]
+    rng = np.random.default_rng(3)
+    lin = rng.integers(1, 127, (sum(counts), 8), dtype=np.uint8)
+    swz = O.assemble_scales(lin, np.concatenate([[0], np.cumsum(counts)]), m["offsets"])
+    full = O.unswizzle_scales(swz, m["P"], 8)
+    np.testing.assert_array_equal(full[0:500], lin[0:500])
+    assert not full[500:512].any()
+    np.testing.assert_array_equal(full[512:1036], lin[500:1024])
+
+
+def test_page_bug9_case_needs_more_than_one_chunk_per_expert():
+    case = _slot_cases()[1]
+    wl = W.moe_workload(case["T"], 64, 32, case["E"], case["top_k"], 0, zipf_s=1.1, with_weights=False)
+    ids, w = O.route(wl.logits, case["top_k"])
+    m = O.sort_slots(ids, w, case["E"])
+    assert m["P"] > case["min_padded_rows_exclusive"]
+    assert m["P"] <= O.slot_capacity(case["T"], case["top_k"], case["E"])
