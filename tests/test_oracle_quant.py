@@ -32,6 +32,9 @@ def test_global_scale_convention():
     assert O.global_scale(0.0) == np.float32(1.0)
     assert O.global_scale(448.0 * 6) == np.float32(1.0)
     assert O.global_scale(2.0) == np.float32(1344.0)
+    # vllm page (checkpoint input_scale paragraph): the decode form of this
+    # scale for a unit amax is 1/2688 = 0.000372
+    assert round(1.0 / float(O.global_scale(1.0)), 6) == 0.000372
     # the tensor amax lands exactly on the largest code pair (scale 448, nibble 6)
     x = np.zeros((1, 16), np.float32)
     x[0, 3] = 3.25
