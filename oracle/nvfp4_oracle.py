@@ -453,10 +453,20 @@ def calibrate_activation_scales(hidden, logits, top_k, w13q, gate_limit=10.0, up
     expert's L1 output (SwiGLU, bf16).  Experts with no rows get gs 1.
     row_limit: calibrate L2 on at most this many rows per expert (the first
     ones in slot order); None uses all rows."""
+    ids, _ = route(logits, top_k)
+    return calibrate_activation_scales_routed(hidden, ids, w13q, gate_limit, up_limit, row_limit)
+
+
+def calibrate_activation_scales_routed(hidden, ids, w13q, gate_limit=10.0, up_limit=10.0, row_limit=None):
+    """The same calibration from given routing: local expert ids [T,k], -1 for
+    an assignment to an expert this layer does not hold ([vllm] "Root cause of
+    CUDA_ERROR_ASSERT index out of bounds" paragraph:
+    compute_activation_global_scales expects local ids; with global ids no row
+    matched a local expert).  Only the ids matter, not the weights."""
     hidden = np.asarray(hidden, dtype=np.float32)
     E = w13q[0].shape[0]
-    ids, w = route(logits, top_k)
-    meta = sort_slots(ids, w, E)
+    ids = np.asarray(ids)
+    meta = sort_slots(ids, np.ones(ids.shape), E)
     a1 = np.ones(E, dtype=np.float32)
     a2 = np.ones(E, dtype=np.float32)
     for e in range(E):

@@ -313,6 +313,45 @@ def test_routed_forward_equals_per_assignment_brute_force():
     assert (ids == -1).any() and (ids >= 0).any()
 
 
+def test_routed_calibration_all_local_equals_logit_calibration():
+    wl, hidden, w13, w2, w13q, w2q, a1, a2 = small_layer()
+    ids, _ = O.route(wl.logits, wl.top_k)
+    r1, r2 = O.calibrate_activation_scales_routed(hidden, ids, w13q)
+    np.testing.assert_array_equal(r1, a1)
+    np.testing.assert_array_equal(r2, a2)
+
+
+def test_routed_calibration_of_one_expert_parallel_rank_by_brute_force():
+    """The page's setting: 48 local experts per rank, this rank holding global
+    experts [240, 288) of 384.  After the remap every local expert's scales
+    come from exactly the tokens that chose its global id; a rank that no
+    token chose keeps scale 1 everywhere (never 0)."""
+    E, start, G, k = 48, 240, 384, 6
+    wl = W.moe_workload(300, 64, 32, E, k, 23)
+    hidden = W.bf16_bits_to_f32(wl.hidden)
+    w13q = O.quantize_expert_weights(W.bf16_bits_to_f32(wl.w13))
+    rng = np.random.default_rng(5)
+    gids = np.stack([rng.choice(G, size=k, replace=False) for _ in range(wl.T)])
+    ids, _ = O.remap_global_ids(gids, np.ones(gids.shape), start, E)
+    a1, a2 = O.calibrate_activation_scales_routed(hidden, ids, w13q)
+    seen = 0
+    for e in range(E):
+        toks = [t for t in range(wl.T) if (gids[t] == start + e).any()]
+        if not toks:
+            assert a1[e] == 1 and a2[e] == 1
+            continue
+        seen += 1
+        x = hidden[toks]
+        assert a1[e] == np.float32(2688.0) / np.float32(np.abs(x).max())
+        h = O.expert_l1(x, a1[e], w13q[0][e], w13q[1][e], w13q[2][e], 10.0, 10.0)
+        assert a2[e] == np.float32(2688.0) / np.float32(np.abs(h).max())
+    assert seen > 30
+    # every token routed to global expert 0, held by another rank
+    none, _ = O.remap_global_ids(np.zeros_like(gids), np.ones(gids.shape), start, E)
+    b1, b2 = O.calibrate_activation_scales_routed(hidden, none, w13q)
+    assert np.all(b1 == 1) and np.all(b2 == 1)
+
+
 # ----------------------------------------------------------------- shared expert
 
 def test_shared_expert_equals_one_expert_top1_moe():
