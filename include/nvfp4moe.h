@@ -270,6 +270,22 @@ int nvfp4_moe_calibrate(const void* hidden, const float* router_logits, int64_t 
                         void* stream);
 
 /*
+ * nvfp4_moe_calibrate_routed -- the same scales from the model router's
+ * global top-k instead of this layer's logits (vllm page, "Root cause of
+ * CUDA_ERROR_ASSERT index out of bounds": compute_activation_global_scales
+ * works on local expert ids; with global ids no row matched a local expert).
+ * topk_ids / topk_weights / experts_start as nvfp4_moe_forward_routed: an
+ * assignment to an expert outside [experts_start, experts_start + E) takes no
+ * row.  The weights are read but do not change the scales.  Other arguments,
+ * outputs and errors as nvfp4_moe_calibrate.
+ */
+int nvfp4_moe_calibrate_routed(const void* hidden, const int32_t* topk_ids, const float* topk_weights,
+                               int32_t experts_start, int64_t T, int64_t H, int64_t I, int E, int top_k,
+                               const void* w13, const void* w13_sf, const float* w13_gs, float gate_limit,
+                               float up_limit, void* workspace, size_t workspace_bytes, float* a1_gs_out,
+                               float* a2_gs_out, void* stream);
+
+/*
  * Byte offsets of the forward's intermediates inside the workspace, for
  * inspection by tests.  Sizes: cap = padded-row capacity
  * (roundup(T*top_k + 127*min(E, T*top_k), 128)); A = T*top_k assignments.

@@ -139,6 +139,17 @@ class MoEForward:
                               w.w13_gs, gate_limit, up_limit, self.workspace, self.ws_bytes, a1, a2, stream)
         return a1, a2
 
+    def calibrate_routed(self, hidden, topk_ids, topk_weights, experts_start, w: MoEWeights, gate_limit=10.0,
+                         up_limit=10.0, stream=None):
+        """The same scales from the model router's global top-k (int32 / f32
+        [T, k]) for the experts [experts_start, experts_start + E) held here."""
+        a1 = torch.empty(self.E, dtype=torch.float32, device=hidden.device)
+        a2 = torch.empty(self.E, dtype=torch.float32, device=hidden.device)
+        B.nvfp4_moe_calibrate_routed(hidden, topk_ids, topk_weights, experts_start, self.T, self.H, self.I, self.E,
+                                     self.top_k, w.w13, w.w13_sf, w.w13_gs, gate_limit, up_limit, self.workspace,
+                                     self.ws_bytes, a1, a2, stream)
+        return a1, a2
+
     def batch_l2_scales(self):
         """The L2 global scales the last call with a2_gs None used (f32 [E])."""
         off = self.layout["calib"] + 4 * self.E

@@ -88,6 +88,10 @@ _se_forward = _sig("nvfp4_shared_expert_forward", c_int, [c_ptr, c_i64, c_i64, c
 _moe_calibrate = _sig("nvfp4_moe_calibrate", c_int, [c_ptr, c_ptr, c_i64, c_i64, c_i64, c_int, c_int, c_ptr,
                                                      c_ptr, c_ptr, c_float, c_float, c_ptr, c_size, c_ptr, c_ptr,
                                                      c_ptr])
+_moe_calibrate_routed = _sig("nvfp4_moe_calibrate_routed", c_int, [c_ptr, c_ptr, c_ptr, ctypes.c_int32, c_i64,
+                                                                     c_i64, c_i64, c_int, c_int, c_ptr, c_ptr,
+                                                                     c_ptr, c_float, c_float, c_ptr, c_size, c_ptr,
+                                                                     c_ptr, c_ptr])
 _device_status = _sig("nvfp4_device_status", c_int, [ctypes.POINTER(c_int), c_int])
 _stage_events = _sig("nvfp4_moe_set_stage_events", c_int, [ctypes.POINTER(c_ptr), c_int])
 _gemm_set_cta_pair = _sig("nvfp4_gemm_set_cta_pair", c_int, [c_int, ctypes.POINTER(c_int)])
@@ -213,6 +217,14 @@ def nvfp4_moe_calibrate(hidden, router_logits, T, H, I, E, top_k, w13, w13_sf, w
     _check(_moe_calibrate(_p(hidden), _p(router_logits), T, H, I, E, top_k, _p(w13), _p(w13_sf), _p(w13_gs),
                           gate_limit, up_limit, _p(workspace), workspace_bytes, _p(a1_gs_out), _p(a2_gs_out),
                           _stream(stream)))
+
+
+def nvfp4_moe_calibrate_routed(hidden, topk_ids, topk_weights, experts_start, T, H, I, E, top_k, w13, w13_sf,
+                               w13_gs, gate_limit, up_limit, workspace, workspace_bytes, a1_gs_out, a2_gs_out,
+                               stream=None):
+    _check(_moe_calibrate_routed(_p(hidden), _p(topk_ids), _p(topk_weights), experts_start, T, H, I, E, top_k,
+                                 _p(w13), _p(w13_sf), _p(w13_gs), gate_limit, up_limit, _p(workspace),
+                                 workspace_bytes, _p(a1_gs_out), _p(a2_gs_out), _stream(stream)))
 
 
 def nvfp4_device_status(reset=False):

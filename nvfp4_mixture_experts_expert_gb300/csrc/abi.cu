@@ -630,10 +630,11 @@ int nvfp4_shared_expert_forward(const void* hidden, int64_t T, int64_t H, int64_
   return NVFP4_OK;
 }
 
-int nvfp4_moe_calibrate(const void* hidden, const float* router_logits, int64_t T, int64_t H, int64_t I, int E,
-                        int top_k, const void* w13, const void* w13_sf, const float* w13_gs, float gate_limit,
-                        float up_limit, void* workspace, size_t workspace_bytes, float* a1_gs_out, float* a2_gs_out,
-                        void* stream) {
+namespace {
+
+int calibrate_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H, int64_t I, int E, int top_k,
+                   const void* w13, const void* w13_sf, const float* w13_gs, float gate_limit, float up_limit,
+                   void* workspace, size_t workspace_bytes, float* a1_gs_out, float* a2_gs_out, void* stream) {
   g_err[0] = 0;
   if (T < 0) return fail(NVFP4_ERR_INVALID_ARG, "T must be >= 0");
   if (H <= 0 || H % 256) return fail(NVFP4_ERR_UNSUPPORTED, "H must be a positive multiple of 256");
@@ -644,9 +645,9 @@ int nvfp4_moe_calibrate(const void* hidden, const float* router_logits, int64_t 
   nvfp4_moe_layout L;
   if (int rc = nvfp4_moe_workspace_layout(T, H, I, E, top_k, &L)) return rc;
   if (!a1_gs_out || !a2_gs_out) return fail(NVFP4_ERR_INVALID_ARG, "null output pointer");
-  if (T > 0 && (!hidden || !router_logits || !w13 || !w13_sf || !w13_gs))
+  if (T > 0 && (!hidden || !w13 || !w13_sf || !w13_gs || (rt.logits ? false : (!rt.topk_ids || !rt.topk_w))))
     return fail(NVFP4_ERR_INVALID_ARG, "null pointer");
-  if (!aligned16(hidden) || !aligned16(w13) || !aligned16(w13_sf) || !aligned16(router_logits))
+  if (!aligned16(hidden) || !aligned16(w13) || !aligned16(w13_sf) || (rt.logits && !aligned16(rt.logits)))
     return fail(NVFP4_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   if (!workspace || workspace_bytes < L.total)
     return fail(NVFP4_ERR_WORKSPACE, "workspace of %zu bytes needed, got %zu", L.total, workspace_bytes);
@@ -705,7 +706,9 @@ int nvfp4_moe_calibrate(const void* hidden, const float* router_logits, int64_t 
   g1.status = dev->status;
   g1.timeout_ns = 2000000000ull;
   const int nb = (int)L.route_blocks;
-  if ((e = launch_route_topk(router_logits, T, E, top_k, ids, wts, bcnt, s)) != cudaSuccess ||
+  if ((e = rt.logits ? launch_route_topk(rt.logits, T, E, top_k, ids, wts, bcnt, s)
+                     : launch_route_external(rt.topk_ids, rt.topk_w, rt.experts_start, T, E, top_k, ids, wts, bcnt,
+                                             s)) != cudaSuccess ||
       (e = launch_slot_scan(bcnt, nb, E, counts, offsets, meta, tile_expert, sorted_ids, row_w, amax, 2 * E, s)) !=
           cudaSuccess ||
       (e = launch_slot_scatter(ids, wts, T, E, top_k, bcnt, offsets, sorted_ids, row_w, inverse, s)) !=
@@ -721,6 +724,29 @@ int nvfp4_moe_calibrate(const void* hidden, const float* router_logits, int64_t 
       (e = launch_gs_from_amax(amax + E, E, a2_gs_out, s)) != cudaSuccess)
     return cuda_fail(e, "calibration launch");
   return NVFP4_OK;
+}
+
+}  // namespace
+
+int nvfp4_moe_calibrate(const void* hidden, const float* router_logits, int64_t T, int64_t H, int64_t I, int E,
+                        int top_k, const void* w13, const void* w13_sf, const float* w13_gs, float gate_limit,
+                        float up_limit, void* workspace, size_t workspace_bytes, float* a1_gs_out, float* a2_gs_out,
+                        void* stream) {
+  if (T > 0 && !router_logits) return fail(NVFP4_ERR_INVALID_ARG, "null pointer");
+  const Routing rt{router_logits, nullptr, nullptr, 0};
+  return calibrate_impl(hidden, rt, T, H, I, E, top_k, w13, w13_sf, w13_gs, gate_limit, up_limit, workspace,
+                        workspace_bytes, a1_gs_out, a2_gs_out, stream);
+}
+
+int nvfp4_moe_calibrate_routed(const void* hidden, const int32_t* topk_ids, const float* topk_weights,
+                               int32_t experts_start, int64_t T, int64_t H, int64_t I, int E, int top_k,
+                               const void* w13, const void* w13_sf, const float* w13_gs, float gate_limit,
+                               float up_limit, void* workspace, size_t workspace_bytes, float* a1_gs_out,
+                               float* a2_gs_out, void* stream) {
+  if (T > 0 && (!topk_ids || !topk_weights)) return fail(NVFP4_ERR_INVALID_ARG, "null pointer");
+  const Routing rt{nullptr, topk_ids, topk_weights, experts_start};
+  return calibrate_impl(hidden, rt, T, H, I, E, top_k, w13, w13_sf, w13_gs, gate_limit, up_limit, workspace,
+                        workspace_bytes, a1_gs_out, a2_gs_out, stream);
 }
 
 int nvfp4_gemm_set_cta_pair(int mode, int* prev_mode) {

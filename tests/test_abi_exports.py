@@ -117,3 +117,23 @@ def test_routed_and_shared_expert_entries_check_arguments_on_host(binding):
         binding.nvfp4_shared_expert_forward(16, 4, 256, 128, 16, 16, 16, 16, 16, 16, 16, 16, -1.0, 10.0, 256,
                                             need, 16, stream=0)
     assert ei.value.status == binding.NVFP4_ERR_INVALID_ARG  # limits must be positive
+
+
+def test_routed_calibration_checks_arguments_on_host(binding):
+    # ids / weights required (T > 0), sizes and top_k as the logit calibration
+    with pytest.raises(binding.Nvfp4Error) as ei:
+        binding.nvfp4_moe_calibrate_routed(16, None, 16, 0, 4, 256, 128, 4, 2, 16, 16, 16, 10.0, 10.0, 256,
+                                           1 << 30, 16, 16, stream=0)
+    assert ei.value.status == binding.NVFP4_ERR_INVALID_ARG
+    with pytest.raises(binding.Nvfp4Error) as ei:
+        binding.nvfp4_moe_calibrate_routed(16, 16, 16, 0, 4, 256, 100, 4, 2, 16, 16, 16, 10.0, 10.0, 256,
+                                           1 << 30, 16, 16, stream=0)
+    assert ei.value.status == binding.NVFP4_ERR_UNSUPPORTED  # I % 128
+    with pytest.raises(binding.Nvfp4Error) as ei:
+        binding.nvfp4_moe_calibrate_routed(16, 16, 16, 0, 4, 256, 128, 2, 3, 16, 16, 16, 10.0, 10.0, 256,
+                                           1 << 30, 16, 16, stream=0)
+    assert ei.value.status == binding.NVFP4_ERR_INVALID_ARG and "top_k" in str(ei.value)
+    with pytest.raises(binding.Nvfp4Error) as ei:
+        binding.nvfp4_moe_calibrate_routed(16, 16, 16, 0, 4, 256, 128, 4, 2, 16, 16, 16, 10.0, 10.0, 256,
+                                           1 << 30, None, 16, stream=0)
+    assert ei.value.status == binding.NVFP4_ERR_INVALID_ARG  # outputs required

@@ -424,6 +424,25 @@ def test_device_calibration_matches_oracle_scales():
     assert host(a1)[3] == 1.0 and host(a2)[3] == 1.0  # the expert with no rows
 
 
+@pytest.mark.parametrize("T", [150, 300])
+def test_routed_calibration_matches_oracle_scales(T):
+    """nvfp4_moe_calibrate_routed from global ids: L1 scales bit-exact, L2
+    scales within 1 %; experts no token chose keep scale 1."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    wl, orc, gids, gw, start = _routed_case(T=T, seed=73)
+    gids[:, :] = np.where(gids == start + 2, start - 1, gids)  # local expert 2 gets no row
+    ids, _ = O.remap_global_ids(gids, gw.astype(np.float64), start, wl.E)
+    a1_ref, a2_ref = O.calibrate_activation_scales_routed(orc.hidden, ids, orc.w13q, wl.gate_limit, wl.up_limit)
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    fwd = api.MoEForward(wl.T, wl.H, wl.I, wl.E, wl.top_k)
+    a1, a2 = fwd.calibrate_routed(bf16_dev(wl.hidden), dev(gids), dev(gw), start, w, wl.gate_limit, wl.up_limit)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host(a1), a1_ref)
+    np.testing.assert_allclose(host(a2), a2_ref, rtol=1e-2)
+    assert host(a1)[2] == 1.0 and host(a2)[2] == 1.0
+
+
 def test_routing_ties_and_signed_zero_match_oracle():
     """Exactly equal logits go to the lower expert; -0 and +0 rank as equal."""
     import torch
