@@ -73,17 +73,22 @@ def _ep_worker(rank, world, port, out):
     sl = slice(lo, lo + per)
     part = tuple(x[sl] for x in w13q[:2]) + (w13q[2][sl],)
     part2 = tuple(x[sl] for x in w2q[:2]) + (w2q[2][sl],)
+    # each rank calibrates its own experts from the same global ids
+    c1, c2 = O.calibrate_activation_scales_routed(hidden, loc_ids, part)
+    scales = [torch.zeros(2 * per, dtype=torch.float32) for _ in range(world)]
+    dist.all_gather(scales, torch.from_numpy(np.concatenate([c1, c2]).astype(np.float32)))
     _, inter = O.moe_forward_routed(hidden, loc_ids, loc_w, part, part2, a1[sl], a2[sl], return_intermediates=True)
     acc = torch.from_numpy(inter["acc"].copy())
     dist.all_reduce(acc)
-    out[rank] = acc.numpy().tolist()
+    out[rank] = (acc.numpy().tolist(), [x.numpy().tolist() for x in scales])
     dist.barrier()
     dist.destroy_process_group()
 
 
 def test_expert_parallel_partial_sums_add_up_to_the_whole_layer():
     """Two gloo ranks, each with half of the experts: the sum of their routed
-    forwards' FP64 accumulators equals the single-process layer's."""
+    forwards' FP64 accumulators equals the single-process layer's, and the
+    scales each rank calibrates for its experts are the whole layer's."""
     import numpy as np
     ctx = mp.get_context("spawn")
     with ctx.Manager() as m:
@@ -92,6 +97,11 @@ def test_expert_parallel_partial_sums_add_up_to_the_whole_layer():
         res = dict(out)
     np_, O, wl, hidden, w13q, w2q, a1, a2, ids, w = _ep_layer()
     _, whole = O.moe_forward_routed(hidden, ids, w, w13q, w2q, a1, a2, return_intermediates=True)
+    per = wl.E // 2
     for r in (0, 1):
-        np.testing.assert_allclose(np.array(res[r]), whole["acc"], rtol=1e-12, atol=1e-15)
+        acc, scales = res[r]
+        np.testing.assert_allclose(np.array(acc), whole["acc"], rtol=1e-12, atol=1e-15)
+        for q in (0, 1):
+            np.testing.assert_array_equal(np.float32(scales[q][:per]), a1[q * per:(q + 1) * per])
+            np.testing.assert_array_equal(np.float32(scales[q][per:]), a2[q * per:(q + 1) * per])
     assert np.abs(whole["acc"]).max() > 0
