@@ -188,7 +188,7 @@ int nvfp4_debug_gemm_stall(const void* A, const void* SFA, const float* a_gs, co
  *   w2             device u8 [E][H][I/2],  w2_sf device u8 [E][H*I/16]
  *   w13_gs, w2_gs, a1_gs, a2_gs   device f32[E] global (encode) scales
  *   a2_gs may be NULL: the L2 activation scales are then taken from this
- *                  batch (vllm page: the L2 scale from the actual L1 output;
+ *                  batch (vllm page: the L2 scale measured on the L1 output;
  *                  cutedsl page: a BF16 L1 output when no calibrated L2 scale
  *                  exists): a2_gs[e] = 2688 / amax(h of expert e's rows), 1
  *                  when that is 0.  L1 writes h in bf16 into the workspace's y
@@ -232,8 +232,8 @@ int nvfp4_moe_forward_routed(const void* hidden, const int32_t* topk_ids, const 
                              void* stream);
 
 /* Shared expert: one NVFP4 SwiGLU FFN applied to every token, no routing
- * (cutedsl page: "CuTeDSLSharedExpertRunner: num_groups=1 GEMM, no
- * scatter/routing", the fused L1+SiLU+L2 pipeline, rows padded to 128 for the
+ * (cutedsl page: the shared-expert runner paragraph -- a single group, no
+ * scatter and no routing -- the fused L1+SiLU+L2 pipeline, rows padded to 128 for the
  * scale layout, all buffers pre-allocated).
  *
  *   out[t] = bf16( L2( requant( SwiGLU( L1( quant(hidden[t]) ) ) ) ) )
@@ -255,7 +255,7 @@ int nvfp4_shared_expert_forward(const void* hidden, int64_t T, int64_t H, int64_
 /*
  * nvfp4_moe_calibrate -- per-expert activation global scales from sample data
  * (vllm page: compute_activation_global_scales -- L1 scale from the gathered
- * hidden rows, L2 scale from the actual L1 output, local expert ids, run
+ * hidden rows, L2 scale measured on the L1 output, local expert ids, run
  * before graph capture so the forward can use fixed scales).
  *   a1_gs_out[e] = 2688 / amax(hidden rows routed to e)
  *   a2_gs_out[e] = 2688 / amax(bf16 SwiGLU output of those rows, with the L1

@@ -65,7 +65,7 @@ E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float64)
 # [bridge] "Bug #4 fix": blocks with amax < 6*2^-9 are forced to scale 0, nibble 0.
 UNDERFLOW_AMAX = F32(6.0 * 2.0 ** -9)
 E4M3_MAX = 448.0
-GS_NUMERATOR = F32(2688.0)  # 448 * 6, [vllm] "Using 1/2688 was wrong" paragraph
+GS_NUMERATOR = F32(2688.0)  # 448 * 6, [vllm] checkpoint input_scale paragraph
 
 
 # --------------------------------------------------------------------------- formats
@@ -185,7 +185,7 @@ def dequant_blocks(nib, s):
 
 
 def pack_nibbles(nib) -> np.ndarray:
-    """R6: byte j = nib[2j] | nib[2j+1] << 4 ([bridge] "packs 2 values per byte along K")."""
+    """R6: byte j = nib[2j] | nib[2j+1] << 4 ([bridge] packing paragraph: two values per byte, along K)."""
     nib = np.asarray(nib, dtype=np.uint8)
     return (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
 
@@ -331,7 +331,7 @@ def nvfp4_gemm(a_nib, a_s, a_gs, b_nib, b_s, b_gs):
 
 
 def swiglu(g, u, gate_limit, up_limit):
-    """R10, [cutedsl] "Fixed SwiGLU clamp: gate clamped BEFORE SiLU": FP64 math,
+    """R10, [cutedsl] SwiGLU clamp fix (the gate is clamped before the SiLU): FP64 math,
     rounded to FP32 then to bf16 (returned as FP32 values)."""
     g = np.minimum(g, gate_limit)
     u = np.clip(u, -up_limit, up_limit)
@@ -406,8 +406,9 @@ def moe_forward_routed(hidden, ids, w, w13q, w2q, a1_gs, a2_gs,
     """The MoE forward from given routing: local expert ids [T,k] (-1 = not
     local, R18) and weights [T,k]; otherwise as moe_forward.
     a2_gs None (R19): each expert's L2 global scale is 2688/amax of its own
-    bf16 L1 output in this batch ([vllm] "L2 gs from the actual L1 GEMM
-    output"; [cutedsl] BF16 L1 output when no calibrated L2 scale exists)."""
+    bf16 L1 output in this batch ([vllm] warm-up paragraph: the L2 scale is
+    measured on the L1 GEMM's output; [cutedsl] BF16 L1 output when no
+    calibrated L2 scale exists)."""
     hidden = np.asarray(hidden, dtype=np.float32)
     T, H = hidden.shape
     E = w13q[0].shape[0]
@@ -436,8 +437,8 @@ def moe_forward_routed(hidden, ids, w, w13q, w2q, a1_gs, a2_gs,
 
 def shared_expert_forward(hidden, w13q, w2q, a1_gs, a2_gs, gate_limit=10.0, up_limit=10.0):
     """The shared expert: one NVFP4 SwiGLU FFN over every token, no routing
-    ([cutedsl] "CuTeDSLSharedExpertRunner: num_groups=1 GEMM, no
-    scatter/routing" and the fused L1+SiLU+L2 paragraph).  w13q / w2q hold one
+    ([cutedsl] shared-expert runner paragraph: a single group, no scatter
+    and no routing; the fused L1+SiLU+L2 paragraph).  w13q / w2q hold one
     expert: (nibbles [1,2I,H], scales, gs [1]); a1_gs / a2_gs scalars.
     Returns bf16 values as FP32 [T, H]."""
     hidden = np.asarray(hidden, dtype=np.float32)
