@@ -119,6 +119,43 @@ def test_gemm_equals_plain_matmul_of_dequantized_operands():
     np.testing.assert_allclose(O.nvfp4_gemm(an, as_, 2, bn, bs, 4), ref, rtol=1e-12, atol=1e-12)
 
 
+def test_grouped_gemm_is_per_group_matmul_with_empty_and_ragged_groups():
+    rng = np.random.default_rng(12)
+    rows, K, N = [5, 0, 17, 1], 32, 12
+    a = rng.standard_normal((sum(rows), K)).astype(np.float32)
+    gs_a = np.float32([2.0, 1.0, 0.5, 3.0])
+    nib, sc = np.zeros((sum(rows), K), np.uint8), np.zeros((sum(rows), K // 16), np.uint8)
+    r0 = 0
+    for g, n in enumerate(rows):
+        nib[r0:r0 + n], sc[r0:r0 + n] = O.quantize_blocks(a[r0:r0 + n], gs_a[g])
+        r0 += n
+    bq = [O.weight_quantize(rng.standard_normal((N, K)).astype(np.float32)) for _ in rows]
+    out = O.grouped_gemm(nib, sc, gs_a, [b[0] for b in bq], [b[1] for b in bq], [b[2] for b in bq], rows)
+    r0 = 0
+    for g, n in enumerate(rows):
+        A = O.dequant_blocks(nib[r0:r0 + n], sc[r0:r0 + n]) / np.float64(gs_a[g])
+        B = O.dequant_blocks(bq[g][0], bq[g][1]) / np.float64(bq[g][2])
+        ref = np.array([[sum(A[i, k] * B[j, k] for k in range(K)) for j in range(N)] for i in range(n)])
+        assert out[g].shape == (n, N)
+        np.testing.assert_allclose(out[g], ref.reshape(n, N), rtol=1e-12, atol=1e-12)
+        r0 += n
+
+
+def test_quantize_tensor_pads_rows_with_zero_codes_and_scales():
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((130, 64)).astype(np.float32)
+    gs = O.global_scale(np.abs(x).max())
+    packed, swz, lin = O.quantize_tensor(x, gs)
+    nib, s = O.quantize_blocks(x, gs)
+    assert packed.shape == (256, 32) and swz.size == 256 * 4
+    np.testing.assert_array_equal(O.unpack_nibbles(packed[:130]), nib)
+    assert not packed[130:].any()
+    full = O.unswizzle_scales(swz, 256, 4)
+    np.testing.assert_array_equal(full[:130], s)
+    np.testing.assert_array_equal(lin, s)
+    assert not full[130:].any()
+
+
 # ----------------------------------------------------------------- MoE
 
 def small_layer(T=48, H=64, I=32, E=5, k=2, seed=11):
