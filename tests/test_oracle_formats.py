@@ -129,3 +129,21 @@ def test_pack_unpack_roundtrip_and_order():
     packed = O.pack_nibbles(nib)
     assert packed.tolist() == [[0x21, 0x43]]  # low nibble = even K index
     np.testing.assert_array_equal(O.unpack_nibbles(packed), nib)
+
+
+def test_bf16_round_matches_torch():
+    """The oracle's FP32 -> bf16 rounding (nearest, ties to even) against
+    torch's conversion: random magnitudes over the whole exponent range, exact
+    ties in both directions, values next to ties, signed zeros and the largest
+    finite values."""
+    rng = np.random.default_rng(4)
+    r = (rng.standard_normal(200000) * np.exp(rng.uniform(-80, 80, 200000))).astype(np.float32)
+    base = rng.integers(0, 1 << 16, 5000).astype(np.uint32) << 16
+    ties = (base | 0x8000).view(np.float32)          # exactly halfway between two bf16 values
+    near = np.concatenate([(base | 0x7FFF).view(np.float32), (base | 0x8001).view(np.float32)])
+    edge = np.float32([0.0, -0.0, 3.3895314e38, -3.3895314e38, 1e-40, -1e-40, 1.0, 1.00390625])
+    x = np.concatenate([r, ties, near, edge])
+    x = x[np.isfinite(x) & (np.abs(x) < 3.389e38)]
+    want = torch.from_numpy(x).to(torch.bfloat16).float().numpy()
+    got = O.bf16_round(x)
+    np.testing.assert_array_equal(got.view(np.uint32), want.view(np.uint32))
