@@ -67,7 +67,8 @@ def test_stored_traffic_only_for_the_source_it_was_measured_on(tmp_path, monkeyp
 
 def test_measured_peaks_and_fallback(tmp_path, monkeypatch):
     p = bench.measured_peaks()
-    assert p["source"] == "measured" and p["hbm_gbs"] > 1000 and p["bf16_tflops_sustained"] > 100
+    if os.path.exists(os.path.join(bench.ROOT, "MEASURED_PEAKS.json")):  # written per machine, not committed
+        assert p["source"] == "measured" and p["hbm_gbs"] > 1000 and p["bf16_tflops_sustained"] > 100
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     f = bench.measured_peaks()
     assert f["source"] == "fallback" and f["hbm_gbs"] == 6800.0
