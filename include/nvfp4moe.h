@@ -16,7 +16,11 @@
  *    before anything is launched; nothing is launched when a call fails.
  *    nvfp4_last_error() gives a one-line reason for the last failure on the
  *    calling thread.  Errors found on the device (a bounded wait that timed
- *    out) are recorded in a device status word, read by nvfp4_device_status().
+ *    out) are recorded in a device status word: for the calls that take a
+ *    workspace (MoE forward, calibration, shared expert) the int at byte 0 of
+ *    that workspace, cleared by the call's first kernel and read with
+ *    nvfp4_read_device_status(); for the others (nvfp4_grouped_gemm) one word
+ *    per device inside the library, read with nvfp4_device_status().
  *  - NVFP4 tensors: E2M1 values packed two per byte along K (element 2j in the
  *    low nibble of byte j), one FP8-E4M3 scale per 16 consecutive K elements,
  *    and an FP32 global scale gs per tensor or group, multiplied into the
@@ -98,8 +102,10 @@ int nvfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, int64_t
  *   - groups > NVFP4_QUANTIZE_NO_ALLOC_MAX_GROUPS is rejected with
  *     NVFP4_ERR_UNSUPPORTED before anything is launched.
  *   - The first call on a device looks up that array's device address (with
- *     the device current) and caches it; make that first call before any
- *     stream capture on the device.
+ *     the device current) and caches it with the id of the CUDA context it
+ *     belongs to; after cudaDeviceReset the next call finds a new context and
+ *     looks the address up again.  Make the first call on a device (and the
+ *     first after a reset) before any stream capture on it.
  *   - Nothing is allocated: no cudaMalloc / cudaFree, no allocating library call.
  *   - Every call on a device shares the array.  Each call rewrites every slot
  *     it reads, so no state survives from one call to the next, but calls
@@ -166,6 +172,27 @@ int nvfp4_debug_gemm_stall(const void* A, const void* SFA, const float* a_gs, co
                            int64_t N, int64_t K, void* D, int64_t ldd, int timeout_ms, void* stream);
 
 /*
+ * nvfp4_debug_mma_rate -- measurement aid: the bare block-scaled FP4 MMA
+ * stream, the ceiling the grouped GEMMs are compared with (no counterpart on
+ * the pages).  Launches `units` CTAs (shapes 0, 3) or CTA pairs (shapes 1, 2);
+ * each stages four operand sets once -- A: 128 rows x 256 FP4 from A, its B
+ * rows from B, the scale tiles from SFA / SFB, bytes taken in order (any
+ * quantizer output) -- and one thread issues iters x 4 back-to-back
+ * tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (K = 64) into one
+ * FP32 TMEM accumulator, then waits for them.  Nothing is stored.
+ *   shape 0: cta_group::1, 128 x 256 per CTA       (2*128*256*256 FLOP per iter)
+ *         1: cta_group::2, 256 x 256 per pair      (2*256*256*256 per iter)
+ *         2: cta_group::2, 256 x 128 per pair      (2*256*128*256 per iter)
+ *         3: cta_group::1, 128 x 128 per CTA       (2*128*128*256 per iter)
+ * Device buffers (16-byte aligned): A >= 64 KB, B >= 128 KB, SFA >= 8 KB,
+ * SFB >= 16 KB.  1 <= units <= 4096, 0 <= iters <= 2^21.  Time it with events
+ * around the call.
+ */
+int nvfp4_debug_mma_rate(const void* A, size_t a_bytes, const void* SFA, size_t sfa_bytes, const void* B,
+                         size_t b_bytes, const void* SFB, size_t sfb_bytes, int shape, int units, int iters,
+                         void* stream);
+
+/*
  * nvfp4_moe_forward -- the NVFP4 mixture-of-experts FFN forward
  * (vllm page: the MoE runner -- 128-row slots, multi-chunk slots "Bug 9",
  * sorted_token_ids gather, quantize_activation_nvfp4 with calibrated global
@@ -191,7 +218,7 @@ int nvfp4_debug_gemm_stall(const void* A, const void* SFA, const float* a_gs, co
  *                  batch (vllm page: the L2 scale measured on the L1 output;
  *                  cutedsl page: a BF16 L1 output when no calibrated L2 scale
  *                  exists): a2_gs[e] = 2688 / amax(h of expert e's rows), 1
- *                  when that is 0.  L1 writes h in bf16 into the workspace's y
+ *                  when that is 0.  L1 writes h in bf16 into the workspace's h
  *                  region with that amax, a quantize pass reads it back, and
  *                  the scales used are left in the workspace (calib region,
  *                  f32 at byte offset 4E).  Same results, bit for bit, as a
@@ -289,14 +316,17 @@ int nvfp4_moe_calibrate_routed(const void* hidden, const int32_t* topk_ids, cons
  * Byte offsets of the forward's intermediates inside the workspace, for
  * inspection by tests.  Sizes: cap = padded-row capacity
  * (roundup(T*top_k + 127*min(E, T*top_k), 128)); A = T*top_k assignments.
+ *   status i32 at byte 0: the call's device status word (NVFP4_OK or
+ *   NVFP4_ERR_DEVICE_TIMEOUT), cleared by the call's first kernel
  *   topk_ids i32[A], topk_w f32[A]   (token-major: index t*top_k + j)
  *   counts i32[E], offsets i32[E+1]  (padded slot starts, multiples of 128)
  *   meta i32[4] = {P (padded rows), P/128, 0, 0}
  *   tile_expert i32[cap/128], sorted_token_ids i32[cap] (-1 pad),
  *   row_weight f32[cap] (0 pad), inverse i32[A] (assignment -> row)
  *   a1 u8[cap][H/2], sfa1 u8[cap*H/16], a2 u8[cap][I/2], sfa2 u8[cap*I/16]
- *   y bf16[cap][max(H, I)] (routing-weighted L2 rows in slot order, row
- *   stride H; with a2_gs NULL first the bf16 L1 output, row stride I),
+ *   y bf16[cap][H] (routing-weighted L2 rows in slot order),
+ *   h bf16[cap][I] (with a2_gs NULL: the bf16 SwiGLU output of L1; not
+ *   written otherwise),
  *   calib u32[2E] (calibration amax bits; with a2_gs NULL, E amax words of
  *   the L1 output, then the E L2 global scales as f32)
  * Only rows < P of the row-indexed buffers are defined after a call; the
@@ -304,19 +334,43 @@ int nvfp4_moe_calibrate_routed(const void* hidden, const int32_t* topk_ids, cons
  * unspecified nibble bytes.
  */
 typedef struct {
-  size_t topk_ids, topk_w, block_counts, counts, offsets, meta, tile_expert, sorted_token_ids, row_weight,
-      inverse, a1, sfa1, a2, sfa2, y, calib, total;
+  size_t status, topk_ids, topk_w, block_counts, counts, offsets, meta, tile_expert, sorted_token_ids, row_weight,
+      inverse, a1, sfa1, a2, sfa2, y, h, calib, total;
   int64_t capacity;
   int64_t route_blocks;
 } nvfp4_moe_layout;
 int nvfp4_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int E, int top_k, nvfp4_moe_layout* out);
 
 /*
- * Device status word shared by all kernels of the library on the current
- * device: NVFP4_OK or NVFP4_ERR_DEVICE_TIMEOUT.  Synchronises the device.
- * reset != 0 clears it afterwards.
+ * Device status word of the calls without a workspace (nvfp4_grouped_gemm,
+ * nvfp4_debug_gemm_stall), one per device: NVFP4_OK or
+ * NVFP4_ERR_DEVICE_TIMEOUT.  Synchronises the device.  reset != 0 clears it
+ * afterwards.
  */
 int nvfp4_device_status(int* status_out, int reset);
+
+/*
+ * Status of the last call that used this workspace (MoE forward, routed
+ * forward, calibration or shared expert): the int at byte 0 of the
+ * workspace, NVFP4_OK or NVFP4_ERR_DEVICE_TIMEOUT.  Each such call clears the
+ * word in its first kernel, so it reports that call only, and calls on other
+ * workspaces (other streams) never touch it.  Reads it on `stream` and waits
+ * for that stream (a host synchronisation: for tests and error handling, not
+ * for the hot path); reset != 0 then clears it.  workspace: 256-byte aligned
+ * device pointer.
+ */
+int nvfp4_read_device_status(const void* workspace, void* stream, int* status_out, int reset);
+
+/*
+ * Failure-detection check of the MoE forward (no counterpart on the pages).
+ * timeout_ms > 0: every following nvfp4_moe_forward / _routed call launches
+ * its L1 GEMM with the operand loads switched off and that wait limit, so the
+ * GEMM gives up, records NVFP4_ERR_DEVICE_TIMEOUT in that call's workspace
+ * status word and returns; the rest of the forward runs on whatever the L2
+ * input buffer held (its output is meaningless, nothing faults).  0 switches
+ * it off.  Process-wide; 0 <= timeout_ms <= 10000.
+ */
+int nvfp4_moe_set_debug_stall(int timeout_ms);
 
 /* GEMM variant (process-wide; every GEMM above and the MoE forward).
  *

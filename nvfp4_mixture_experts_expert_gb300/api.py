@@ -155,6 +155,10 @@ class MoEForward:
         off = self.layout["calib"] + 4 * self.E
         return self.workspace[off:off + 4 * self.E].view(torch.float32)
 
+    def status(self, stream=None, reset=False):
+        """Device status word of the last call on this workspace (waits for the stream)."""
+        return B.nvfp4_read_device_status(self.workspace, stream, reset)
+
     def view(self, name, dtype, count):
         """A view of one intermediate of the last call (see nvfp4_moe_workspace_layout)."""
         off = self.layout[name]
@@ -170,6 +174,10 @@ class SharedExpertForward:
         self.T, self.H, self.I = T, H, I
         self.ws_bytes = max(B.nvfp4_shared_expert_workspace_size(T, H, I), 256)
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
+
+    def status(self, stream=None, reset=False):
+        """Device status word of the last call on this workspace (waits for the stream)."""
+        return B.nvfp4_read_device_status(self.workspace, stream, reset)
 
     def __call__(self, hidden, w: MoEWeights, a1_gs, a2_gs, gate_limit=10.0, up_limit=10.0, out=None, stream=None):
         if out is None:

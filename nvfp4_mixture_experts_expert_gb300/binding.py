@@ -46,8 +46,8 @@ class Nvfp4Error(RuntimeError):
 
 class MoeLayout(ctypes.Structure):
     _fields_ = [(n, c_size) for n in (
-        "topk_ids", "topk_w", "block_counts", "counts", "offsets", "meta", "tile_expert",
-        "sorted_token_ids", "row_weight", "inverse", "a1", "sfa1", "a2", "sfa2", "y", "calib", "total")] + [
+        "status", "topk_ids", "topk_w", "block_counts", "counts", "offsets", "meta", "tile_expert",
+        "sorted_token_ids", "row_weight", "inverse", "a1", "sfa1", "a2", "sfa2", "y", "h", "calib", "total")] + [
         ("capacity", c_i64), ("route_blocks", c_i64)]
 
 
@@ -93,6 +93,10 @@ _moe_calibrate_routed = _sig("nvfp4_moe_calibrate_routed", c_int, [c_ptr, c_ptr,
                                                                      c_ptr, c_float, c_float, c_ptr, c_size, c_ptr,
                                                                      c_ptr, c_ptr])
 _device_status = _sig("nvfp4_device_status", c_int, [ctypes.POINTER(c_int), c_int])
+_read_status = _sig("nvfp4_read_device_status", c_int, [c_ptr, c_ptr, ctypes.POINTER(c_int), c_int])
+_debug_stall = _sig("nvfp4_moe_set_debug_stall", c_int, [c_int])
+_mma_rate = _sig("nvfp4_debug_mma_rate", c_int, [c_ptr, c_size, c_ptr, c_size, c_ptr, c_size, c_ptr, c_size, c_int,
+                                                 c_int, c_int, c_ptr])
 _stage_events = _sig("nvfp4_moe_set_stage_events", c_int, [ctypes.POINTER(c_ptr), c_int])
 _gemm_set_cta_pair = _sig("nvfp4_gemm_set_cta_pair", c_int, [c_int, ctypes.POINTER(c_int)])
 
@@ -231,6 +235,25 @@ def nvfp4_device_status(reset=False):
     st = c_int(-1)
     _check(_device_status(ctypes.byref(st), 1 if reset else 0))
     return st.value
+
+
+def nvfp4_read_device_status(workspace, stream=None, reset=False):
+    """Status word of the last call that used this workspace (waits for `stream`)."""
+    st = c_int(-1)
+    _check(_read_status(_p(workspace), _stream(stream), ctypes.byref(st), 1 if reset else 0))
+    return st.value
+
+
+def nvfp4_moe_set_debug_stall(timeout_ms):
+    """> 0: following MoE forwards run their L1 GEMM with no operand loads (it times
+    out after timeout_ms and records the timeout in the call's workspace); 0: off."""
+    _check(_debug_stall(int(timeout_ms)))
+
+
+def nvfp4_debug_mma_rate(A, a_bytes, SFA, sfa_bytes, B, b_bytes, SFB, sfb_bytes, shape, units, iters, stream=None):
+    """The bare block-scaled FP4 MMA stream (see include/nvfp4moe.h); time it with events."""
+    _check(_mma_rate(_p(A), a_bytes, _p(SFA), sfa_bytes, _p(B), b_bytes, _p(SFB), sfb_bytes, shape, units, iters,
+                     _stream(stream)))
 
 
 def nvfp4_gemm_set_cta_pair(mode):

@@ -126,6 +126,7 @@ int64_t moe_capacity(int64_t T, int E, int k) {
 
 void* g_stage_events[8] = {};
 int g_n_stage_events = 0;
+int g_debug_stall_ms = 0;  // > 0: MoE forwards launch their L1 GEMM with no operand loads (failure-detection test)
 
 inline void stage_mark(int i, cudaStream_t s) {
   if (g_n_stage_events == 8 && g_stage_events[i]) cudaEventRecord((cudaEvent_t)g_stage_events[i], s);
@@ -295,6 +296,7 @@ int nvfp4_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int E, int top_k
     off = (size_t)round_up((int64_t)off + (bytes > 0 ? bytes : 0), 1024);
     return at;
   };
+  out->status = take(16);  // first, at byte 0: nvfp4_read_device_status finds it from the workspace pointer
   out->topk_ids = take(A * 4);
   out->topk_w = take(A * 4);
   out->block_counts = take(nb * E * 4);
@@ -309,7 +311,8 @@ int nvfp4_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int E, int top_k
   out->sfa1 = take(cap * H / 16);
   out->a2 = take(cap * I / 2);
   out->sfa2 = take(cap * I / 16);
-  out->y = take(cap * (H > I ? H : I) * 2);  // also the bf16 L1 output when L2 scales come from the batch
+  out->y = take(cap * H * 2);
+  out->h = take(cap * I * 2);  // bf16 L1 output when the L2 scales come from the batch
   out->calib = take((int64_t)2 * E * 4);
   out->total = off;
   out->capacity = cap;
@@ -378,8 +381,10 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
   uint8_t* a2 = ws + L.a2;
   uint8_t* sfa2 = ws + L.sfa2;
   uint16_t* ybuf = (uint16_t*)(ws + L.y);
+  uint16_t* hbuf = (uint16_t*)(ws + L.h);
+  int* status = (int*)(ws + L.status);
   const int64_t cap = L.capacity;
-  // No L2 scales given: L1 stores its bf16 SwiGLU output (in the y region)
+  // No L2 scales given: L1 stores its bf16 SwiGLU output (in the h region)
   // and per-expert amax, and a quantize pass derives the scales from them.
   const bool batch_l2_scale = a2_gs == nullptr;
   uint32_t* l2_amax = (uint32_t*)(ws + L.calib);
@@ -410,15 +415,19 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
   g1.q_sf = sfa2;
   g1.q_gs = a2_gs;
   if (batch_l2_scale) {
-    g1.D = ybuf;
+    g1.D = hbuf;
     g1.ldd = I;
     g1.amax_bits = l2_amax;
   }
   g1.I = (int)I;
   g1.gate_limit = gate_limit;
   g1.up_limit = up_limit;
-  g1.status = dev->status;
+  g1.status = status;
   g1.timeout_ns = 2000000000ull;
+  if (g_debug_stall_ms > 0) {
+    g1.debug_no_loads = 1;
+    g1.timeout_ns = (uint64_t)g_debug_stall_ms * 1000000ull;
+  }
 
   g2.sfa = sfa2;
   g2.sfb = (const uint8_t*)w2_sf;
@@ -438,7 +447,7 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
   g2.row_w = row_w;
   g2.H = (int)H;
   g2.pair_hint = T * top_k >= (int64_t)256 * E;  // experts average two or more m-tiles
-  g2.status = dev->status;
+  g2.status = status;
   g2.timeout_ns = 2000000000ull;
 
   const int nb = (int)L.route_blocks;
@@ -448,13 +457,14 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
     return cuda_fail(e, "amax reset");
   if (T <= kSmallRouteTokens) {  // one block: routing, offsets and slots without launch boundaries
     if ((e = launch_route_small(rt.logits, rt.topk_ids, rt.topk_w, rt.experts_start, T, E, top_k, ids, wts, counts,
-                                offsets, meta, tile_expert, sorted_ids, row_w, inverse, s)) != cudaSuccess)
+                                offsets, meta, tile_expert, sorted_ids, row_w, inverse, status, s)) != cudaSuccess)
       return cuda_fail(e, "route launch");
     stage_mark(1, s);
     stage_mark(2, s);
   } else {
-    e = rt.logits ? launch_route_topk(rt.logits, T, E, top_k, ids, wts, bcnt, s)
-                  : launch_route_external(rt.topk_ids, rt.topk_w, rt.experts_start, T, E, top_k, ids, wts, bcnt, s);
+    e = rt.logits ? launch_route_topk(rt.logits, T, E, top_k, ids, wts, bcnt, status, s)
+                  : launch_route_external(rt.topk_ids, rt.topk_w, rt.experts_start, T, E, top_k, ids, wts, bcnt,
+                                          status, s);
     if (e != cudaSuccess) return cuda_fail(e, "route launch");
     stage_mark(1, s);
     if ((e = launch_slot_scan(bcnt, nb, E, counts, offsets, meta, tile_expert, sorted_ids, row_w, nullptr, 0, s,
@@ -474,7 +484,7 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
   if ((e = launch_gemm(batch_l2_scale ? kEpiSwigluAmax : kEpiSwigluQuant, g1, (int)t1, dev->sms, s, true)) !=
       cudaSuccess)
     return cuda_fail(e, "L1 launch");
-  if (batch_l2_scale && (e = launch_slot_quantize(ybuf, I, meta, tile_expert, cap, l2_amax, E, l2_gs, a2, sfa2,
+  if (batch_l2_scale && (e = launch_slot_quantize(hbuf, I, meta, tile_expert, cap, l2_amax, E, l2_gs, a2, sfa2,
                                                   dev->sms, s, true)) != cudaSuccess)
     return cuda_fail(e, "L2 activation quantize launch");
   stage_mark(5, s);
@@ -515,7 +525,7 @@ int nvfp4_moe_forward_routed(const void* hidden, const int32_t* topk_ids, const 
 // ------------------------------------------------------------------ shared expert
 namespace {
 struct SharedExpertLayout {
-  size_t a1, sfa1, a2, sfa2, total;
+  size_t status, a1, sfa1, a2, sfa2, total;
   int64_t rows;  // T rounded up to 128
 };
 SharedExpertLayout shared_expert_layout(int64_t T, int64_t H, int64_t I) {
@@ -527,6 +537,7 @@ SharedExpertLayout shared_expert_layout(int64_t T, int64_t H, int64_t I) {
     off = (size_t)round_up((int64_t)off + bytes, 1024);
     return at;
   };
+  L.status = take(16);  // byte 0, as in the MoE forward's workspace
   L.a1 = take(L.rows * H / 2);
   L.sfa1 = take(L.rows * H / 16);
   L.a2 = take(L.rows * I / 2);
@@ -570,6 +581,7 @@ int nvfp4_shared_expert_forward(const void* hidden, int64_t T, int64_t H, int64_
   uint8_t* sfa1 = ws + L.sfa1;
   uint8_t* a2 = ws + L.a2;
   uint8_t* sfa2 = ws + L.sfa2;
+  int* status = (int*)(ws + L.status);
   GemmArgs g1, g2;
   memset(&g1, 0, sizeof(g1));
   memset(&g2, 0, sizeof(g2));
@@ -597,7 +609,7 @@ int nvfp4_shared_expert_forward(const void* hidden, int64_t T, int64_t H, int64_
   g1.I = (int)I;
   g1.gate_limit = gate_limit;
   g1.up_limit = up_limit;
-  g1.status = dev->status;
+  g1.status = status;
   g1.timeout_ns = 2000000000ull;
   // L2: one group, bf16 rows straight into out (rows >= T not stored)
   g2.sfa = sfa2;
@@ -617,11 +629,11 @@ int nvfp4_shared_expert_forward(const void* hidden, int64_t T, int64_t H, int64_
   g2.D = (uint16_t*)out;
   g2.ldd = H;
   g2.d_vec32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
-  g2.status = dev->status;
+  g2.status = status;
   g2.timeout_ns = 2000000000ull;
   cudaError_t e;
-  if ((e = launch_quantize((const uint16_t*)hidden, T, H, H, 0, 1, a1_gs, nullptr, a1, sfa1, L.rows, dev->sms, s)) !=
-      cudaSuccess)
+  if ((e = launch_quantize((const uint16_t*)hidden, T, H, H, 0, 1, a1_gs, nullptr, a1, sfa1, L.rows, dev->sms, s,
+                           status)) != cudaSuccess)
     return cuda_fail(e, "quantize launch");
   const int64_t t1 = L.rows / 128 * g1.n_tiles, t2 = L.rows / 128 * g2.n_tiles;
   if ((e = launch_gemm(kEpiSwigluQuant, g1, (int)t1, dev->sms, s, true)) != cudaSuccess)
@@ -672,10 +684,12 @@ int calibrate_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H, 
   uint8_t* a1 = ws + L.a1;
   uint8_t* sfa1 = ws + L.sfa1;
   uint32_t* amax = (uint32_t*)(ws + L.calib);
+  int* status = (int*)(ws + L.status);
   const int64_t cap = L.capacity;
   cudaError_t e;
   if (T == 0) {  // no rows: every expert gets gs 1
-    if ((e = launch_slot_scan(bcnt, 0, E, counts, offsets, meta, tile_expert, sorted_ids, row_w, amax, 2 * E, s)) !=
+    if ((e = cudaMemsetAsync(status, 0, sizeof(int), s)) != cudaSuccess ||
+        (e = launch_slot_scan(bcnt, 0, E, counts, offsets, meta, tile_expert, sorted_ids, row_w, amax, 2 * E, s)) !=
             cudaSuccess ||
         (e = launch_gs_from_amax(amax, E, a1_gs_out, s)) != cudaSuccess ||
         (e = launch_gs_from_amax(amax + E, E, a2_gs_out, s)) != cudaSuccess)
@@ -703,12 +717,12 @@ int calibrate_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H, 
   g1.gate_limit = gate_limit;
   g1.up_limit = up_limit;
   g1.amax_bits = amax + E;
-  g1.status = dev->status;
+  g1.status = status;
   g1.timeout_ns = 2000000000ull;
   const int nb = (int)L.route_blocks;
-  if ((e = rt.logits ? launch_route_topk(rt.logits, T, E, top_k, ids, wts, bcnt, s)
+  if ((e = rt.logits ? launch_route_topk(rt.logits, T, E, top_k, ids, wts, bcnt, status, s)
                      : launch_route_external(rt.topk_ids, rt.topk_w, rt.experts_start, T, E, top_k, ids, wts, bcnt,
-                                             s)) != cudaSuccess ||
+                                             status, s)) != cudaSuccess ||
       (e = launch_slot_scan(bcnt, nb, E, counts, offsets, meta, tile_expert, sorted_ids, row_w, amax, 2 * E, s)) !=
           cudaSuccess ||
       (e = launch_slot_scatter(ids, wts, T, E, top_k, bcnt, offsets, sorted_ids, row_w, inverse, s)) !=
@@ -764,6 +778,33 @@ int nvfp4_device_status(int* status_out, int reset) {
   if (int rc = device_info(&dev)) return rc;
   cudaError_t e = gemm_read_status(status_out, reset);
   return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "status read");
+}
+
+int nvfp4_read_device_status(const void* workspace, void* stream, int* status_out, int reset) {
+  g_err[0] = 0;
+  if (!workspace || !status_out) return fail(NVFP4_ERR_INVALID_ARG, "null pointer");
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(NVFP4_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  DeviceInfo* dev = nullptr;
+  if (int rc = device_info(&dev)) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && reset) {
+    e = cudaMemsetAsync(const_cast<void*>(workspace), 0, sizeof(int), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  *status_out = v;
+  return NVFP4_OK;
+}
+
+int nvfp4_moe_set_debug_stall(int timeout_ms) {
+  g_err[0] = 0;
+  if (timeout_ms < 0 || timeout_ms > 10000) return fail(NVFP4_ERR_INVALID_ARG, "timeout_ms must be in [0, 10000]");
+  g_debug_stall_ms = timeout_ms;
+  return NVFP4_OK;
 }
 
 int nvfp4_moe_set_stage_events(void* const* events, int n_events) {

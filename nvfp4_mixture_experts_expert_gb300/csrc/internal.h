@@ -31,9 +31,11 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 constexpr int kAmaxBlocksPerGroup = 128;
 cudaError_t launch_group_amax(const uint16_t* x, int64_t rows, int64_t K, int64_t ld_x, int64_t gstride_x,
                               int groups, float* partial, float* gs_out, cudaStream_t s);
+// status_reset (may be null): a per-call device status word the kernel clears
+// before anything later in the stream can record into it.
 cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, int64_t ld_x, int64_t gstride_x,
                             int groups, const float* gs, float* gs_copy, uint8_t* fp4, uint8_t* sf,
-                            int64_t rows_padded, int num_sms, cudaStream_t s);
+                            int64_t rows_padded, int num_sms, cudaStream_t s, int* status_reset = nullptr);
 cudaError_t launch_assemble_scales(const uint8_t* sf_linear, int64_t sf_cols, const int32_t* offsets,
                                    const int32_t* padded_offsets, int groups, int64_t rows_capacity,
                                    uint8_t* sf_swz, int num_sms, cudaStream_t s);
@@ -57,18 +59,21 @@ cudaError_t launch_slot_quantize(const uint16_t* h, int64_t K, const int32_t* me
 
 // ---------------------------------------------------------------- route.cu
 constexpr int kRouteTokensPerBlock = 16;
+// The routing kernels open a forward: each clears the call's device status
+// word (status_reset, may be null) before any later kernel of the call runs.
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
-                              int32_t* block_counts, cudaStream_t s);
+                              int32_t* block_counts, int* status_reset, cudaStream_t s);
 // Expert-parallel routing from given global top-k ids / weights (see route.cu).
 cudaError_t launch_route_external(const int32_t* topk_ids, const float* topk_w, int32_t start, int64_t T, int E,
-                                  int k, int32_t* ids, float* w, int32_t* block_counts, cudaStream_t s);
+                                  int k, int32_t* ids, float* w, int32_t* block_counts, int* status_reset,
+                                  cudaStream_t s);
 // Small batches: routing (logits, or external ids when logits is null),
 // offsets, tile table, pad rows and slot permutation in one block.
 constexpr int64_t kSmallRouteTokens = 256;
 cudaError_t launch_route_small(const float* logits, const int32_t* ext_ids, const float* ext_w, int32_t start,
                                int64_t T, int E, int k, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
                                int32_t* meta, int32_t* tile_expert, int32_t* sorted_ids, float* row_w,
-                               int32_t* inverse, cudaStream_t s);
+                               int32_t* inverse, int* status_reset, cudaStream_t s);
 cudaError_t launch_slot_scan(int32_t* block_counts, int nblocks, int E, int32_t* counts, int32_t* offsets,
                              int32_t* meta, int32_t* tile_expert, int32_t* sorted_ids, float* row_w,
                              uint32_t* zero_words, int n_zero_words, cudaStream_t s, bool pdl = false);

@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
                                                        int64_t ld_x, int64_t gstride_x, int groups,
                                                        const float* __restrict__ gs, float* __restrict__ gs_copy,
                                                        uint8_t* __restrict__ fp4, uint8_t* __restrict__ sf,
-                                                       int64_t rows_padded) {
+                                                       int64_t rows_padded, int* __restrict__ status_reset) {
   pdl_trigger();
   __shared__ float2 tab[128];
   if (threadIdx.x < 128) {
@@ -267,6 +267,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
   pdl_wait();  // the global scales may come from the amax kernels just before
   if (gs_copy && blockIdx.x == 0)
     for (int i = threadIdx.x; i < groups; i += blockDim.x) gs_copy[i] = gs[i];
+  if (status_reset && blockIdx.x == 0 && threadIdx.x == 0) *status_reset = 0;
   const float rcp6 = __frcp_rn(6.0f);
   const int lane = threadIdx.x & 31;
   const int64_t segs = (K + 1023) / 1024;
@@ -407,13 +408,13 @@ cudaError_t launch_group_amax(const uint16_t* x, int64_t rows, int64_t K, int64_
 
 cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, int64_t ld_x, int64_t gstride_x,
                             int groups, const float* gs, float* gs_copy, uint8_t* fp4, uint8_t* sf,
-                            int64_t rows_padded, int num_sms, cudaStream_t s) {
+                            int64_t rows_padded, int num_sms, cudaStream_t s, int* status_reset) {
   const int64_t warps = rows_padded * ((K + 1023) / 1024) * groups;
   const int grid = grid_for(warps * 32, 256, num_sms, 8);
   const bool a32 = (reinterpret_cast<uintptr_t>(x) & 31u) == 0 && ld_x % 16 == 0 && gstride_x % 16 == 0;
   auto* kernel = a32 ? quantize_kernel<true> : quantize_kernel<false>;
   return launch_kernel(kernel, dim3(grid), dim3(256), 0, s, true, x, rows, K, ld_x, gstride_x, groups, gs, gs_copy,
-                       fp4, sf, rows_padded);
+                       fp4, sf, rows_padded, status_reset);
 }
 
 cudaError_t launch_assemble_scales(const uint8_t* sf_linear, int64_t sf_cols, const int32_t* offsets,

@@ -17,7 +17,9 @@
 // next.  Calls whose kernels overlap on the GPU (different streams with no
 // ordering between them) race on the array and give wrong scales; order them
 // on one stream, or use nvfp4_quantize with a workspace of your own.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <cstdarg>
 #include <cstdio>
@@ -33,7 +35,15 @@ constexpr int kNoAllocMaxGroups = NVFP4_QUANTIZE_NO_ALLOC_MAX_GROUPS;
 static __device__ __align__(256) float g_no_alloc_amax_partials[kNoAllocMaxGroups * nvfp4::kAmaxBlocksPerGroup];
 
 constexpr int kMaxDevices = 64;
-float* g_scratch_addr[kMaxDevices] = {};
+// Per device: the scratch address and the id of the CUDA context it was
+// looked up in.  A context id is unique for the life of the process, so after
+// cudaDeviceReset (a new primary context, the module loaded again at another
+// address) the next call sees a different id and looks the address up anew.
+struct ScratchEntry {
+  float* addr = nullptr;
+  unsigned long long ctx_id = 0;
+};
+ScratchEntry g_scratch[kMaxDevices];
 std::mutex g_scratch_mu;
 
 // Failures are reported through the library's nvfp4_last_error().
@@ -49,9 +59,32 @@ int fail(int code, const char* fmt, ...) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Id of the calling thread's current CUDA context (driver entry points
+// fetched through the runtime, so the library does not link libcuda).
+int current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_current || !get_id) return fail(NVFP4_ERR_CUDA, "driver context entry points unavailable");
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return fail(NVFP4_ERR_CUDA, "no current CUDA context");
+  if (get_id(ctx, id) != CUDA_SUCCESS) return fail(NVFP4_ERR_CUDA, "cuCtxGetId failed");
+  return NVFP4_OK;
+}
+
 // Device address of the scratch array on the current device.  The symbol's
-// host-side name is only a stand-in, so the address is looked up once per
-// device (with that device current) and cached.
+// host-side name is only a stand-in, so the address is looked up with the
+// device current, once per device and context, and cached.
 int scratch_on_current_device(float** out, int* sms) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -64,15 +97,23 @@ int scratch_on_current_device(float** out, int* sms) {
     return fail(NVFP4_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
   if (major != 10 || minor != 3)
     return fail(NVFP4_ERR_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a", dev, major, minor);
+  // cudaSetDevice initialises the device's primary context and makes it
+  // current (it already is: dev is the current device), so it has an id
+  if ((e = cudaSetDevice(dev)) != cudaSuccess)
+    return fail(NVFP4_ERR_CUDA, "cudaSetDevice: %s", cudaGetErrorString(e));
+  unsigned long long ctx_id = 0;
+  if (int rc = current_context_id(&ctx_id)) return rc;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchEntry& ent = g_scratch[dev];
+  if (!ent.addr || ent.ctx_id != ctx_id) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_no_alloc_amax_partials);
     if (e != cudaSuccess || !p)
       return fail(NVFP4_ERR_CUDA, "cudaGetSymbolAddress of the scratch array: %s", cudaGetErrorString(e));
-    g_scratch_addr[dev] = static_cast<float*>(p);
+    ent.addr = static_cast<float*>(p);
+    ent.ctx_id = ctx_id;
   }
-  *out = g_scratch_addr[dev];
+  *out = ent.addr;
   return NVFP4_OK;
 }
 

@@ -104,13 +104,14 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, in
 template <int NK>
 __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
     const float* __restrict__ logits, int64_t T, int E, int k, int32_t* __restrict__ ids, float* __restrict__ w,
-    int32_t* __restrict__ block_counts) {
+    int32_t* __restrict__ block_counts, int* __restrict__ status_reset) {
   pdl_trigger();
   __shared__ int32_t hist[kMaxExperts];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   pdl_wait();  // the logits may come from the kernel just before
+  if (status_reset && blockIdx.x == 0 && threadIdx.x == 0) *status_reset = 0;
   const int64_t t0 = (int64_t)blockIdx.x * kRouteTokensPerBlock;
   const int64_t t1 = min(T, t0 + kRouteTokensPerBlock);
   for (int64_t t = t0 + warp; t < t1; t += kRouteWarps) route_token<NK>(logits, t, E, k, lane, ids, w, hist);
@@ -126,12 +127,14 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_topk_kernel(
 // as route_topk_kernel.
 __global__ void __launch_bounds__(kRouteWarps * 32) route_external_kernel(
     const int32_t* __restrict__ topk_ids, const float* __restrict__ topk_w, int32_t start, int64_t T, int E, int k,
-    int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ block_counts) {
+    int32_t* __restrict__ ids, float* __restrict__ w, int32_t* __restrict__ block_counts,
+    int* __restrict__ status_reset) {
   pdl_trigger();
   __shared__ int32_t hist[kMaxExperts];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   pdl_wait();  // the ids may come from the kernel just before
+  if (status_reset && blockIdx.x == 0 && threadIdx.x == 0) *status_reset = 0;
   const int64_t f0 = (int64_t)blockIdx.x * kRouteTokensPerBlock * k;
   const int64_t f1 = min(T, (int64_t)(blockIdx.x + 1) * kRouteTokensPerBlock) * k;
   for (int64_t f = f0 + threadIdx.x; f < f1; f += blockDim.x) {
@@ -356,7 +359,7 @@ __global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallWarps
     int32_t start, int64_t T, int E, int k, int32_t* __restrict__ ids, float* __restrict__ w,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ meta,
     int32_t* __restrict__ tile_expert, int32_t* __restrict__ sorted_ids, float* __restrict__ row_w,
-    int32_t* __restrict__ inverse) {
+    int32_t* __restrict__ inverse, int* __restrict__ status_reset) {
   pdl_trigger();
   __shared__ int32_t hist[kMaxExperts];     // this CTA's tokens' rows per expert
   __shared__ int32_t total[kMaxExperts];    // all CTAs' rows per expert
@@ -372,6 +375,7 @@ __global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallWarps
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   pdl_wait();  // the logits or ids may come from the kernel just before
+  if (status_reset && rank == 0 && threadIdx.x == 0) *status_reset = 0;
   // phase 1: routing of this CTA's tokens and their per-expert counts
   if (logits) {
     if (t0 + warp < t1)
@@ -494,32 +498,33 @@ __global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallWarps
 }  // namespace
 
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
-                              int32_t* block_counts, cudaStream_t s) {
+                              int32_t* block_counts, int* status_reset, cudaStream_t s) {
   const int64_t nb = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
   const dim3 grid((unsigned)nb), block(kRouteWarps * 32);
   auto* kernel = E <= 32 ? route_topk_kernel<1> : E <= 64 ? route_topk_kernel<2> : E <= 128 ? route_topk_kernel<4>
                                                                                             : route_topk_kernel<8>;
-  return launch_kernel(kernel, grid, block, 0, s, true, logits, T, E, k, ids, w, block_counts);
+  return launch_kernel(kernel, grid, block, 0, s, true, logits, T, E, k, ids, w, block_counts, status_reset);
 }
 
 cudaError_t launch_route_external(const int32_t* topk_ids, const float* topk_w, int32_t start, int64_t T, int E,
-                                  int k, int32_t* ids, float* w, int32_t* block_counts, cudaStream_t s) {
+                                  int k, int32_t* ids, float* w, int32_t* block_counts, int* status_reset,
+                                  cudaStream_t s) {
   const int64_t nb = (T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
   return launch_kernel(route_external_kernel, dim3((unsigned)nb), dim3(kRouteWarps * 32), 0, s, true, topk_ids, topk_w,
-                       start, T, E, k, ids, w, block_counts);
+                       start, T, E, k, ids, w, block_counts, status_reset);
 }
 
 cudaError_t launch_route_small(const float* logits, const int32_t* ext_ids, const float* ext_w, int32_t start,
                                int64_t T, int E, int k, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
                                int32_t* meta, int32_t* tile_expert, int32_t* sorted_ids, float* row_w,
-                               int32_t* inverse, cudaStream_t s) {
+                               int32_t* inverse, int* status_reset, cudaStream_t s) {
   auto* kernel = (!logits || E <= 32) ? route_small_kernel<1>
                  : E <= 64            ? route_small_kernel<2>
                  : E <= 128           ? route_small_kernel<4>
                                       : route_small_kernel<8>;
   // one cluster (the kernel's compile-time cluster shape)
   return launch_kernel(kernel, dim3(kSmallCtas), dim3(kSmallWarps * 32), 0, s, true, logits, ext_ids, ext_w, start,
-                       T, E, k, ids, w, counts, offsets, meta, tile_expert, sorted_ids, row_w, inverse);
+                       T, E, k, ids, w, counts, offsets, meta, tile_expert, sorted_ids, row_w, inverse, status_reset);
 }
 
 cudaError_t launch_slot_scan(int32_t* block_counts, int nblocks, int E, int32_t* counts, int32_t* offsets,

@@ -28,7 +28,7 @@ import numpy as np
 __all__ = [
     "f32_to_bf16_bits", "bf16_bits_to_f32", "MoEWorkload", "GemmWorkload",
     "GroupedLinearWorkload", "moe_workload", "tiny_moe", "decode_moe",
-    "prefill_moe", "dense_gemm", "grouped_linear", "gemm_workload",
+    "prefill_moe", "dense_gemm", "grouped_linear", "gemm_workload", "random_nvfp4_codes",
 ]
 
 GATE_LIMIT = 10.0
@@ -209,3 +209,15 @@ def grouped_linear(seed=0, T=2048, G=8, D=2048, R=1024, name="grouped_linear"):
     w_gs = rng.uniform(0.5, 2.0, size=G).astype(np.float32)
     return GroupedLinearWorkload(name=name, T=T, G=G, D=D, R=R, x=f32_to_bf16_bits(x),
                                  w=f32_to_bf16_bits(w), w_gs=w_gs)
+
+
+def random_nvfp4_codes(groups, rows, K, seed, scale_code_range=(0x28, 0x40)):
+    """Random NVFP4 operand codes for timing runs (the arithmetic cost of a
+    consumer does not depend on the values): E2M1 codes uniform over all 16,
+    E4M3 scale codes uniform in scale_code_range, global scales 1.
+    Returns (codes uint8 [groups, rows, K], scale codes uint8 [groups, rows, K/16],
+    global scales float32 [groups])."""
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(0, 16, size=(groups, rows, K), dtype=np.uint8)
+    scales = rng.integers(scale_code_range[0], scale_code_range[1], size=(groups, rows, K // 16), dtype=np.uint8)
+    return codes, scales, np.ones(groups, dtype=np.float32)

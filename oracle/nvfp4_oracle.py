@@ -330,13 +330,19 @@ def nvfp4_gemm(a_nib, a_s, a_gs, b_nib, b_s, b_gs):
     return (A @ B.T) / (np.float64(a_gs) * np.float64(b_gs))
 
 
-def swiglu(g, u, gate_limit, up_limit):
-    """R10, [cutedsl] SwiGLU clamp fix (the gate is clamped before the SiLU): FP64 math,
-    rounded to FP32 then to bf16 (returned as FP32 values)."""
+def swiglu_exact(g, u, gate_limit, up_limit):
+    """R10, [cutedsl] SwiGLU clamp fix (the gate is clamped before the SiLU):
+    silu(min(g, gate_limit)) * clamp(u, -up_limit, up_limit) in FP64, before
+    any rounding."""
     g = np.minimum(g, gate_limit)
     u = np.clip(u, -up_limit, up_limit)
-    h = g / (1.0 + np.exp(-g)) * u
-    return bf16_round(h.astype(np.float32))
+    return g / (1.0 + np.exp(-g)) * u
+
+
+def swiglu(g, u, gate_limit, up_limit):
+    """R10: the SwiGLU value of swiglu_exact rounded to FP32 then to bf16 (the
+    fused epilogue emits bf16 on the bridge page); returned as FP32 values."""
+    return bf16_round(swiglu_exact(g, u, gate_limit, up_limit).astype(np.float32))
 
 
 def bf16_round(x):

@@ -32,12 +32,14 @@ def test_workspace_layout_is_consistent(binding):
     T, H, I, E, k = 8192, 4096, 2048, 48, 6
     L = binding.nvfp4_moe_workspace_layout(T, H, I, E, k)
     assert L["capacity"] == 55296  # roundup(T*k + 127*E, 128)
-    order = ["topk_ids", "topk_w", "block_counts", "counts", "offsets", "meta", "tile_expert",
-             "sorted_token_ids", "row_weight", "inverse", "a1", "sfa1", "a2", "sfa2", "y", "calib"]
+    order = ["status", "topk_ids", "topk_w", "block_counts", "counts", "offsets", "meta", "tile_expert",
+             "sorted_token_ids", "row_weight", "inverse", "a1", "sfa1", "a2", "sfa2", "y", "h", "calib"]
     offs = [L[n] for n in order]
     assert offs == sorted(offs) and all(o % 1024 == 0 for o in offs)
+    assert L["status"] == 0  # the status word sits at byte 0 of the workspace
     assert L["sfa1"] - L["a1"] >= L["capacity"] * H // 2
-    assert L["calib"] - L["y"] >= L["capacity"] * H * 2
+    assert L["h"] - L["y"] >= L["capacity"] * H * 2
+    assert L["calib"] - L["h"] >= L["capacity"] * I * 2
     assert binding.nvfp4_moe_workspace_size(T, H, I, E, k) == L["total"]
 
 
@@ -137,3 +139,17 @@ def test_routed_calibration_checks_arguments_on_host(binding):
         binding.nvfp4_moe_calibrate_routed(16, 16, 16, 0, 4, 256, 128, 4, 2, 16, 16, 16, 10.0, 10.0, 256,
                                            1 << 30, None, 16, stream=0)
     assert ei.value.status == binding.NVFP4_ERR_INVALID_ARG  # outputs required
+
+
+def test_status_reader_and_debug_stall_check_arguments_on_host(binding):
+    with pytest.raises(binding.Nvfp4Error) as ei:
+        binding.nvfp4_read_device_status(None, stream=0)
+    assert ei.value.status == binding.NVFP4_ERR_INVALID_ARG
+    with pytest.raises(binding.Nvfp4Error) as ei:
+        binding.nvfp4_read_device_status(16, stream=0)  # not 256-byte aligned
+    assert ei.value.status == binding.NVFP4_ERR_INVALID_ARG
+    for bad in (-1, 10001):
+        with pytest.raises(binding.Nvfp4Error) as ei:
+            binding.nvfp4_moe_set_debug_stall(bad)
+        assert ei.value.status == binding.NVFP4_ERR_INVALID_ARG
+    binding.nvfp4_moe_set_debug_stall(0)

@@ -78,3 +78,31 @@ def test_whole_job_value_and_workload_names():
     assert bench.whole_job_throughput(8192, 4, 1.0) == pytest.approx(8192 * 4 / 1e-3)
     assert "T=8192" in bench.workload_name("prefill") and "E=48" in bench.workload_name("prefill")
     assert "T=128" in bench.workload_name("decode") and "E=32" in bench.workload_name("decode")
+
+
+@pytest.mark.parametrize("n_pieces", [1, 3, 11])
+def test_oracle_pieces_are_one_oracle_forward(n_pieces):
+    """The reference arm and the CPU baseline time the oracle's forward as
+    consecutive pieces; together they must be exactly one moe_forward call
+    (same output, bit for bit) whatever the number of pieces."""
+    import numpy as np
+    from oracle import nvfp4_oracle as O
+    from nvfp4_mixture_experts_expert_gb300 import workloads as W
+    wl = W.moe_workload(96, 256, 128, 7, 2, 3, logit_bias_std=1.0)
+    hidden = W.bf16_bits_to_f32(wl.hidden)
+    st = dict(T=wl.T, H=wl.H, I=wl.I, E=wl.E, k=wl.top_k, hidden=hidden, logits=wl.logits,
+              w13q=W.random_nvfp4_codes(wl.E, 2 * wl.I, wl.H, 5), w2q=W.random_nvfp4_codes(wl.E, wl.H, wl.I, 6),
+              a1=np.full(wl.E, O.global_scale(np.abs(hidden).max()), np.float32),
+              a2=np.full(wl.E, 200.0, np.float32))
+    times, cpu_s, out = bench.oracle_timed_pieces(st, n_pieces, warmup=2)
+    assert len(times) == n_pieces and cpu_s >= 0
+    ref = O.moe_forward(hidden, wl.logits, wl.top_k, st["w13q"], st["w2q"], st["a1"], st["a2"],
+                        bench.GATE_LIMIT, bench.UP_LIMIT)
+    np.testing.assert_array_equal(out.view(np.uint32), ref.view(np.uint32))
+
+
+def test_expert_pieces_cover_every_expert_once():
+    for E, n in [(48, 20), (48, 400), (32, 1), (5, 5)]:
+        groups = bench.expert_pieces(E, n)
+        assert len(groups) == n
+        assert sum(groups, []) == list(range(E))

@@ -671,3 +671,44 @@ def test_small_batch_forward_replays_from_a_cuda_graph():
         g.replay()
         torch.cuda.synchronize()
         np.testing.assert_array_equal(host(out.view(torch.int16)), host(ref.view(torch.int16)))
+
+
+def test_device_status_belongs_to_the_call_workspace():
+    """Two forwards on two streams, each with its own workspace.  The one on
+    stream 2 runs its L1 GEMM with the operand loads switched off (the
+    failure-detection hook): its bounded waits give up after 300 ms and record
+    the timeout in that call's workspace word only.  The forward on stream 1,
+    the library-wide word and, afterwards, a normal forward on the stalled
+    workspace all read OK; the normal results match the oracle."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api, binding as B
+    wl = W.moe_workload(300, 256, 128, 4, 2, 31)
+    orc = OracleMoE(wl)
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    hidden, logits = bf16_dev(wl.hidden), dev(wl.logits)
+    a1, a2 = dev(orc.a1_gs), dev(orc.a2_gs)
+    fa = api.MoEForward(wl.T, wl.H, wl.I, wl.E, wl.top_k)
+    fb = api.MoEForward(wl.T, wl.H, wl.I, wl.E, wl.top_k)
+    out_a = torch.empty((wl.T, wl.H), dtype=torch.bfloat16, device="cuda")
+    out_b = torch.empty_like(out_a)
+    torch.cuda.synchronize()
+    B.nvfp4_device_status(reset=True)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    B.nvfp4_moe_set_debug_stall(300)
+    try:
+        fb(hidden, logits, w, a1, a2, wl.gate_limit, wl.up_limit, out=out_b, stream=s2)
+    finally:
+        B.nvfp4_moe_set_debug_stall(0)
+    fa(hidden, logits, w, a1, a2, wl.gate_limit, wl.up_limit, out=out_a, stream=s1)
+    torch.cuda.synchronize()
+    assert fb.status(stream=s2) == B.NVFP4_ERR_DEVICE_TIMEOUT
+    assert fa.status(stream=s1) == B.NVFP4_OK
+    assert B.nvfp4_device_status() == B.NVFP4_OK
+    ref = orc.forward()[0]
+    got_a = bf16_host(out_a)
+    assert rel_frob(got_a, ref) <= 2e-2 and cosine(got_a, ref) >= 0.999
+    # the stalled workspace runs a normal forward next, with a clean status
+    fb(hidden, logits, w, a1, a2, wl.gate_limit, wl.up_limit, out=out_b, stream=s2)
+    torch.cuda.synchronize()
+    assert fb.status(stream=s2) == B.NVFP4_OK
+    np.testing.assert_array_equal(bf16_host(out_b).view(np.uint32), got_a.view(np.uint32))

@@ -23,9 +23,11 @@ def test_shared_expert_matches_oracle(T):
     wl, orc = _layer(T)
     w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
     se = api.SharedExpertForward(wl.T, wl.H, wl.I)
+    se.workspace[:4].fill_(0xFF)  # the call's first kernel clears the workspace status word
     buf = torch.full((wl.T + 3, wl.H), float("nan"), dtype=torch.bfloat16, device="cuda")
     se(bf16_dev(wl.hidden), w, dev(orc.a1_gs), dev(orc.a2_gs), wl.gate_limit, wl.up_limit, out=buf[:wl.T])
     torch.cuda.synchronize()
+    assert se.status() == 0
     got = bf16_host(buf)
     assert np.all(np.isnan(got[wl.T:]))  # only the T rows of out are written
     ref = O.shared_expert_forward(W.bf16_bits_to_f32(wl.hidden), orc.w13q, orc.w2q, orc.a1_gs[0], orc.a2_gs[0],

@@ -16,10 +16,15 @@ from helpers import bf16_dev, host
 pytestmark = pytest.mark.gpu
 
 
-def quantize_both_ways(bits, rows, K, ld_x, group_stride_x, groups, rows_padded):
+def quantize_both_ways(bits, rows, K, ld_x, group_stride_x, groups, rows_padded, x_offset_elems=0):
     import torch
     from nvfp4_mixture_experts_expert_gb300 import binding as B
     x = bf16_dev(bits)
+    if x_offset_elems:  # a view that starts x_offset_elems into a copy: only 16-byte aligned
+        buf = torch.zeros(x.numel() + x_offset_elems, dtype=torch.bfloat16, device="cuda")
+        buf[x_offset_elems:] = x.reshape(-1)
+        x = buf[x_offset_elems:]
+        assert x.data_ptr() % 32 == 16
 
     def outputs():
         return (torch.full((groups * rows_padded, K // 2), 0xAB, dtype=torch.uint8, device="cuda"),
@@ -50,6 +55,28 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point():
     for a, b in zip(got2, ref2):
         np.testing.assert_array_equal(a, b)
     assert not np.array_equal(got2[2][:3], got[2])
+
+
+def test_no_rows_gives_unit_scales_and_zero_padding():
+    """rows == 0: every group's amax reduction reads nothing (all partials 0),
+    so gs must come out as 1 and every padded row as zero bytes -- exactly what
+    the workspace entry point writes."""
+    bits = np.zeros((2, 1, 128), np.uint16)
+    got, ref = quantize_both_ways(bits, 0, 128, 128, 128, 2, 128)
+    for a, b in zip(got, ref):
+        np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(got[2], np.ones(2, np.float32))
+    assert not got[0].any() and not got[1].any()
+
+
+def test_only_16_byte_aligned_input():
+    """x starting 16 bytes past a 32-byte boundary takes the quantize kernel's
+    two-load path; results still equal the workspace entry point's."""
+    rng = np.random.default_rng(13)
+    x = W.f32_to_bf16_bits(rng.standard_normal((2, 130, 256)).astype(np.float32))
+    got, ref = quantize_both_ways(x, 130, 256, 256, 130 * 256, 2, 256, x_offset_elems=8)
+    for a, b in zip(got, ref):
+        np.testing.assert_array_equal(a, b)
 
 
 def test_rejects_more_groups_than_the_fixed_scratch_holds():
