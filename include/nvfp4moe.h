@@ -184,13 +184,20 @@ int nvfp4_debug_gemm_stall(const void* A, const void* SFA, const float* a_gs, co
  *         1: cta_group::2, 256 x 256 per pair      (2*256*256*256 per iter)
  *         2: cta_group::2, 256 x 128 per pair      (2*256*128*256 per iter)
  *         3: cta_group::1, 128 x 128 per CTA       (2*128*128*256 per iter)
+ * flags add, each on its own warps and for as long as the stream runs, one
+ * activity of the real GEMM pipeline, to see which of them slows the tensor
+ * pipe: 1 a tcgen05.commit after every 4 MMAs; 2 the scale tiles re-staged
+ * into TMEM (tcgen05.st, same values); 4 the operand sets re-copied into
+ * shared memory with bulk copies (same bytes); 8 the accumulator read with
+ * tcgen05.ld plus FP32 work; 16 a tcgen05.fence::after_thread_sync before
+ * each 4-MMA stage; 32 an mbarrier wait (already complete) before each stage.
  * Device buffers (16-byte aligned): A >= 64 KB, B >= 128 KB, SFA >= 8 KB,
- * SFB >= 16 KB.  1 <= units <= 4096, 0 <= iters <= 2^21.  Time it with events
- * around the call.
+ * SFB >= 16 KB.  1 <= units <= 4096, 0 <= iters <= 2^21, 0 <= flags <= 63.
+ * Time it with events around the call.
  */
 int nvfp4_debug_mma_rate(const void* A, size_t a_bytes, const void* SFA, size_t sfa_bytes, const void* B,
                          size_t b_bytes, const void* SFB, size_t sfb_bytes, int shape, int units, int iters,
-                         void* stream);
+                         int flags, void* stream);
 
 /*
  * nvfp4_moe_forward -- the NVFP4 mixture-of-experts FFN forward
@@ -360,6 +367,25 @@ int nvfp4_device_status(int* status_out, int reset);
  * device pointer.
  */
 int nvfp4_read_device_status(const void* workspace, void* stream, int* status_out, int reset);
+
+/*
+ * Debug timeline of the GEMM pipeline (no counterpart on the pages): every
+ * following GEMM launch with epilogue `kind` (0 bf16 output, 1 SwiGLU +
+ * requantization, 2 routing-weighted rows, 3 SwiGLU amax; 4: the
+ * nvfp4_debug_mma_rate kernel, words 5 and 6 only) writes SM-clock stamps
+ * (%clock64, cycles) of its first CTA's roles into `buffer` (device, 8-byte
+ * aligned, (stages + tiles) * 8 words): 8 words per ring stage for the first
+ * `stages` stages -- producer slot free, copies issued, scale warp saw the
+ * data, scales staged, MMA starts waiting, MMA may issue, MMA instructions
+ * issued, stage committed -- then 8 words per tile for the first `tiles`
+ * tiles -- MMA waits for the accumulator, accumulator free, epilogue saw it
+ * full, epilogue released it, epilogue finished.  Words not reached stay as
+ * they were.  buffer NULL switches it off.  Process-wide; for performance
+ * analysis only.  Kinds 0-3 need a library built with -DNVFP4_GEMM_TRACE
+ * (the recording points cost the GEMM loops even when switched off, so the
+ * default build leaves them out); otherwise NVFP4_ERR_UNSUPPORTED.
+ */
+int nvfp4_debug_gemm_trace(void* buffer, int stages, int tiles, int kind);
 
 /*
  * Failure-detection check of the MoE forward (no counterpart on the pages).

@@ -95,8 +95,9 @@ _moe_calibrate_routed = _sig("nvfp4_moe_calibrate_routed", c_int, [c_ptr, c_ptr,
 _device_status = _sig("nvfp4_device_status", c_int, [ctypes.POINTER(c_int), c_int])
 _read_status = _sig("nvfp4_read_device_status", c_int, [c_ptr, c_ptr, ctypes.POINTER(c_int), c_int])
 _debug_stall = _sig("nvfp4_moe_set_debug_stall", c_int, [c_int])
+_gemm_trace = _sig("nvfp4_debug_gemm_trace", c_int, [c_ptr, c_int, c_int, c_int])
 _mma_rate = _sig("nvfp4_debug_mma_rate", c_int, [c_ptr, c_size, c_ptr, c_size, c_ptr, c_size, c_ptr, c_size, c_int,
-                                                 c_int, c_int, c_ptr])
+                                                 c_int, c_int, c_int, c_ptr])
 _stage_events = _sig("nvfp4_moe_set_stage_events", c_int, [ctypes.POINTER(c_ptr), c_int])
 _gemm_set_cta_pair = _sig("nvfp4_gemm_set_cta_pair", c_int, [c_int, ctypes.POINTER(c_int)])
 
@@ -244,16 +245,23 @@ def nvfp4_read_device_status(workspace, stream=None, reset=False):
     return st.value
 
 
+def nvfp4_debug_gemm_trace(buffer, stages=0, tiles=0, kind=-1):
+    """Record the GEMM pipeline timeline of CTA 0 into `buffer` (int64 device tensor of
+    (stages + tiles) * 8 words) for launches of epilogue `kind`; buffer None: off."""
+    _check(_gemm_trace(_p(buffer), stages, tiles, kind))
+
+
 def nvfp4_moe_set_debug_stall(timeout_ms):
     """> 0: following MoE forwards run their L1 GEMM with no operand loads (it times
     out after timeout_ms and records the timeout in the call's workspace); 0: off."""
     _check(_debug_stall(int(timeout_ms)))
 
 
-def nvfp4_debug_mma_rate(A, a_bytes, SFA, sfa_bytes, B, b_bytes, SFB, sfb_bytes, shape, units, iters, stream=None):
+def nvfp4_debug_mma_rate(A, a_bytes, SFA, sfa_bytes, B, b_bytes, SFB, sfb_bytes, shape, units, iters, flags=0,
+                         stream=None):
     """The bare block-scaled FP4 MMA stream (see include/nvfp4moe.h); time it with events."""
     _check(_mma_rate(_p(A), a_bytes, _p(SFA), sfa_bytes, _p(B), b_bytes, _p(SFB), sfb_bytes, shape, units, iters,
-                     _stream(stream)))
+                     flags, _stream(stream)))
 
 
 def nvfp4_gemm_set_cta_pair(mode):

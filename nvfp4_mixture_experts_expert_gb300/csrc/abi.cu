@@ -800,6 +800,21 @@ int nvfp4_read_device_status(const void* workspace, void* stream, int* status_ou
   return NVFP4_OK;
 }
 
+int nvfp4_debug_gemm_trace(void* buffer, int stages, int tiles, int kind) {
+  g_err[0] = 0;
+  if (!buffer) {
+    gemm_set_trace(nullptr, 0, 0, -1);
+    return NVFP4_OK;
+  }
+  if (kind < 0 || kind > 4 || stages < 0 || tiles < 0 || (int64_t)(stages + tiles) * 8 > (int64_t)1 << 28)
+    return fail(NVFP4_ERR_INVALID_ARG, "kind must be 0..4 and the buffer at most 2^28 words");
+  if (kind < 4 && !gemm_trace_built())
+    return fail(NVFP4_ERR_UNSUPPORTED, "GEMM timelines need a build with -DNVFP4_GEMM_TRACE");
+  if (reinterpret_cast<uintptr_t>(buffer) & 7u) return fail(NVFP4_ERR_INVALID_ARG, "buffer must be 8-byte aligned");
+  gemm_set_trace(static_cast<unsigned long long*>(buffer), stages, tiles, kind);
+  return NVFP4_OK;
+}
+
 int nvfp4_moe_set_debug_stall(int timeout_ms) {
   g_err[0] = 0;
   if (timeout_ms < 0 || timeout_ms > 10000) return fail(NVFP4_ERR_INVALID_ARG, "timeout_ms must be in [0, 10000]");

@@ -149,6 +149,31 @@ constexpr size_t smem_bytes_for(int G) {
          8 * (3 * Cfg<PAIR>::STAGES + 4) + 16 + 8 * (size_t)(G + 1) + 16;
 }
 
+// Debug timeline (nvfp4_debug_gemm_trace): SM clock (%clock64) stamps of
+// CTA 0's roles, per ring stage g (count of stages since the kernel started)
+// and per tile t; off (one predicated branch) unless the host asked for it.
+//   stage words: 0 producer slot free, 1 producer copies issued, 2 scale warp
+//     saw the data, 3 scale warp staged, 4 MMA starts waiting, 5 MMA may issue,
+//     6 MMA instructions issued, 7 stage committed
+//   tile words:  0 MMA waits for the accumulator, 1 accumulator free, 2 epilogue
+//     saw it full, 3 epilogue released it, 4 epilogue finished the tile
+// Compiled in only with -DNVFP4_GEMM_TRACE: even switched off at run time the
+// checks cost the hot loops about 15 % (measured on the prefill L1 GEMM).
+#ifdef NVFP4_GEMM_TRACE
+__device__ __forceinline__ void trace_stage(const GemmArgs& p, int g, int ev) {
+  if (p.trace && blockIdx.x == 0 && g < p.trace_stages) p.trace[(int64_t)g * 8 + ev] = clock64();
+}
+__device__ __forceinline__ void trace_tile(const GemmArgs& p, int t, int ev) {
+  if (p.trace && blockIdx.x == 0 && t < p.trace_tiles)
+    p.trace[(int64_t)p.trace_stages * 8 + (int64_t)t * 8 + ev] = clock64();
+}
+constexpr bool kTraceBuild = true;
+#else
+__device__ __forceinline__ void trace_stage(const GemmArgs&, int, int) {}
+__device__ __forceinline__ void trace_tile(const GemmArgs&, int, int) {}
+constexpr bool kTraceBuild = false;
+#endif
+
 __device__ __forceinline__ int find_group(const int* off, int G, int row) {
   int lo = 0, hi = G;  // largest g in [0, G) with off[g] <= row
   while (hi - lo > 1) {
@@ -207,6 +232,7 @@ __device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total,
   for (int s = 0; s < C::STAGES; ++s) issued_parity[s] = -1;
   uint32_t stage = 0, phase = 0;
   bool ok = true;
+  int gstage = 0;  // stages issued so far (debug timeline)
   const int kt = p.K / 64;  // scale tiles per 128-row band
   if (!p.debug_no_loads) {
     for (int it = start; it < total && ok && !*abort; it += step) {
@@ -224,6 +250,7 @@ __device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total,
           ok = false;
           break;
         }
+        trace_stage(p, gstage, 0);
         uint8_t* st = L.stages + stage * C::STAGE_BYTES;
         const uint32_t bar = smem_u32(&L.full[stage]);
         mbar_arrive_expect_tx(bar, A_BYTES + C::B_BYTES + 3 * nmma * 512);
@@ -239,6 +266,7 @@ __device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total,
         bulk_load(smem_u32(sf_st + SFA_BYTES), sfb0 + kb * 2048, nmma * 512, bar);
         bulk_load(smem_u32(sf_st + SFA_BYTES + 2048), sfb1 + kb * 2048, nmma * 512, bar);
         issued_parity[stage] = (int)phase;
+        trace_stage(p, gstage++, 1);
         if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -285,6 +313,8 @@ __device__ void sf_loop(const GemmArgs& p, const SmemLayout& L, int total, int s
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
   uint32_t stage = 0, phase = 0;
+  int gstage = 0;
+  const bool tracer = kTraceBuild && warp == SF_WARP0 && lane == 0;
   for (int it = start; it < total; it += step) {
     bool ok = true;
     for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -294,6 +324,7 @@ __device__ void sf_loop(const GemmArgs& p, const SmemLayout& L, int total, int s
         ok = false;
         break;
       }
+      if (tracer) trace_stage(p, gstage, 2);
       // columns of a stage: SFA of K-steps 0-3 (4 each), then per K-step the
       // SFB tiles of B rows 0-127 and 128-255 (4 each); unused K-steps of a
       // partial last stage carry stale scales that no MMA reads
@@ -318,6 +349,8 @@ __device__ void sf_loop(const GemmArgs& p, const SmemLayout& L, int total, int s
         if (PAIR && rank) mbar_arrive_remote(mapa_shared(smem_u32(&L.sf_full[stage]), 0));
         else mbar_arrive(smem_u32(&L.sf_full[stage]));
       }
+      if (tracer) trace_stage(p, gstage, 3);
+      ++gstage;
       if (++stage == C::STAGES) {
         stage = 0;
         phase ^= 1u;
@@ -335,18 +368,24 @@ __device__ void mma_loop(const GemmArgs& p, const SmemLayout& L, int total, int 
   const uint32_t idesc = idesc_nvf4(PAIR ? 2 * BM : BM, BN);
   uint32_t stage = 0, phase = 0, acc_phase = 0;
   bool issued_any = false;
-  for (int it = start; it < total && !*abort; it += step) {
+  int gstage = 0, tile = 0;
+  const bool tr = kTraceBuild && p.trace != nullptr && blockIdx.x == 0;
+  for (int it = start; it < total && !*abort; it += step, ++tile) {
+    if (tr) trace_tile(p, tile, 0);
     if (!wait_bounded(smem_u32(L.acc_empty), acc_phase ^ 1u, abort, p.status, p.timeout_ns)) break;
+    if (tr) trace_tile(p, tile, 1);
     tc_fence_after();
     bool ok = true;
     for (int kb = 0; kb < p.num_kb; ++kb) {
       const int nmma = min(4, (p.K - kb * 256) / 64);
       // sf_full[stage] implies full[stage] (in both CTAs of a pair): the scale
       // warps waited for the stage's data first
+      if (tr) trace_stage(p, gstage, 4);
       if (!wait_bounded(smem_u32(&L.sf_full[stage]), phase, abort, p.status, p.timeout_ns)) {
         ok = false;
         break;
       }
+      if (tr) trace_stage(p, gstage, 5);
       tc_fence_after();
       const uint32_t a_s = smem_u32(L.stages + stage * C::STAGE_BYTES);
       const uint32_t b_s = a_s + A_BYTES;
@@ -358,8 +397,11 @@ __device__ void mma_loop(const GemmArgs& p, const SmemLayout& L, int total, int 
         else tc_mma_nvf4(tmem, ad, bd, idesc, sf_col + 4 * i, sf_col + 16 + 8 * i, (kb | i) != 0);
       }
       issued_any = true;
+      if (tr) trace_stage(p, gstage, 6);
       if constexpr (PAIR) tc_commit_pair_mc(smem_u32(&L.empty[stage]), 3);
       else tc_commit(smem_u32(&L.empty[stage]));
+      if (tr) trace_stage(p, gstage, 7);
+      ++gstage;
       if (++stage == C::STAGES) {
         stage = 0;
         phase ^= 1u;
@@ -433,7 +475,9 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
   // the accumulator is released on the leader's barrier (remote for the peer)
   const uint32_t acc_empty = PAIR && rank ? mapa_shared(smem_u32(L.acc_empty), 0) : smem_u32(L.acc_empty);
   uint32_t acc_phase = 0;
-  for (int it = start; it < total; it += step) {
+  const bool tracer = kTraceBuild && warp == EPI_WARP0 && lane == 0;
+  int tile = 0;
+  for (int it = start; it < total; it += step, ++tile) {
     // the tile and its per-tile parameters, loaded while the MMAs run
     const Work w = decode_work<PAIR>(L, p, it, rank);
     const int g = w.g, nt = w.nt;
@@ -452,6 +496,7 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
     if (lane == 0) ok = wait_bounded_backoff(smem_u32(L.acc_full), acc_phase, abort, p.status, p.timeout_ns, 200);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) break;
+    if (tracer) trace_tile(p, tile, 2);
     __syncwarp();
     tc_fence_after();
     // SwiGLU kinds: gate columns [half*64, +64) and up columns 128 + [half*64, +64);
@@ -472,6 +517,7 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
       else mbar_arrive(acc_empty);
     }
     acc_phase ^= 1u;
+    if (tracer) trace_tile(p, tile, 3);
 
     if (!w.valid) continue;  // the pair's second tile does not exist: nothing to store
     const float alpha = 1.0f / (gs_a * gs_b);
@@ -617,6 +663,7 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
         }
       }
     }
+    if (tracer) trace_tile(p, tile, 4);
   }
   if constexpr (PAIR && EPI == kEpiCombine) {
     if (lane == 0) bulk_wait_all();  // the warp's bulk stores are complete before its CTA exits
@@ -837,8 +884,33 @@ int gemm_set_pair_mode(int mode) {
   return prev;
 }
 
-cudaError_t launch_gemm(int kind, const GemmArgs& args, int units_upper, int num_sms, cudaStream_t s, bool pdl) {
-  if (args.G < 1 || args.G > MAX_GROUPS) return cudaErrorInvalidValue;
+namespace {
+unsigned long long* g_trace_buf = nullptr;
+int g_trace_stages = 0, g_trace_tiles = 0, g_trace_kind = -1;
+}  // namespace
+
+bool gemm_trace_built() { return kTraceBuild; }
+
+void gemm_set_trace(unsigned long long* buf, int stages, int tiles, int kind) {
+  g_trace_buf = buf;
+  g_trace_stages = stages;
+  g_trace_tiles = tiles;
+  g_trace_kind = buf ? kind : -1;
+}
+void gemm_get_trace(unsigned long long** buf, int* stages, int* kind) {
+  *buf = g_trace_buf;
+  *stages = g_trace_stages;
+  *kind = g_trace_kind;
+}
+
+cudaError_t launch_gemm(int kind, const GemmArgs& args_in, int units_upper, int num_sms, cudaStream_t s, bool pdl) {
+  if (args_in.G < 1 || args_in.G > MAX_GROUPS) return cudaErrorInvalidValue;
+  GemmArgs args = args_in;
+  if (kind == g_trace_kind) {
+    args.trace = g_trace_buf;
+    args.trace_stages = g_trace_stages;
+    args.trace_tiles = g_trace_tiles;
+  }
   switch (kind) {
     case kEpiBf16: return launch_kind<kEpiBf16>(args, units_upper, num_sms, s, pdl);
     case kEpiSwigluQuant: return launch_kind<kEpiSwigluQuant>(args, units_upper, num_sms, s, pdl);

@@ -135,6 +135,11 @@ struct GemmArgs {
   int* status;
   unsigned long long timeout_ns;
   int debug_no_loads;  // test hook: the producer issues nothing, so consumers time out
+  // optional timeline of CTA 0 (nvfp4_debug_gemm_trace): 8 words per ring
+  // stage for trace_stages stages, then 8 words per tile for trace_tiles tiles
+  unsigned long long* trace;
+  int trace_stages;
+  int trace_tiles;
 };
 
 size_t gemm_smem_bytes(int G);
@@ -152,6 +157,11 @@ cudaError_t launch_gemm(int kind, const GemmArgs& args, int units_upper, int num
 // mode.
 bool gemm_pair_enabled(int kind, bool hint);
 int gemm_set_pair_mode(int mode);
+// Debug timeline of the next GEMM launches of epilogue kind `kind` (-1: off;
+// 4: the MMA-rate kernel).
+void gemm_set_trace(unsigned long long* buf, int stages, int tiles, int kind);
+bool gemm_trace_built();  // the GEMM kernels were compiled with NVFP4_GEMM_TRACE
+void gemm_get_trace(unsigned long long** buf, int* stages, int* kind);
 cudaError_t gemm_status_ptr(int** ptr);
 cudaError_t gemm_read_status(int* out, int reset);
 

@@ -61,9 +61,46 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of a barrier phase (no suspend): true once the phase of
+// `parity` has completed.  Used to look ahead without stalling the caller.
+__device__ __forceinline__ uint32_t mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok;
+}
+
+// try_wait with a suspend-time hint: a thread whose phase has not completed
+// sleeps until it completes (or the hint elapses) instead of re-polling the
+// barrier, leaving the shared-memory barrier path to the threads that work.
+template <bool kCluster = false>
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  if constexpr (kCluster) {
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, "
+        "0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+  }
+  return ok != 0;
+}
+
 // Wait for the phase of `parity` to complete.  Gives up when *abort is set by
 // another role, or after timeout_ns, in which case it sets *abort and the
-// device status word and returns false.  Never spins unboundedly.
+// device status word and returns false.  Never spins unboundedly: between
+// checks of the abort flag and the clock the thread sleeps in the barrier
+// (each try at most 20 us).
 // kCluster: acquire at cluster scope (the phase was completed by arrivals
 // from the peer CTA of a cluster pair).
 template <bool kCluster = false>
@@ -74,7 +111,27 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait<kCluster>(bar, parity)) return true;
+      if (mbar_try_wait_sleep<kCluster>(bar, parity, 20000u)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      *abort = 1;
+      if (status) atomicExch(status, 6 /* NVFP4_ERR_DEVICE_TIMEOUT */);
+      return false;
+    }
+  }
+}
+
+// wait_bounded for a waiter on the critical path: it polls with the
+// non-blocking test (no suspend, so it resumes the moment the phase
+// completes); one lane per warp should call it.  Same give-up rules.
+__device__ __forceinline__ bool wait_bounded_spin(uint32_t bar, uint32_t parity, volatile int* abort, int* status,
+                                                  uint64_t timeout_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_test_wait(bar, parity)) return true;
     if (*abort) return false;
     if (global_timer_ns() - t0 > timeout_ns) {
       *abort = 1;
@@ -141,6 +198,17 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// One lane of the (converged) warp: true for exactly one thread.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n.reg .pred p;\n.reg .b32 r;\nelect.sync r|p, 0xffffffff;\nselp.u32 %0, 1, 0, p;\n}"
+      : "=r"(pred)
+      :
+      : "memory");
+  return pred != 0;
 }
 
 // ------------------------------------------------------------------ clusters
@@ -253,6 +321,19 @@ __device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t a_desc, ui
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
+// Shared memory -> TMEM copy of one 512-byte scale tile (32 lines of 16
+// bytes, contiguous) into 4 columns of the issuing CTA's TMEM, every line
+// written to the same lane of each of the four 32-lane quarters -- the
+// block-scaled MMA's scale layout.  Ordered with later tcgen05.mma of the
+// same thread (both run in the tensor pipe).  sdesc: shared memory
+// descriptor of the tile (no swizzle, 8-line groups 128 bytes apart).
+__device__ __forceinline__ void tc_cp_scale_tile(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void tc_cp_scale_tile_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // One 32-byte global store (the address must be 32-byte aligned): a whole
 // L2 sector per lane instead of two half-sector requests.
 __device__ __forceinline__ void st_global_v8(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t e,
