@@ -16,11 +16,14 @@
 //                    scales taken from the batch, cutedsl page's BF16 L1 output)
 //
 // Design (persistent over output tiles, warp-specialised, one CTA per SM):
-//   warp 0   TMA producer: per K-stage of 256 elements, the A box (128 rows x
-//            128 bytes), the B box(es) (SWIZZLE_128B) and the matching 512-byte
-//            scale tiles (plain bulk copies), into a shared-memory ring.
+//   warp 0   operand producer: per K-stage of 256 elements, the A box (128
+//            rows x 128 bytes) and the B box(es) (SWIZZLE_128B) by TMA, into
+//            an operand ring.
+//   warp 2   scale producer: the stage's 512-byte scale tiles (plain bulk
+//            copies) into a scale ring of their own.
 //   warp 1   TMEM allocator and MMA issuer: 4 MMAs of K=64 per stage into a
-//            128-lane x 256-column FP32 accumulator in TMEM.
+//            128-lane x 256-column FP32 accumulator in TMEM, issued by one
+//            elected lane from a warp-uniform loop.
 //   warps 4-11 epilogue: each warp owns the 32 TMEM lanes of its quarter
 //            (warp % 4), i.e. 32 output rows, and one half of the tile's
 //            columns; it reads the accumulator with tcgen05.ld.
@@ -29,12 +32,14 @@
 //   Registers are re-balanced per warpgroup with setmaxnreg (the epilogue
 //   holds a 128-column accumulator row per thread).
 // Two variants:
-//   single   one CTA computes a 128 x 256 tile; 4-stage ring of 54 KB stages.
+//   single   one CTA computes a 128 x 256 tile; 4-stage operand ring of 48 KB
+//            stages, 4-slot scale ring of 6 KB.
 //   pair     a cluster of two CTAs on two SMs computes a 256 x 256 tile with
 //            tcgen05 cta_group::2: each CTA holds 128 rows of A and one
 //            128-row half of the B tile (the gate or up half for SwiGLU) plus
 //            all of the stage's scale tiles, so an SM reads 8 KB of operands
-//            per 128x256x64 MMA instead of 12 KB; 5-stage ring of 38 KB stages.
+//            per 128x256x64 MMA instead of 12 KB; 5-stage operand ring of
+//            32 KB stages, 5-slot scale ring of 6 KB.
 //            The leader CTA (rank 0) issues the MMAs; its commits are
 //            multicast to both CTAs' barriers.  The peer's scale warps arrive
 //            on the leader's sf_full (its operands have landed and its scales
@@ -49,6 +54,14 @@
 // in-register.  Work units (m-tiles or m-tile pairs) are ordered unit major,
 // n-tile minor (n-major is available); units map to groups through the
 // 128-aligned group offsets read from device memory (no host sync).
+// What bounds this pipeline was measured (a scratch copy with per-role
+// timelines, and the bare MMA stream of nvfp4_debug_mma_rate with each
+// pipeline activity added in turn): one thread issues every MMA and the
+// tensor pipe queues few, so the issuing loop is warp-uniform and short; a
+// stage's chain of hand-offs (slot freed by the MMA commit -> copies ->
+// scale staging -> MMA) must fit in the ring, so the scale warps stage from a
+// ring of their own as soon as the TMEM columns are free, and the waits on
+// that chain poll instead of suspending.
 // Every mbarrier wait is bounded (timeout -> device status word, abort, drain
 // of copies/MMAs in flight, TMEM freed, return); in the pair variant every
 // CTA runs to the final cluster barrier before the collective TMEM release,
@@ -76,7 +89,8 @@ constexpr int TMEM_COLS = 512;
 constexpr int SF_COL0 = 256;         // scale columns start after the accumulator
 constexpr int SF_COLS_PER_STAGE = 48;  // 4 x (4 SFA + 8 SFB)
 // Warp roles, by warpgroup (setmaxnreg re-balances registers per warpgroup):
-//   WG0  warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer (warps 2-3 idle)
+//   WG0  warp 0 operand producer, warp 1 TMEM allocator + MMA issuer, warp 2
+//        scale producer (warp 3 idle)
 //   WG1-2 warps 4-11 epilogue: two per TMEM lane quarter, each owning half of the columns
 //   WG3  warps 12-15 scale staging: one per TMEM lane quarter
 constexpr int EPI_WARP0 = 4;
@@ -96,7 +110,9 @@ template <bool PAIR>
 struct Cfg {
   static constexpr int STAGES = PAIR ? 5 : 4;
   static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK_BYTES;  // B rows this CTA loads per stage
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // operand ring slot (A and this CTA's B rows)
+  static constexpr int SF_STAGES = STAGES;                // scale ring slots (its own ring, see sf_loop)
+  static constexpr int SF_SLOT_BYTES = SFA_BYTES + SFB_BYTES;
   static constexpr int EPI_BYTES = PAIR ? NUM_EPI_WARPS * EPI_STAGE_BYTES : 0;
   static_assert(SF_COL0 + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
@@ -109,12 +125,15 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
 
 struct SmemLayout {
   uint8_t* stages;
+  uint8_t* sf_slots;   // scale ring: SF_STAGES slots of the stage's 512-byte scale tiles
   uint8_t* epi_stage;  // pair variant: per-warp output staging for coalesced stores
   uint64_t* full;
   uint64_t* empty;
   uint64_t* acc_full;
   uint64_t* acc_empty;
   uint64_t* drain;
+  uint64_t* sf_data;     // [SF_STAGES] a scale slot has landed in shared memory
+  uint64_t* sf_empty;    // [SF_STAGES] the scale warps have read a scale slot
   uint64_t* sf_full;     // [STAGES] scale tiles of a stage are in TMEM
   uint32_t* tmem_slot;
   int* abort_flag;
@@ -128,11 +147,14 @@ __device__ __forceinline__ SmemLayout carve(uint8_t* raw, int G) {
   SmemLayout L;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
   L.stages = base;
-  L.epi_stage = base + C::STAGES * C::STAGE_BYTES;
+  L.sf_slots = base + C::STAGES * C::STAGE_BYTES;
+  L.epi_stage = L.sf_slots + C::SF_STAGES * C::SF_SLOT_BYTES;
   uint8_t* p = L.epi_stage + C::EPI_BYTES;
   L.full = reinterpret_cast<uint64_t*>(p);
   L.empty = L.full + C::STAGES;
-  L.sf_full = L.empty + C::STAGES;
+  L.sf_data = L.empty + C::STAGES;
+  L.sf_empty = L.sf_data + C::SF_STAGES;
+  L.sf_full = L.sf_empty + C::SF_STAGES;
   L.acc_full = L.sf_full + C::STAGES;
   L.acc_empty = L.acc_full + 1;
   L.drain = L.acc_empty + 1;
@@ -145,8 +167,9 @@ __device__ __forceinline__ SmemLayout carve(uint8_t* raw, int G) {
 
 template <bool PAIR>
 constexpr size_t smem_bytes_for(int G) {
-  return 1024 + (size_t)Cfg<PAIR>::STAGES * Cfg<PAIR>::STAGE_BYTES + Cfg<PAIR>::EPI_BYTES +
-         8 * (3 * Cfg<PAIR>::STAGES + 4) + 16 + 8 * (size_t)(G + 1) + 16;
+  return 1024 + (size_t)Cfg<PAIR>::STAGES * Cfg<PAIR>::STAGE_BYTES +
+         (size_t)Cfg<PAIR>::SF_STAGES * Cfg<PAIR>::SF_SLOT_BYTES + Cfg<PAIR>::EPI_BYTES +
+         8 * (3 * Cfg<PAIR>::STAGES + 2 * Cfg<PAIR>::SF_STAGES + 4) + 16 + 8 * (size_t)(G + 1) + 16;
 }
 
 // Debug timeline (nvfp4_debug_gemm_trace): SM clock (%clock64) stamps of
@@ -220,53 +243,94 @@ __device__ __forceinline__ Work decode_work(const SmemLayout& L, const GemmArgs&
   return w;
 }
 
-// ------------------------------------------------------------------ producer
+// ------------------------------------------------------------------ producers
 // Work items it = start, start + step, ... (step = CTAs, or CTA pairs).
-template <bool PAIR>
+// Two producer warps: SCALES == false copies a stage's A and B boxes with TMA
+// into the operand ring once the MMAs that read the slot have committed
+// (empty); SCALES == true copies the stage's 512-byte scale tiles with bulk
+// copies into the scale ring once the scale warps have read the slot
+// (sf_empty), so it runs ahead.  Each runs on its whole warp: addresses are
+// warp-uniform and one elected lane issues; lane 0 polls the barriers.  The
+// parity each slot was last issued with is kept in registers (a bitmask),
+// for the drain after an abort.
+template <bool PAIR, bool SCALES>
 __device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total, int start, int step,
                               uint32_t rank) {
   using C = Cfg<PAIR>;
+  constexpr int kSlots = SCALES ? C::SF_STAGES : C::STAGES;
+  constexpr uint32_t kSlotBytes = SCALES ? C::SF_SLOT_BYTES : C::STAGE_BYTES;
   volatile int* abort = L.abort_flag;
-  int issued_parity[C::STAGES];
-#pragma unroll
-  for (int s = 0; s < C::STAGES; ++s) issued_parity[s] = -1;
+  const int lane = threadIdx.x & 31;
+  const bool leader = elect_one();
+  uint32_t issued = 0, issued_parity = 0;  // bit s: slot s issued at least once / with parity 1
   uint32_t stage = 0, phase = 0;
-  bool ok = true;
+  int ok = 1;
   int gstage = 0;  // stages issued so far (debug timeline)
+  const bool tr = kTraceBuild && !SCALES && leader;
   const int kt = p.K / 64;  // scale tiles per 128-row band
+  const uint32_t empty0 = smem_u32(SCALES ? L.sf_empty : L.empty);
+  const uint32_t done0 = smem_u32(SCALES ? L.sf_data : L.full);
+  const uint32_t slot0 = smem_u32(SCALES ? L.sf_slots : L.stages);
   if (!p.debug_no_loads) {
     for (int it = start; it < total && ok && !*abort; it += step) {
       const Work w = decode_work<PAIR>(L, p, it, rank);
       const int b_r0 = w.nt * p.b_tile_stride;
       const int b_r1 = b_r0 + p.b_second_offset;
-      const int64_t b_row0 = (int64_t)w.g * p.b_rows_per_group + b_r0;
-      const int64_t b_row1 = (int64_t)w.g * p.b_rows_per_group + b_r1;
+      const int32_t a_row = w.mt * BM;
+      const int32_t b_row0 = w.g * p.b_rows_per_group + b_r0;
+      const int32_t b_row1 = w.g * p.b_rows_per_group + b_r1;
       const uint8_t* sfa = p.sfa + (int64_t)w.mt * kt * 512;
       const uint8_t* sfb0 = p.sfb + w.g * p.sfb_group_bytes + (int64_t)(b_r0 >> 7) * kt * 512;
       const uint8_t* sfb1 = p.sfb + w.g * p.sfb_group_bytes + (int64_t)(b_r1 >> 7) * kt * 512;
       for (int kb = 0; kb < p.num_kb; ++kb) {
-        const int nmma = min(4, (p.K - kb * 256) / 64);
-        if (!wait_bounded(smem_u32(&L.empty[stage]), phase ^ 1u, abort, p.status, p.timeout_ns)) {
-          ok = false;
-          break;
+        if (lane == 0) ok = wait_bounded_spin(empty0 + 8 * stage, phase ^ 1u, abort, p.status, p.timeout_ns);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (tr) trace_stage(p, gstage, 0);
+        const uint32_t st = slot0 + stage * kSlotBytes;
+        const uint32_t bar = done0 + 8 * stage;
+        if (leader) {
+          if constexpr (SCALES) {
+            const uint32_t bytes = (uint32_t)min(4, (p.K - kb * 256) / 64) * 512;
+            mbar_arrive_expect_tx(bar, 3 * bytes);
+            bulk_load(st, sfa + kb * 2048, bytes, bar);
+            bulk_load(st + SFA_BYTES, sfb0 + kb * 2048, bytes, bar);
+            bulk_load(st + SFA_BYTES + 2048, sfb1 + kb * 2048, bytes, bar);
+          } else {
+            mbar_arrive_expect_tx(bar, A_BYTES + C::B_BYTES);
+            tma_load_2d(st, &p.tmap_a, kb * BK_BYTES, a_row, bar);
+            if constexpr (PAIR) {  // this CTA's half of the B tile
+              tma_load_2d(st + A_BYTES, &p.tmap_b, kb * BK_BYTES, rank ? b_row1 : b_row0, bar);
+            } else {
+              tma_load_2d(st + A_BYTES, &p.tmap_b, kb * BK_BYTES, b_row0, bar);
+              tma_load_2d(st + A_BYTES + C::B_BYTES / 2, &p.tmap_b, kb * BK_BYTES, b_row1, bar);
+            }
+          }
         }
-        trace_stage(p, gstage, 0);
-        uint8_t* st = L.stages + stage * C::STAGE_BYTES;
-        const uint32_t bar = smem_u32(&L.full[stage]);
-        mbar_arrive_expect_tx(bar, A_BYTES + C::B_BYTES + 3 * nmma * 512);
-        tma_load_2d(smem_u32(st), &p.tmap_a, kb * BK_BYTES, w.mt * BM, bar);
-        if constexpr (PAIR) {  // this CTA's half of the B tile
-          tma_load_2d(smem_u32(st + A_BYTES), &p.tmap_b, kb * BK_BYTES, (int32_t)(rank ? b_row1 : b_row0), bar);
-        } else {
-          tma_load_2d(smem_u32(st + A_BYTES), &p.tmap_b, kb * BK_BYTES, (int32_t)b_row0, bar);
-          tma_load_2d(smem_u32(st + A_BYTES + C::B_BYTES / 2), &p.tmap_b, kb * BK_BYTES, (int32_t)b_row1, bar);
+        __syncwarp();
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (tr) trace_stage(p, gstage, 1);
+        ++gstage;
+        if (++stage == kSlots) {
+          stage = 0;
+          phase ^= 1u;
         }
-        uint8_t* sf_st = st + A_BYTES + C::B_BYTES;
-        bulk_load(smem_u32(sf_st), sfa + kb * 2048, nmma * 512, bar);
-        bulk_load(smem_u32(sf_st + SFA_BYTES), sfb0 + kb * 2048, nmma * 512, bar);
-        bulk_load(smem_u32(sf_st + SFA_BYTES + 2048), sfb1 + kb * 2048, nmma * 512, bar);
-        issued_parity[stage] = (int)phase;
-        trace_stage(p, gstage++, 1);
+      }
+    }
+  }
+  if (lane == 0) {
+    if (*abort || !ok) {  // let copies already issued land before the CTA exits
+#pragma unroll
+      for (int s = 0; s < kSlots; ++s)
+        if (issued & (1u << s)) {
+          volatile int no_abort = 0;
+          wait_bounded(done0 + 8 * s, (issued_parity >> s) & 1u, &no_abort, nullptr, p.timeout_ns);
+        }
+    } else if constexpr (PAIR && !SCALES) {
+      // the leader's last multicast releases land in this CTA before it may exit
+      for (int i = 0; i < C::STAGES; ++i) {
+        if (!wait_bounded(empty0 + 8 * stage, phase ^ 1u, abort, p.status, p.timeout_ns)) break;
         if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -274,23 +338,7 @@ __device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total,
       }
     }
   }
-  if (*abort || !ok) {  // let copies already issued land before the CTA exits
-#pragma unroll
-    for (int s = 0; s < C::STAGES; ++s)
-      if (issued_parity[s] >= 0) {
-        volatile int no_abort = 0;
-        wait_bounded(smem_u32(&L.full[s]), (uint32_t)issued_parity[s], &no_abort, nullptr, p.timeout_ns);
-      }
-  } else if constexpr (PAIR) {
-    // the leader's last multicast releases land in this CTA before it may exit
-    for (int i = 0; i < C::STAGES; ++i) {
-      if (!wait_bounded(smem_u32(&L.empty[stage]), phase ^ 1u, abort, p.status, p.timeout_ns)) break;
-      if (++stage == C::STAGES) {
-        stage = 0;
-        phase ^= 1u;
-      }
-    }
-  }
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ scale staging
@@ -300,11 +348,15 @@ __device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total,
 // lane 32q + l, 4 columns per tile -- the layout the block-scaled MMA reads
 // (each quarter holds the same 32 lines; SFB tiles cover all N rows).  Two
 // store instructions per warp per stage replace 12 tcgen05.cp copies, which
-// would queue in the tensor pipe ahead of the MMAs.  A stage's columns are
-// rewritten only after its shared-memory slot was refilled, i.e. after the
-// MMAs that read them committed.  sf_full[stage] counts the 4 warps (8 in the
-// pair variant: the peer's warps arrive on the leader's barrier, which also
-// tells the leader that the peer's operands have landed).
+// would occupy the tensor pipe ahead of the MMAs.
+// The scale tiles come through their own shared-memory ring: a warp reads a
+// slot into registers and frees it (sf_empty), so the scale producer runs
+// ahead.  A stage's TMEM columns are rewritten once the MMAs that read them
+// have committed (empty[stage]); the stores (a few hundred cycles) run while
+// the stage's operands are still in flight.  sf_full[stage] tells the MMA
+// issuer the scales are in TMEM; it counts the 4 warps (8 in the pair variant:
+// the peer's warps arrive on the leader's barrier, and only after their CTA's
+// operands landed, which the leader cannot see otherwise).
 template <bool PAIR>
 __device__ void sf_loop(const GemmArgs& p, const SmemLayout& L, int total, int start, int step, uint32_t tmem,
                         uint32_t rank) {
@@ -312,23 +364,19 @@ __device__ void sf_loop(const GemmArgs& p, const SmemLayout& L, int total, int s
   volatile int* abort = L.abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-  uint32_t stage = 0, phase = 0;
+  uint32_t stage = 0, phase = 0;  // operand / TMEM stage
+  uint32_t slot = 0, sphase = 0;  // scale ring slot
   int gstage = 0;
   const bool tracer = kTraceBuild && warp == SF_WARP0 && lane == 0;
   for (int it = start; it < total; it += step) {
-    bool ok = true;
+    int ok = 1;
     for (int kb = 0; kb < p.num_kb; ++kb) {
-      int landed = 1;
-      if (lane == 0) landed = wait_bounded(smem_u32(&L.full[stage]), phase, abort, p.status, p.timeout_ns);
-      if (!__shfl_sync(0xffffffffu, landed, 0)) {
-        ok = false;
-        break;
-      }
-      if (tracer) trace_stage(p, gstage, 2);
+      if (lane == 0) ok = wait_bounded_spin(smem_u32(&L.sf_data[slot]), sphase, abort, p.status, p.timeout_ns);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       // columns of a stage: SFA of K-steps 0-3 (4 each), then per K-step the
       // SFB tiles of B rows 0-127 and 128-255 (4 each); unused K-steps of a
       // partial last stage carry stale scales that no MMA reads
-      const uint8_t* sf = L.stages + stage * C::STAGE_BYTES + A_BYTES + C::B_BYTES + 16 * lane;
+      const uint8_t* sf = L.sf_slots + slot * C::SF_SLOT_BYTES + 16 * lane;
       uint32_t r[48];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -339,12 +387,22 @@ __device__ void sf_loop(const GemmArgs& p, const SmemLayout& L, int total, int s
         r[16 + 8 * i + 0] = b0.x, r[16 + 8 * i + 1] = b0.y, r[16 + 8 * i + 2] = b0.z, r[16 + 8 * i + 3] = b0.w;
         r[16 + 8 * i + 4] = b1.x, r[16 + 8 * i + 5] = b1.y, r[16 + 8 * i + 6] = b1.z, r[16 + 8 * i + 7] = b1.w;
       }
+      if (tracer) trace_stage(p, gstage, 2);
+      // the stage's TMEM scale columns are free once its previous MMAs committed
+      if (lane == 0) ok = wait_bounded_spin(smem_u32(&L.empty[stage]), phase ^ 1u, abort, p.status, p.timeout_ns);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      tc_fence_after();
       const uint32_t col = t_lane + SF_COL0 + stage * SF_COLS_PER_STAGE;
       tmem_store_32(col, r);
       tmem_store_16_hi(col + 32, r);
+      __syncwarp();  // every lane's reads of the slot are done (its registers went to the stores)
+      if (lane == 0) mbar_arrive(smem_u32(&L.sf_empty[slot]));
       tmem_store_wait();
       tc_fence_before();
-      __syncwarp();
+      if constexpr (PAIR) {
+        if (lane == 0) ok = wait_bounded_spin(smem_u32(&L.full[stage]), phase, abort, p.status, p.timeout_ns);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
       if (lane == 0) {
         if (PAIR && rank) mbar_arrive_remote(mapa_shared(smem_u32(&L.sf_full[stage]), 0));
         else mbar_arrive(smem_u32(&L.sf_full[stage]));
@@ -355,68 +413,143 @@ __device__ void sf_loop(const GemmArgs& p, const SmemLayout& L, int total, int s
         stage = 0;
         phase ^= 1u;
       }
+      if (++slot == C::SF_STAGES) {
+        slot = 0;
+        sphase ^= 1u;
+      }
     }
-    if (!ok) break;
+    if (!__shfl_sync(0xffffffffu, ok, 0)) break;
   }
 }
 
 // ------------------------------------------------------------------ MMA issuer
+// One thread issues every MMA of the CTA (or CTA pair), and the tensor pipe
+// queues few of them: a cycle spent elsewhere is a cycle the pipe may idle.
+// The loop therefore runs on the whole warp, so that every operand (slot
+// descriptors built once -- a slot adds STAGE_BYTES, a K-step 32 bytes, in
+// the 16-byte units of the start-address field -- TMEM addresses, stage and
+// phase) is warp-uniform, and one elected lane issues the MMAs and commits
+// (a commit tracks the MMAs of the thread that issues it).  A full stage's 4
+// MMAs are unrolled, and the next stage's barriers are tested without
+// blocking while this stage's MMAs issue; lane 0 polls when they were not
+// ready.  A stage may issue once its scales are in TMEM (sf_full) and, in
+// the single variant, its operands have landed (full; in the pair variant
+// sf_full says so).
+template <bool PAIR>
+__device__ __forceinline__ void issue_stage(uint32_t tmem, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t sf_col,
+                                            uint32_t first_acc, int nmma, bool full, uint32_t next_bar,
+                                            uint32_t next_bar2, uint32_t next_parity, uint32_t& next_ready) {
+  uint32_t r1 = 1u, r2 = 1u;
+  if (full) {
+    if constexpr (PAIR) {
+      tc_mma_nvf4_pair(tmem, ad, bd, idesc, sf_col, sf_col + 16, first_acc);
+      if (next_bar) r1 = mbar_test_wait(next_bar, next_parity);
+      tc_mma_nvf4_pair(tmem, ad + 2, bd + 2, idesc, sf_col + 4, sf_col + 24, 1u);
+      if (next_bar2) r2 = mbar_test_wait(next_bar2, next_parity);
+      tc_mma_nvf4_pair(tmem, ad + 4, bd + 4, idesc, sf_col + 8, sf_col + 32, 1u);
+      tc_mma_nvf4_pair(tmem, ad + 6, bd + 6, idesc, sf_col + 12, sf_col + 40, 1u);
+    } else {
+      tc_mma_nvf4(tmem, ad, bd, idesc, sf_col, sf_col + 16, first_acc);
+      if (next_bar) r1 = mbar_test_wait(next_bar, next_parity);
+      tc_mma_nvf4(tmem, ad + 2, bd + 2, idesc, sf_col + 4, sf_col + 24, 1u);
+      if (next_bar2) r2 = mbar_test_wait(next_bar2, next_parity);
+      tc_mma_nvf4(tmem, ad + 4, bd + 4, idesc, sf_col + 8, sf_col + 32, 1u);
+      tc_mma_nvf4(tmem, ad + 6, bd + 6, idesc, sf_col + 12, sf_col + 40, 1u);
+    }
+  } else {
+    for (int i = 0; i < nmma; ++i) {
+      const uint32_t acc = i ? 1u : first_acc;
+      if constexpr (PAIR)
+        tc_mma_nvf4_pair(tmem, ad + 2 * i, bd + 2 * i, idesc, sf_col + 4 * i, sf_col + 16 + 8 * i, acc);
+      else
+        tc_mma_nvf4(tmem, ad + 2 * i, bd + 2 * i, idesc, sf_col + 4 * i, sf_col + 16 + 8 * i, acc);
+    }
+    if (next_bar) r1 = mbar_test_wait(next_bar, next_parity);
+    if (next_bar2) r2 = mbar_test_wait(next_bar2, next_parity);
+  }
+  next_ready = r1 & r2;
+}
+
 template <bool PAIR>
 __device__ void mma_loop(const GemmArgs& p, const SmemLayout& L, int total, int start, int step, uint32_t tmem) {
   using C = Cfg<PAIR>;
   volatile int* abort = L.abort_flag;
+  const int lane = threadIdx.x & 31;
+  const bool leader = elect_one();
+  const int leader_lane = __ffs(__ballot_sync(0xffffffffu, leader)) - 1;
   const uint32_t idesc = idesc_nvf4(PAIR ? 2 * BM : BM, BN);
+  const uint64_t a_desc0 = smem_desc(smem_u32(L.stages), 16, 1024, 2);
+  const uint64_t b_desc0 = smem_desc(smem_u32(L.stages) + A_BYTES, 16, 1024, 2);
+  constexpr uint64_t kSlotDesc = C::STAGE_BYTES >> 4;
+  const uint32_t sf_full0 = smem_u32(L.sf_full), empty0 = smem_u32(L.empty), full0 = smem_u32(L.full);
+  const int num_kb = p.num_kb;
+  const bool tr = kTraceBuild && p.trace != nullptr && blockIdx.x == 0 && leader;
   uint32_t stage = 0, phase = 0, acc_phase = 0;
   bool issued_any = false;
   int gstage = 0, tile = 0;
-  const bool tr = kTraceBuild && p.trace != nullptr && blockIdx.x == 0;
-  for (int it = start; it < total && !*abort; it += step, ++tile) {
+  int ok = 1;
+  for (int it = start; it < total && ok && !*abort; it += step, ++tile) {
     if (tr) trace_tile(p, tile, 0);
-    if (!wait_bounded(smem_u32(L.acc_empty), acc_phase ^ 1u, abort, p.status, p.timeout_ns)) break;
+    if (lane == 0) ok = wait_bounded_spin(smem_u32(L.acc_empty), acc_phase ^ 1u, abort, p.status, p.timeout_ns);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) break;
     if (tr) trace_tile(p, tile, 1);
-    tc_fence_after();
-    bool ok = true;
-    for (int kb = 0; kb < p.num_kb; ++kb) {
-      const int nmma = min(4, (p.K - kb * 256) / 64);
-      // sf_full[stage] implies full[stage] (in both CTAs of a pair): the scale
-      // warps waited for the stage's data first
-      if (tr) trace_stage(p, gstage, 4);
-      if (!wait_bounded(smem_u32(&L.sf_full[stage]), phase, abort, p.status, p.timeout_ns)) {
-        ok = false;
-        break;
-      }
+    if (lane == 0) {
+      ok = wait_bounded_spin(sf_full0 + 8 * stage, phase, abort, p.status, p.timeout_ns);
+      if (!PAIR && ok) ok = wait_bounded_spin(full0 + 8 * stage, phase, abort, p.status, p.timeout_ns);
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    for (int kb = 0; ok && kb < num_kb; ++kb) {
       if (tr) trace_stage(p, gstage, 5);
       tc_fence_after();
-      const uint32_t a_s = smem_u32(L.stages + stage * C::STAGE_BYTES);
-      const uint32_t b_s = a_s + A_BYTES;
-      const uint32_t sf_col = tmem + SF_COL0 + stage * SF_COLS_PER_STAGE;
-      for (int i = 0; i < nmma; ++i) {
-        const uint64_t ad = smem_desc(a_s + 32 * i, 16, 1024, 2);
-        const uint64_t bd = smem_desc(b_s + 32 * i, 16, 1024, 2);
-        if constexpr (PAIR) tc_mma_nvf4_pair(tmem, ad, bd, idesc, sf_col + 4 * i, sf_col + 16 + 8 * i, (kb | i) != 0);
-        else tc_mma_nvf4(tmem, ad, bd, idesc, sf_col + 4 * i, sf_col + 16 + 8 * i, (kb | i) != 0);
+      const int rem = p.K - kb * 256;
+      const uint32_t next_stage = stage + 1 == C::STAGES ? 0u : stage + 1;
+      const uint32_t next_phase = stage + 1 == C::STAGES ? phase ^ 1u : phase;
+      const bool more = kb + 1 < num_kb;
+      uint32_t next_ready = 1;
+      if (leader) {
+        issue_stage<PAIR>(tmem, a_desc0 + stage * kSlotDesc, b_desc0 + stage * kSlotDesc, idesc,
+                          tmem + SF_COL0 + stage * SF_COLS_PER_STAGE, kb != 0, min(4, rem / 64), rem >= 256,
+                          more ? sf_full0 + 8 * next_stage : 0u, more && !PAIR ? full0 + 8 * next_stage : 0u,
+                          next_phase, next_ready);
+        if (tr) trace_stage(p, gstage, 6);
+        if constexpr (PAIR) tc_commit_pair_mc(empty0 + 8 * stage, 3);
+        else tc_commit(empty0 + 8 * stage);
+        if (tr) trace_stage(p, gstage, 7);
       }
+      next_ready = __shfl_sync(0xffffffffu, next_ready, leader_lane);
       issued_any = true;
-      if (tr) trace_stage(p, gstage, 6);
-      if constexpr (PAIR) tc_commit_pair_mc(smem_u32(&L.empty[stage]), 3);
-      else tc_commit(smem_u32(&L.empty[stage]));
-      if (tr) trace_stage(p, gstage, 7);
       ++gstage;
-      if (++stage == C::STAGES) {
-        stage = 0;
-        phase ^= 1u;
+      stage = next_stage;
+      phase = next_phase;
+      if (!next_ready) {
+        if (tr) trace_stage(p, gstage, 4);
+        if (lane == 0) {
+          ok = wait_bounded_spin(sf_full0 + 8 * stage, phase, abort, p.status, p.timeout_ns);
+          if (!PAIR && ok) ok = wait_bounded_spin(full0 + 8 * stage, phase, abort, p.status, p.timeout_ns);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
     }
     if (!ok) break;
-    if constexpr (PAIR) tc_commit_pair_mc(smem_u32(L.acc_full), 3);
-    else tc_commit(smem_u32(L.acc_full));
+    if (leader) {
+      if constexpr (PAIR) tc_commit_pair_mc(smem_u32(L.acc_full), 3);
+      else tc_commit(smem_u32(L.acc_full));
+    }
+    __syncwarp();
     acc_phase ^= 1u;
   }
   if (*abort && issued_any) {  // every MMA / copy issued must finish before TMEM is freed
-    if constexpr (PAIR) tc_commit_pair(smem_u32(L.drain));
-    else tc_commit(smem_u32(L.drain));
-    volatile int no_abort = 0;
-    wait_bounded(smem_u32(L.drain), 0, &no_abort, nullptr, p.timeout_ns);
+    if (leader) {
+      if constexpr (PAIR) tc_commit_pair(smem_u32(L.drain));
+      else tc_commit(smem_u32(L.drain));
+    }
+    __syncwarp();
+    if (lane == 0) {
+      volatile int no_abort = 0;
+      wait_bounded(smem_u32(L.drain), 0, &no_abort, nullptr, p.timeout_ns);
+    }
+    __syncwarp();
   }
 }
 
@@ -493,7 +626,7 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
     int ok = 1;
     // off the critical path (the accumulator is released right after its
     // load): poll with short sleeps rather than spinning beside the MMA warp
-    if (lane == 0) ok = wait_bounded_backoff(smem_u32(L.acc_full), acc_phase, abort, p.status, p.timeout_ns, 200);
+    if (lane == 0) ok = wait_bounded_spin(smem_u32(L.acc_full), acc_phase, abort, p.status, p.timeout_ns);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) break;
     if (tracer) trace_tile(p, tile, 2);
@@ -685,6 +818,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid
       mbar_init(smem_u32(&L.empty[s]), 1);
       mbar_init(smem_u32(&L.sf_full[s]), PAIR ? 8 : 4);  // scale warps of this CTA (and of the peer)
     }
+    for (int s = 0; s < C::SF_STAGES; ++s) {
+      mbar_init(smem_u32(&L.sf_data[s]), 1);
+      mbar_init(smem_u32(&L.sf_empty[s]), 4);  // this CTA's scale warps
+    }
     mbar_init(smem_u32(L.acc_full), 1);
     mbar_init(smem_u32(L.acc_empty), PAIR ? 2 * NUM_EPI_WARPS : NUM_EPI_WARPS);
     mbar_init(smem_u32(L.drain), 1);
@@ -746,9 +883,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid
   if (warp < EPI_WARP0) {
     regs_dec<REGS_SMALL>();
     if (warp == 0) {
-      if (lane == 0) producer_loop<PAIR>(p, L, total, start, step, rank);
+      producer_loop<PAIR, false>(p, L, total, start, step, rank);
     } else if (warp == 1) {
-      if (lane == 0 && rank == 0) mma_loop<PAIR>(p, L, total, start, step, tmem);
+      if (rank == 0) mma_loop<PAIR>(p, L, total, start, step, tmem);
+    } else if (warp == 2) {
+      producer_loop<PAIR, true>(p, L, total, start, step, rank);
     }
   } else if (warp < SF_WARP0) {
     regs_inc<REGS_EPI>();
