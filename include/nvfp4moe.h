@@ -78,7 +78,7 @@ const char* nvfp4_last_error(void);
  *            nvfp4_quantize_workspace_size(groups) bytes when gs == NULL
  *            (ignored otherwise).
  * Requirements: K % 64 == 0, rows_padded % 128 == 0, rows <= rows_padded,
- * ld_x % 8 == 0, group_stride_x % 8 == 0, groups >= 1.
+ * ld_x % 8 == 0, group_stride_x % 8 == 0, 1 <= groups <= 65535.
  */
 size_t nvfp4_quantize_workspace_size(int groups);
 int nvfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, int64_t group_stride_x, int groups,
@@ -373,7 +373,8 @@ int nvfp4_read_device_status(const void* workspace, void* stream, int* status_ou
  * following GEMM launch with epilogue `kind` (0 bf16 output, 1 SwiGLU +
  * requantization, 2 routing-weighted rows, 3 SwiGLU amax; 4: the
  * nvfp4_debug_mma_rate kernel, words 5 and 6 only) writes SM-clock stamps
- * (%clock64, cycles) of its first CTA's roles into `buffer` (device, 8-byte
+ * (%clock64, cycles) of one CTA's roles (CTA 0, or kind + 256 * c for CTA c
+ * of kinds 0-3) into `buffer` (device, 8-byte
  * aligned, (stages + tiles) * 8 words): 8 words per ring stage for the first
  * `stages` stages -- producer slot free, copies issued, scale warp saw the
  * data, scales staged, MMA starts waiting, MMA may issue, MMA instructions

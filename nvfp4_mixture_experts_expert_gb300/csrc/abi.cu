@@ -182,8 +182,11 @@ static int grouped_gemm_impl(const void* A, const void* SFA, const float* a_gs, 
   a.timeout_ns = timeout_ns;
   a.debug_no_loads = debug_no_loads;
   const int64_t max_tiles = rows_capacity / 128 * a.n_tiles;
+  // programmatic dependent launch: the prologue (barriers, tensor-map prefetch)
+  // overlaps the tail of the kernel before it (typically the A quantization);
+  // everything that reads inputs waits for that kernel first
   cudaError_t e = launch_gemm(kEpiBf16, a, (int)(max_tiles < INT32_MAX ? max_tiles : INT32_MAX), dev->sms,
-                              (cudaStream_t)stream);
+                              (cudaStream_t)stream, true);
   return e == cudaSuccess ? NVFP4_OK : cuda_fail(e, "gemm launch");
 }
 
@@ -214,7 +217,7 @@ int nvfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, int64_t
                    const float* gs, float* gs_out, void* workspace, size_t workspace_bytes, void* fp4, void* sf,
                    int64_t rows_padded, void* stream) {
   g_err[0] = 0;
-  if (groups < 1) return fail(NVFP4_ERR_INVALID_ARG, "groups must be >= 1");
+  if (groups < 1 || groups > 65535) return fail(NVFP4_ERR_INVALID_ARG, "groups must be in [1, 65535]");
   if (K <= 0 || K % 64) return fail(NVFP4_ERR_INVALID_ARG, "K must be a positive multiple of 64");
   if (rows < 0 || rows_padded < rows || rows_padded % 128)
     return fail(NVFP4_ERR_INVALID_ARG, "need 0 <= rows <= rows_padded and rows_padded % 128 == 0");
@@ -231,18 +234,16 @@ int nvfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, int64_t
   if (int rc = device_info(&dev)) return rc;
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e;
-  const float* use_gs = gs;
-  float* copy = gs_out;
-  if (!gs) {
-    if ((e = launch_group_amax((const uint16_t*)x, rows, K, ld_x, group_stride_x, groups, (float*)workspace, gs_out,
-                               s)) != cudaSuccess)
-      return cuda_fail(e, "amax launch");
-    use_gs = gs_out;
-    copy = nullptr;
-  }
+  // gs == NULL: the amax kernel leaves partial maxima in the workspace and the
+  // quantize kernel reduces them to gs itself (a separate gs kernel runs only
+  // when there is nothing to quantize).
+  const float* partial = gs ? nullptr : (const float*)workspace;
+  if (!gs && (e = launch_group_amax((const uint16_t*)x, rows, K, ld_x, group_stride_x, groups, (float*)workspace,
+                                    rows_padded > 0 ? nullptr : gs_out, dev->sms, s)) != cudaSuccess)
+    return cuda_fail(e, "amax launch");
   if (rows_padded > 0 &&
-      (e = launch_quantize((const uint16_t*)x, rows, K, ld_x, group_stride_x, groups, use_gs, copy, (uint8_t*)fp4,
-                           (uint8_t*)sf, rows_padded, dev->sms, s)) != cudaSuccess)
+      (e = launch_quantize((const uint16_t*)x, rows, K, ld_x, group_stride_x, groups, gs, gs_out, (uint8_t*)fp4,
+                           (uint8_t*)sf, rows_padded, dev->sms, s, nullptr, partial)) != cudaSuccess)
     return cuda_fail(e, "quantize launch");
   return NVFP4_OK;
 }
@@ -806,9 +807,10 @@ int nvfp4_debug_gemm_trace(void* buffer, int stages, int tiles, int kind) {
     gemm_set_trace(nullptr, 0, 0, -1);
     return NVFP4_OK;
   }
-  if (kind < 0 || kind > 4 || stages < 0 || tiles < 0 || (int64_t)(stages + tiles) * 8 > (int64_t)1 << 28)
-    return fail(NVFP4_ERR_INVALID_ARG, "kind must be 0..4 and the buffer at most 2^28 words");
-  if (kind < 4 && !gemm_trace_built())
+  const int k = kind & 0xFF, cta = kind >> 8;  // bits 8 and up: the CTA to record
+  if (kind < 0 || k > 4 || cta > 4095 || (k == 4 && cta) || stages < 0 || tiles < 0 || (int64_t)(stages + tiles) * 8 > (int64_t)1 << 28)
+    return fail(NVFP4_ERR_INVALID_ARG, "kind must be 0..4 (+ 256 * CTA) and the buffer at most 2^28 words");
+  if (k < 4 && !gemm_trace_built())
     return fail(NVFP4_ERR_UNSUPPORTED, "GEMM timelines need a build with -DNVFP4_GEMM_TRACE");
   if (reinterpret_cast<uintptr_t>(buffer) & 7u) return fail(NVFP4_ERR_INVALID_ARG, "buffer must be 8-byte aligned");
   gemm_set_trace(static_cast<unsigned long long*>(buffer), stages, tiles, kind);

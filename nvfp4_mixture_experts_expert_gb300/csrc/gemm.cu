@@ -173,8 +173,8 @@ constexpr size_t smem_bytes_for(int G) {
 }
 
 // Debug timeline (nvfp4_debug_gemm_trace): SM clock (%clock64) stamps of
-// CTA 0's roles, per ring stage g (count of stages since the kernel started)
-// and per tile t; off (one predicated branch) unless the host asked for it.
+// one CTA's roles (trace_cta), per ring stage g (count of stages since the
+// kernel started) and per tile t.
 //   stage words: 0 producer slot free, 1 producer copies issued, 2 scale warp
 //     saw the data, 3 scale warp staged, 4 MMA starts waiting, 5 MMA may issue,
 //     6 MMA instructions issued, 7 stage committed
@@ -184,10 +184,10 @@ constexpr size_t smem_bytes_for(int G) {
 // checks cost the hot loops about 15 % (measured on the prefill L1 GEMM).
 #ifdef NVFP4_GEMM_TRACE
 __device__ __forceinline__ void trace_stage(const GemmArgs& p, int g, int ev) {
-  if (p.trace && blockIdx.x == 0 && g < p.trace_stages) p.trace[(int64_t)g * 8 + ev] = clock64();
+  if (p.trace && (int)blockIdx.x == p.trace_cta && g < p.trace_stages) p.trace[(int64_t)g * 8 + ev] = clock64();
 }
 __device__ __forceinline__ void trace_tile(const GemmArgs& p, int t, int ev) {
-  if (p.trace && blockIdx.x == 0 && t < p.trace_tiles)
+  if (p.trace && (int)blockIdx.x == p.trace_cta && t < p.trace_tiles)
     p.trace[(int64_t)p.trace_stages * 8 + (int64_t)t * 8 + ev] = clock64();
 }
 constexpr bool kTraceBuild = true;
@@ -483,7 +483,7 @@ __device__ void mma_loop(const GemmArgs& p, const SmemLayout& L, int total, int 
   constexpr uint64_t kSlotDesc = C::STAGE_BYTES >> 4;
   const uint32_t sf_full0 = smem_u32(L.sf_full), empty0 = smem_u32(L.empty), full0 = smem_u32(L.full);
   const int num_kb = p.num_kb;
-  const bool tr = kTraceBuild && p.trace != nullptr && blockIdx.x == 0 && leader;
+  const bool tr = kTraceBuild && p.trace != nullptr && (int)blockIdx.x == p.trace_cta && leader;
   uint32_t stage = 0, phase = 0, acc_phase = 0;
   bool issued_any = false;
   int gstage = 0, tile = 0;
@@ -1045,10 +1045,11 @@ void gemm_get_trace(unsigned long long** buf, int* stages, int* kind) {
 cudaError_t launch_gemm(int kind, const GemmArgs& args_in, int units_upper, int num_sms, cudaStream_t s, bool pdl) {
   if (args_in.G < 1 || args_in.G > MAX_GROUPS) return cudaErrorInvalidValue;
   GemmArgs args = args_in;
-  if (kind == g_trace_kind) {
+  if (kind == (g_trace_kind & 0xFF)) {  // bits 8 and up of the traced kind: the CTA
     args.trace = g_trace_buf;
     args.trace_stages = g_trace_stages;
     args.trace_tiles = g_trace_tiles;
+    args.trace_cta = g_trace_kind >> 8;
   }
   switch (kind) {
     case kEpiBf16: return launch_kind<kEpiBf16>(args, units_upper, num_sms, s, pdl);

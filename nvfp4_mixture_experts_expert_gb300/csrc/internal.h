@@ -27,15 +27,21 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 }
 
 // ---------------------------------------------------------------- quant.cu
-// Per-group amax of bf16 rows into partial maxima, then gs = 2688/amax.
+// Per-group amax of bf16 rows into partial maxima (groups x kAmaxBlocksPerGroup
+// floats, amax_blocks_per_group(groups, num_sms) of each group's slots
+// written), then, when gs_out is given, gs = 2688/amax by a second kernel.
 constexpr int kAmaxBlocksPerGroup = 128;
+int amax_blocks_per_group(int groups, int num_sms);
 cudaError_t launch_group_amax(const uint16_t* x, int64_t rows, int64_t K, int64_t ld_x, int64_t gstride_x,
-                              int groups, float* partial, float* gs_out, cudaStream_t s);
+                              int groups, float* partial, float* gs_out, int num_sms, cudaStream_t s);
 // status_reset (may be null): a per-call device status word the kernel clears
-// before anything later in the stream can record into it.
+// before anything later in the stream can record into it.  amax_partial (may
+// be null): the amax kernel's partial maxima; the kernel then derives each
+// group's gs from them (gs unused) and writes it to gs_copy.
 cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, int64_t ld_x, int64_t gstride_x,
                             int groups, const float* gs, float* gs_copy, uint8_t* fp4, uint8_t* sf,
-                            int64_t rows_padded, int num_sms, cudaStream_t s, int* status_reset = nullptr);
+                            int64_t rows_padded, int num_sms, cudaStream_t s, int* status_reset = nullptr,
+                            const float* amax_partial = nullptr);
 cudaError_t launch_assemble_scales(const uint8_t* sf_linear, int64_t sf_cols, const int32_t* offsets,
                                    const int32_t* padded_offsets, int groups, int64_t rows_capacity,
                                    uint8_t* sf_swz, int num_sms, cudaStream_t s);
@@ -140,6 +146,7 @@ struct GemmArgs {
   unsigned long long* trace;
   int trace_stages;
   int trace_tiles;
+  int trace_cta;  // the CTA whose roles are recorded
 };
 
 size_t gemm_smem_bytes(int G);

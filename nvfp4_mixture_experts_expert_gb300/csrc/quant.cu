@@ -21,25 +21,46 @@ __device__ __forceinline__ uint4 ldg_nc(const uint16_t* p) {
 }
 
 // ---------------------------------------------------------------- amax
-__global__ void group_amax_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ld_x,
-                                  int64_t gstride_x, float* __restrict__ partial) {
+// Partial max |x| of group blockIdx.y over the blocks of the x grid: the
+// group's rows are read as one sequence of 16-byte vectors (row r, vector c
+// at index r*K/8 + c), strided over the whole grid, kAmaxUnroll independent
+// loads in flight per thread.  Thread i's (row, vector) pair advances by the
+// grid stride incrementally, so the loop has no 64-bit division.
+constexpr int kAmaxThreads = 512;
+constexpr int kAmaxUnroll = 4;
+
+__global__ void __launch_bounds__(kAmaxThreads) group_amax_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                                  int64_t K, int64_t ld_x, int64_t gstride_x,
+                                                                  float* __restrict__ partial, int partial_stride) {
   pdl_trigger();
   pdl_wait();
   const int g = blockIdx.y;
-  const int nb = gridDim.x;
-  const int64_t vec_per_row = K / 8;
-  const int64_t total = rows * vec_per_row;
-  const int64_t per_block = (total + nb - 1) / nb;
-  const int64_t begin = per_block * blockIdx.x;
-  const int64_t end = min(total, begin + per_block);
+  const int64_t vpr = K / 8;
+  const int64_t total = rows * vpr;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t sr = stride / vpr, sc = stride - sr * vpr;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  int64_t r = i / vpr, c = i - r * vpr;
   const uint16_t* xg = x + (int64_t)g * gstride_x;
   uint32_t m = 0;  // max of |bf16| bit patterns (monotone for non-negative floats)
-  for (int64_t i = begin + threadIdx.x; i < end; i += blockDim.x) {
-    const int64_t r = i / vec_per_row, c = i - r * vec_per_row;
-    const uint4 v = ldg_nc(xg + r * ld_x + c * 8);
-    const uint32_t u[4] = {v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu, v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu};
+  for (; i < total; i += kAmaxUnroll * stride) {
+    uint4 v[kAmaxUnroll];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) m = max(m, max(u[q] & 0xFFFFu, u[q] >> 16));
+    for (int u = 0; u < kAmaxUnroll; ++u) {
+      v[u] = i + u * stride < total ? ldg_nc(xg + r * ld_x + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+      c += sc;
+      r += sr;
+      if (c >= vpr) {
+        c -= vpr;
+        ++r;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kAmaxUnroll; ++u) {
+      const uint32_t w[4] = {v[u].x & 0x7FFF7FFFu, v[u].y & 0x7FFF7FFFu, v[u].z & 0x7FFF7FFFu, v[u].w & 0x7FFF7FFFu};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) m = max(m, max(w[q] & 0xFFFFu, w[q] >> 16));
+    }
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -50,19 +71,33 @@ __global__ void group_amax_kernel(const uint16_t* __restrict__ x, int64_t rows, 
     m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0u;
 #pragma unroll
     for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (threadIdx.x == 0) partial[(int64_t)g * nb + blockIdx.x] = __uint_as_float(m << 16);
+    if (threadIdx.x == 0) partial[(int64_t)g * partial_stride + blockIdx.x] = __uint_as_float(m << 16);
   }
 }
 
 // gs = 2688 / amax (IEEE division), 1 when the group is all zero.
-__global__ void group_gs_kernel(const float* __restrict__ partial, int nb, int groups, float* __restrict__ gs) {
+__device__ __forceinline__ float gs_from_group_amax(float a) { return a > 0.f ? __fdiv_rn(kGsNumerator, a) : 1.0f; }
+
+// The global scale of group g from its nb partial maxima, reduced by one warp
+// (max is exact and order-free, so every warp gets the same bits).
+__device__ __forceinline__ float warp_group_gs(const float* __restrict__ partial, int partial_stride, int nb,
+                                               int64_t g, int lane) {
+  float a = 0.f;
+  for (int i = lane; i < nb; i += 32) a = fmaxf(a, partial[g * partial_stride + i]);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  return gs_from_group_amax(a);
+}
+
+__global__ void group_gs_kernel(const float* __restrict__ partial, int partial_stride, int nb, int groups,
+                                float* __restrict__ gs) {
   pdl_trigger();
   pdl_wait();
   const int g = blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= groups) return;
   float a = 0.f;
-  for (int i = 0; i < nb; ++i) a = fmaxf(a, partial[(int64_t)g * nb + i]);
-  gs[g] = a > 0.f ? __fdiv_rn(kGsNumerator, a) : 1.0f;
+  for (int i = 0; i < nb; ++i) a = fmaxf(a, partial[(int64_t)g * partial_stride + i]);
+  gs[g] = gs_from_group_amax(a);
 }
 
 // ---------------------------------------------------------------- scale assembly
@@ -251,11 +286,15 @@ __global__ void __launch_bounds__(256) gather_quantize_kernel(const uint16_t* __
 // the segment's two chunks, one 32-byte load per block, 8 bytes of nibbles
 // per lane and a 32-bit scale word per 4 lanes.  K is a multiple of 64, so the
 // 4 lanes of a scale word are all inside or all outside the row.
+// The global scale of group g is gs[g], or, with amax_partial given, reduced
+// by the warp from the amax kernel's nb partial maxima (once per group a warp
+// meets; the warp on a group's first item stores it to gs_copy).
 template <bool kAligned32>
 __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K,
                                                        int64_t ld_x, int64_t gstride_x, int groups,
                                                        const float* __restrict__ gs, float* __restrict__ gs_copy,
-                                                       uint8_t* __restrict__ fp4, uint8_t* __restrict__ sf,
+                                                       const float* __restrict__ amax_partial, int partial_stride,
+                                                       int nb, uint8_t* __restrict__ fp4, uint8_t* __restrict__ sf,
                                                        int64_t rows_padded, int* __restrict__ status_reset) {
   pdl_trigger();
   __shared__ float2 tab[128];
@@ -265,7 +304,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
   }
   __syncthreads();
   pdl_wait();  // the global scales may come from the amax kernels just before
-  if (gs_copy && blockIdx.x == 0)
+  if (!amax_partial && gs_copy && blockIdx.x == 0)
     for (int i = threadIdx.x; i < groups; i += blockDim.x) gs_copy[i] = gs[i];
   if (status_reset && blockIdx.x == 0 && threadIdx.x == 0) *status_reset = 0;
   const float rcp6 = __frcp_rn(6.0f);
@@ -274,22 +313,30 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
   const int64_t per_group = rows_padded * segs;
   const int64_t items = per_group * groups;
   const int64_t sf_cols = K / 16;
+  int64_t have_g = -1;
+  float gsv = 0.f;
   for (int64_t item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); item < items;
        item += (int64_t)gridDim.x * (blockDim.x >> 5)) {
     const int64_t g = item / per_group;
     const int64_t rem = item - g * per_group;
     const int64_t r = rem / segs, e0 = (rem - r * segs) * 1024;
     const int64_t orow = g * rows_padded + r;
-    const float gsv = gs[g];
+    uint32_t raw[2][8];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int64_t el = e0 + c * 512 + lane * 16;
+      if (r < rows && el < K) ld_block32<kAligned32>(x + g * gstride_x + r * ld_x + el, raw[c]);
+    }
+    if (g != have_g) {
+      gsv = amax_partial ? warp_group_gs(amax_partial, partial_stride, nb, g, lane) : gs[g];
+      have_g = g;
+    }
+    if (amax_partial && gs_copy && rem == 0 && lane == 0) gs_copy[g] = gsv;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int64_t el = e0 + c * 512 + lane * 16;
       uint32_t lo = 0u, hi = 0u, sc = 0u;
-      if (r < rows && el < K) {
-        uint32_t raw[8];
-        ld_block32<kAligned32>(x + g * gstride_x + r * ld_x + el, raw);
-        sc = quant_block16_bf16(raw, block_amax_bf16(raw), gsv, rcp6, tab, lo, hi);
-      }
+      if (r < rows && el < K) sc = quant_block16_bf16(raw[c], block_amax_bf16(raw[c]), gsv, rcp6, tab, lo, hi);
       const uint32_t word = sc | (__shfl_down_sync(0xffffffffu, sc, 1) << 8) |
                             (__shfl_down_sync(0xffffffffu, sc, 2) << 16) |
                             (__shfl_down_sync(0xffffffffu, sc, 3) << 24);
@@ -397,24 +444,32 @@ int grid_for(int64_t items, int threads, int num_sms, int per_sm) {
 
 }  // namespace
 
+int amax_blocks_per_group(int groups, int num_sms) {
+  const int want = (2 * num_sms + groups - 1) / groups;
+  return want < 1 ? 1 : (want < kAmaxBlocksPerGroup ? want : kAmaxBlocksPerGroup);
+}
+
 cudaError_t launch_group_amax(const uint16_t* x, int64_t rows, int64_t K, int64_t ld_x, int64_t gstride_x,
-                              int groups, float* partial, float* gs_out, cudaStream_t s) {
-  dim3 grid(kAmaxBlocksPerGroup, groups);
-  cudaError_t e = launch_kernel(group_amax_kernel, grid, dim3(256), 0, s, true, x, rows, K, ld_x, gstride_x, partial);
-  if (e != cudaSuccess) return e;
+                              int groups, float* partial, float* gs_out, int num_sms, cudaStream_t s) {
+  const int nb = amax_blocks_per_group(groups, num_sms);
+  cudaError_t e = launch_kernel(group_amax_kernel, dim3(nb, groups), dim3(kAmaxThreads), 0, s, true, x, rows, K, ld_x,
+                                gstride_x, partial, (int)kAmaxBlocksPerGroup);
+  if (e != cudaSuccess || !gs_out) return e;
   return launch_kernel(group_gs_kernel, dim3((groups + 127) / 128), dim3(128), 0, s, true, (const float*)partial,
-                       (int)kAmaxBlocksPerGroup, groups, gs_out);
+                       (int)kAmaxBlocksPerGroup, nb, groups, gs_out);
 }
 
 cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, int64_t ld_x, int64_t gstride_x,
                             int groups, const float* gs, float* gs_copy, uint8_t* fp4, uint8_t* sf,
-                            int64_t rows_padded, int num_sms, cudaStream_t s, int* status_reset) {
+                            int64_t rows_padded, int num_sms, cudaStream_t s, int* status_reset,
+                            const float* amax_partial) {
   const int64_t warps = rows_padded * ((K + 1023) / 1024) * groups;
   const int grid = grid_for(warps * 32, 256, num_sms, 8);
   const bool a32 = (reinterpret_cast<uintptr_t>(x) & 31u) == 0 && ld_x % 16 == 0 && gstride_x % 16 == 0;
   auto* kernel = a32 ? quantize_kernel<true> : quantize_kernel<false>;
   return launch_kernel(kernel, dim3(grid), dim3(256), 0, s, true, x, rows, K, ld_x, gstride_x, groups, gs, gs_copy,
-                       fp4, sf, rows_padded, status_reset);
+                       amax_partial, (int)kAmaxBlocksPerGroup, amax_blocks_per_group(groups, num_sms), fp4, sf,
+                       rows_padded, status_reset);
 }
 
 cudaError_t launch_assemble_scales(const uint8_t* sf_linear, int64_t sf_cols, const int32_t* offsets,

@@ -142,11 +142,11 @@ int nvfp4_quantize_no_alloc(const void* x, int64_t rows, int64_t K, int64_t ld_x
   if (int rc = scratch_on_current_device(&scratch, &sms)) return rc;
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = nvfp4::launch_group_amax((const uint16_t*)x, rows, K, ld_x, group_stride_x, groups, scratch,
-                                           gs_out, s);
+                                           rows_padded > 0 ? nullptr : gs_out, sms, s);
   if (e != cudaSuccess) return fail(NVFP4_ERR_CUDA, "amax launch: %s", cudaGetErrorString(e));
   if (rows_padded > 0 &&
-      (e = nvfp4::launch_quantize((const uint16_t*)x, rows, K, ld_x, group_stride_x, groups, gs_out, nullptr,
-                                  (uint8_t*)fp4, (uint8_t*)sf, rows_padded, sms, s)) != cudaSuccess)
+      (e = nvfp4::launch_quantize((const uint16_t*)x, rows, K, ld_x, group_stride_x, groups, nullptr, gs_out,
+                                  (uint8_t*)fp4, (uint8_t*)sf, rows_padded, sms, s, nullptr, scratch)) != cudaSuccess)
     return fail(NVFP4_ERR_CUDA, "quantize launch: %s", cudaGetErrorString(e));
   return NVFP4_OK;
 }

@@ -121,3 +121,67 @@ def test_quantize_ties_saturation_and_thresholds():
     fp4, sf, _ = api().quantize(bf16_dev(bits), gs=dev(np.float32([1.0])))
     np.testing.assert_array_equal(host(fp4), packed)
     np.testing.assert_array_equal(host(sf), swz)
+
+
+@pytest.mark.parametrize("rows,K,ld_x,groups", [(2048, 3584, 3584, 1), (301, 192, 256, 1), (77, 320, 3 * 320, 3),
+                                               (5, 64, 64, 300)])
+def test_global_scale_sees_every_element_and_no_padding(rows, K, ld_x, groups):
+    """gs = 2688 / amax must see each element of each group exactly where the
+    strides put it: a single peak at the first, the last and random places of
+    one group (a larger value sits in every padding column, which must not
+    count) moves that group's scale and no other."""
+    import torch
+    rng = np.random.default_rng(rows + K + groups)
+    gstride = K if ld_x == groups * K else rows * ld_x  # interleaved (T, G, D) or stacked groups
+    n = gstride * (groups - 1) + (rows - 1) * ld_x + K if gstride == K else groups * rows * ld_x
+    base = np.zeros(n, np.float32)
+    valid = np.zeros(n, bool)
+    for g in range(groups):
+        for r in range(rows):
+            at = g * gstride + r * ld_x
+            base[at:at + K] = rng.uniform(-1, 1, K)
+            valid[at:at + K] = True
+    base[~valid] = 1e6
+    places = [(0, 0, 0), (groups - 1, rows - 1, K - 1)] + [
+        (int(rng.integers(groups)), int(rng.integers(rows)), int(rng.integers(K))) for _ in range(4)]
+    for g0, r0, c0 in places:
+        x = base.copy()
+        x[g0 * gstride + r0 * ld_x + c0] = -37.0
+        bits = W.f32_to_bf16_bits(x)
+        _, _, gs = api().quantize_groups(bf16_dev(bits), rows, K, ld_x, gstride, groups)
+        gs = host(gs)
+        xb = W.bf16_bits_to_f32(bits)
+        for g in range(groups):
+            xs = np.concatenate([xb[g * gstride + r * ld_x:g * gstride + r * ld_x + K] for r in range(rows)])
+            assert gs[g] == O.global_scale(np.abs(xs).max()), (g0, r0, c0, g)
+        assert gs[g0] == O.global_scale(np.float32(37.0))
+    torch.cuda.synchronize()
+
+
+def test_many_small_groups_bytes_and_scales():
+    """300 groups of 5 rows (the amax grid gives each group very few blocks)."""
+    G, T, D = 300, 5, 64
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((G, T, D)) * np.exp(rng.standard_normal((G, 1, 1)) * 3)).astype(np.float32)
+    bits = W.f32_to_bf16_bits(x)
+    xb = W.bf16_bits_to_f32(bits)
+    fp4, sf, gs = api().quantize_groups(bf16_dev(bits), T, D, D, T * D, G, rows_padded=128)
+    fp4, sf, gs = host(fp4), host(sf), host(gs)
+    for g in range(G):
+        gsg = O.global_scale(np.abs(xb[g]).max())
+        assert gs[g] == gsg
+        packed, swz, _, _ = oracle_packed_rows(xb[g], gsg, 128)
+        np.testing.assert_array_equal(fp4[g * 128:(g + 1) * 128], packed)
+        np.testing.assert_array_equal(sf[g * 128 * D // 16:(g + 1) * 128 * D // 16], swz)
+
+
+def test_scales_only_when_nothing_to_quantize():
+    """rows = rows_padded = 0: no bytes to write, every group's gs is 1."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import binding as B
+    G = 5
+    gs_out = torch.full((G,), -1.0, dtype=torch.float32, device="cuda")
+    wsb = B.nvfp4_quantize_workspace_size(G)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    B.nvfp4_quantize(None, 0, 128, 128, 0, G, None, gs_out, ws, wsb, None, None, 0)
+    assert (host(gs_out) == 1.0).all()
