@@ -97,7 +97,7 @@ int nvfp4_quantize(const void* x, int64_t rows, int64_t K, int64_t ld_x, int64_t
  * Same arguments and results as nvfp4_quantize with gs == NULL (gs_out
  * receives 2688/amax per group), minus the workspace.  Instead, the partial
  * maxima of the amax reduction live in a fixed array inside the library's
- * device image (NVFP4_QUANTIZE_NO_ALLOC_MAX_GROUPS x 128 floats = 32 KB on
+ * device image (NVFP4_QUANTIZE_NO_ALLOC_MAX_GROUPS x 1024 floats = 256 KB on
  * every GPU that loads the library, held until the process exits).
  *   - groups > NVFP4_QUANTIZE_NO_ALLOC_MAX_GROUPS is rejected with
  *     NVFP4_ERR_UNSUPPORTED before anything is launched.

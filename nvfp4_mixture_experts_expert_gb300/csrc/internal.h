@@ -30,7 +30,7 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 // Per-group amax of bf16 rows into partial maxima (groups x kAmaxBlocksPerGroup
 // floats, amax_blocks_per_group(groups, num_sms) of each group's slots
 // written), then, when gs_out is given, gs = 2688/amax by a second kernel.
-constexpr int kAmaxBlocksPerGroup = 128;
+constexpr int kAmaxBlocksPerGroup = 1024;
 int amax_blocks_per_group(int groups, int num_sms);
 cudaError_t launch_group_amax(const uint16_t* x, int64_t rows, int64_t K, int64_t ld_x, int64_t gstride_x,
                               int groups, float* partial, float* gs_out, int num_sms, cudaStream_t s);

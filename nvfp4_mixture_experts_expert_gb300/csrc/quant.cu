@@ -26,10 +26,11 @@ __device__ __forceinline__ uint4 ldg_nc(const uint16_t* p) {
 // at index r*K/8 + c), strided over the whole grid, kAmaxUnroll independent
 // loads in flight per thread.  Thread i's (row, vector) pair advances by the
 // grid stride incrementally, so the loop has no 64-bit division.
-constexpr int kAmaxThreads = 512;
-constexpr int kAmaxUnroll = 4;
+constexpr int kAmaxThreads = 256;
+constexpr int kAmaxUnroll = 8;   // 128 bytes in flight per thread
+constexpr int kAmaxBlocksPerSm = 4;
 
-__global__ void __launch_bounds__(kAmaxThreads) group_amax_kernel(const uint16_t* __restrict__ x, int64_t rows,
+__global__ void __launch_bounds__(kAmaxThreads, kAmaxBlocksPerSm) group_amax_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                                   int64_t K, int64_t ld_x, int64_t gstride_x,
                                                                   float* __restrict__ partial, int partial_stride) {
   pdl_trigger();
@@ -445,7 +446,7 @@ int grid_for(int64_t items, int threads, int num_sms, int per_sm) {
 }  // namespace
 
 int amax_blocks_per_group(int groups, int num_sms) {
-  const int want = (2 * num_sms + groups - 1) / groups;
+  const int want = (kAmaxBlocksPerSm * num_sms + groups - 1) / groups;
   return want < 1 ? 1 : (want < kAmaxBlocksPerGroup ? want : kAmaxBlocksPerGroup);
 }
 
