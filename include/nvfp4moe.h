@@ -336,13 +336,15 @@ int nvfp4_moe_calibrate_routed(const void* hidden, const int32_t* topk_ids, cons
  *   written otherwise),
  *   calib u32[2E] (calibration amax bits; with a2_gs NULL, E amax words of
  *   the L1 output, then the E L2 global scales as f32)
+ *   tile_done i32[cap/128] (L1 n-tiles finished per m-tile: the L2 GEMM
+ *   starts on an m-tile once all of its L1 output is stored)
  * Only rows < P of the row-indexed buffers are defined after a call; the
  * pad rows of a1 hold zero block scales (every value exactly 0) and
  * unspecified nibble bytes.
  */
 typedef struct {
   size_t status, topk_ids, topk_w, block_counts, counts, offsets, meta, tile_expert, sorted_token_ids, row_weight,
-      inverse, a1, sfa1, a2, sfa2, y, h, calib, total;
+      inverse, a1, sfa1, a2, sfa2, y, h, calib, tile_done, total;
   int64_t capacity;
   int64_t route_blocks;
 } nvfp4_moe_layout;
@@ -398,6 +400,16 @@ int nvfp4_debug_gemm_trace(void* buffer, int stages, int tiles, int kind);
  * it off.  Process-wide; 0 <= timeout_ms <= 10000.
  */
 int nvfp4_moe_set_debug_stall(int timeout_ms);
+
+/*
+ * nvfp4_moe_set_overlap -- measurement switch (process-wide, default 1): with
+ * 1, a forward given its L2 scales lets its L2 GEMM start on the SMs the L1
+ * GEMM's last partial round of tiles leaves idle, each L2 tile waiting (on
+ * the device, bounded) until the L1 output of its m-tile is stored; with 0
+ * the L2 GEMM waits for the whole L1 GEMM.  Results are identical either way.
+ * prev (may be NULL) receives the previous setting.
+ */
+int nvfp4_moe_set_overlap(int enable, int* prev);
 
 /* GEMM variant (process-wide; every GEMM above and the MoE forward).
  *

@@ -47,7 +47,8 @@ class Nvfp4Error(RuntimeError):
 class MoeLayout(ctypes.Structure):
     _fields_ = [(n, c_size) for n in (
         "status", "topk_ids", "topk_w", "block_counts", "counts", "offsets", "meta", "tile_expert",
-        "sorted_token_ids", "row_weight", "inverse", "a1", "sfa1", "a2", "sfa2", "y", "h", "calib", "total")] + [
+        "sorted_token_ids", "row_weight", "inverse", "a1", "sfa1", "a2", "sfa2", "y", "h", "calib", "tile_done",
+        "total")] + [
         ("capacity", c_i64), ("route_blocks", c_i64)]
 
 
@@ -99,6 +100,7 @@ _gemm_trace = _sig("nvfp4_debug_gemm_trace", c_int, [c_ptr, c_int, c_int, c_int]
 _mma_rate = _sig("nvfp4_debug_mma_rate", c_int, [c_ptr, c_size, c_ptr, c_size, c_ptr, c_size, c_ptr, c_size, c_int,
                                                  c_int, c_int, c_int, c_ptr])
 _stage_events = _sig("nvfp4_moe_set_stage_events", c_int, [ctypes.POINTER(c_ptr), c_int])
+_moe_set_overlap = _sig("nvfp4_moe_set_overlap", c_int, [c_int, ctypes.POINTER(c_int)])
 _gemm_set_cta_pair = _sig("nvfp4_gemm_set_cta_pair", c_int, [c_int, ctypes.POINTER(c_int)])
 
 
@@ -262,6 +264,14 @@ def nvfp4_debug_mma_rate(A, a_bytes, SFA, sfa_bytes, B, b_bytes, SFB, sfb_bytes,
     """The bare block-scaled FP4 MMA stream (see include/nvfp4moe.h); time it with events."""
     _check(_mma_rate(_p(A), a_bytes, _p(SFA), sfa_bytes, _p(B), b_bytes, _p(SFB), sfb_bytes, shape, units, iters,
                      flags, _stream(stream)))
+
+
+def nvfp4_moe_set_overlap(enable):
+    """1 (default): the L2 GEMM takes the L1 output m-tile by m-tile; 0: after
+    the whole L1 GEMM.  Returns the previous setting."""
+    prev = c_int(-1)
+    _check(_moe_set_overlap(int(enable), ctypes.byref(prev)))
+    return prev.value
 
 
 def nvfp4_gemm_set_cta_pair(mode):

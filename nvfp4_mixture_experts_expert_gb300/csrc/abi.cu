@@ -127,6 +127,7 @@ int64_t moe_capacity(int64_t T, int E, int k) {
 void* g_stage_events[8] = {};
 int g_n_stage_events = 0;
 int g_debug_stall_ms = 0;  // > 0: MoE forwards launch their L1 GEMM with no operand loads (failure-detection test)
+int g_l1_l2_overlap = 1;   // the L2 GEMM takes the L1 output per m-tile (nvfp4_moe_set_overlap)
 
 inline void stage_mark(int i, cudaStream_t s) {
   if (g_n_stage_events == 8 && g_stage_events[i]) cudaEventRecord((cudaEvent_t)g_stage_events[i], s);
@@ -315,6 +316,7 @@ int nvfp4_moe_workspace_layout(int64_t T, int64_t H, int64_t I, int E, int top_k
   out->y = take(cap * H * 2);
   out->h = take(cap * I * 2);  // bf16 L1 output when the L2 scales come from the batch
   out->calib = take((int64_t)2 * E * 4);
+  out->tile_done = take(cap / 128 * 4);
   out->total = off;
   out->capacity = cap;
   out->route_blocks = nb;
@@ -450,6 +452,14 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
   g2.pair_hint = T * top_k >= (int64_t)256 * E;  // experts average two or more m-tiles
   g2.status = status;
   g2.timeout_ns = 2000000000ull;
+  // with given L2 scales the L2 GEMM takes the L1 output m-tile by m-tile (the
+  // L2 scales from the batch need the whole L1 output first)
+  int* tile_done = batch_l2_scale || !g_l1_l2_overlap ? nullptr : (int*)(ws + L.tile_done);
+  g1.tile_done = tile_done;
+  g1.late_trigger = tile_done != nullptr;
+  g2.tile_done = tile_done;
+  g2.tile_done_target = tile_done ? g1.n_tiles : 0;
+  if (g_debug_stall_ms > 0) g2.timeout_ns = g1.timeout_ns;  // the stalled L1 never completes its m-tiles
 
   const int nb = (int)L.route_blocks;
   cudaError_t e;
@@ -478,7 +488,7 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
   }
   stage_mark(3, s);
   if ((e = launch_gather_quantize((const uint16_t*)hidden, H, T, top_k, ids, inverse, counts, offsets, E, a1_gs,
-                                  cap, a1, sfa1, s, true)) != cudaSuccess)
+                                  cap, a1, sfa1, s, true, tile_done)) != cudaSuccess)
     return cuda_fail(e, "gather launch");
   stage_mark(4, s);
   const int64_t t1 = cap / 128 * g1.n_tiles, t2 = cap / 128 * g2.n_tiles;
@@ -814,6 +824,14 @@ int nvfp4_debug_gemm_trace(void* buffer, int stages, int tiles, int kind) {
     return fail(NVFP4_ERR_UNSUPPORTED, "GEMM timelines need a build with -DNVFP4_GEMM_TRACE");
   if (reinterpret_cast<uintptr_t>(buffer) & 7u) return fail(NVFP4_ERR_INVALID_ARG, "buffer must be 8-byte aligned");
   gemm_set_trace(static_cast<unsigned long long*>(buffer), stages, tiles, kind);
+  return NVFP4_OK;
+}
+
+int nvfp4_moe_set_overlap(int enable, int* prev) {
+  g_err[0] = 0;
+  if (enable != 0 && enable != 1) return fail(NVFP4_ERR_INVALID_ARG, "enable must be 0 or 1");
+  if (prev) *prev = g_l1_l2_overlap;
+  g_l1_l2_overlap = enable;
   return NVFP4_OK;
 }
 

@@ -137,6 +137,7 @@ struct SmemLayout {
   uint64_t* sf_full;     // [STAGES] scale tiles of a stage are in TMEM
   uint32_t* tmem_slot;
   int* abort_flag;
+  int* tile_arrivals;  // [2] epilogue warps done with the L1 tile of that parity (tile_done hand-off)
   int* offsets;   // [G+1] padded row offsets
   int* unit_off;  // [G+1] first work unit (m-tile or m-tile pair) of each group
 };
@@ -160,6 +161,7 @@ __device__ __forceinline__ SmemLayout carve(uint8_t* raw, int G) {
   L.drain = L.acc_empty + 1;
   L.tmem_slot = reinterpret_cast<uint32_t*>(L.drain + 1);
   L.abort_flag = reinterpret_cast<int*>(L.tmem_slot + 1);
+  L.tile_arrivals = L.abort_flag + 1;  // [2], by tile parity
   L.offsets = reinterpret_cast<int*>(L.abort_flag + 3);
   L.unit_off = L.offsets + G + 1;
   return L;
@@ -243,6 +245,27 @@ __device__ __forceinline__ Work decode_work(const SmemLayout& L, const GemmArgs&
   return w;
 }
 
+// Bounded wait (one lane) until a counter another kernel increments reaches
+// target; same give-up rules as the barrier waits.
+__device__ __forceinline__ bool wait_count_bounded(const int* counter, int target, volatile int* abort, int* status,
+                                                   uint64_t timeout_ns) {
+  if (ld_acquire_gpu(counter) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i) {
+      __nanosleep(100);
+      if (ld_acquire_gpu(counter) >= target) return true;
+    }
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      *abort = 1;
+      if (status) atomicExch(status, 6 /* NVFP4_ERR_DEVICE_TIMEOUT */);
+      return false;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ producers
 // Work items it = start, start + step, ... (step = CTAs, or CTA pairs).
 // Two producer warps: SCALES == false copies a stage's A and B boxes with TMA
@@ -271,9 +294,18 @@ __device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total,
   const uint32_t empty0 = smem_u32(SCALES ? L.sf_empty : L.empty);
   const uint32_t done0 = smem_u32(SCALES ? L.sf_data : L.full);
   const uint32_t slot0 = smem_u32(SCALES ? L.sf_slots : L.stages);
+  const bool per_tile = p.tile_done && p.tile_done_target > 0;  // L2 fed per m-tile by L1
+  int ready_mt = -1;
   if (!p.debug_no_loads) {
     for (int it = start; it < total && ok && !*abort; it += step) {
       const Work w = decode_work<PAIR>(L, p, it, rank);
+      if (per_tile && w.mt != ready_mt) {
+        if (lane == 0) ok = wait_count_bounded(p.tile_done + w.mt, p.tile_done_target, abort, p.status, p.timeout_ns);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        (void)ld_acquire_gpu(p.tile_done + w.mt);  // every lane, then the copies may read the m-tile
+        fence_proxy_async_global();
+        ready_mt = w.mt;
+      }
       const int b_r0 = w.nt * p.b_tile_stride;
       const int b_r1 = b_r0 + p.b_second_offset;
       const int32_t a_row = w.mt * BM;
@@ -719,6 +751,15 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
       st_global_v8(p.q_out + row * (p.I / 2) + f0 / 2, words[0], words[1], words[2], words[3], words[4], words[5],
                    words[6], words[7]);
       *reinterpret_cast<uint32_t*>(p.q_sf + sf_offset(row, f0 / 16, p.I / 16)) = scales;
+      if (p.tile_done) {  // the last epilogue warp done with this tile counts it for the L2 GEMM
+        __threadfence();
+        __syncwarp();
+        if (lane == 0 && atomicAdd(&L.tile_arrivals[tile & 1], 1) == NUM_EPI_WARPS - 1) {
+          L.tile_arrivals[tile & 1] = 0;
+          __threadfence();
+          atomicAdd(p.tile_done + w.mt, 1);
+        }
+      }
     } else if constexpr (EPI == kEpiSwigluAmax) {
       // amax of the bf16 SwiGLU output of this row's 64 features; with D set,
       // the bf16 values themselves too (row-major, ldd elements per row)
@@ -811,7 +852,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid
   const SmemLayout L = carve<PAIR>(smem_raw, p.G);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
-  pdl_trigger();
+  if (!p.late_trigger) pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(smem_u32(&L.full[s]), 1);
@@ -826,9 +867,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid
     mbar_init(smem_u32(L.acc_empty), PAIR ? 2 * NUM_EPI_WARPS : NUM_EPI_WARPS);
     mbar_init(smem_u32(L.drain), 1);
     *L.abort_flag = 0;
+    L.tile_arrivals[0] = L.tile_arrivals[1] = 0;
     fence_mbar_init();
   }
-  pdl_wait();  // everything below reads what earlier kernels wrote
+  // everything below reads what earlier kernels wrote; an L2 GEMM fed per
+  // m-tile by the L1 GEMM before it instead waits for each m-tile (producers),
+  // and was launched only once every kernel before L1 had completed
+  if (!(EPI == kEpiCombine && p.tile_done && p.tile_done_target > 0)) pdl_wait();
+  if (p.late_trigger) pdl_trigger();
   if (p.host_rows > 0) {  // one group of host-known size
     if (threadIdx.x == 0) {
       L.offsets[0] = 0;

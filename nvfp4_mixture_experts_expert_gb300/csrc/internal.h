@@ -49,7 +49,7 @@ cudaError_t launch_assemble_scales(const uint8_t* sf_linear, int64_t sf_cols, co
 cudaError_t launch_gather_quantize(const uint16_t* hidden, int64_t H, int64_t T, int top_k,
                                    const int32_t* topk_ids, const int32_t* inverse, const int32_t* counts,
                                    const int32_t* offsets, int E, const float* a1_gs, int64_t capacity, uint8_t* a1,
-                                   uint8_t* sfa1, cudaStream_t s, bool pdl = false);
+                                   uint8_t* sfa1, cudaStream_t s, bool pdl = false, int* tile_done = nullptr);
 // Calibration: per-expert amax of the gathered hidden rows (as float bits, atomicMax
 // into a zeroed array), and gs = 2688/amax (1 for an empty / all-zero expert).
 cudaError_t launch_gather_amax(const uint16_t* hidden, int64_t H, const int32_t* sorted_ids,
@@ -137,6 +137,17 @@ struct GemmArgs {
   const int32_t* sorted_ids;
   const float* row_w;
   int H;
+  // Hand-off of the MoE forward's L1 output to the L2 GEMM per m-tile, so
+  // that the L2 GEMM runs on the SMs the L1 GEMM's last partial round leaves
+  // idle.  L1 (kEpiSwigluQuant): tile_done[mt] += 1 once a tile's A2 rows and
+  // scales are stored; late_trigger: its dependent launch is released only
+  // after its own dependency wait (so the L2 kernel starts after every kernel
+  // before L1 completed).  L2 (kEpiCombine, tile_done_target > 0): no
+  // dependency wait; before it loads m-tile mt it waits until
+  // tile_done[mt] == tile_done_target.  tile_done is zeroed by the gather.
+  int* tile_done;
+  int tile_done_target;
+  int late_trigger;
   // bounded waits
   int* status;
   unsigned long long timeout_ns;

@@ -211,7 +211,8 @@ __global__ void __launch_bounds__(256) gather_quantize_kernel(const uint16_t* __
                                                               const int32_t* __restrict__ counts,
                                                               const int32_t* __restrict__ offsets, int E,
                                                               const float* __restrict__ a1_gs, int64_t capacity,
-                                                              uint8_t* __restrict__ a1, uint8_t* __restrict__ sfa1) {
+                                                              uint8_t* __restrict__ a1, uint8_t* __restrict__ sfa1,
+                                                              int* __restrict__ tile_done) {
   pdl_trigger();
   __shared__ float2 tab[128];
   if (threadIdx.x < 128) {
@@ -220,6 +221,8 @@ __global__ void __launch_bounds__(256) gather_quantize_kernel(const uint16_t* __
   }
   __syncthreads();
   pdl_wait();
+  if (tile_done && blockIdx.x == 0)  // the L1 -> L2 per-m-tile counters of this forward start at 0
+    for (int64_t i = threadIdx.x; i < capacity / 128; i += blockDim.x) tile_done[i] = 0;
   const float rcp6 = __frcp_rn(6.0f);
   const int lane = threadIdx.x & 31;
   const int64_t item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -487,7 +490,7 @@ cudaError_t launch_assemble_scales(const uint8_t* sf_linear, int64_t sf_cols, co
 cudaError_t launch_gather_quantize(const uint16_t* hidden, int64_t H, int64_t T, int top_k,
                                    const int32_t* topk_ids, const int32_t* inverse, const int32_t* counts,
                                    const int32_t* offsets, int E, const float* a1_gs, int64_t capacity, uint8_t* a1,
-                                   uint8_t* sfa1, cudaStream_t s, bool pdl) {
+                                   uint8_t* sfa1, cudaStream_t s, bool pdl, int* tile_done) {
   const int chunks = T <= kSmallRouteTokens ? 1 : kGatherChunks;
   const int64_t segs = (H + 512 * chunks - 1) / (512 * chunks);
   const int64_t warps = T * segs + (int64_t)E * 128;
@@ -497,7 +500,7 @@ cudaError_t launch_gather_quantize(const uint16_t* hidden, int64_t H, int64_t T,
                              : (a32 ? gather_quantize_kernel<true, kGatherChunks>
                                     : gather_quantize_kernel<false, kGatherChunks>);
   return launch_kernel(kernel, dim3((unsigned)grid), dim3(256), 0, s, pdl, hidden, H, T, top_k, topk_ids, inverse,
-                       counts, offsets, E, a1_gs, capacity, a1, sfa1);
+                       counts, offsets, E, a1_gs, capacity, a1, sfa1, tile_done);
 }
 
 cudaError_t launch_gather_amax(const uint16_t* hidden, int64_t H, const int32_t* sorted_ids,

@@ -33,13 +33,14 @@ def test_workspace_layout_is_consistent(binding):
     L = binding.nvfp4_moe_workspace_layout(T, H, I, E, k)
     assert L["capacity"] == 55296  # roundup(T*k + 127*E, 128)
     order = ["status", "topk_ids", "topk_w", "block_counts", "counts", "offsets", "meta", "tile_expert",
-             "sorted_token_ids", "row_weight", "inverse", "a1", "sfa1", "a2", "sfa2", "y", "h", "calib"]
+             "sorted_token_ids", "row_weight", "inverse", "a1", "sfa1", "a2", "sfa2", "y", "h", "calib", "tile_done"]
     offs = [L[n] for n in order]
     assert offs == sorted(offs) and all(o % 1024 == 0 for o in offs)
     assert L["status"] == 0  # the status word sits at byte 0 of the workspace
     assert L["sfa1"] - L["a1"] >= L["capacity"] * H // 2
     assert L["h"] - L["y"] >= L["capacity"] * H * 2
     assert L["calib"] - L["h"] >= L["capacity"] * I * 2
+    assert L["total"] - L["tile_done"] >= L["capacity"] // 128 * 4
     assert binding.nvfp4_moe_workspace_size(T, H, I, E, k) == L["total"]
 
 
@@ -153,3 +154,14 @@ def test_status_reader_and_debug_stall_check_arguments_on_host(binding):
             binding.nvfp4_moe_set_debug_stall(bad)
         assert ei.value.status == binding.NVFP4_ERR_INVALID_ARG
     binding.nvfp4_moe_set_debug_stall(0)
+
+
+def test_overlap_switch(binding):
+    prev = binding.nvfp4_moe_set_overlap(0)
+    try:
+        assert prev == 1
+        assert binding.nvfp4_moe_set_overlap(1) == 0
+        with pytest.raises(binding.Nvfp4Error):
+            binding.nvfp4_moe_set_overlap(2)
+    finally:
+        binding.nvfp4_moe_set_overlap(prev)
