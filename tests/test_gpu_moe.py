@@ -712,3 +712,42 @@ def test_device_status_belongs_to_the_call_workspace():
     torch.cuda.synchronize()
     assert fb.status(stream=s2) == B.NVFP4_OK
     np.testing.assert_array_equal(bf16_host(out_b).view(np.uint32), got_a.view(np.uint32))
+
+
+# ----------------------------------------------------------------- L1 -> L2 hand-off per m-tile
+
+@pytest.mark.parametrize("T,E,k", [(300, 5, 3), (128, 32, 6), (1000, 9, 2)])
+def test_l1_l2_overlap_is_bit_identical(T, E, k):
+    """The L2 GEMM taking the L1 output m-tile by m-tile (each L2 tile waits on
+    the device until all of its m-tile's L1 n-tiles are stored) gives exactly
+    the forward where it waits for the whole L1 GEMM: L2 input, output, and a
+    clean status; repeated forwards reuse the per-m-tile counters."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api, binding as B
+    wl = W.moe_workload(T, 1024, 512, E, k, 53, logit_bias_std=1.0)
+    orc = OracleMoE(wl)
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    fwd = api.MoEForward(wl.T, wl.H, wl.I, wl.E, wl.top_k)
+    args = (bf16_dev(wl.hidden), dev(wl.logits), w, dev(orc.a1_gs), dev(orc.a2_gs), wl.gate_limit, wl.up_limit)
+    res = {}
+    prev = B.nvfp4_moe_set_overlap(0)
+    try:
+        for ov in (0, 1, 1):
+            B.nvfp4_moe_set_overlap(ov)
+            out = fwd(*args)
+            torch.cuda.synchronize()
+            P = int(host(fwd.view("meta", torch.int32, 1))[0])
+            res.setdefault(ov, []).append((host(out.view(torch.int16)).copy(),
+                                           host(fwd.view("a2", torch.uint8, P * wl.I // 2)).copy()))
+            assert fwd.status() == 0
+    finally:
+        B.nvfp4_moe_set_overlap(prev)
+    for got in res[1]:
+        for a, b in zip(got, res[0][0]):
+            np.testing.assert_array_equal(a, b)
+    P = orc.meta["P"]
+    done = host(fwd.view("tile_done", torch.int32, P // 128))
+    assert (done == wl.I // 128).all()  # every m-tile counted all of its L1 n-tiles
+    ref, _ = orc.forward()
+    rf, cs = rel_frob(bf16_host(out), ref), cosine(bf16_host(out), ref)
+    assert rf <= 2e-2 and cs >= 0.999, (rf, cs)
