@@ -24,15 +24,16 @@ __device__ __forceinline__ uint4 ldg_nc(const uint16_t* p) {
 // Partial max |x| of group blockIdx.y over the blocks of the x grid: the
 // group's rows are read as one sequence of 16-byte vectors (row r, vector c
 // at index r*K/8 + c), strided over the whole grid, kAmaxUnroll independent
-// loads in flight per thread.  Thread i's (row, vector) pair advances by the
-// grid stride incrementally, so the loop has no 64-bit division.
+// loads in flight per thread.  Thread i's vector pointer advances by the
+// grid stride with additions (no division in the loop), and the maxima of
+// the two bf16 halves of a word are kept packed (one vmax per word).
 constexpr int kAmaxThreads = 256;
 constexpr int kAmaxUnroll = 8;   // 128 bytes in flight per thread
 constexpr int kAmaxBlocksPerSm = 4;
 
-__global__ void __launch_bounds__(kAmaxThreads, kAmaxBlocksPerSm) group_amax_kernel(const uint16_t* __restrict__ x, int64_t rows,
-                                                                  int64_t K, int64_t ld_x, int64_t gstride_x,
-                                                                  float* __restrict__ partial, int partial_stride) {
+__global__ void __launch_bounds__(kAmaxThreads, kAmaxBlocksPerSm)
+    group_amax_kernel(const uint16_t* __restrict__ x, int64_t rows, int64_t K, int64_t ld_x, int64_t gstride_x,
+                      float* __restrict__ partial, int partial_stride) {
   pdl_trigger();
   pdl_wait();
   const int g = blockIdx.y;
@@ -41,28 +42,33 @@ __global__ void __launch_bounds__(kAmaxThreads, kAmaxBlocksPerSm) group_amax_ker
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t sr = stride / vpr, sc = stride - sr * vpr;
   int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  int64_t r = i / vpr, c = i - r * vpr;
-  const uint16_t* xg = x + (int64_t)g * gstride_x;
-  uint32_t m = 0;  // max of |bf16| bit patterns (monotone for non-negative floats)
+  const int64_t r0 = i / vpr;
+  int64_t c = i - r0 * vpr;
+  // the thread's next vector, advanced by the grid stride with pointer adds
+  const uint16_t* ptr = x + (int64_t)g * gstride_x + r0 * ld_x + c * 8;
+  const int64_t step_elems = sr * ld_x + sc * 8, wrap_elems = ld_x - vpr * 8;
+  uint32_t m = 0;  // max of |bf16| bit patterns per half (monotone for non-negative floats)
   for (; i < total; i += kAmaxUnroll * stride) {
     uint4 v[kAmaxUnroll];
 #pragma unroll
     for (int u = 0; u < kAmaxUnroll; ++u) {
-      v[u] = i + u * stride < total ? ldg_nc(xg + r * ld_x + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+      v[u] = i + u * stride < total ? ldg_nc(ptr) : make_uint4(0u, 0u, 0u, 0u);
+      ptr += step_elems;
       c += sc;
-      r += sr;
       if (c >= vpr) {
         c -= vpr;
-        ++r;
+        ptr += wrap_elems;
       }
     }
 #pragma unroll
     for (int u = 0; u < kAmaxUnroll; ++u) {
-      const uint32_t w[4] = {v[u].x & 0x7FFF7FFFu, v[u].y & 0x7FFF7FFFu, v[u].z & 0x7FFF7FFFu, v[u].w & 0x7FFF7FFFu};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) m = max(m, max(w[q] & 0xFFFFu, w[q] >> 16));
+      m = __vmaxu2(m, v[u].x & 0x7FFF7FFFu);
+      m = __vmaxu2(m, v[u].y & 0x7FFF7FFFu);
+      m = __vmaxu2(m, v[u].z & 0x7FFF7FFFu);
+      m = __vmaxu2(m, v[u].w & 0x7FFF7FFFu);
     }
   }
+  m = max(m & 0xFFFFu, m >> 16);
 #pragma unroll
   for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
   __shared__ uint32_t red[32];
@@ -319,11 +325,16 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
   const int64_t sf_cols = K / 16;
   int64_t have_g = -1;
   float gsv = 0.f;
-  for (int64_t item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); item < items;
-       item += (int64_t)gridDim.x * (blockDim.x >> 5)) {
-    const int64_t g = item / per_group;
-    const int64_t rem = item - g * per_group;
-    const int64_t r = rem / segs, e0 = (rem - r * segs) * 1024;
+  // item = (g * rows_padded + r) * segs + sg, stepped by the grid's warp
+  // count with additions and at most one carry per level (no division in the loop)
+  const int64_t first = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t step = (int64_t)gridDim.x * (blockDim.x >> 5);
+  int64_t g = first / per_group, r = (first - g * per_group) / segs;
+  int64_t sg = first - g * per_group - r * segs;
+  const int64_t dg = step / per_group, dr = (step - dg * per_group) / segs;
+  const int64_t ds = step - dg * per_group - dr * segs;
+  for (int64_t item = first; item < items; item += step) {
+    const int64_t rem = r * segs + sg, e0 = sg * 1024;
     const int64_t orow = g * rows_padded + r;
     uint32_t raw[2][8];
 #pragma unroll
@@ -349,6 +360,17 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
         if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(orow, el / 16, sf_cols)) = word;
       }
     }
+    sg += ds;
+    if (sg >= segs) {
+      sg -= segs;
+      ++r;
+    }
+    r += dr;
+    if (r >= rows_padded) {
+      r -= rows_padded;
+      ++g;
+    }
+    g += dg;
   }
 }
 
@@ -416,9 +438,13 @@ __global__ void __launch_bounds__(256) slot_quantize_kernel(const uint16_t* __re
   const int64_t P = min((int64_t)meta[0], capacity);
   const int64_t segs = (K + 1023) / 1024;
   const int64_t sf_cols = K / 16;
-  for (int64_t item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); item < P * segs;
-       item += (int64_t)gridDim.x * (blockDim.x >> 5)) {
-    const int64_t r = item / segs, e0 = (item - r * segs) * 1024;
+  // item = r * segs + sg, stepped with additions (no division in the loop)
+  const int64_t first = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t step = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t dr = step / segs, ds = step - dr * segs;
+  int64_t r = first / segs, sg = first - r * segs;
+  for (int64_t item = first; item < P * segs; item += step, r += dr) {
+    const int64_t e0 = sg * 1024;
     const float gsv = gs_of_amax_bits(amax_bits[tile_expert[r >> 7]]);
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
@@ -436,6 +462,11 @@ __global__ void __launch_bounds__(256) slot_quantize_kernel(const uint16_t* __re
         *reinterpret_cast<uint2*>(fp4 + r * (K / 2) + el / 2) = make_uint2(lo, hi);
         if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(r, el / 16, sf_cols)) = word;
       }
+    }
+    sg += ds;
+    if (sg >= segs) {
+      sg -= segs;
+      ++r;
     }
   }
 }
