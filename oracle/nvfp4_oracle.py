@@ -50,6 +50,15 @@ notes):
       given, expert e's L2 global scale is 2688 / amax of its own bf16 L1
       output h in this forward (1 when that amax is 0); h is quantized with it
       exactly as with a given scale.
+  R20 FP8 L1 output (the survey's FP8/BF16 L1-output option when no
+      calibrated L2 scale exists; the pages name the option, not a format):
+      the bf16 h is stored as OCP E4M3 values in blocks of 16 consecutive
+      features of a row, each block with a power-of-two scale 2^k, k the least
+      integer with max|h_block| <= 448 * 2^k (clamped to [-126, 126]; k = 0
+      for an all-zero block): code = E4M3(h / 2^k), round to nearest even, a
+      zero magnitude without sign.  h8 = dec(code) * 2^k replaces h from there
+      on: the L2 scale is 2688 / amax(h8) of the expert's rows (R19) and h8 is
+      quantized with it.
 """
 from __future__ import annotations
 
@@ -352,6 +361,38 @@ def bf16_round(x):
     return u.astype(np.uint32).view(np.float32)
 
 
+def fp8_block_exponent(amax) -> np.ndarray:
+    """R20: the least k with amax <= 448 * 2^k, clamped to [-126, 126]; 0 for
+    amax == 0.  448 = 1.75 * 2^8, so with amax = m * 2^E (m in [1, 2)):
+    k = E - 8, plus 1 when m > 1.75."""
+    a = np.asarray(amax, dtype=np.float64)
+    f, ex = np.frexp(a)                      # a = f * 2^ex, f in [0.5, 1)
+    k = (ex.astype(np.int64) - 1) - 8 + (2.0 * f > 1.75)
+    k = np.clip(k, -126, 126)
+    return np.where(a > 0, k, 0).astype(np.int64)
+
+
+def fp8_block_encode(h):
+    """R20: h [n, I] (bf16 values, I % 16 == 0) -> E4M3 codes uint8 [n, I] and
+    block exponents k int64 [n, I/16]."""
+    h = np.asarray(h, dtype=np.float64)
+    n, I = h.shape
+    blk = h.reshape(n, I // 16, 16)
+    k = fp8_block_exponent(np.max(np.abs(blk), axis=2))
+    scaled = blk / np.exp2(k)[:, :, None]     # exact: a power of two
+    mag = e4m3_encode(np.abs(scaled)).astype(np.uint8)
+    sign = np.where((scaled < 0) & (mag != 0), 0x80, 0).astype(np.uint8)
+    return (mag | sign).reshape(n, I), k
+
+
+def fp8_block_decode(codes, k):
+    """R20: dec(code) * 2^k as FP32 values [n, I]."""
+    codes = np.asarray(codes)
+    n, I = codes.shape
+    v = e4m3_decode(codes).reshape(n, I // 16, 16) * np.exp2(np.asarray(k, dtype=np.float64))[:, :, None]
+    return v.reshape(n, I).astype(np.float32)
+
+
 # --------------------------------------------------------------------------- the MoE forward
 
 def quantize_expert_weights(w, gs=None):
@@ -397,24 +438,27 @@ def remap_global_ids(topk_ids, topk_weights, experts_start, num_experts):
 
 
 def moe_forward(hidden, logits, top_k, w13q, w2q, a1_gs, a2_gs,
-                gate_limit=10.0, up_limit=10.0, return_intermediates=False):
+                gate_limit=10.0, up_limit=10.0, return_intermediates=False, l1_fp8=False):
     """The sparse MoE forward: route -> slots -> per expert (quantize, L1,
     SwiGLU, requantize, L2) -> routing-weighted combine.  hidden [T,H] FP32
     values (bf16-exact); w13q/w2q = (nibbles, scales, gs) per expert.
     Returns bf16 values as FP32 [T, H]."""
     ids, w = route(logits, top_k)
     return moe_forward_routed(hidden, ids, w, w13q, w2q, a1_gs, a2_gs, gate_limit, up_limit,
-                              return_intermediates)
+                              return_intermediates, l1_fp8)
 
 
 def moe_forward_routed(hidden, ids, w, w13q, w2q, a1_gs, a2_gs,
-                       gate_limit=10.0, up_limit=10.0, return_intermediates=False):
+                       gate_limit=10.0, up_limit=10.0, return_intermediates=False, l1_fp8=False):
     """The MoE forward from given routing: local expert ids [T,k] (-1 = not
     local, R18) and weights [T,k]; otherwise as moe_forward.
     a2_gs None (R19): each expert's L2 global scale is 2688/amax of its own
     bf16 L1 output in this batch ([vllm] warm-up paragraph: the L2 scale is
     measured on the L1 GEMM's output; [cutedsl] BF16 L1 output when no
-    calibrated L2 scale exists)."""
+    calibrated L2 scale exists).  l1_fp8 (with a2_gs None, R20): h is first
+    stored as FP8 blocks and the L2 input is taken from those values."""
+    if l1_fp8 and a2_gs is not None:
+        raise ValueError("the FP8 L1 output applies when the L2 scales come from the batch")
     hidden = np.asarray(hidden, dtype=np.float32)
     T, H = hidden.shape
     E = w13q[0].shape[0]
@@ -430,6 +474,8 @@ def moe_forward_routed(hidden, ids, w, w13q, w2q, a1_gs, a2_gs,
         toks = meta["sorted_token_ids"][lo:lo + n]
         h = expert_l1(hidden[toks], a1_gs[e], w13q[0][e], w13q[1][e], w13q[2][e],
                       gate_limit, up_limit)
+        if l1_fp8:
+            h = fp8_block_decode(*fp8_block_encode(h))
         a2e = global_scale(np.max(np.abs(h))) if a2_gs is None else a2_gs[e]
         Y = expert_l2(h, a2e, w2q[0][e], w2q[1][e], w2q[2][e])
         np.add.at(acc, toks, meta["row_weight"][lo:lo + n, None] * Y)
