@@ -280,6 +280,19 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     batch_scale_ms = max_over_ranks(b0.elapsed_time(b1) / n_bs, world)
 
+    # the same with the L1 output kept as FP8 blocks instead of bf16
+    def step_batch_scale_fp8():
+        fwd(L["hidden"], L["logits"], w, L["a1"], None, GATE_LIMIT, UP_LIMIT, out=out, l1_output="fp8")
+
+    for _ in range(3):
+        step_batch_scale_fp8()
+    b0.record(stream)
+    for _ in range(n_bs):
+        step_batch_scale_fp8()
+    b1.record(stream)
+    torch.cuda.synchronize()
+    batch_scale_fp8_ms = max_over_ranks(b0.elapsed_time(b1) / n_bs, world)
+
     # ---- per-stage breakdown in a separate pass, events recorded by the library
     # on the launching stream before each stage
     n_stage = max(1, min(args.steps, 20))
@@ -368,6 +381,10 @@ def run_ours(args, world, rank, local):
                            "ms_per_step": round(batch_scale_ms, 4),
                            "note": f"{n_bs} forwards with a2_gs NULL: bf16 L1 output + per-expert amax, "
                                    "then a quantize pass with scales from the batch (8 launches + 1 memset)"},
+        "batch_l2_scale_fp8": {"value": round(whole_job_throughput(T, world, batch_scale_fp8_ms), 1), "unit": UNIT,
+                               "ms_per_step": round(batch_scale_fp8_ms, 4),
+                               "note": f"{n_bs} forwards as batch_l2_scale with the L1 output kept as FP8 blocks "
+                                       "(E4M3, a power-of-two scale per 16 features) instead of bf16"},
         "e2e": {"value": round(whole_job_throughput(T, world, e2e_ms), 1), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": pipe.h2d_bytes, "d2h_bytes_per_step": pipe.d2h_bytes,
                 "mode": "api.HostPipeline: pinned host inputs uploaded and output downloaded every step; "

@@ -243,6 +243,28 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
                       float gate_limit, float up_limit, void* workspace, size_t workspace_bytes, void* out,
                       void* stream);
 
+/*
+ * nvfp4_moe_forward_l1_fp8 -- nvfp4_moe_forward with the L2 activation scales
+ * taken from the batch (a2_gs NULL behaviour) and the L1 output kept as FP8
+ * instead of bf16 until it is requantized (the FP8/BF16 L1-output option; the
+ * pages name the option, the format is this library's reading of it): the
+ * bf16 SwiGLU output h is stored as OCP E4M3 codes in blocks of 16 features
+ * of a row, each block with a power-of-two scale 2^k, k the least integer
+ * with max|h_block| <= 448 * 2^k (clamped to [-126, 126], 0 for a zero
+ * block), code = E4M3(h / 2^k) rounded to nearest even with no negative zero;
+ * h8 = dec(code) * 2^k then replaces h: a2_gs[e] = 2688 / amax(h8 of expert
+ * e's rows) and h8 is quantized to NVFP4 with it.  Half the bytes of the bf16
+ * round trip.  In the layout the h region holds the codes [capacity][I] and
+ * then the block exponents k + 127 [capacity][I/16]; the scales land in calib
+ * as with a2_gs NULL.  Arguments, requirements and errors as
+ * nvfp4_moe_forward without a2_gs.
+ */
+int nvfp4_moe_forward_l1_fp8(const void* hidden, const float* router_logits, int64_t T, int64_t H, int64_t I,
+                             int E, int top_k, const void* w13, const void* w13_sf, const float* w13_gs,
+                             const void* w2, const void* w2_sf, const float* w2_gs, const float* a1_gs,
+                             float gate_limit, float up_limit, void* workspace, size_t workspace_bytes, void* out,
+                             void* stream);
+
 /* The same forward with expert parallelism: routing comes from the model's
  * router as global top-k ids (vllm page, "Root cause of CUDA_ERROR_ASSERT
  * index out of bounds", fixes 1-2: experts_start_idx; global ids remapped to

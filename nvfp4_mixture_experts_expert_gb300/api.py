@@ -109,14 +109,24 @@ class MoEForward:
         self.layout = B.nvfp4_moe_workspace_layout(T, H, I, E, top_k)
 
     def __call__(self, hidden, logits, w: MoEWeights, a1_gs, a2_gs, gate_limit=10.0, up_limit=10.0, out=None,
-                 stream=None):
+                 stream=None, l1_output="bf16"):
         """a2_gs None: each expert's L2 activation scale is taken from this
-        batch's own L1 output (read back with batch_l2_scales())."""
+        batch's own L1 output (read back with batch_l2_scales()), kept as bf16
+        or (l1_output="fp8") as FP8 blocks until it is requantized."""
         if out is None:
             out = torch.empty((self.T, self.H), dtype=torch.bfloat16, device=hidden.device)
-        B.nvfp4_moe_forward(hidden, logits, self.T, self.H, self.I, self.E, self.top_k, w.w13, w.w13_sf,
-                            w.w13_gs, w.w2, w.w2_sf, w.w2_gs, a1_gs, a2_gs, gate_limit, up_limit,
-                            self.workspace, self.ws_bytes, out, stream)
+        if l1_output == "fp8":
+            if a2_gs is not None:
+                raise ValueError("the FP8 L1 output applies when the L2 scales come from the batch (a2_gs None)")
+            B.nvfp4_moe_forward_l1_fp8(hidden, logits, self.T, self.H, self.I, self.E, self.top_k, w.w13, w.w13_sf,
+                                       w.w13_gs, w.w2, w.w2_sf, w.w2_gs, a1_gs, gate_limit, up_limit,
+                                       self.workspace, self.ws_bytes, out, stream)
+        elif l1_output == "bf16":
+            B.nvfp4_moe_forward(hidden, logits, self.T, self.H, self.I, self.E, self.top_k, w.w13, w.w13_sf,
+                                w.w13_gs, w.w2, w.w2_sf, w.w2_gs, a1_gs, a2_gs, gate_limit, up_limit,
+                                self.workspace, self.ws_bytes, out, stream)
+        else:
+            raise ValueError(f"l1_output must be 'bf16' or 'fp8', not {l1_output!r}")
         return out
 
     def routed(self, hidden, topk_ids, topk_weights, experts_start, w: MoEWeights, a1_gs, a2_gs, gate_limit=10.0,

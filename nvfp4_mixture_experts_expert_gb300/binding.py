@@ -78,6 +78,9 @@ _moe_layout = _sig("nvfp4_moe_workspace_layout", c_int, [c_i64, c_i64, c_i64, c_
 _moe_forward = _sig("nvfp4_moe_forward", c_int, [c_ptr, c_ptr, c_i64, c_i64, c_i64, c_int, c_int, c_ptr, c_ptr,
                                                  c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_float, c_float, c_ptr,
                                                  c_size, c_ptr, c_ptr])
+_moe_forward_l1_fp8 = _sig("nvfp4_moe_forward_l1_fp8", c_int, [c_ptr, c_ptr, c_i64, c_i64, c_i64, c_int, c_int,
+                                                               c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr, c_ptr,
+                                                               c_float, c_float, c_ptr, c_size, c_ptr, c_ptr])
 _moe_forward_routed = _sig("nvfp4_moe_forward_routed", c_int, [c_ptr, c_ptr, c_ptr, ctypes.c_int32, c_i64, c_i64,
                                                                c_i64, c_int, c_int, c_ptr, c_ptr, c_ptr, c_ptr,
                                                                c_ptr, c_ptr, c_ptr, c_ptr, c_float, c_float, c_ptr,
@@ -197,6 +200,13 @@ def nvfp4_moe_forward(hidden, router_logits, T, H, I, E, top_k, w13, w13_sf, w13
     _check(_moe_forward(_p(hidden), _p(router_logits), T, H, I, E, top_k, _p(w13), _p(w13_sf), _p(w13_gs),
                         _p(w2), _p(w2_sf), _p(w2_gs), _p(a1_gs), _p(a2_gs), gate_limit, up_limit,
                         _p(workspace), workspace_bytes, _p(out), _stream(stream)))
+
+
+def nvfp4_moe_forward_l1_fp8(hidden, router_logits, T, H, I, E, top_k, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, a1_gs,
+                             gate_limit, up_limit, workspace, workspace_bytes, out, stream=None):
+    _check(_moe_forward_l1_fp8(_p(hidden), _p(router_logits), T, H, I, E, top_k, _p(w13), _p(w13_sf), _p(w13_gs),
+                               _p(w2), _p(w2_sf), _p(w2_gs), _p(a1_gs), gate_limit, up_limit, _p(workspace),
+                               workspace_bytes, _p(out), _stream(stream)))
 
 
 def nvfp4_moe_forward_routed(hidden, topk_ids, topk_weights, experts_start, T, H, I, E, top_k, w13, w13_sf,

@@ -342,9 +342,10 @@ struct Routing {
 int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H, int64_t I, int E, int top_k,
                      const void* w13, const void* w13_sf, const float* w13_gs, const void* w2, const void* w2_sf,
                      const float* w2_gs, const float* a1_gs, const float* a2_gs, float gate_limit, float up_limit,
-                     void* workspace, size_t workspace_bytes, void* out, void* stream) {
+                     void* workspace, size_t workspace_bytes, void* out, void* stream, bool l1_fp8 = false) {
   g_err[0] = 0;
   if (T < 0) return fail(NVFP4_ERR_INVALID_ARG, "T must be >= 0");
+  if (l1_fp8 && a2_gs) return fail(NVFP4_ERR_INVALID_ARG, "the FP8 L1 output takes its L2 scales from the batch");
   if (H <= 0 || H % 256) return fail(NVFP4_ERR_UNSUPPORTED, "H must be a positive multiple of 256");
   if (I <= 0 || I % 128) return fail(NVFP4_ERR_UNSUPPORTED, "I must be a positive multiple of 128");
   if (E < 1 || E > 256) return fail(NVFP4_ERR_UNSUPPORTED, "E must be in [1, 256]");
@@ -417,10 +418,16 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
   g1.q_out = a2;
   g1.q_sf = sfa2;
   g1.q_gs = a2_gs;
+  // the h region holds the bf16 h, or the FP8 codes [cap][I] followed by the
+  // block exponents [cap][I/16]
+  uint8_t* h8 = l1_fp8 ? (uint8_t*)hbuf : nullptr;
+  uint8_t* h8_k = l1_fp8 ? (uint8_t*)hbuf + cap * I : nullptr;
   if (batch_l2_scale) {
-    g1.D = hbuf;
+    g1.D = l1_fp8 ? nullptr : hbuf;
     g1.ldd = I;
     g1.amax_bits = l2_amax;
+    g1.h8 = h8;
+    g1.h8_k = h8_k;
   }
   g1.I = (int)I;
   g1.gate_limit = gate_limit;
@@ -495,8 +502,11 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
   if ((e = launch_gemm(batch_l2_scale ? kEpiSwigluAmax : kEpiSwigluQuant, g1, (int)t1, dev->sms, s, true)) !=
       cudaSuccess)
     return cuda_fail(e, "L1 launch");
-  if (batch_l2_scale && (e = launch_slot_quantize(hbuf, I, meta, tile_expert, cap, l2_amax, E, l2_gs, a2, sfa2,
-                                                  dev->sms, s, true)) != cudaSuccess)
+  if (batch_l2_scale &&
+      (e = l1_fp8 ? launch_slot_quantize_fp8(h8, h8_k, I, meta, tile_expert, cap, l2_amax, E, l2_gs, a2, sfa2,
+                                             dev->sms, s, true)
+                  : launch_slot_quantize(hbuf, I, meta, tile_expert, cap, l2_amax, E, l2_gs, a2, sfa2, dev->sms, s,
+                                         true)) != cudaSuccess)
     return cuda_fail(e, "L2 activation quantize launch");
   stage_mark(5, s);
   if ((e = launch_gemm(kEpiCombine, g2, (int)t2, dev->sms, s, true)) != cudaSuccess)
@@ -519,6 +529,17 @@ int nvfp4_moe_forward(const void* hidden, const float* router_logits, int64_t T,
   const Routing rt{router_logits, nullptr, nullptr, 0};
   return moe_forward_impl(hidden, rt, T, H, I, E, top_k, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, a1_gs, a2_gs,
                           gate_limit, up_limit, workspace, workspace_bytes, out, stream);
+}
+
+int nvfp4_moe_forward_l1_fp8(const void* hidden, const float* router_logits, int64_t T, int64_t H, int64_t I,
+                             int E, int top_k, const void* w13, const void* w13_sf, const float* w13_gs,
+                             const void* w2, const void* w2_sf, const float* w2_gs, const float* a1_gs,
+                             float gate_limit, float up_limit, void* workspace, size_t workspace_bytes, void* out,
+                             void* stream) {
+  if (T > 0 && !router_logits) return fail(NVFP4_ERR_INVALID_ARG, "null pointer");
+  const Routing rt{router_logits, nullptr, nullptr, 0};
+  return moe_forward_impl(hidden, rt, T, H, I, E, top_k, w13, w13_sf, w13_gs, w2, w2_sf, w2_gs, a1_gs, nullptr,
+                          gate_limit, up_limit, workspace, workspace_bytes, out, stream, true);
 }
 
 int nvfp4_moe_forward_routed(const void* hidden, const int32_t* topk_ids, const float* topk_weights,

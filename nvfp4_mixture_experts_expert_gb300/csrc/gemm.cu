@@ -12,8 +12,9 @@
 //                    top_k rows (vllm page: scatter_add with zero-weight pads)
 //   kEpiSwigluAmax   MoE calibration: per-expert amax of the bf16 SwiGLU output
 //                    (vllm page: L2 global scale from the actual L1 output);
-//                    optionally stores that bf16 output (forward with L2
-//                    scales taken from the batch, cutedsl page's BF16 L1 output)
+//                    optionally stores that output, as bf16 or as FP8 blocks
+//                    (forward with L2 scales taken from the batch, the FP8/BF16
+//                    L1-output option)
 //
 // Design (persistent over output tiles, warp-specialised, one CTA per SM):
 //   warp 0   operand producer: per K-stage of 256 elements, the A box (128
@@ -762,7 +763,8 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
       }
     } else if constexpr (EPI == kEpiSwigluAmax) {
       // amax of the bf16 SwiGLU output of this row's 64 features; with D set,
-      // the bf16 values themselves too (row-major, ldd elements per row)
+      // the bf16 values themselves too (row-major, ldd elements per row); with
+      // h8 set, their FP8 block form instead (and the amax of what is stored)
       uint32_t m = 0;
       uint32_t hw[32];
 #pragma unroll
@@ -777,7 +779,38 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
         hw[q] = pack_bf16x2(h0, h1);
         m = max(m, max(hw[q] & 0x7FFFu, (hw[q] >> 16) & 0x7FFFu));
       }
-      if (p.D) {
+      m <<= 16;  // float bits of the largest |h|
+      if (p.h8) {
+        // FP8 blocks: per 16 features the least power-of-two scale that fits the
+        // block into E4M3, the codes of h / 2^k, and the largest stored value
+        const int64_t f0 = (int64_t)nt * 128 + half * 64;
+        uint32_t codes[16], kword = 0, top = 0;
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) {
+          uint32_t bm = 0;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) bm = __vmaxu2(bm, hw[8 * blk + q] & 0x7FFF7FFFu);
+          const float a = __uint_as_float(max(bm & 0xFFFFu, bm >> 16) << 16);
+          const int k = fp8_block_k(a);
+          const float inv = pow2f(-k);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t w0 = hw[8 * blk + 2 * q], w1 = hw[8 * blk + 2 * q + 1];
+            codes[4 * blk + q] = drop_negative_zero_bytes(
+                e4m3x2_code(bf16_lo(w0) * inv, bf16_hi(w0) * inv) |
+                (e4m3x2_code(bf16_lo(w1) * inv, bf16_hi(w1) * inv) << 16));
+          }
+          top = max(top, __float_as_uint(e4m3_value(e4m3_code(a * inv)) * pow2f(k)));
+          kword |= (uint32_t)(k + 127) << (8 * blk);
+        }
+        // 64-byte aligned: I is a multiple of 128 and f0 of 64
+        uint8_t* dst = p.h8 + row * p.I + f0;
+        st_global_v8(dst, codes[0], codes[1], codes[2], codes[3], codes[4], codes[5], codes[6], codes[7]);
+        st_global_v8(dst + 32, codes[8], codes[9], codes[10], codes[11], codes[12], codes[13], codes[14],
+                     codes[15]);
+        *reinterpret_cast<uint32_t*>(p.h8_k + row * (p.I / 16) + f0 / 16) = kword;
+        m = top;
+      } else if (p.D) {
         // 32-byte aligned: the caller passes a 32-byte aligned D and ldd a multiple of 16
         uint16_t* drow = p.D + row * p.ldd + (int64_t)nt * 128 + half * 64;
 #pragma unroll
@@ -787,7 +820,7 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
       }
 #pragma unroll
       for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0 && m) atomicMax(&p.amax_bits[g], m << 16);
+      if (lane == 0 && m) atomicMax(&p.amax_bits[g], m);
     } else if constexpr (PAIR) {  // kEpiCombine through the warp's staging buffer
       // Routing-weighted rows in slot order for the token combine; pad rows
       // carry weight 0 and are written as zeros (nothing reads them).  Each

@@ -62,6 +62,10 @@ cudaError_t launch_gs_from_amax(const uint32_t* amax_bits, int n, float* gs, cud
 cudaError_t launch_slot_quantize(const uint16_t* h, int64_t K, const int32_t* meta, const int32_t* tile_expert,
                                  int64_t capacity, const uint32_t* amax_bits, int E, float* gs_out, uint8_t* fp4,
                                  uint8_t* sf, int num_sms, cudaStream_t s, bool pdl = false);
+// The same from the FP8 block form of h (codes [rows][K], exponents [rows][K/16]).
+cudaError_t launch_slot_quantize_fp8(const uint8_t* h8, const uint8_t* h8_k, int64_t K, const int32_t* meta,
+                                     const int32_t* tile_expert, int64_t capacity, const uint32_t* amax_bits, int E,
+                                     float* gs_out, uint8_t* fp4, uint8_t* sf, int num_sms, cudaStream_t s, bool pdl);
 
 // ---------------------------------------------------------------- route.cu
 constexpr int kRouteTokensPerBlock = 16;
@@ -130,8 +134,13 @@ struct GemmArgs {
   int I;
   float gate_limit;
   float up_limit;
-  // kEpiSwigluAmax: per-group amax of h (float bits, atomicMax)
+  // kEpiSwigluAmax: per-group amax of h (float bits, atomicMax).  With h8
+  // set, h is stored as FP8 blocks instead of bf16 in D: E4M3 codes
+  // [rows][I] in h8 and, per 16 features, the block exponent k + 127 in
+  // h8_k [rows][I/16]; the amax is then that of the stored values.
   uint32_t* amax_bits;
+  uint8_t* h8;
+  uint8_t* h8_k;
   // kEpiCombine
   uint16_t* y;  // bf16 [rows][H], routing-weighted L2 rows in slot order
   const int32_t* sorted_ids;

@@ -129,6 +129,43 @@ __device__ __forceinline__ uint32_t quant_block16_pairs(const uint64_t (&xs2)[8]
   return s;
 }
 
+// FP8 block form of the L1 output: E4M3 codes in blocks of 16 values with a
+// power-of-two scale 2^k, k the least integer with amax <= 448 * 2^k
+// (448 = 1.75 * 2^8: with amax = m * 2^E, k = E - 8, plus 1 when m > 1.75),
+// clamped to [-126, 126]; 0 for an all-zero block.
+__device__ __forceinline__ int fp8_block_k(float amax) {
+  const uint32_t b = __float_as_uint(amax);
+  if (amax == 0.f) return 0;
+  if ((b >> 23) == 0) return -126;  // below 2^-126: the clamp
+  const int k = (int)(b >> 23) - 127 - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+  return k < -126 ? -126 : (k > 126 ? 126 : k);
+}
+__device__ __forceinline__ float pow2f(int k) { return __uint_as_float((uint32_t)(127 + k) << 23); }  // |k| <= 126
+
+// Two E4M3 codes (round to nearest even, saturating): element lo in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2_code(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// Values of the two E4M3 codes in the low 16 bits of c (low byte -> lo),
+// through the exact E4M3 -> f16 conversion and f16 -> f32.
+__device__ __forceinline__ void e4m3x2_value(uint32_t c, float& lo, float& hi) {
+  uint32_t h2;
+  asm("{\n.reg .b16 t;\ncvt.u16.u32 t, %1;\ncvt.rn.f16x2.e4m3x2 %0, t;\n}" : "=r"(h2) : "r"(c));
+  asm("{\n.reg .b16 a, b;\nmov.b32 {a, b}, %2;\ncvt.f32.f16 %0, a;\ncvt.f32.f16 %1, b;\n}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2));
+}
+
+// Clear the sign bit of every byte whose magnitude bits are zero (-0 -> 0).
+__device__ __forceinline__ uint32_t drop_negative_zero_bytes(uint32_t w) {
+  const uint32_t mag = w & 0x7F7F7F7Fu;
+  const uint32_t nonzero = (mag + 0x7F7F7F7Fu) & 0x80808080u;
+  return mag | (w & nonzero);
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 

@@ -471,6 +471,72 @@ __global__ void __launch_bounds__(256) slot_quantize_kernel(const uint16_t* __re
   }
 }
 
+// slot_quantize_kernel from the FP8 block form of h: a lane's 16-element
+// block is 16 code bytes and one exponent byte; the values dec(code) * 2^k
+// are exact in FP32 and quantized exactly as the bf16 values are.
+__global__ void __launch_bounds__(256) slot_quantize_fp8_kernel(const uint8_t* __restrict__ h8,
+                                                                const uint8_t* __restrict__ h8_k, int64_t K,
+                                                                const int32_t* __restrict__ meta,
+                                                                const int32_t* __restrict__ tile_expert,
+                                                                int64_t capacity,
+                                                                const uint32_t* __restrict__ amax_bits, int E,
+                                                                float* __restrict__ gs_out, uint8_t* __restrict__ fp4,
+                                                                uint8_t* __restrict__ sf) {
+  pdl_trigger();
+  pdl_wait();  // h8, the amax words and the slot table come from the kernels before
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < E; i += blockDim.x) gs_out[i] = gs_of_amax_bits(amax_bits[i]);
+  const float rcp6 = __frcp_rn(6.0f);
+  const int lane = threadIdx.x & 31;
+  const int64_t P = min((int64_t)meta[0], capacity);
+  const int64_t segs = (K + 1023) / 1024;
+  const int64_t sf_cols = K / 16;
+  const int64_t first = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t step = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t dr = step / segs, ds = step - dr * segs;
+  int64_t r = first / segs, sg = first - r * segs;
+  for (int64_t item = first; item < P * segs; item += step, r += dr) {
+    const int64_t e0 = sg * 1024;
+    const float gsv = gs_of_amax_bits(amax_bits[tile_expert[r >> 7]]);
+    const uint64_t gs2 = f2_pack(gsv, gsv);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int64_t el = e0 + c * 512 + lane * 16;
+      uint32_t lo = 0u, hi = 0u, sc = 0u;
+      if (el < K) {
+        const uint4 cw = __ldg(reinterpret_cast<const uint4*>(h8 + r * K + el));
+        const float scale = pow2f((int)h8_k[r * sf_cols + el / 16] - 127);
+        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+        uint64_t xs2[8];
+        float b = 0.f;
+        const uint64_t scale2 = f2_pack(scale, scale);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float v0, v1;
+          e4m3x2_value(words[q >> 1] >> (16 * (q & 1)), v0, v1);
+          xs2[q] = f2_mul(f2_mul(f2_pack(v0, v1), scale2), gs2);
+          float x0, x1;
+          f2_unpack(xs2[q], x0, x1);
+          b = fmaxf(b, fmaxf(fabsf(x0), fabsf(x1)));
+        }
+        sc = quant_block16_pairs(xs2, b, rcp6, lo, hi);
+      }
+      const uint32_t word = sc | (__shfl_down_sync(0xffffffffu, sc, 1) << 8) |
+                            (__shfl_down_sync(0xffffffffu, sc, 2) << 16) |
+                            (__shfl_down_sync(0xffffffffu, sc, 3) << 24);
+      if (el < K) {
+        *reinterpret_cast<uint2*>(fp4 + r * (K / 2) + el / 2) = make_uint2(lo, hi);
+        if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sf + sf_offset(r, el / 16, sf_cols)) = word;
+      }
+    }
+    sg += ds;
+    if (sg >= segs) {
+      sg -= segs;
+      ++r;
+    }
+  }
+}
+
 int grid_for(int64_t items, int threads, int num_sms, int per_sm) {
   const int64_t need = (items + threads - 1) / threads;
   const int64_t cap = (int64_t)num_sms * per_sm;
@@ -553,6 +619,14 @@ cudaError_t launch_slot_quantize(const uint16_t* h, int64_t K, const int32_t* me
   const int grid = grid_for(capacity * ((K + 1023) / 1024) * 32, 256, num_sms, 8);
   return launch_kernel(slot_quantize_kernel, dim3(grid), dim3(256), 0, s, pdl, h, K, meta, tile_expert, capacity,
                        amax_bits, E, gs_out, fp4, sf);
+}
+
+cudaError_t launch_slot_quantize_fp8(const uint8_t* h8, const uint8_t* h8_k, int64_t K, const int32_t* meta,
+                                     const int32_t* tile_expert, int64_t capacity, const uint32_t* amax_bits, int E,
+                                     float* gs_out, uint8_t* fp4, uint8_t* sf, int num_sms, cudaStream_t s, bool pdl) {
+  const int grid = grid_for(capacity * ((K + 1023) / 1024) * 32, 256, num_sms, 8);
+  return launch_kernel(slot_quantize_fp8_kernel, dim3(grid), dim3(256), 0, s, pdl, h8, h8_k, K, meta, tile_expert,
+                       capacity, amax_bits, E, gs_out, fp4, sf);
 }
 
 }  // namespace nvfp4

@@ -751,3 +751,58 @@ def test_l1_l2_overlap_is_bit_identical(T, E, k):
     ref, _ = orc.forward()
     rf, cs = rel_frob(bf16_host(out), ref), cosine(bf16_host(out), ref)
     assert rf <= 2e-2 and cs >= 0.999, (rf, cs)
+
+
+# ----------------------------------------------------------------- FP8 L1 output (reading R20)
+
+@pytest.mark.parametrize("T,H,I,E,k,dead", [(120, 512, 256, 6, 2, (3,)), (700, 256, 512, 5, 3, ())])
+def test_fp8_l1_output_matches_oracle(T, H, I, E, k, dead):
+    """L2 scales from the batch with the L1 output kept as FP8 blocks.  The L1
+    GEMM computes the same bf16 h as in the bf16 mode (read from that mode),
+    so every later step is checked bit for bit: the E4M3 codes and block
+    exponents against the oracle's encoding of that h, each expert's L2 scale
+    against 2688 / amax of the stored values, the requantized L2 input against
+    the oracle's quantization of the stored values; then the output end to end."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api
+    wl = W.moe_workload(T, H, I, E, k, 95, dead_experts=dead)
+    orc = OracleMoE(wl)
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    fwd = api.MoEForward(T, H, I, E, k)
+    hidden, logits, a1 = bf16_dev(wl.hidden), dev(wl.logits), dev(orc.a1_gs)
+    fwd(hidden, logits, w, a1, None, wl.gate_limit, wl.up_limit)
+    torch.cuda.synchronize()
+    m = orc.meta
+    P, cap = m["P"], fwd.layout["capacity"]
+    h16 = W.bf16_bits_to_f32(host(fwd.view("h", torch.int16, P * I)).view(np.uint16).reshape(P, I))
+    out = fwd(hidden, logits, w, a1, None, wl.gate_limit, wl.up_limit, l1_output="fp8")
+    torch.cuda.synchronize()
+    assert fwd.status() == 0
+    region = host(fwd.view("h", torch.uint8, cap * I + cap * I // 16))
+    codes = region[:P * I].reshape(P, I)
+    kbytes = region[cap * I:cap * I + P * I // 16].reshape(P, I // 16)
+    scales = host(fwd.batch_l2_scales())
+    a2 = host(fwd.view("a2", torch.uint8, P * I // 2)).reshape(P, I // 2)
+    s_lin = O.unswizzle_scales(host(fwd.view("sfa2", torch.uint8, P * I // 16)), P, I // 16)
+    for e in range(E):
+        lo, n = int(m["offsets"][e]), int(m["counts"][e])
+        if n == 0:
+            assert scales[e] == 1.0
+            continue
+        ref_codes, ref_k = O.fp8_block_encode(h16[lo:lo + n])
+        np.testing.assert_array_equal(codes[lo:lo + n], ref_codes)
+        np.testing.assert_array_equal(kbytes[lo:lo + n].astype(np.int64) - 127, ref_k)
+        h8 = O.fp8_block_decode(codes[lo:lo + n], kbytes[lo:lo + n].astype(np.int64) - 127)
+        assert scales[e] == O.global_scale(np.max(np.abs(h8))), e
+        nib, s = O.quantize_blocks(h8, scales[e])
+        np.testing.assert_array_equal(a2[lo:lo + n], O.pack_nibbles(nib))
+        np.testing.assert_array_equal(s_lin[lo:lo + n], s)
+    for e in dead:
+        assert scales[e] == 1.0
+    ref = O.moe_forward(orc.hidden, wl.logits, k, orc.w13q, orc.w2q, orc.a1_gs, None, wl.gate_limit, wl.up_limit,
+                        l1_fp8=True)
+    got = bf16_host(out)
+    rf, cs = rel_frob(got, ref), cosine(got, ref)
+    assert rf <= 2e-2 and cs >= 0.999, (rf, cs)
+    with pytest.raises(ValueError):
+        fwd(hidden, logits, w, a1, dev(orc.a2_gs), wl.gate_limit, wl.up_limit, l1_output="fp8")
