@@ -520,6 +520,9 @@ MMA_SHAPES = {0: ("cta_group::1 128x256", 128, 256), 1: ("cta_group::2 256x256",
               2: ("cta_group::2 256x128", 256, 128), 3: ("cta_group::1 128x128", 128, 128)}
 
 
+MMA_RATE_FLAGS = 128  # nvfp4_debug_mma_rate: the MMA loop on the whole warp with one elected lane issuing
+
+
 def fp4_ceiling_measurement(local):
     """The bare block-scaled FP4 MMA stream (nvfp4_debug_mma_rate) on every SM,
     per tile shape, on operands made by the library's quantizer: CUDA events
@@ -539,10 +542,10 @@ def fp4_ceiling_measurement(local):
         flop_iter = 2.0 * m * n * 256
         iters = 4096
         args = (fa, fa.numel(), sfa, sfa.numel(), fb, fb.numel(), sfb, sfb.numel(), shape, units)
-        B.nvfp4_debug_mma_rate(*args, iters)  # warm-up
+        B.nvfp4_debug_mma_rate(*args, iters, MMA_RATE_FLAGS)  # warm-up
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        B.nvfp4_debug_mma_rate(*args, iters)
+        B.nvfp4_debug_mma_rate(*args, iters, MMA_RATE_FLAGS)
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1)
@@ -550,7 +553,7 @@ def fp4_ceiling_measurement(local):
         clk = ClockSampler(local)
         e0.record()
         for _ in range(10):
-            B.nvfp4_debug_mma_rate(*args, iters)
+            B.nvfp4_debug_mma_rate(*args, iters, MMA_RATE_FLAGS)
         e1.record()
         torch.cuda.synchronize()
         c = clk.stop()
@@ -560,7 +563,8 @@ def fp4_ceiling_measurement(local):
                      "sm_mhz": c["sm_mhz"] if c else None, "reasons": c["reasons"] if c else None}
     res["status"] = B.nvfp4_device_status()
     res["note"] = ("bare MMA stream: 4 operand sets staged once per CTA, iters x 4 back-to-back MMAs (K=64) "
-                   "into one accumulator, no loads, hand-offs or epilogue")
+                   "into one accumulator, issued as the GEMM issues them (warp-uniform loop, one elected lane), "
+                   "no loads, hand-offs or epilogue")
     return res
 
 
