@@ -190,9 +190,15 @@ int nvfp4_debug_gemm_stall(const void* A, const void* SFA, const float* a_gs, co
  * into TMEM (tcgen05.st, same values); 4 the operand sets re-copied into
  * shared memory with bulk copies (same bytes); 8 the accumulator read with
  * tcgen05.ld plus FP32 work; 16 a tcgen05.fence::after_thread_sync before
- * each 4-MMA stage; 32 an mbarrier wait (already complete) before each stage.
+ * each 4-MMA stage; 32 an mbarrier wait (already complete) before each stage;
+ * 64 the MMA thread copies the stage's scale tiles into TMEM with tcgen05.cp;
+ * 128 the MMA loop runs on the whole warp (warp-uniform operands) with one
+ * elected lane issuing, as the GEMM does; 256 (with 128) a 4-slot ring
+ * protocol between the MMA warp and a second warp; 512 (with 384) the scale
+ * warps as a second hop in that ring; 1024 (with 896) tcgen05 fences around
+ * their arrivals.
  * Device buffers (16-byte aligned): A >= 64 KB, B >= 128 KB, SFA >= 8 KB,
- * SFB >= 16 KB.  1 <= units <= 4096, 0 <= iters <= 2^21, 0 <= flags <= 63.
+ * SFB >= 16 KB.  1 <= units <= 4096, 0 <= iters <= 2^21, 0 <= flags <= 2047.
  * Time it with events around the call.
  */
 int nvfp4_debug_mma_rate(const void* A, size_t a_bytes, const void* SFA, size_t sfa_bytes, const void* B,
