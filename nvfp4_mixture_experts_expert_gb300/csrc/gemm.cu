@@ -91,7 +91,7 @@ constexpr int SF_COL0 = 256;         // scale columns start after the accumulato
 constexpr int SF_COLS_PER_STAGE = 48;  // 4 x (4 SFA + 8 SFB)
 // Warp roles, by warpgroup (setmaxnreg re-balances registers per warpgroup):
 //   WG0  warp 0 operand producer, warp 1 TMEM allocator + MMA issuer, warp 2
-//        scale producer (warp 3 idle)
+//        scale producer, warp 3 the L1 -> L2 hand-off (when it is on)
 //   WG1-2 warps 4-11 epilogue: two per TMEM lane quarter, each owning half of the columns
 //   WG3  warps 12-15 scale staging: one per TMEM lane quarter
 constexpr int EPI_WARP0 = 4;
@@ -138,7 +138,7 @@ struct SmemLayout {
   uint64_t* sf_full;     // [STAGES] scale tiles of a stage are in TMEM
   uint32_t* tmem_slot;
   int* abort_flag;
-  int* tile_arrivals;  // [2] epilogue warps done with the L1 tile of that parity (tile_done hand-off)
+  int* stored;    // L1 -> L2 hand-off: epilogue warps done storing a tile, counted over the kernel
   int* offsets;   // [G+1] padded row offsets
   int* unit_off;  // [G+1] first work unit (m-tile or m-tile pair) of each group
 };
@@ -162,7 +162,7 @@ __device__ __forceinline__ SmemLayout carve(uint8_t* raw, int G) {
   L.drain = L.acc_empty + 1;
   L.tmem_slot = reinterpret_cast<uint32_t*>(L.drain + 1);
   L.abort_flag = reinterpret_cast<int*>(L.tmem_slot + 1);
-  L.tile_arrivals = L.abort_flag + 1;  // [2], by tile parity
+  L.stored = L.abort_flag + 1;
   L.offsets = reinterpret_cast<int*>(L.abort_flag + 3);
   L.unit_off = L.offsets + G + 1;
   return L;
@@ -752,13 +752,11 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
       st_global_v8(p.q_out + row * (p.I / 2) + f0 / 2, words[0], words[1], words[2], words[3], words[4], words[5],
                    words[6], words[7]);
       *reinterpret_cast<uint32_t*>(p.q_sf + sf_offset(row, f0 / 16, p.I / 16)) = scales;
-      if (p.tile_done) {  // the last epilogue warp done with this tile counts it for the L2 GEMM
-        __threadfence();
+      if (p.tile_done) {  // this warp's part of the tile is stored; warp 3 publishes the tile
         __syncwarp();
-        if (lane == 0 && atomicAdd(&L.tile_arrivals[tile & 1], 1) == NUM_EPI_WARPS - 1) {
-          L.tile_arrivals[tile & 1] = 0;
-          __threadfence();
-          atomicAdd(p.tile_done + w.mt, 1);
+        if (lane == 0) {
+          __threadfence_block();
+          atomicAdd_block(L.stored, 1);
         }
       }
     } else if constexpr (EPI == kEpiSwigluAmax) {
@@ -878,6 +876,49 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
   }
 }
 
+// L1 -> L2 hand-off (warp 3, otherwise idle): the epilogue warps count the
+// tiles they have stored in a shared counter (a CTA-scope fence before each
+// count), so tile number j of this CTA is stored once the counter reaches
+// 8 * (j + 1); one lane waits for that, fences at GPU scope and adds the tile
+// to its m-tile's counter, which the L2 GEMM's producers acquire before they
+// copy the m-tile.  One GPU-scope fence per tile instead of one per epilogue
+// thread, and a counter that only grows (no phase to alias).
+template <bool PAIR>
+__device__ void handoff_loop(const GemmArgs& p, const SmemLayout& L, int total, int start, int step, uint32_t rank) {
+  volatile int* abort = L.abort_flag;
+  volatile int* stored = L.stored;
+  const int lane = threadIdx.x & 31;
+  int done = 0;  // valid tiles of this CTA published so far
+  for (int it = start; it < total && !*abort; it += step) {
+    const Work w = decode_work<PAIR>(L, p, it, rank);
+    if (!w.valid) continue;  // the pair's second tile does not exist: its epilogue stores nothing
+    ++done;
+    int ok = 1;
+    if (lane == 0 && *stored < NUM_EPI_WARPS * done) {
+      const uint64_t t0 = global_timer_ns();
+      while (*stored < NUM_EPI_WARPS * done) {
+        __nanosleep(200);
+        if (*abort) {
+          ok = 0;
+          break;
+        }
+        if (global_timer_ns() - t0 > p.timeout_ns) {
+          *abort = 1;
+          if (p.status) atomicExch(p.status, 6 /* NVFP4_ERR_DEVICE_TIMEOUT */);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+    if (lane == 0) {
+      __threadfence();
+      atomicAdd(p.tile_done + w.mt, 1);
+    }
+  }
+  __syncwarp();
+}
+
 template <int EPI, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid_constant__ GemmArgs p) {
   using C = Cfg<PAIR>;
@@ -900,7 +941,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid
     mbar_init(smem_u32(L.acc_empty), PAIR ? 2 * NUM_EPI_WARPS : NUM_EPI_WARPS);
     mbar_init(smem_u32(L.drain), 1);
     *L.abort_flag = 0;
-    L.tile_arrivals[0] = L.tile_arrivals[1] = 0;
+    *L.stored = 0;
     fence_mbar_init();
   }
   // everything below reads what earlier kernels wrote; an L2 GEMM fed per
@@ -967,6 +1008,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid
       if (rank == 0) mma_loop<PAIR>(p, L, total, start, step, tmem);
     } else if (warp == 2) {
       producer_loop<PAIR, true>(p, L, total, start, step, rank);
+    } else if (EPI == kEpiSwigluQuant && p.tile_done) {
+      handoff_loop<PAIR>(p, L, total, start, step, rank);
     }
   } else if (warp < SF_WARP0) {
     regs_inc<REGS_EPI>();
