@@ -142,14 +142,18 @@ int nvfp4_assemble_scales(const void* sf_linear, int64_t sf_cols, const int32_t*
  *   D[g][i][n] = bf16( alpha_g * sum_k A[padded_offsets[g] + i][k] * B[g][n][k] ),
  *   alpha_g = 1 / (a_gs[g] * b_gs[g]), FP32 accumulation.
  *   A    device u8 [rows_capacity][K/2], SFA tile layout over rows_capacity rows
- *   B    device u8 [G][N][K/2] (K-major),  SFB [G][N*K/16] tile layout per group
+ *   B    device u8 [G][N][K/2] (K-major),  SFB [G][roundup(N,128)*K/16] tile
+ *        layout per group (a group's scale rows padded to whole 128-row tiles)
  *   a_gs, b_gs      device f32[G]
  *   padded_offsets  device i32[G+1], multiples of 128, padded_offsets[G] <= rows_capacity
  *   counts          device i32[G] rows actually stored per group (<= its padded
  *                   range), or NULL to store every padded row
  *   D    device bf16; row i of group g starts at D + g*group_stride_d + i*ldd (elements)
- * Requirements: K % 64 == 0, N % 256 == 0, ldd % 8 == 0, group_stride_d % 8 == 0,
- * rows_capacity % 128 == 0, 1 <= G <= 1024.
+ * Requirements: K % 64 == 0, N % 8 == 0, ldd % 8 == 0, group_stride_d % 8 == 0,
+ * rows_capacity % 128 == 0, 1 <= G <= 1024.  Tiles are 128 x 256: with N not a
+ * multiple of 256 the last tile of a row block computes columns past N (from
+ * the next group's B rows, or zeros past the last group's) and stores only
+ * the columns below N.
  */
 int nvfp4_grouped_gemm(const void* A, const void* SFA, const float* a_gs, const void* B, const void* SFB,
                        const float* b_gs, const int32_t* padded_offsets, const int32_t* counts, int groups,

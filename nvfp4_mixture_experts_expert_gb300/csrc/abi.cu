@@ -144,7 +144,7 @@ static int grouped_gemm_impl(const void* A, const void* SFA, const float* a_gs, 
   g_err[0] = 0;
   if (groups < 1 || groups > 1024) return fail(NVFP4_ERR_INVALID_ARG, "groups must be in [1, 1024]");
   if (K <= 0 || K % 64) return fail(NVFP4_ERR_INVALID_ARG, "K must be a positive multiple of 64");
-  if (N <= 0 || N % 256) return fail(NVFP4_ERR_UNSUPPORTED, "N must be a positive multiple of 256");
+  if (N <= 0 || N % 8) return fail(NVFP4_ERR_INVALID_ARG, "N must be a positive multiple of 8");
   if (rows_capacity < 0 || rows_capacity % 128) return fail(NVFP4_ERR_INVALID_ARG, "rows_capacity % 128 != 0");
   if (ldd % 8 || group_stride_d % 8 || ldd < 0 || group_stride_d < 0)
     return fail(NVFP4_ERR_INVALID_ARG, "ldd and group_stride_d must be non-negative multiples of 8");
@@ -170,11 +170,17 @@ static int grouped_gemm_impl(const void* A, const void* SFA, const float* a_gs, 
   a.G = groups;
   a.K = (int)K;
   a.num_kb = (int)((K + 255) / 256);
+  // a ragged N: ceil(N / 256) tiles per row block; the columns past N are
+  // computed (from the next group's B rows, or zeros past the last group) and
+  // not stored; each group's scales span whole 128-row tiles
+  const int64_t n128 = round_up(N, 128);
   a.b_rows_per_group = (int)N;
-  a.n_tiles = (int)(N / 256);
+  a.n_tiles = (int)((N + 255) / 256);
   a.b_second_offset = 128;
   a.b_tile_stride = 256;
-  a.sfb_group_bytes = N * (K / 16);
+  a.sfb_group_bytes = n128 * (K / 16);
+  a.n_valid = N % 256 ? (int)N : 0;
+  a.sfb_tiles = N % 256 ? (int)(n128 / 128) : 0;
   a.D = (uint16_t*)D;
   a.d_vec32 = (reinterpret_cast<uintptr_t>(D) & 31u) == 0 && ldd % 16 == 0 && group_stride_d % 16 == 0;
   a.ldd = ldd;

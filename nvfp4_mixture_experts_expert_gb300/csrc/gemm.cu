@@ -314,7 +314,8 @@ __device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total,
       const int32_t b_row1 = w.g * p.b_rows_per_group + b_r1;
       const uint8_t* sfa = p.sfa + (int64_t)w.mt * kt * 512;
       const uint8_t* sfb0 = p.sfb + w.g * p.sfb_group_bytes + (int64_t)(b_r0 >> 7) * kt * 512;
-      const uint8_t* sfb1 = p.sfb + w.g * p.sfb_group_bytes + (int64_t)(b_r1 >> 7) * kt * 512;
+      const int sf_t1 = p.sfb_tiles > 0 && (b_r1 >> 7) >= p.sfb_tiles ? (b_r0 >> 7) : (b_r1 >> 7);
+      const uint8_t* sfb1 = p.sfb + w.g * p.sfb_group_bytes + (int64_t)sf_t1 * kt * 512;
       for (int kb = 0; kb < p.num_kb; ++kb) {
         if (lane == 0) ok = wait_bounded_spin(empty0 + 8 * stage, phase ^ 1u, abort, p.status, p.timeout_ns);
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -692,21 +693,33 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
       const uint64_t alpha2 = f2_pack(alpha, alpha);
       const int64_t i_local = row - L.offsets[g];
       const bool valid = p.counts ? i_local < p.counts[g] : (p.host_count <= 0 || i_local < p.host_count);
-      if (valid) {
-        uint16_t* drow = p.D + g * p.gstride_d + i_local * p.ldd + (int64_t)nt * BN + half * (BN / 2);
+      // columns of this thread's 32-column chunks that exist (a ragged N ends
+      // inside a tile; the stores stop at the last 8-column group below it)
+      const int col0 = nt * BN + half * (BN / 2);
+      const int ncols = p.n_valid > 0 ? min(BN / 2, p.n_valid - col0) : BN / 2;
+      if (valid && ncols > 0) {
+        uint16_t* drow = p.D + g * p.gstride_d + i_local * p.ldd + col0;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             pk[j] = scaled_bf16x2(v[c][2 * j], v[c][2 * j + 1], alpha2);
-          if (p.d_vec32) {
-            st_global_v8(drow + c * 32, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
-            st_global_v8(drow + c * 32 + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
+          if (c * 32 + 32 <= ncols) {
+            if (p.d_vec32) {
+              st_global_v8(drow + c * 32, pk[0], pk[1], pk[2], pk[3], pk[4], pk[5], pk[6], pk[7]);
+              st_global_v8(drow + c * 32 + 16, pk[8], pk[9], pk[10], pk[11], pk[12], pk[13], pk[14], pk[15]);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(drow + c * 32);
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            }
           } else {
             uint4* dst = reinterpret_cast<uint4*>(drow + c * 32);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            for (int j = 0; j < 4; ++j)
+              if (c * 32 + 8 * j + 8 <= ncols) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
           }
         }
       }

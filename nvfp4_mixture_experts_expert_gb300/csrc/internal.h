@@ -116,6 +116,12 @@ struct GemmArgs {
   int b_tile_stride;     // B rows between consecutive n-tiles
   int n_major;           // tile order: 0 = m-tile major, 1 = n-tile major
   int64_t sfb_group_bytes;
+  // kEpiBf16 with a ragged N (0: every column of every tile is stored): the
+  // columns stored per group, and the 128-row scale tiles a group has (a
+  // tile's second B half beyond them takes the first half's scales; those
+  // columns are not stored)
+  int n_valid;
+  int sfb_tiles;
   // kEpiBf16
   uint16_t* D;
   int64_t ldd;

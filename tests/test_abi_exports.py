@@ -64,8 +64,8 @@ def test_quantize_rejects_bad_arguments_on_host(binding, args, code):
 
 def test_gemm_and_moe_reject_unsupported_shapes(binding):
     with pytest.raises(binding.Nvfp4Error) as ei:
-        binding.nvfp4_grouped_gemm(16, 16, 16, 16, 16, 16, 16, None, 1, 128, 200, 64, 16, 200, 0, stream=0)
-    assert ei.value.status == binding.NVFP4_ERR_UNSUPPORTED
+        binding.nvfp4_grouped_gemm(16, 16, 16, 16, 16, 16, 16, None, 1, 128, 204, 64, 16, 208, 0, stream=0)
+    assert ei.value.status == binding.NVFP4_ERR_INVALID_ARG  # N must be a multiple of 8
     with pytest.raises(binding.Nvfp4Error) as ei:
         binding.nvfp4_moe_forward(16, 16, 4, 4096, 2048, 48, 9, 16, 16, 16, 16, 16, 16, 16, 16, 10.0, 10.0,
                                   16, 1 << 30, 16, stream=0)

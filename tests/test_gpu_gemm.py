@@ -36,7 +36,8 @@ def make_problem(counts, N, K, seed, b_gs=None):
     w = W.bf16_bits_to_f32(W.f32_to_bf16_bits(rng.standard_normal((G, N, K)).astype(np.float32) * np.float32(0.02)))
     bn, bs, bg = O.quantize_expert_weights(w, gs=b_gs)
     Bp = np.stack([O.pack_nibbles(bn[g]) for g in range(G)])
-    SFB = np.stack([O.assemble_scales(bs[g], np.array([0, N]), np.array([0, N])) for g in range(G)])
+    n128 = (N + 127) // 128 * 128  # a group's scales span whole 128-row tiles
+    SFB = np.stack([O.assemble_scales(bs[g], np.array([0, N]), np.array([0, n128])) for g in range(G)])
     ref = [O.nvfp4_gemm(a_deq[g][0], a_deq[g][1], a_gs[g], bn[g], bs[g], bg[g]) for g in range(G)]
     return dict(A=A, SFA=SFA, a_gs=a_gs, B=Bp, SFB=SFB, b_gs=bg, padded=padded, counts=np.int32(counts),
                 cap=cap, ref=ref, G=G, N=N, K=K)
@@ -175,3 +176,30 @@ def test_stalled_pipeline_reports_timeout_and_context_survives(cta_pair):
     assert not D.any()  # nothing was stored
     check(pb, run_gpu(pb))  # the context still works and the result is right
     assert B.nvfp4_device_status() == 0
+
+
+
+@pytest.mark.parametrize("counts,N,K", [
+    ([300], 200, 256),            # N not a multiple of 16: the last 8 columns stored alone
+    ([100, 0, 260], 136, 320),    # one 128-row B half plus 8 columns of the next
+    ([37, 129, 5], 384, 512),     # a tile and a half
+    ([64], 8, 128),               # a single 8-column group
+])
+def test_grouped_gemm_ragged_n_matches_oracle(counts, N, K, cta_pair):
+    """N a multiple of 8 only: the columns past N in a group's last tile are
+    computed from the next group's B rows (or zeros past the last group) and
+    never stored; each group's scales span whole 128-row tiles."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import binding as B
+    pb = make_problem(counts, N, K, seed=sum(counts) + N + K)
+    G = pb["G"]
+    maxrows = int(np.diff(pb["padded"]).max())
+    ld = N + 8  # a gap after each row that must stay untouched
+    D = torch.full((G, maxrows, ld), float("nan"), dtype=torch.bfloat16, device="cuda")
+    B.nvfp4_grouped_gemm(dev(pb["A"]), dev(pb["SFA"]), dev(pb["a_gs"]), dev(pb["B"]), dev(pb["SFB"]),
+                         dev(pb["b_gs"]), dev(pb["padded"]), dev(pb["counts"]), G, pb["cap"], N, K, D, ld,
+                         maxrows * ld)
+    torch.cuda.synchronize()
+    got = bf16_host(D)
+    check(pb, got[:, :, :N])
+    assert np.all(np.isnan(got[:, :, N:]))
