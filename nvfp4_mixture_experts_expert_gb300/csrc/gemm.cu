@@ -43,9 +43,10 @@
 //            32 KB stages, 5-slot scale ring of 6 KB.
 //            The leader CTA (rank 0) issues the MMAs; its commits are
 //            multicast to both CTAs' barriers.  The peer's scale warps arrive
-//            on the leader's sf_full (its operands have landed and its scales
-//            are in its TMEM); its epilogue warps release the accumulator on
-//            the leader's barrier.  An expert's m-tiles are paired in order;
+//            on the leader's sf_full (its scales are in its TMEM), its warp 3
+//            relays the arrival of its operands to the leader's peer_full, and
+//            its epilogue warps release the accumulator on the leader's
+//            barrier.  An expert's m-tiles are paired in order;
 //            an odd last tile is paired with a copy of itself whose rows the
 //            peer does not store.
 // A tile is 128 (per CTA) rows x 256 MMA columns.  For the SwiGLU epilogue the
@@ -91,7 +92,7 @@ constexpr int SF_COL0 = 256;         // scale columns start after the accumulato
 constexpr int SF_COLS_PER_STAGE = 48;  // 4 x (4 SFA + 8 SFB)
 // Warp roles, by warpgroup (setmaxnreg re-balances registers per warpgroup):
 //   WG0  warp 0 operand producer, warp 1 TMEM allocator + MMA issuer, warp 2
-//        scale producer, warp 3 the L1 -> L2 hand-off (when it is on)
+//        scale producer, warp 3 (pair variant, peer CTA) operand-arrival relay
 //   WG1-2 warps 4-11 epilogue: two per TMEM lane quarter, each owning half of the columns
 //   WG3  warps 12-15 scale staging: one per TMEM lane quarter
 constexpr int EPI_WARP0 = 4;
@@ -133,12 +134,13 @@ struct SmemLayout {
   uint64_t* acc_full;
   uint64_t* acc_empty;
   uint64_t* drain;
+  uint64_t* peer_full;  // [STAGES] pair variant, leader: the peer CTA's operands of a stage have landed
   uint64_t* sf_data;     // [SF_STAGES] a scale slot has landed in shared memory
   uint64_t* sf_empty;    // [SF_STAGES] the scale warps have read a scale slot
   uint64_t* sf_full;     // [STAGES] scale tiles of a stage are in TMEM
   uint32_t* tmem_slot;
   int* abort_flag;
-  int* stored;    // L1 -> L2 hand-off: epilogue warps done storing a tile, counted over the kernel
+  int* stored;    // [2] L1 -> L2 hand-off: epilogue warps done storing the tile of that parity
   int* offsets;   // [G+1] padded row offsets
   int* unit_off;  // [G+1] first work unit (m-tile or m-tile pair) of each group
 };
@@ -160,7 +162,8 @@ __device__ __forceinline__ SmemLayout carve(uint8_t* raw, int G) {
   L.acc_full = L.sf_full + C::STAGES;
   L.acc_empty = L.acc_full + 1;
   L.drain = L.acc_empty + 1;
-  L.tmem_slot = reinterpret_cast<uint32_t*>(L.drain + 1);
+  L.peer_full = L.drain + 1;
+  L.tmem_slot = reinterpret_cast<uint32_t*>(L.peer_full + C::STAGES);
   L.abort_flag = reinterpret_cast<int*>(L.tmem_slot + 1);
   L.stored = L.abort_flag + 1;
   L.offsets = reinterpret_cast<int*>(L.abort_flag + 3);
@@ -172,7 +175,7 @@ template <bool PAIR>
 constexpr size_t smem_bytes_for(int G) {
   return 1024 + (size_t)Cfg<PAIR>::STAGES * Cfg<PAIR>::STAGE_BYTES +
          (size_t)Cfg<PAIR>::SF_STAGES * Cfg<PAIR>::SF_SLOT_BYTES + Cfg<PAIR>::EPI_BYTES +
-         8 * (3 * Cfg<PAIR>::STAGES + 2 * Cfg<PAIR>::SF_STAGES + 4) + 16 + 8 * (size_t)(G + 1) + 16;
+         8 * (4 * Cfg<PAIR>::STAGES + 2 * Cfg<PAIR>::SF_STAGES + 4) + 16 + 8 * (size_t)(G + 1) + 16;
 }
 
 // Debug timeline (nvfp4_debug_gemm_trace): SM clock (%clock64) stamps of
@@ -389,8 +392,9 @@ __device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total,
 // have committed (empty[stage]); the stores (a few hundred cycles) run while
 // the stage's operands are still in flight.  sf_full[stage] tells the MMA
 // issuer the scales are in TMEM; it counts the 4 warps (8 in the pair variant:
-// the peer's warps arrive on the leader's barrier, and only after their CTA's
-// operands landed, which the leader cannot see otherwise).
+// the peer's warps arrive on the leader's barrier).  The operands of a stage
+// are on the full barrier of each CTA; the leader sees the peer's through
+// peer_full, arrived on by the peer's relay warp (relay_loop).
 template <bool PAIR>
 __device__ void sf_loop(const GemmArgs& p, const SmemLayout& L, int total, int start, int step, uint32_t tmem,
                         uint32_t rank) {
@@ -433,10 +437,6 @@ __device__ void sf_loop(const GemmArgs& p, const SmemLayout& L, int total, int s
       if (lane == 0) mbar_arrive(smem_u32(&L.sf_empty[slot]));
       tmem_store_wait();
       tc_fence_before();
-      if constexpr (PAIR) {
-        if (lane == 0) ok = wait_bounded_spin(smem_u32(&L.full[stage]), phase, abort, p.status, p.timeout_ns);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      }
       if (lane == 0) {
         if (PAIR && rank) mbar_arrive_remote(mapa_shared(smem_u32(&L.sf_full[stage]), 0));
         else mbar_arrive(smem_u32(&L.sf_full[stage]));
@@ -466,14 +466,15 @@ __device__ void sf_loop(const GemmArgs& p, const SmemLayout& L, int total, int s
 // (a commit tracks the MMAs of the thread that issues it).  A full stage's 4
 // MMAs are unrolled, and the next stage's barriers are tested without
 // blocking while this stage's MMAs issue; lane 0 polls when they were not
-// ready.  A stage may issue once its scales are in TMEM (sf_full) and, in
-// the single variant, its operands have landed (full; in the pair variant
-// sf_full says so).
+// ready.  A stage may issue once its scales are in TMEM (sf_full) and its
+// operands have landed (full; in the pair variant also the peer's, relayed
+// to peer_full).
 template <bool PAIR>
 __device__ __forceinline__ void issue_stage(uint32_t tmem, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t sf_col,
                                             uint32_t first_acc, int nmma, bool full, uint32_t next_bar,
-                                            uint32_t next_bar2, uint32_t next_parity, uint32_t& next_ready) {
-  uint32_t r1 = 1u, r2 = 1u;
+                                            uint32_t next_bar2, uint32_t next_bar3, uint32_t next_parity,
+                                            uint32_t& next_ready) {
+  uint32_t r1 = 1u, r2 = 1u, r3 = 1u;
   if (full) {
     if constexpr (PAIR) {
       tc_mma_nvf4_pair(tmem, ad, bd, idesc, sf_col, sf_col + 16, first_acc);
@@ -481,6 +482,7 @@ __device__ __forceinline__ void issue_stage(uint32_t tmem, uint64_t ad, uint64_t
       tc_mma_nvf4_pair(tmem, ad + 2, bd + 2, idesc, sf_col + 4, sf_col + 24, 1u);
       if (next_bar2) r2 = mbar_test_wait(next_bar2, next_parity);
       tc_mma_nvf4_pair(tmem, ad + 4, bd + 4, idesc, sf_col + 8, sf_col + 32, 1u);
+      if (next_bar3) r3 = mbar_test_wait(next_bar3, next_parity);
       tc_mma_nvf4_pair(tmem, ad + 6, bd + 6, idesc, sf_col + 12, sf_col + 40, 1u);
     } else {
       tc_mma_nvf4(tmem, ad, bd, idesc, sf_col, sf_col + 16, first_acc);
@@ -500,8 +502,9 @@ __device__ __forceinline__ void issue_stage(uint32_t tmem, uint64_t ad, uint64_t
     }
     if (next_bar) r1 = mbar_test_wait(next_bar, next_parity);
     if (next_bar2) r2 = mbar_test_wait(next_bar2, next_parity);
+    if (next_bar3) r3 = mbar_test_wait(next_bar3, next_parity);
   }
-  next_ready = r1 & r2;
+  next_ready = r1 & r2 & r3;
 }
 
 template <bool PAIR>
@@ -516,6 +519,7 @@ __device__ void mma_loop(const GemmArgs& p, const SmemLayout& L, int total, int 
   const uint64_t b_desc0 = smem_desc(smem_u32(L.stages) + A_BYTES, 16, 1024, 2);
   constexpr uint64_t kSlotDesc = C::STAGE_BYTES >> 4;
   const uint32_t sf_full0 = smem_u32(L.sf_full), empty0 = smem_u32(L.empty), full0 = smem_u32(L.full);
+  const uint32_t peer0 = smem_u32(L.peer_full);  // pair variant: the peer's operands (relayed)
   const int num_kb = p.num_kb;
   const bool tr = kTraceBuild && p.trace != nullptr && (int)blockIdx.x == p.trace_cta && leader;
   uint32_t stage = 0, phase = 0, acc_phase = 0;
@@ -530,7 +534,8 @@ __device__ void mma_loop(const GemmArgs& p, const SmemLayout& L, int total, int 
     if (tr) trace_tile(p, tile, 1);
     if (lane == 0) {
       ok = wait_bounded_spin(sf_full0 + 8 * stage, phase, abort, p.status, p.timeout_ns);
-      if (!PAIR && ok) ok = wait_bounded_spin(full0 + 8 * stage, phase, abort, p.status, p.timeout_ns);
+      if (ok) ok = wait_bounded_spin(full0 + 8 * stage, phase, abort, p.status, p.timeout_ns);
+      if (PAIR && ok) ok = wait_bounded_spin(peer0 + 8 * stage, phase, abort, p.status, p.timeout_ns);
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
     for (int kb = 0; ok && kb < num_kb; ++kb) {
@@ -544,7 +549,8 @@ __device__ void mma_loop(const GemmArgs& p, const SmemLayout& L, int total, int 
       if (leader) {
         issue_stage<PAIR>(tmem, a_desc0 + stage * kSlotDesc, b_desc0 + stage * kSlotDesc, idesc,
                           tmem + SF_COL0 + stage * SF_COLS_PER_STAGE, kb != 0, min(4, rem / 64), rem >= 256,
-                          more ? sf_full0 + 8 * next_stage : 0u, more && !PAIR ? full0 + 8 * next_stage : 0u,
+                          more ? sf_full0 + 8 * next_stage : 0u, more ? full0 + 8 * next_stage : 0u,
+                          more && PAIR ? peer0 + 8 * next_stage : 0u,
                           next_phase, next_ready);
         if (tr) trace_stage(p, gstage, 6);
         if constexpr (PAIR) tc_commit_pair_mc(empty0 + 8 * stage, 3);
@@ -560,7 +566,8 @@ __device__ void mma_loop(const GemmArgs& p, const SmemLayout& L, int total, int 
         if (tr) trace_stage(p, gstage, 4);
         if (lane == 0) {
           ok = wait_bounded_spin(sf_full0 + 8 * stage, phase, abort, p.status, p.timeout_ns);
-          if (!PAIR && ok) ok = wait_bounded_spin(full0 + 8 * stage, phase, abort, p.status, p.timeout_ns);
+          if (ok) ok = wait_bounded_spin(full0 + 8 * stage, phase, abort, p.status, p.timeout_ns);
+          if (PAIR && ok) ok = wait_bounded_spin(peer0 + 8 * stage, phase, abort, p.status, p.timeout_ns);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
       }
@@ -765,11 +772,16 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
       st_global_v8(p.q_out + row * (p.I / 2) + f0 / 2, words[0], words[1], words[2], words[3], words[4], words[5],
                    words[6], words[7]);
       *reinterpret_cast<uint32_t*>(p.q_sf + sf_offset(row, f0 / 16, p.I / 16)) = scales;
-      if (p.tile_done) {  // this warp's part of the tile is stored; warp 3 publishes the tile
+      if (p.tile_done) {  // the last of the eight epilogue warps done storing publishes the tile
         __syncwarp();
         if (lane == 0) {
           __threadfence_block();
-          atomicAdd_block(L.stored, 1);
+          int* slot = L.stored + (tile & 1);
+          if (atomicAdd_block(slot, 1) == NUM_EPI_WARPS - 1) {
+            *slot = 0;  // reused two tiles on: no warp reaches that tile before every warp left this one
+            __threadfence();
+            atomicAdd(p.tile_done + w.mt, 1);
+          }
         }
       }
     } else if constexpr (EPI == kEpiSwigluAmax) {
@@ -889,44 +901,29 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
   }
 }
 
-// L1 -> L2 hand-off (warp 3, otherwise idle): the epilogue warps count the
-// tiles they have stored in a shared counter (a CTA-scope fence before each
-// count), so tile number j of this CTA is stored once the counter reaches
-// 8 * (j + 1); one lane waits for that, fences at GPU scope and adds the tile
-// to its m-tile's counter, which the L2 GEMM's producers acquire before they
-// copy the m-tile.  One GPU-scope fence per tile instead of one per epilogue
-// thread, and a counter that only grows (no phase to alias).
+// Pair variant, warp 3 of the peer CTA: relays the arrival of its stage
+// operands (its own full barrier) to the leader's peer_full barrier, so that
+// the leader's MMA waits for both CTAs' operands without the scale warps
+// standing in the chain (they only report their scales, and run ahead).
 template <bool PAIR>
-__device__ void handoff_loop(const GemmArgs& p, const SmemLayout& L, int total, int start, int step, uint32_t rank) {
+__device__ void relay_loop(const GemmArgs& p, const SmemLayout& L, int total, int start, int step) {
+  using C = Cfg<PAIR>;
   volatile int* abort = L.abort_flag;
-  volatile int* stored = L.stored;
   const int lane = threadIdx.x & 31;
-  int done = 0;  // valid tiles of this CTA published so far
-  for (int it = start; it < total && !*abort; it += step) {
-    const Work w = decode_work<PAIR>(L, p, it, rank);
-    if (!w.valid) continue;  // the pair's second tile does not exist: its epilogue stores nothing
-    ++done;
-    int ok = 1;
-    if (lane == 0 && *stored < NUM_EPI_WARPS * done) {
-      const uint64_t t0 = global_timer_ns();
-      while (*stored < NUM_EPI_WARPS * done) {
-        __nanosleep(200);
-        if (*abort) {
-          ok = 0;
-          break;
-        }
-        if (global_timer_ns() - t0 > p.timeout_ns) {
-          *abort = 1;
-          if (p.status) atomicExch(p.status, 6 /* NVFP4_ERR_DEVICE_TIMEOUT */);
-          ok = 0;
-          break;
-        }
+  uint32_t stage = 0, phase = 0;
+  int ok = 1;
+  for (int it = start; it < total && ok; it += step) {
+    for (int kb = 0; kb < p.num_kb; ++kb) {
+      if (lane == 0) {
+        ok = wait_bounded_spin(smem_u32(&L.full[stage]), phase, abort, p.status, p.timeout_ns);
+        if (ok) mbar_arrive_remote(mapa_shared(smem_u32(&L.peer_full[stage]), 0));
       }
-    }
-    if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-    if (lane == 0) {
-      __threadfence();
-      atomicAdd(p.tile_done + w.mt, 1);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (++stage == C::STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
     }
   }
   __syncwarp();
@@ -945,6 +942,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid
       mbar_init(smem_u32(&L.full[s]), 1);
       mbar_init(smem_u32(&L.empty[s]), 1);
       mbar_init(smem_u32(&L.sf_full[s]), PAIR ? 8 : 4);  // scale warps of this CTA (and of the peer)
+      mbar_init(smem_u32(&L.peer_full[s]), 1);          // the peer's relay warp
     }
     for (int s = 0; s < C::SF_STAGES; ++s) {
       mbar_init(smem_u32(&L.sf_data[s]), 1);
@@ -954,7 +952,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid
     mbar_init(smem_u32(L.acc_empty), PAIR ? 2 * NUM_EPI_WARPS : NUM_EPI_WARPS);
     mbar_init(smem_u32(L.drain), 1);
     *L.abort_flag = 0;
-    *L.stored = 0;
+    L.stored[0] = L.stored[1] = 0;
     fence_mbar_init();
   }
   // everything below reads what earlier kernels wrote; an L2 GEMM fed per
@@ -1021,8 +1019,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid
       if (rank == 0) mma_loop<PAIR>(p, L, total, start, step, tmem);
     } else if (warp == 2) {
       producer_loop<PAIR, true>(p, L, total, start, step, rank);
-    } else if (EPI == kEpiSwigluQuant && p.tile_done) {
-      handoff_loop<PAIR>(p, L, total, start, step, rank);
+    } else if (PAIR && rank == 1) {
+      relay_loop<PAIR>(p, L, total, start, step);
     }
   } else if (warp < SF_WARP0) {
     regs_inc<REGS_EPI>();
