@@ -210,7 +210,7 @@ __device__ __forceinline__ uint32_t quant_block16_bf16(const uint32_t (&w)[8], f
 }
 
 template <bool kAligned32, int kChunks>
-__global__ void __launch_bounds__(256) gather_quantize_kernel(const uint16_t* __restrict__ hidden, int64_t H,
+__global__ void __launch_bounds__(256, 4) gather_quantize_kernel(const uint16_t* __restrict__ hidden, int64_t H,
                                                               int64_t T, int top_k,
                                                               const int32_t* __restrict__ topk_ids,
                                                               const int32_t* __restrict__ inverse,
@@ -258,22 +258,25 @@ __global__ void __launch_bounds__(256) gather_quantize_kernel(const uint16_t* __
       const int e = topk_ids[t * top_k + lane];
       my_gs = e >= 0 ? a1_gs[e] : 1.f;
     }
+    // the column part of each lane's scale byte offset in the tile layout (the
+    // row part is added per slot row): each lane stores its own scale byte
+    int64_t sf_col_off[kChunks];
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) sf_col_off[c] = sf_offset(0, (e0 + c * 512 + lane * 16) / 16, sf_cols);
 #pragma unroll 2  // two slots' blocks in flight per lane (independent dependency chains)
     for (int j = 0; j < top_k; ++j) {
       const int64_t r = __shfl_sync(0xffffffffu, my_row, j);
       const float gs = __shfl_sync(0xffffffffu, my_gs, j);
       const bool row_ok = r >= 0 && r < capacity;
+      const int64_t sf_row_off = sf_offset(r, 0, sf_cols);
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) {
         const int64_t el = e0 + c * 512 + lane * 16;
         uint32_t lo, hi;
         const uint32_t sc = quant_block16_bf16(raw[c], amax[c], gs, rcp6, tab, lo, hi);
-        const uint32_t word = sc | (__shfl_down_sync(0xffffffffu, sc, 1) << 8) |
-                              (__shfl_down_sync(0xffffffffu, sc, 2) << 16) |
-                              (__shfl_down_sync(0xffffffffu, sc, 3) << 24);
         if (row_ok && el < H) {
           *reinterpret_cast<uint2*>(a1 + r * (H / 2) + el / 2) = make_uint2(lo, hi);
-          if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(sfa1 + sf_offset(r, el / 16, sf_cols)) = word;
+          sfa1[sf_row_off + sf_col_off[c]] = (uint8_t)sc;
         }
       }
     }
