@@ -368,9 +368,8 @@ int nvfp4_moe_calibrate_routed(const void* hidden, const int32_t* topk_ids, cons
  *   written otherwise),
  *   calib u32[2E] (calibration amax bits; with a2_gs NULL, E amax words of
  *   the L1 output, then the E L2 global scales as f32)
- *   tile_done i32[cap/128] (L1 output stored per m-tile, counted 2 per
- *   finished L1 n-tile, 1 per half of a tail-split one: the L2 GEMM starts
- *   on an m-tile once all of its L1 output is stored)
+ *   tile_done i32[cap/128] (L1 n-tiles finished per m-tile: the L2 GEMM
+ *   starts on an m-tile once all of its L1 output is stored)
  * Only rows < P of the row-indexed buffers are defined after a call; the
  * pad rows of a1 hold zero block scales (every value exactly 0) and
  * unspecified nibble bytes.
@@ -462,25 +461,6 @@ int nvfp4_moe_set_overlap(int enable, int* prev);
  * thread-safe with respect to launches issued concurrently from other host
  * threads; no device work. */
 int nvfp4_gemm_set_cta_pair(int mode, int* prev_mode);
-
-/*
- * nvfp4_gemm_set_tail_split -- the single-CTA GEMMs' last round, in halves.
- *
- * A single-CTA GEMM walks its 128 x 256 output tiles in rounds of one tile
- * per CTA.  With the split on (enable 1, the default) a last round that fills
- * at most half of the grid runs each of its tiles as two 128 x 128 halves
- * (N = 128 MMAs, half of the tile's B rows each; for the SwiGLU L1 GEMM the
- * half of the gate rows and the matching half of the up rows), so twice as
- * many SMs share that round's weight stream.  It applies to the grouped GEMM
- * when N is a multiple of 256, and to the MoE forward's, the calibration's
- * and the shared expert's GEMMs when they run single CTAs (decode-sized
- * batches); CTA pairs never split.  Each output element is the same sum in
- * the same order either way: results are bit-identical.  prev_enable (may be
- * null) receives the previous setting.  Returns NVFP4_OK, or
- * NVFP4_ERR_INVALID_ARG (setting unchanged) for a value other than 0 or 1.
- * Not thread-safe with respect to launches issued concurrently from other
- * host threads; no device work. */
-int nvfp4_gemm_set_tail_split(int enable, int* prev_enable);
 
 /*
  * Optional per-stage timing of nvfp4_moe_forward: when set, the forward

@@ -105,7 +105,6 @@ _mma_rate = _sig("nvfp4_debug_mma_rate", c_int, [c_ptr, c_size, c_ptr, c_size, c
 _stage_events = _sig("nvfp4_moe_set_stage_events", c_int, [ctypes.POINTER(c_ptr), c_int])
 _moe_set_overlap = _sig("nvfp4_moe_set_overlap", c_int, [c_int, ctypes.POINTER(c_int)])
 _gemm_set_cta_pair = _sig("nvfp4_gemm_set_cta_pair", c_int, [c_int, ctypes.POINTER(c_int)])
-_gemm_set_tail_split = _sig("nvfp4_gemm_set_tail_split", c_int, [c_int, ctypes.POINTER(c_int)])
 
 
 def _p(t):
@@ -290,14 +289,6 @@ def nvfp4_gemm_set_cta_pair(mode):
     GEMM only (default).  Returns the previous mode."""
     prev = c_int(-1)
     _check(_gemm_set_cta_pair(int(mode), ctypes.byref(prev)))
-    return prev.value
-
-
-def nvfp4_gemm_set_tail_split(enable):
-    """1 (default): a single-CTA GEMM's last round, when at most half full, runs
-    as N-halves of its tiles; 0: whole tiles only.  Returns the previous setting."""
-    prev = c_int(-1)
-    _check(_gemm_set_tail_split(int(enable), ctypes.byref(prev)))
     return prev.value
 
 

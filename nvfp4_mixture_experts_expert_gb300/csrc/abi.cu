@@ -86,26 +86,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // K-major packed FP4 matrix [rows][K/2] bytes; box 128 bytes x 128 rows, 128-byte swizzle.
-int make_fp4_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows = 128) {
+int make_fp4_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K) {
   auto fn = encode_fn();
   if (!fn) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   const cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-  const cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
+  const cuuint32_t box[2] = {128, 128};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-  return NVFP4_OK;
-}
-
-// SwiGLU GEMMs: the tail split's half tiles take 64 gate and 64 up rows of W13
-// (a second map of the same rows with a 64-row box).
-int enable_swiglu_halves(GemmArgs* g, const void* w13, int64_t rows, int64_t K) {
-  if (int rc = make_fp4_map(&g->tmap_b_half, w13, rows, K, 64)) return rc;
-  g->half_gate_up = 1;
-  g->tail_split = 1;
   return NVFP4_OK;
 }
 
@@ -190,7 +181,6 @@ static int grouped_gemm_impl(const void* A, const void* SFA, const float* a_gs, 
   a.sfb_group_bytes = n128 * (K / 16);
   a.n_valid = N % 256 ? (int)N : 0;
   a.sfb_tiles = N % 256 ? (int)(n128 / 128) : 0;
-  a.tail_split = N % 256 == 0;  // whole tiles only
   a.D = (uint16_t*)D;
   a.d_vec32 = (reinterpret_cast<uintptr_t>(D) & 31u) == 0 && ldd % 16 == 0 && group_stride_d % 16 == 0;
   a.ldd = ldd;
@@ -415,11 +405,9 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
   memset(&g2, 0, sizeof(g2));
   if (int rc = make_fp4_map(&g1.tmap_a, a1, cap, H)) return rc;
   if (int rc = make_fp4_map(&g1.tmap_b, w13, (int64_t)E * 2 * I, H)) return rc;
-  if (int rc = enable_swiglu_halves(&g1, w13, (int64_t)E * 2 * I, H)) return rc;
   if (int rc = make_fp4_map(&g2.tmap_a, a2, cap, I)) return rc;
   if (int rc = make_fp4_map(&g2.tmap_b, w2, (int64_t)E * H, I)) return rc;
   if (int rc = make_bf16_store_map(&g2.tmap_y, ybuf, cap, H)) return rc;
-  g2.tail_split = 1;
   g1.sfa = sfa1;
   g1.sfb = (const uint8_t*)w13_sf;
   g1.padded_offsets = offsets;
@@ -483,7 +471,7 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
   g1.tile_done = tile_done;
   g1.late_trigger = tile_done != nullptr;
   g2.tile_done = tile_done;
-  g2.tile_done_target = tile_done ? 2 * g1.n_tiles : 0;  // a whole L1 tile counts 2, a half 1
+  g2.tile_done_target = tile_done ? g1.n_tiles : 0;
   if (g_debug_stall_ms > 0) g2.timeout_ns = g1.timeout_ns;  // the stalled L1 never completes its m-tiles
 
   const int nb = (int)L.route_blocks;
@@ -637,10 +625,8 @@ int nvfp4_shared_expert_forward(const void* hidden, int64_t T, int64_t H, int64_
   memset(&g2, 0, sizeof(g2));
   if (int rc = make_fp4_map(&g1.tmap_a, a1, L.rows, H)) return rc;
   if (int rc = make_fp4_map(&g1.tmap_b, w13, 2 * I, H)) return rc;
-  if (int rc = enable_swiglu_halves(&g1, w13, 2 * I, H)) return rc;
   if (int rc = make_fp4_map(&g2.tmap_a, a2, L.rows, I)) return rc;
   if (int rc = make_fp4_map(&g2.tmap_b, w2, H, I)) return rc;
-  g2.tail_split = 1;
   // L1: one group, SwiGLU + requantization into A2 (gate rows 0..I-1, up rows I..2I-1)
   g1.sfa = sfa1;
   g1.sfb = (const uint8_t*)w13_sf;
@@ -752,7 +738,6 @@ int calibrate_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H, 
   memset(&g1, 0, sizeof(g1));
   if (int rc = make_fp4_map(&g1.tmap_a, a1, cap, H)) return rc;
   if (int rc = make_fp4_map(&g1.tmap_b, w13, (int64_t)E * 2 * I, H)) return rc;
-  if (int rc = enable_swiglu_halves(&g1, w13, (int64_t)E * 2 * I, H)) return rc;
   g1.sfa = sfa1;
   g1.sfb = (const uint8_t*)w13_sf;
   g1.padded_offsets = offsets;
@@ -821,14 +806,6 @@ int nvfp4_gemm_set_cta_pair(int mode, int* prev_mode) {
   if (mode < 0 || mode > 2) return fail(NVFP4_ERR_INVALID_ARG, "mode must be 0, 1 or 2");
   const int prev = gemm_set_pair_mode(mode);
   if (prev_mode) *prev_mode = prev;
-  return NVFP4_OK;
-}
-
-int nvfp4_gemm_set_tail_split(int enable, int* prev_enable) {
-  g_err[0] = 0;
-  if (enable != 0 && enable != 1) return fail(NVFP4_ERR_INVALID_ARG, "enable must be 0 or 1");
-  const int prev = gemm_set_tail_split(enable);
-  if (prev_enable) *prev_enable = prev;
   return NVFP4_OK;
 }
 

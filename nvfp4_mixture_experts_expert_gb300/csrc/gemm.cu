@@ -49,10 +49,6 @@
 //            barrier.  An expert's m-tiles are paired in order;
 //            an odd last tile is paired with a copy of itself whose rows the
 //            peer does not store.
-// Tail split (single variant): when the last round of whole tiles would fill
-// at most half of the grid, each of its tiles runs as two 128 x 128 halves
-// (N = 128 MMAs over half of the tile's B rows), so twice as many SMs stream
-// that round's weights; every output element is the same sum either way.
 // A tile is 128 (per CTA) rows x 256 MMA columns.  For the SwiGLU epilogue the
 // two B boxes are the gate rows [n0, n0+128) and the up rows [I+n0, I+n0+128)
 // of the expert's W13, so gate and up of one output feature sit in the same
@@ -111,7 +107,6 @@ static_assert(128 * (2 * REGS_SMALL + 2 * REGS_EPI) <= NUM_THREADS * REGS_LAUNCH
 constexpr int MAX_GROUPS = 1024;
 constexpr int MAX_GROUPS_PAIR = 256;        // the pair variant's shared memory also holds the staging buffers
 constexpr int EPI_STAGE_BYTES = 32 * 128;   // per epilogue warp (pair): 32 rows x 64 bf16 columns
-int g_gemm_tail_split = 1;  // host: tail split of the GEMMs that allow it (gemm_set_tail_split)
 
 template <bool PAIR>
 struct Cfg {
@@ -223,28 +218,14 @@ __device__ __forceinline__ int find_group(const int* off, int G, int row) {
 // unit is two consecutive m-tiles of one group (rank 0 takes the first); the
 // second of an odd group's last pair does not exist (valid = false) and that
 // CTA reloads the first tile so every copy stays inside the operands.
-// Tail split (single CTAs): items [0, split) are whole tiles; items split + 2j
-// and split + 2j + 1 are the N-halves (half 0 and 1) of whole tile split + j.
 struct Work {
   int g, mt, nt;
-  int half;  // -1: the whole tile; 0 / 1: that N-half of it
   bool valid;
 };
 
-// First split item: the whole tiles minus the ones cut into halves (== total
-// when nothing is split).
-__device__ __forceinline__ int split_base(const SmemLayout& L, const GemmArgs& p, int total) {
-  return 2 * (L.unit_off[p.G] * p.n_tiles) - total;
-}
-__device__ __forceinline__ int item_half(int it, int split) { return it >= split ? (it - split) & 1 : -1; }
-
 template <bool PAIR>
-__device__ __forceinline__ Work decode_work(const SmemLayout& L, const GemmArgs& p, int it, uint32_t rank,
-                                            int split) {
+__device__ __forceinline__ Work decode_work(const SmemLayout& L, const GemmArgs& p, int it, uint32_t rank) {
   const int nu = L.unit_off[p.G];
-  Work w;
-  w.half = PAIR ? -1 : item_half(it, split);  // pairs never split
-  if (w.half >= 0) it = split + ((it - split) >> 1);
   int u, nt;
   if (p.n_major) {
     nt = it / nu;
@@ -253,6 +234,7 @@ __device__ __forceinline__ Work decode_work(const SmemLayout& L, const GemmArgs&
     u = it / p.n_tiles;
     nt = it - u * p.n_tiles;
   }
+  Work w;
   w.g = find_group(L.unit_off, p.G, u);
   w.nt = nt;
   const int t0 = L.offsets[w.g] / BM, k = u - L.unit_off[w.g];
@@ -317,11 +299,10 @@ __device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total,
   const uint32_t done0 = smem_u32(SCALES ? L.sf_data : L.full);
   const uint32_t slot0 = smem_u32(SCALES ? L.sf_slots : L.stages);
   const bool per_tile = p.tile_done && p.tile_done_target > 0;  // L2 fed per m-tile by L1
-  const int split = split_base(L, p, total);
   int ready_mt = -1;
   if (!p.debug_no_loads) {
     for (int it = start; it < total && ok && !*abort; it += step) {
-      const Work w = decode_work<PAIR>(L, p, it, rank, split);
+      const Work w = decode_work<PAIR>(L, p, it, rank);
       if (per_tile && w.mt != ready_mt) {
         if (lane == 0) ok = wait_count_bounded(p.tile_done + w.mt, p.tile_done_target, abort, p.status, p.timeout_ns);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -353,18 +334,13 @@ __device__ void producer_loop(const GemmArgs& p, const SmemLayout& L, int total,
             bulk_load(st + SFA_BYTES, sfb0 + kb * 2048, bytes, bar);
             bulk_load(st + SFA_BYTES + 2048, sfb1 + kb * 2048, bytes, bar);
           } else {
-            mbar_arrive_expect_tx(bar, A_BYTES + (w.half < 0 ? C::B_BYTES : C::B_BYTES / 2));
+            mbar_arrive_expect_tx(bar, A_BYTES + C::B_BYTES);
             tma_load_2d(st, &p.tmap_a, kb * BK_BYTES, a_row, bar);
             if constexpr (PAIR) {  // this CTA's half of the B tile
               tma_load_2d(st + A_BYTES, &p.tmap_b, kb * BK_BYTES, rank ? b_row1 : b_row0, bar);
-            } else if (w.half < 0) {
+            } else {
               tma_load_2d(st + A_BYTES, &p.tmap_b, kb * BK_BYTES, b_row0, bar);
               tma_load_2d(st + A_BYTES + C::B_BYTES / 2, &p.tmap_b, kb * BK_BYTES, b_row1, bar);
-            } else if (p.half_gate_up) {  // 64 gate rows, then the matching 64 up rows
-              tma_load_2d(st + A_BYTES, &p.tmap_b_half, kb * BK_BYTES, b_row0 + 64 * w.half, bar);
-              tma_load_2d(st + A_BYTES + C::B_BYTES / 4, &p.tmap_b_half, kb * BK_BYTES, b_row1 + 64 * w.half, bar);
-            } else {  // one of the tile's two 128-row boxes
-              tma_load_2d(st + A_BYTES, &p.tmap_b, kb * BK_BYTES, w.half ? b_row1 : b_row0, bar);
             }
           }
         }
@@ -430,30 +406,21 @@ __device__ void sf_loop(const GemmArgs& p, const SmemLayout& L, int total, int s
   uint32_t slot = 0, sphase = 0;  // scale ring slot
   int gstage = 0;
   const bool tracer = kTraceBuild && warp == SF_WARP0 && lane == 0;
-  const int split = split_base(L, p, total);
   for (int it = start; it < total; it += step) {
     int ok = 1;
-    const int hh = PAIR ? -1 : item_half(it, split);
     for (int kb = 0; kb < p.num_kb; ++kb) {
       if (lane == 0) ok = wait_bounded_spin(smem_u32(&L.sf_data[slot]), sphase, abort, p.status, p.timeout_ns);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       // columns of a stage: SFA of K-steps 0-3 (4 each), then per K-step the
       // SFB tiles of B rows 0-127 and 128-255 (4 each); unused K-steps of a
-      // partial last stage carry stale scales that no MMA reads.  A half
-      // tile's N = 128 MMA reads one SFB tile: word c of line l is B row
-      // 32c + l, so a SwiGLU half (gate rows 64h.., then up rows 64h..) takes
-      // words 2h, 2h+1 of the gate tile's line and of the up tile's line.
+      // partial last stage carry stale scales that no MMA reads
       const uint8_t* sf = L.sf_slots + slot * C::SF_SLOT_BYTES + 16 * lane;
       uint32_t r[48];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint4 a = *reinterpret_cast<const uint4*>(sf + 512 * i);
-        uint4 b0 = *reinterpret_cast<const uint4*>(sf + SFA_BYTES + 512 * i);
+        const uint4 b0 = *reinterpret_cast<const uint4*>(sf + SFA_BYTES + 512 * i);
         const uint4 b1 = *reinterpret_cast<const uint4*>(sf + SFA_BYTES + 2048 + 512 * i);
-        if (hh >= 0) {
-          if (p.half_gate_up) b0 = hh ? make_uint4(b0.z, b0.w, b1.z, b1.w) : make_uint4(b0.x, b0.y, b1.x, b1.y);
-          else if (hh) b0 = b1;
-        }
         r[4 * i + 0] = a.x, r[4 * i + 1] = a.y, r[4 * i + 2] = a.z, r[4 * i + 3] = a.w;
         r[16 + 8 * i + 0] = b0.x, r[16 + 8 * i + 1] = b0.y, r[16 + 8 * i + 2] = b0.z, r[16 + 8 * i + 3] = b0.w;
         r[16 + 8 * i + 4] = b1.x, r[16 + 8 * i + 5] = b1.y, r[16 + 8 * i + 6] = b1.z, r[16 + 8 * i + 7] = b1.w;
@@ -547,9 +514,7 @@ __device__ void mma_loop(const GemmArgs& p, const SmemLayout& L, int total, int 
   const int lane = threadIdx.x & 31;
   const bool leader = elect_one();
   const int leader_lane = __ffs(__ballot_sync(0xffffffffu, leader)) - 1;
-  const uint32_t idesc_whole = idesc_nvf4(PAIR ? 2 * BM : BM, BN);
-  const uint32_t idesc_half = idesc_nvf4(BM, BN / 2);  // a tail-split half tile (single CTAs)
-  const int split = split_base(L, p, total);
+  const uint32_t idesc = idesc_nvf4(PAIR ? 2 * BM : BM, BN);
   const uint64_t a_desc0 = smem_desc(smem_u32(L.stages), 16, 1024, 2);
   const uint64_t b_desc0 = smem_desc(smem_u32(L.stages) + A_BYTES, 16, 1024, 2);
   constexpr uint64_t kSlotDesc = C::STAGE_BYTES >> 4;
@@ -563,7 +528,6 @@ __device__ void mma_loop(const GemmArgs& p, const SmemLayout& L, int total, int 
   int ok = 1;
   for (int it = start; it < total && ok && !*abort; it += step, ++tile) {
     if (tr) trace_tile(p, tile, 0);
-    const uint32_t idesc = !PAIR && item_half(it, split) >= 0 ? idesc_half : idesc_whole;
     if (lane == 0) ok = wait_bounded_spin(smem_u32(L.acc_empty), acc_phase ^ 1u, abort, p.status, p.timeout_ns);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) break;
@@ -670,23 +634,6 @@ __device__ __forceinline__ void silu_clamped_product2(float g0, float g1, float 
   f2_unpack(f2_mul(f2_mul(g2, sig2), f2_pack(u0, u1)), h0, h1);
 }
 
-// L1 -> L2 hand-off: the last of the eight epilogue warps done with a tile
-// (after its stores) adds the tile's share to its m-tile's counter: 2 for a
-// whole tile, 1 for each half of a split one.
-__device__ __forceinline__ void publish_tile(const GemmArgs& p, const SmemLayout& L, int tile, int mt, int share,
-                                             int lane) {
-  __syncwarp();
-  if (lane == 0) {
-    __threadfence_block();
-    int* slot = L.stored + (tile & 1);
-    if (atomicAdd_block(slot, 1) == NUM_EPI_WARPS - 1) {
-      *slot = 0;  // reused two tiles on: no warp reaches that tile before every warp left this one
-      __threadfence();
-      atomicAdd(p.tile_done + mt, share);
-    }
-  }
-}
-
 // Each epilogue thread first copies its 128 accumulator columns (one row)
 // from TMEM into registers and releases the accumulator, so the MMAs of the
 // next tile overlap all of the epilogue arithmetic and stores below.
@@ -703,16 +650,11 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
   const uint32_t acc_empty = PAIR && rank ? mapa_shared(smem_u32(L.acc_empty), 0) : smem_u32(L.acc_empty);
   uint32_t acc_phase = 0;
   const bool tracer = kTraceBuild && warp == EPI_WARP0 && lane == 0;
-  const int split = split_base(L, p, total);
   int tile = 0;
   for (int it = start; it < total; it += step, ++tile) {
     // the tile and its per-tile parameters, loaded while the MMAs run
-    const Work w = decode_work<PAIR>(L, p, it, rank, split);
+    const Work w = decode_work<PAIR>(L, p, it, rank);
     const int g = w.g, nt = w.nt;
-    // a half tile (N = 128 accumulator columns) is read by the first four
-    // warps, one per lane quarter; the other four only release it
-    const bool idle = w.half >= 0 && half == 1;
-    const int sub = w.half >= 0 ? w.half : half;  // which half of the whole tile's output columns
     const int64_t row = (int64_t)w.mt * BM + row_in_tile;
     const float gs_a = p.a_gs[g], gs_b = p.b_gs[g];
     float tile_param = 0.f;  // SwiGLU requant: the L2 activation scale; combine: the row's weight
@@ -732,15 +674,15 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
     __syncwarp();
     tc_fence_after();
     // SwiGLU kinds: gate columns [half*64, +64) and up columns 128 + [half*64, +64);
-    // other kinds: columns [half*128, +128).  A half tile: gate [0, 64) and up
-    // [64, 128), or columns [0, 128).  (Two 64-column loads: a 128-column load
-    // needs more registers than the kernel is compiled with.)
-    constexpr bool kSwiglu = EPI == kEpiSwigluQuant || EPI == kEpiSwigluAmax;
-    const uint32_t c0 = w.half >= 0 ? 0u : (uint32_t)(kSwiglu ? half * 64 : half * 128);
-    const uint32_t c1 = w.half >= 0 ? 64u : (uint32_t)(kSwiglu ? 128 + half * 64 : half * 128 + 64);
+    // other kinds: columns [half*128, +128).
     uint32_t v[4][32];
-    tmem_load_64(t_base + c0, v[0], v[1]);
-    tmem_load_64(t_base + c1, v[2], v[3]);
+    if constexpr (EPI == kEpiSwigluQuant || EPI == kEpiSwigluAmax) {
+      tmem_load_64(t_base + half * 64, v[0], v[1]);
+      tmem_load_64(t_base + 128 + half * 64, v[2], v[3]);
+    } else {  // (a 128-column load needs more registers than the kernel is compiled with)
+      tmem_load_64(t_base + half * 128, v[0], v[1]);
+      tmem_load_64(t_base + half * 128 + 64, v[2], v[3]);
+    }
     tmem_load_wait();
     tc_fence_before();
     __syncwarp();
@@ -752,11 +694,6 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
     if (tracer) trace_tile(p, tile, 3);
 
     if (!w.valid) continue;  // the pair's second tile does not exist: nothing to store
-    if (idle) {
-      if constexpr (EPI == kEpiSwigluQuant)
-        if (p.tile_done) publish_tile(p, L, tile, w.mt, 1, lane);
-      continue;
-    }
     const float alpha = 1.0f / (gs_a * gs_b);
 
     if constexpr (EPI == kEpiBf16) {
@@ -765,7 +702,7 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
       const bool valid = p.counts ? i_local < p.counts[g] : (p.host_count <= 0 || i_local < p.host_count);
       // columns of this thread's 32-column chunks that exist (a ragged N ends
       // inside a tile; the stores stop at the last 8-column group below it)
-      const int col0 = nt * BN + sub * (BN / 2);
+      const int col0 = nt * BN + half * (BN / 2);
       const int ncols = p.n_valid > 0 ? min(BN / 2, p.n_valid - col0) : BN / 2;
       if (valid && ncols > 0) {
         uint16_t* drow = p.D + g * p.gstride_d + i_local * p.ldd + col0;
@@ -794,7 +731,7 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
         }
       }
     } else if constexpr (EPI == kEpiSwigluQuant) {
-      // output features [nt*128 + sub*64, +64) of one row = 4 quantization blocks
+      // output features [nt*128 + half*64, +64) of one row = 4 quantization blocks
       // (pairs of features per instruction where the arithmetic allows it;
       // every value is rounded exactly as by the scalar operations)
       const float qgs = tile_param;
@@ -830,12 +767,23 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
         words[blk * 2] = lo;
         words[blk * 2 + 1] = hi;
       }
-      const int64_t f0 = (int64_t)nt * 128 + sub * 64;  // first output feature of this thread
+      const int64_t f0 = (int64_t)nt * 128 + half * 64;  // first output feature of this thread
       // workspace rows: 32-byte aligned (I/2 and f0/2 are multiples of 32 bytes)
       st_global_v8(p.q_out + row * (p.I / 2) + f0 / 2, words[0], words[1], words[2], words[3], words[4], words[5],
                    words[6], words[7]);
       *reinterpret_cast<uint32_t*>(p.q_sf + sf_offset(row, f0 / 16, p.I / 16)) = scales;
-      if (p.tile_done) publish_tile(p, L, tile, w.mt, w.half >= 0 ? 1 : 2, lane);
+      if (p.tile_done) {  // the last of the eight epilogue warps done storing publishes the tile
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence_block();
+          int* slot = L.stored + (tile & 1);
+          if (atomicAdd_block(slot, 1) == NUM_EPI_WARPS - 1) {
+            *slot = 0;  // reused two tiles on: no warp reaches that tile before every warp left this one
+            __threadfence();
+            atomicAdd(p.tile_done + w.mt, 1);
+          }
+        }
+      }
     } else if constexpr (EPI == kEpiSwigluAmax) {
       // amax of the bf16 SwiGLU output of this row's 64 features; with D set,
       // the bf16 values themselves too (row-major, ldd elements per row); with
@@ -858,7 +806,7 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
       if (p.h8) {
         // FP8 blocks: per 16 features the least power-of-two scale that fits the
         // block into E4M3, the codes of h / 2^k, and the largest stored value
-        const int64_t f0 = (int64_t)nt * 128 + sub * 64;
+        const int64_t f0 = (int64_t)nt * 128 + half * 64;
         uint32_t codes[16], kword = 0, top = 0;
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {
@@ -887,7 +835,7 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
         m = top;
       } else if (p.D) {
         // 32-byte aligned: the caller passes a 32-byte aligned D and ldd a multiple of 16
-        uint16_t* drow = p.D + row * p.ldd + (int64_t)nt * 128 + sub * 64;
+        uint16_t* drow = p.D + row * p.ldd + (int64_t)nt * 128 + half * 64;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           st_global_v8(drow + c * 16, hw[8 * c], hw[8 * c + 1], hw[8 * c + 2], hw[8 * c + 3], hw[8 * c + 4],
@@ -932,7 +880,7 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
       if (row_id >= 0) {
         const float wgt = tile_param * alpha;
         const uint64_t wgt2 = f2_pack(wgt, wgt);
-        uint16_t* dst = p.y + row * p.H + (int64_t)nt * BN + sub * (BN / 2);
+        uint16_t* dst = p.y + row * p.H + (int64_t)nt * BN + half * (BN / 2);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
@@ -1058,17 +1006,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) nvfp4_gemm_kernel(const __grid
   else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *L.tmem_slot;
-  const int whole = L.unit_off[p.G] * p.n_tiles;
+  const int total = L.unit_off[p.G] * p.n_tiles;
   const int start = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int step = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-  // tail split: the r whole tiles of a last round that fills at most half of
-  // the grid become 2r half tiles, at most one per CTA (its last item)
-  int tail = 0;
-  if (!PAIR && p.tail_split) {
-    tail = whole % step;
-    if (2 * tail > step) tail = 0;
-  }
-  const int total = whole + tail;
 
   // each warpgroup changes its register budget first thing in its own branch
   if (warp < EPI_WARP0) {
@@ -1193,14 +1133,7 @@ cudaError_t launch_kind(const GemmArgs& a, int units_upper, int num_sms, cudaStr
       return launch_one<EPI, true>(a, want < pairs ? (want < 1 ? 1 : want) : pairs, s, pdl);
     }
   }
-  // with the tail split, up to twice as many items as whole tiles
-  if (a.tail_split && !g_gemm_tail_split) {
-    GemmArgs b = a;
-    b.tail_split = 0;
-    return launch_one<EPI, false>(b, units_upper < num_sms ? (units_upper < 1 ? 1 : units_upper) : num_sms, s, pdl);
-  }
-  const int64_t items = (int64_t)units_upper * (a.tail_split ? 2 : 1);
-  return launch_one<EPI, false>(a, items < num_sms ? (items < 1 ? 1 : (int)items) : num_sms, s, pdl);
+  return launch_one<EPI, false>(a, units_upper < num_sms ? (units_upper < 1 ? 1 : units_upper) : num_sms, s, pdl);
 }
 
 }  // namespace
@@ -1220,11 +1153,6 @@ bool gemm_pair_enabled(int kind, bool hint) {
 int gemm_set_pair_mode(int mode) {
   const int prev = g_gemm_pair_mode;
   g_gemm_pair_mode = mode;
-  return prev;
-}
-int gemm_set_tail_split(int enable) {
-  const int prev = g_gemm_tail_split;
-  g_gemm_tail_split = enable;
   return prev;
 }
 

@@ -101,7 +101,6 @@ struct GemmArgs {
   CUtensorMap tmap_a;  // A: [rows][K/2] bytes, box 128 B x 128 rows, 128-byte swizzle
   CUtensorMap tmap_b;  // B: [G * b_rows_per_group][K/2] bytes, same box
   CUtensorMap tmap_y;  // kEpiCombine, pair variant: y as bf16 [rows][H], box 64 x 32, 128-byte swizzle
-  CUtensorMap tmap_b_half;  // half_gate_up: B as tmap_b with a 64-row box (a half tile's gate and up rows)
   const uint8_t* sfa;  // tile-layout scales of A (rows x K/16)
   const uint8_t* sfb;  // tile-layout scales of B, sfb_group_bytes per group
   const int32_t* padded_offsets;  // [G+1]
@@ -123,14 +122,6 @@ struct GemmArgs {
   // columns are not stored)
   int n_valid;
   int sfb_tiles;
-  // Tail split (single CTAs, whole tiles only: n_valid == 0).  When the last
-  // round of whole tiles fills at most half of the grid, each of its tiles
-  // runs as two N = 128 halves on two SMs.  A half of a SwiGLU tile
-  // (half_gate_up) is 64 gate rows and the matching 64 up rows (two 64-row
-  // boxes of tmap_b_half); a half of any other tile is one of its two 128-row
-  // B boxes.
-  int tail_split;
-  int half_gate_up;
   // kEpiBf16
   uint16_t* D;
   int64_t ldd;
@@ -163,13 +154,12 @@ struct GemmArgs {
   int H;
   // Hand-off of the MoE forward's L1 output to the L2 GEMM per m-tile, so
   // that the L2 GEMM runs on the SMs the L1 GEMM's last partial round leaves
-  // idle.  L1 (kEpiSwigluQuant): tile_done[mt] += 2 once a whole tile's A2
-  // rows and scales are stored (+= 1 per half tile); late_trigger: its
-  // dependent launch is released only after its own dependency wait (so the
-  // L2 kernel starts after every kernel before L1 completed).  L2
-  // (kEpiCombine, tile_done_target > 0): no dependency wait; before it loads
-  // m-tile mt it waits until tile_done[mt] == tile_done_target (twice the L1
-  // tiles per m-tile).  tile_done is zeroed by the gather.
+  // idle.  L1 (kEpiSwigluQuant): tile_done[mt] += 1 once a tile's A2 rows and
+  // scales are stored; late_trigger: its dependent launch is released only
+  // after its own dependency wait (so the L2 kernel starts after every kernel
+  // before L1 completed).  L2 (kEpiCombine, tile_done_target > 0): no
+  // dependency wait; before it loads m-tile mt it waits until
+  // tile_done[mt] == tile_done_target.  tile_done is zeroed by the gather.
   int* tile_done;
   int tile_done_target;
   int late_trigger;
@@ -200,9 +190,6 @@ cudaError_t launch_gemm(int kind, const GemmArgs& args, int units_upper, int num
 // mode.
 bool gemm_pair_enabled(int kind, bool hint);
 int gemm_set_pair_mode(int mode);
-// Tail split of the single-CTA GEMMs that allow it (GemmArgs::tail_split): 1 on
-// (default), 0 off; returns the previous setting.
-int gemm_set_tail_split(int enable);
 // Debug timeline of the next GEMM launches of epilogue kind `kind` (-1: off;
 // 4: the MMA-rate kernel).
 void gemm_set_trace(unsigned long long* buf, int stages, int tiles, int kind);

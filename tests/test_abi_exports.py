@@ -156,18 +156,6 @@ def test_status_reader_and_debug_stall_check_arguments_on_host(binding):
     binding.nvfp4_moe_set_debug_stall(0)
 
 
-def test_tail_split_switch(binding):
-    prev = binding.nvfp4_gemm_set_tail_split(0)
-    try:
-        assert prev == 1
-        assert binding.nvfp4_gemm_set_tail_split(1) == 0
-        with pytest.raises(binding.Nvfp4Error):
-            binding.nvfp4_gemm_set_tail_split(2)
-        assert binding.nvfp4_gemm_set_tail_split(1) == 1
-    finally:
-        binding.nvfp4_gemm_set_tail_split(prev)
-
-
 def test_overlap_switch(binding):
     prev = binding.nvfp4_moe_set_overlap(0)
     try:

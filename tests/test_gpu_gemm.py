@@ -105,30 +105,6 @@ def test_pair_and_single_cta_gemm_are_bit_identical():
         np.testing.assert_array_equal(d_pair[g, :c], d_single[g, :c])
 
 
-@pytest.mark.parametrize("counts,N,K", [
-    ([128], 256, 256),                  # one whole tile: its two halves on two CTAs
-    ([2560], 2048, 256),                # 160 tiles on 152 SMs: 144 whole, the last 8 as 16 halves
-    ([300, 0, 129, 640, 5], 512, 768),  # several groups, every tile split
-])
-def test_tail_split_is_bit_identical_and_matches_oracle(counts, N, K):
-    """Single-CTA GEMM with the last round's tiles run as N = 128 halves gives
-    exactly the whole-tile result, and both match the oracle."""
-    from nvfp4_mixture_experts_expert_gb300 import binding as B
-    pb = make_problem(counts, N, K, seed=sum(counts) + 3 * N + K)
-    prev_pair = B.nvfp4_gemm_set_cta_pair(False)
-    prev = B.nvfp4_gemm_set_tail_split(1)
-    try:
-        d_split = run_gpu(pb)
-        B.nvfp4_gemm_set_tail_split(0)
-        d_whole = run_gpu(pb)
-    finally:
-        B.nvfp4_gemm_set_tail_split(prev)
-        B.nvfp4_gemm_set_cta_pair(prev_pair)
-    for g, c in enumerate(pb["counts"]):
-        np.testing.assert_array_equal(d_split[g, :c], d_whole[g, :c])
-    check(pb, d_split)
-
-
 def test_gemm_rows_beyond_counts_are_not_written():
     pb = make_problem([10, 50], 256, 256, seed=1)
     D = run_gpu(pb)

@@ -747,44 +747,7 @@ def test_l1_l2_overlap_is_bit_identical(T, E, k):
             np.testing.assert_array_equal(a, b)
     P = orc.meta["P"]
     done = host(fwd.view("tile_done", torch.int32, P // 128))
-    assert (done == 2 * (wl.I // 128)).all()  # every m-tile counted all of its L1 n-tiles (2 each)
-    ref, _ = orc.forward()
-    rf, cs = rel_frob(bf16_host(out), ref), cosine(bf16_host(out), ref)
-    assert rf <= 2e-2 and cs >= 0.999, (rf, cs)
-
-
-@pytest.mark.parametrize("T,H,I,E,k", [(256, 512, 1024, 20, 2), (64, 256, 512, 8, 2)])
-def test_tail_split_forward_is_bit_identical(T, H, I, E, k):
-    """Decode-sized forward (single-CTA GEMMs): with the last round of L1 tiles
-    run as gate/up halves (the first case: ~160 L1 tiles on 152 SMs, the last
-    8 split; every L2 tile split) the L2 input, the output and the per-m-tile
-    hand-off counts equal those of whole tiles, and the output matches the
-    oracle."""
-    import torch
-    from nvfp4_mixture_experts_expert_gb300 import api, binding as B
-    wl = W.moe_workload(T, H, I, E, k, 61, logit_bias_std=0.5)
-    orc = OracleMoE(wl)
-    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
-    fwd = api.MoEForward(wl.T, wl.H, wl.I, wl.E, wl.top_k)
-    args = (bf16_dev(wl.hidden), dev(wl.logits), w, dev(orc.a1_gs), dev(orc.a2_gs), wl.gate_limit, wl.up_limit)
-    res = {}
-    prev = B.nvfp4_gemm_set_tail_split(0)
-    try:
-        for split in (0, 1, 1):
-            B.nvfp4_gemm_set_tail_split(split)
-            out = fwd(*args)
-            torch.cuda.synchronize()
-            P = int(host(fwd.view("meta", torch.int32, 1))[0])
-            done = host(fwd.view("tile_done", torch.int32, P // 128)).copy()
-            assert (done == 2 * (I // 128)).all(), done
-            res.setdefault(split, []).append((host(out.view(torch.int16)).copy(),
-                                              host(fwd.view("a2", torch.uint8, P * I // 2)).copy()))
-            assert fwd.status() == 0
-    finally:
-        B.nvfp4_gemm_set_tail_split(prev)
-    for got in res[1]:
-        for a, b in zip(got, res[0][0]):
-            np.testing.assert_array_equal(a, b)
+    assert (done == wl.I // 128).all()  # every m-tile counted all of its L1 n-tiles
     ref, _ = orc.forward()
     rf, cs = rel_frob(bf16_host(out), ref), cosine(bf16_host(out), ref)
     assert rf <= 2e-2 and cs >= 0.999, (rf, cs)
