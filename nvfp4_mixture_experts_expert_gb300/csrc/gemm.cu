@@ -665,8 +665,8 @@ __device__ void epilogue_loop(const GemmArgs& p, const SmemLayout& L, int total,
       if constexpr (!PAIR) row_id = p.sorted_ids[row];
     }
     int ok = 1;
-    // off the critical path (the accumulator is released right after its
-    // load): poll with short sleeps rather than spinning beside the MMA warp
+    // polled (a suspending wait, or 128 ns sleeps between polls, timed the
+    // same or slower: the spinning lanes do not slow the MMA warp measurably)
     if (lane == 0) ok = wait_bounded_spin(smem_u32(L.acc_full), acc_phase, abort, p.status, p.timeout_ns);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) break;
