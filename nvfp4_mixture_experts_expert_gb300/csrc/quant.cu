@@ -85,6 +85,10 @@ __global__ void __launch_bounds__(kAmaxThreads, kAmaxBlocksPerSm)
 // gs = 2688 / amax (IEEE division), 1 when the group is all zero.
 __device__ __forceinline__ float gs_from_group_amax(float a) { return a > 0.f ? __fdiv_rn(kGsNumerator, a) : 1.0f; }
 
+// quantize_kernel: up to this many groups' global scales are reduced per
+// block into shared memory.
+constexpr int kSharedGsGroups = 1024;
+
 // The global scale of group g from its nb partial maxima, reduced by one warp
 // (max is exact and order-free, so every warp gets the same bits).
 __device__ __forceinline__ float warp_group_gs(const float* __restrict__ partial, int partial_stride, int nb,
@@ -236,7 +240,8 @@ __global__ void __launch_bounds__(256, 4) gather_quantize_kernel(const uint16_t*
   const int64_t segs = (H + seg_elems - 1) / seg_elems;
   const int64_t sf_cols = H / 16;
   if (item < T * segs) {
-    const int64_t t = item / segs, e0 = (item - t * segs) * seg_elems;
+    const int64_t t = item < (1ll << 31) ? (int64_t)((uint32_t)item / (uint32_t)segs) : item / segs;
+    const int64_t e0 = (item - t * segs) * seg_elems;
     uint32_t raw[kChunks][8];
     float amax[kChunks];
 #pragma unroll
@@ -311,6 +316,8 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
                                                        int64_t rows_padded, int* __restrict__ status_reset) {
   pdl_trigger();
   __shared__ float2 tab[128];
+  __shared__ float s_gs[kSharedGsGroups];
+  __shared__ float s_red[8];
   if (threadIdx.x < 128) {
     const float d = e4m3_value(threadIdx.x);
     tab[threadIdx.x] = make_float2(d, threadIdx.x ? __frcp_rn(d) : 0.f);
@@ -321,7 +328,32 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
     for (int i = threadIdx.x; i < groups; i += blockDim.x) gs_copy[i] = gs[i];
   if (status_reset && blockIdx.x == 0 && threadIdx.x == 0) *status_reset = 0;
   const float rcp6 = __frcp_rn(6.0f);
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // Global scales from the amax kernel's partial maxima: with few groups the
+  // block reduces each group's partials once into shared memory (max is
+  // exact and order-free: every block gets the same bits), instead of every
+  // warp reducing its group's partials.
+  const bool shared_gs = amax_partial && groups <= kSharedGsGroups;
+  if (shared_gs) {
+    if (groups == 1) {
+      float a = 0.f;
+      for (int i = threadIdx.x; i < nb; i += blockDim.x) a = fmaxf(a, amax_partial[i]);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+      if (lane == 0) s_red[warp] = a;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w) a = fmaxf(a, s_red[w]);
+        s_gs[0] = gs_from_group_amax(a);
+      }
+    } else {
+      for (int gg = warp; gg < groups; gg += blockDim.x >> 5) {
+        const float v = warp_group_gs(amax_partial, partial_stride, nb, gg, lane);
+        if (lane == 0) s_gs[gg] = v;
+      }
+    }
+    __syncthreads();
+  }
   const int64_t segs = (K + 1023) / 1024;
   const int64_t per_group = rows_padded * segs;
   const int64_t items = per_group * groups;
@@ -329,13 +361,25 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
   int64_t have_g = -1;
   float gsv = 0.f;
   // item = (g * rows_padded + r) * segs + sg, stepped by the grid's warp
-  // count with additions and at most one carry per level (no division in the loop)
-  const int64_t first = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  // count with additions and at most one carry per level (no division in the
+  // loop; the start and the step are split with 32-bit divisions when the
+  // item count allows)
+  const int64_t first = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;
   const int64_t step = (int64_t)gridDim.x * (blockDim.x >> 5);
-  int64_t g = first / per_group, r = (first - g * per_group) / segs;
-  int64_t sg = first - g * per_group - r * segs;
-  const int64_t dg = step / per_group, dr = (step - dg * per_group) / segs;
-  const int64_t ds = step - dg * per_group - dr * segs;
+  int64_t g, r, sg, dg, dr, ds;
+  if (items + step < (1ll << 31)) {
+    const uint32_t pg = (uint32_t)per_group, ns = (uint32_t)segs;
+    const uint32_t f = (uint32_t)first, st = (uint32_t)step;
+    const uint32_t g32 = f / pg, f_in = f - g32 * pg, r32 = f_in / ns;
+    const uint32_t dg32 = st / pg, st_in = st - dg32 * pg, dr32 = st_in / ns;
+    g = g32, r = r32, sg = f_in - r32 * ns;
+    dg = dg32, dr = dr32, ds = st_in - dr32 * ns;
+  } else {
+    g = first / per_group, r = (first - g * per_group) / segs;
+    sg = first - g * per_group - r * segs;
+    dg = step / per_group, dr = (step - dg * per_group) / segs;
+    ds = step - dg * per_group - dr * segs;
+  }
   for (int64_t item = first; item < items; item += step) {
     const int64_t rem = r * segs + sg, e0 = sg * 1024;
     const int64_t orow = g * rows_padded + r;
@@ -346,7 +390,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
       if (r < rows && el < K) ld_block32<kAligned32>(x + g * gstride_x + r * ld_x + el, raw[c]);
     }
     if (g != have_g) {
-      gsv = amax_partial ? warp_group_gs(amax_partial, partial_stride, nb, g, lane) : gs[g];
+      gsv = shared_gs ? s_gs[g] : amax_partial ? warp_group_gs(amax_partial, partial_stride, nb, g, lane) : gs[g];
       have_g = g;
     }
     if (amax_partial && gs_copy && rem == 0 && lane == 0) gs_copy[g] = gsv;
