@@ -141,28 +141,6 @@ __device__ __forceinline__ bool wait_bounded_spin(uint32_t bar, uint32_t parity,
   }
 }
 
-// wait_bounded for a waiter that is off the critical path: it sleeps
-// sleep_ns between polls instead of spinning, leaving issue slots to the
-// other warps of its SM sub-partition.  Same give-up rules.
-__device__ __forceinline__ bool wait_bounded_backoff(uint32_t bar, uint32_t parity, volatile int* abort,
-                                                     int* status, uint64_t timeout_ns, uint32_t sleep_ns) {
-  if (mbar_try_wait<false>(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i) {
-      __nanosleep(sleep_ns);
-      if (mbar_try_wait<false>(bar, parity)) return true;
-    }
-    if (*abort) return false;
-    if (global_timer_ns() - t0 > timeout_ns) {
-      *abort = 1;
-      if (status) atomicExch(status, 6 /* NVFP4_ERR_DEVICE_TIMEOUT */);
-      return false;
-    }
-  }
-}
-
 // ------------------------------------------------------------------ TMA
 // Bulk tensor store of one box from shared memory (bulk-group completion),
 // the group commit, and the waits for the group's shared-memory reads / full
