@@ -463,6 +463,22 @@ int nvfp4_moe_set_overlap(int enable, int* prev);
 int nvfp4_gemm_set_cta_pair(int mode, int* prev_mode);
 
 /*
+ * nvfp4_moe_set_swap_l2 -- the L2 GEMM of small batches with swapped operands.
+ *
+ * With enable 1, a forward whose L2 GEMM runs single CTAs (T * top_k <
+ * 256 * E: decode-sized batches) and whose E is at most 256 computes the L2
+ * GEMM with 128-row tiles of the expert's W2 as the MMA's M operand and 64
+ * of the expert's slot rows as N, over the expert's real rows only, instead
+ * of 128-row slot tiles against 256 W2 rows; the routing-weighted bf16 rows
+ * it stores (y) are the same, bit for bit.  enable 0 (the default): always
+ * the slot-major GEMM, which measured as fast or faster (the weight stream
+ * of both runs at the memory rate).  prev_enable (may be null) receives the
+ * previous setting.  Returns NVFP4_OK, or NVFP4_ERR_INVALID_ARG (setting
+ * unchanged) for a value other than 0 or 1.  Not thread-safe with respect
+ * to launches issued concurrently from other host threads; no device work. */
+int nvfp4_moe_set_swap_l2(int enable, int* prev_enable);
+
+/*
  * Optional per-stage timing of nvfp4_moe_forward: when set, the forward
  * records events[i] (cudaEvent_t) on its stream before stage i, i = 0..6, and
  * events[7] after the last stage (stages: route, slot scan, slot scatter,

@@ -105,6 +105,7 @@ _mma_rate = _sig("nvfp4_debug_mma_rate", c_int, [c_ptr, c_size, c_ptr, c_size, c
 _stage_events = _sig("nvfp4_moe_set_stage_events", c_int, [ctypes.POINTER(c_ptr), c_int])
 _moe_set_overlap = _sig("nvfp4_moe_set_overlap", c_int, [c_int, ctypes.POINTER(c_int)])
 _gemm_set_cta_pair = _sig("nvfp4_gemm_set_cta_pair", c_int, [c_int, ctypes.POINTER(c_int)])
+_moe_set_swap_l2 = _sig("nvfp4_moe_set_swap_l2", c_int, [c_int, ctypes.POINTER(c_int)])
 
 
 def _p(t):
@@ -289,6 +290,14 @@ def nvfp4_gemm_set_cta_pair(mode):
     GEMM only (default).  Returns the previous mode."""
     prev = c_int(-1)
     _check(_gemm_set_cta_pair(int(mode), ctypes.byref(prev)))
+    return prev.value
+
+
+def nvfp4_moe_set_swap_l2(enable):
+    """1: the L2 GEMM of small batches runs with W2 tiles as the MMA's M operand
+    and 64 slot rows as N; 0 (default): always slot-major.  Returns the previous setting."""
+    prev = c_int(-1)
+    _check(_moe_set_swap_l2(int(enable), ctypes.byref(prev)))
     return prev.value
 
 

@@ -86,12 +86,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // K-major packed FP4 matrix [rows][K/2] bytes; box 128 bytes x 128 rows, 128-byte swizzle.
-int make_fp4_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K) {
+int make_fp4_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows = 128) {
   auto fn = encode_fn();
   if (!fn) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   const cuuint64_t dims[2] = {(cuuint64_t)(K / 2), (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
-  const cuuint32_t box[2] = {128, 128};
+  const cuuint32_t box[2] = {128, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -128,6 +128,7 @@ void* g_stage_events[8] = {};
 int g_n_stage_events = 0;
 int g_debug_stall_ms = 0;  // > 0: MoE forwards launch their L1 GEMM with no operand loads (failure-detection test)
 int g_l1_l2_overlap = 1;   // the L2 GEMM takes the L1 output per m-tile (nvfp4_moe_set_overlap)
+int g_swap_l2 = 0;         // small batches: the L2 GEMM with swapped operands (nvfp4_moe_set_swap_l2)
 
 inline void stage_mark(int i, cudaStream_t s) {
   if (g_n_stage_events == 8 && g_stage_events[i]) cudaEventRecord((cudaEvent_t)g_stage_events[i], s);
@@ -515,8 +516,34 @@ int moe_forward_impl(const void* hidden, const Routing& rt, int64_t T, int64_t H
                                          true)) != cudaSuccess)
     return cuda_fail(e, "L2 activation quantize launch");
   stage_mark(5, s);
-  if ((e = launch_gemm(kEpiCombine, g2, (int)t2, dev->sms, s, true)) != cudaSuccess)
+  if (g_swap_l2 && !g2.pair_hint && E <= 256) {
+    // small batches: W2 tiles as the MMA's M operand, 64 slot rows as N
+    SwapArgs sw;
+    memset(&sw, 0, sizeof(sw));
+    sw.tmap_w = g2.tmap_b;
+    if (int rc = make_fp4_map(&sw.tmap_x, a2, cap, I, 64)) return rc;
+    sw.sfw = g2.sfb;
+    sw.sfx = g2.sfa;
+    sw.offsets = offsets;
+    sw.counts = counts;
+    sw.x_gs = g2.a_gs;
+    sw.w_gs = g2.b_gs;
+    sw.row_w = row_w;
+    sw.y = ybuf;
+    sw.G = E;
+    sw.K = (int)I;
+    sw.num_kb = g2.num_kb;
+    sw.H = (int)H;
+    sw.n_wtiles = (int)(H / 128);
+    sw.sfw_group_bytes = g2.sfb_group_bytes;
+    sw.tile_done = g2.tile_done;
+    sw.tile_done_target = g2.tile_done_target;
+    sw.status = status;
+    sw.timeout_ns = g2.timeout_ns;
+    if ((e = launch_gemm_swap(sw, dev->sms, s, true)) != cudaSuccess) return cuda_fail(e, "L2 launch");
+  } else if ((e = launch_gemm(kEpiCombine, g2, (int)t2, dev->sms, s, true)) != cudaSuccess) {
     return cuda_fail(e, "L2 launch");
+  }
   stage_mark(6, s);
   if ((e = launch_token_combine(ybuf, inverse, T, H, top_k, (uint16_t*)out, s, true)) != cudaSuccess)
     return cuda_fail(e, "combine launch");
@@ -806,6 +833,14 @@ int nvfp4_gemm_set_cta_pair(int mode, int* prev_mode) {
   if (mode < 0 || mode > 2) return fail(NVFP4_ERR_INVALID_ARG, "mode must be 0, 1 or 2");
   const int prev = gemm_set_pair_mode(mode);
   if (prev_mode) *prev_mode = prev;
+  return NVFP4_OK;
+}
+
+int nvfp4_moe_set_swap_l2(int enable, int* prev_enable) {
+  g_err[0] = 0;
+  if (enable != 0 && enable != 1) return fail(NVFP4_ERR_INVALID_ARG, "enable must be 0 or 1");
+  if (prev_enable) *prev_enable = g_swap_l2;
+  g_swap_l2 = enable;
   return NVFP4_OK;
 }
 

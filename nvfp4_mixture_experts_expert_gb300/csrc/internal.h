@@ -177,6 +177,34 @@ struct GemmArgs {
 
 size_t gemm_smem_bytes(int G);
 
+// gemm_swap.cu: the MoE L2 GEMM for small batches with W2 tiles as the MMA's
+// M = 128 operand and 64 slot rows as N (see there); same output as the
+// routing-weighted epilogue of launch_gemm(kEpiCombine).
+struct SwapArgs {
+  CUtensorMap tmap_w;  // W2: [G * H][K/2] bytes, box 128 B x 128 rows, 128-byte swizzle
+  CUtensorMap tmap_x;  // L1 output (A2): [rows][K/2] bytes, box 128 B x 64 rows, 128-byte swizzle
+  const uint8_t* sfw;  // W2 tile-layout scales, sfw_group_bytes per group
+  const uint8_t* sfx;  // A2 tile-layout scales (slot rows)
+  const int32_t* offsets;  // [G+1] 128-aligned slot offsets
+  const int32_t* counts;   // [G] real rows per group
+  const float* x_gs;       // [G] A2 global scales
+  const float* w_gs;       // [G] W2 global scales
+  const float* row_w;      // [rows] routing weights in slot order
+  uint16_t* y;             // bf16 [rows][H]
+  int G;
+  int K;        // I
+  int num_kb;   // ceil(K / 256)
+  int H;        // output features (W2 rows per group), a multiple of 128
+  int n_wtiles; // H / 128
+  int64_t sfw_group_bytes;
+  int* tile_done;  // as GemmArgs (L1 -> L2 hand-off per m-tile)
+  int tile_done_target;
+  int* status;
+  unsigned long long timeout_ns;
+};
+size_t gemm_swap_smem_bytes(int G);
+cudaError_t launch_gemm_swap(const SwapArgs& args, int num_sms, cudaStream_t s, bool pdl);
+
 // abi.cu: sets the text nvfp4_last_error() returns on the calling thread.
 void set_last_error(const char* msg);
 // units_upper: an upper bound on the work items (128-row m-tiles x n-tiles);

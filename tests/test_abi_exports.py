@@ -156,6 +156,18 @@ def test_status_reader_and_debug_stall_check_arguments_on_host(binding):
     binding.nvfp4_moe_set_debug_stall(0)
 
 
+def test_swap_l2_switch(binding):
+    prev = binding.nvfp4_moe_set_swap_l2(1)
+    try:
+        assert prev == 0
+        assert binding.nvfp4_moe_set_swap_l2(0) == 1
+        with pytest.raises(binding.Nvfp4Error):
+            binding.nvfp4_moe_set_swap_l2(2)
+        assert binding.nvfp4_moe_set_swap_l2(0) == 0
+    finally:
+        binding.nvfp4_moe_set_swap_l2(prev)
+
+
 def test_overlap_switch(binding):
     prev = binding.nvfp4_moe_set_overlap(0)
     try:

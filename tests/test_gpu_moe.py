@@ -753,6 +753,47 @@ def test_l1_l2_overlap_is_bit_identical(T, E, k):
     assert rf <= 2e-2 and cs >= 0.999, (rf, cs)
 
 
+@pytest.mark.parametrize("T,H,I,E,k", [(128, 512, 256, 8, 6), (300, 256, 512, 12, 3), (64, 1024, 384, 5, 2)])
+def test_swapped_l2_gemm_is_bit_identical(T, H, I, E, k):
+    """Small batches: the L2 GEMM with W2 tiles as the MMA's M operand and 64
+    slot rows as N stores exactly the routing-weighted rows of the slot-major
+    GEMM, with and without the L1 -> L2 hand-off, and the forward matches the
+    oracle.  Expert sizes: 128 rows exactly and 78-125 (first case); 276,
+    176, 134, 52, 1 and empty experts (second); at most 59 rows with I = 384,
+    a partial last K-stage (third)."""
+    import torch
+    from nvfp4_mixture_experts_expert_gb300 import api, binding as B
+    wl = W.moe_workload(T, H, I, E, k, 71, logit_bias_std=1.5)
+    orc = OracleMoE(wl)
+    w = api.quantize_moe_weights(bf16_dev(wl.w13), bf16_dev(wl.w2))
+    fwd = api.MoEForward(wl.T, wl.H, wl.I, wl.E, wl.top_k)
+    args = (bf16_dev(wl.hidden), dev(wl.logits), w, dev(orc.a1_gs), dev(orc.a2_gs), wl.gate_limit, wl.up_limit)
+    res = {}
+    prev = B.nvfp4_moe_set_swap_l2(0)
+    prev_ov = B.nvfp4_moe_set_overlap(1)
+    try:
+        for sw, ov in ((0, 1), (1, 1), (1, 0)):
+            B.nvfp4_moe_set_swap_l2(sw)
+            B.nvfp4_moe_set_overlap(ov)
+            out = fwd(*args)
+            torch.cuda.synchronize()
+            P = int(host(fwd.view("meta", torch.int32, 1))[0])
+            real = orc.meta["sorted_token_ids"] >= 0
+            y = host(fwd.view("y", torch.int16, P * H)).reshape(P, H)[real].copy()
+            res[(sw, ov)] = (host(out.view(torch.int16)).copy(), y)
+            assert fwd.status() == 0
+    finally:
+        B.nvfp4_moe_set_swap_l2(prev)
+        B.nvfp4_moe_set_overlap(prev_ov)
+    for key in ((1, 1), (1, 0)):
+        for a, b in zip(res[key], res[(0, 1)]):
+            np.testing.assert_array_equal(a, b)
+    ref, _ = orc.forward()
+    got = bf16_host(torch.from_numpy(res[(1, 1)][0]).view(torch.bfloat16))
+    rf, cs = rel_frob(got, ref), cosine(got, ref)
+    assert rf <= 2e-2 and cs >= 0.999, (rf, cs)
+
+
 # ----------------------------------------------------------------- FP8 L1 output (reading R20)
 
 @pytest.mark.parametrize("T,H,I,E,k,dead", [(120, 512, 256, 6, 2, (3,)), (700, 256, 512, 5, 3, ())])
