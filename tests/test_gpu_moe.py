@@ -792,6 +792,18 @@ def test_swapped_l2_gemm_is_bit_identical(T, H, I, E, k):
     got = bf16_host(torch.from_numpy(res[(1, 1)][0]).view(torch.bfloat16))
     rf, cs = rel_frob(got, ref), cosine(got, ref)
     assert rf <= 2e-2 and cs >= 0.999, (rf, cs)
+    # L2 scales from the batch (device-computed): the same rows either way
+    batch = {}
+    try:
+        for sw in (0, 1):
+            B.nvfp4_moe_set_swap_l2(sw)
+            out = fwd(bf16_dev(wl.hidden), dev(wl.logits), w, dev(orc.a1_gs), None, wl.gate_limit, wl.up_limit)
+            torch.cuda.synchronize()
+            batch[sw] = host(out.view(torch.int16)).copy()
+            assert fwd.status() == 0
+    finally:
+        B.nvfp4_moe_set_swap_l2(prev)
+    np.testing.assert_array_equal(batch[1], batch[0])
 
 
 # ----------------------------------------------------------------- FP8 L1 output (reading R20)
