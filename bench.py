@@ -65,6 +65,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-extras", action="store_true", help="skip the decode-size side measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--swap-l2", type=int, choices=[0, 1], default=0,
+                    help="1: small batches run the L2 GEMM with swapped operands (nvfp4_moe_set_swap_l2)")
     return ap.parse_args()
 
 
@@ -213,6 +215,7 @@ def run_ours(args, world, rank, local):
     import numpy as np
     import torch
     from nvfp4_mixture_experts_expert_gb300 import binding as B
+    B.nvfp4_moe_set_swap_l2(args.swap_l2)
     L = build_layer(args.workload, args.seed, rank)
     T, H, I, E, k = L["T"], L["H"], L["I"], L["E"], L["k"]
     fwd, w = L["fwd"], L["w"]
@@ -367,6 +370,7 @@ def run_ours(args, world, rank, local):
         "config": {"workload": workload_name(args.workload), "tokens_per_gpu": T, "hidden": H,
                    "intermediate": I, "experts": E, "top_k": k, "padded_rows": P,
                    "parallelism": f"dp{world} over tokens (replicated local experts)",
+                   "swapped_l2": bool(args.swap_l2),
                    "l2_flush": "not needed: weights (0.76 GB NVFP4) and activations exceed the 129 MB L2"},
         "roofline": roofline,
         "stages_ms": {n: round(v, 4) for n, v in stages.items()},
